@@ -1,0 +1,152 @@
+"""FP64 CPU oracle for packed native-resolution 2D-RoPE varlen attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s cpu_baseline / reference leg may import this package.  The product
+path (``packed_resolution_diffusion_pack_b300``) never imports it, and this
+package never imports the product path: the two share nothing but the seeded
+input generator in ``synth``.
+
+The arithmetic lives in ``mf_oracle.c`` (plain C, double precision, one query row
+at a time, OpenMP across (sample, head) pairs).  This module only compiles it with
+gcc and marshals numpy arrays.  Each function cites the page passage it follows in
+the C source.  Pins that tie the oracle to something other than itself are in
+``tests/test_oracle_*.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mf_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+
+ROPE_BASE = 10000.0
+
+
+def compile_source(src: str, so: str) -> str:
+    """gcc -O2 -fopenmp a C source file into a shared library."""
+    tmp = so + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                           "-D_DEFAULT_SOURCE", src, "-o", tmp, "-lm"])
+    os.replace(tmp, so)
+    return so
+
+
+def build(force: bool = False) -> str:
+    """Compile mf_oracle.c into _build/liboracle.so."""
+    os.makedirs(_BUILD, exist_ok=True)
+    so = os.path.join(_BUILD, "liboracle.so")
+    if force or not os.path.exists(so) or os.path.getmtime(so) < os.path.getmtime(_SRC):
+        compile_source(_SRC, so)
+    return so
+
+
+_libs: dict = {}
+
+
+def lib(so: str | None = None):
+    """The compiled oracle; ``so`` selects another build of the same source
+    (tests that plant a mistake in a copy of the oracle use this)."""
+    key = so or "default"
+    if key not in _libs:
+        L = ctypes.CDLL(so or build())
+        p, i64, f64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double, ctypes.c_int
+        L.oracle_pack.argtypes = [p, i64, p, p]
+        L.oracle_rope2d.argtypes = [p, p, i64, i64, i64, f64, i32, p]
+        L.oracle_attn_fwd.argtypes = [p, p, p, p, i64, p, i64, i64, i64, f64, f64, p, p]
+        L.oracle_attn_bwd.argtypes = [p, p, p, p, p, i64, p, i64, i64, i64, f64, f64, p, p, p]
+        for f in (L.oracle_pack, L.oracle_rope2d, L.oracle_attn_fwd, L.oracle_attn_bwd):
+            f.restype = ctypes.c_int
+        _libs[key] = L
+    return _libs[key]
+
+
+def _f64(x) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def pack(specs, so: str | None = None):
+    """(cu_seqlens int64[n+1], pos int64[T, 2]) for specs [(text_len, H, W)]."""
+    s = np.ascontiguousarray(np.asarray(specs, dtype=np.int64).reshape(-1, 3))
+    n = s.shape[0]
+    cu = np.zeros(n + 1, dtype=np.int64)
+    if lib(so).oracle_pack(s.ctypes.data, n, cu.ctypes.data, None) != 0:
+        raise ValueError("negative spec entry")
+    pos = np.zeros((int(cu[-1]), 2), dtype=np.int64)
+    lib(so).oracle_pack(s.ctypes.data, n, cu.ctypes.data, pos.ctypes.data)
+    return cu, pos
+
+
+def rope2d(x, pos, inverse: bool = False, base: float = ROPE_BASE, so: str | None = None):
+    """R(+theta) x (or R(-theta) x) for x [T, heads, d] float64, pos [T, 2]."""
+    x = _f64(x)
+    T, h, d = x.shape
+    y = np.empty_like(x)
+    p = np.ascontiguousarray(pos, dtype=np.int64)
+    rc = lib(so).oracle_rope2d(x.ctypes.data, p.ctypes.data, T, h, d, base,
+                                    -1 if inverse else 1, y.ctypes.data)
+    if rc != 0:
+        raise ValueError("head_dim must be a multiple of 4")
+    return y
+
+
+def attn_fwd(q, k, v, cu, pos, scale=None, base: float = ROPE_BASE, so: str | None = None):
+    """O [T, h, d] and LSE [h, T] (float64).  pos=None: no rotation."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, h, d = q.shape
+    cu = np.ascontiguousarray(cu, dtype=np.int64)
+    p = None if pos is None else np.ascontiguousarray(pos, dtype=np.int64)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = np.zeros_like(q)
+    lse = np.zeros((h, T), dtype=np.float64)
+    lib(so).oracle_attn_fwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, cu.ctypes.data,
+                                 len(cu) - 1, _ptr(p), T, h, d, scale, base, o.ctypes.data,
+                                 lse.ctypes.data)
+    return o, lse
+
+
+def attn_bwd(q, k, v, d_o, cu, pos, scale=None, base: float = ROPE_BASE, so: str | None = None):
+    """dQ, dK, dV [T, h, d] (float64) with respect to the un-rotated q, k, v."""
+    q, k, v, d_o = _f64(q), _f64(k), _f64(v), _f64(d_o)
+    T, h, d = q.shape
+    cu = np.ascontiguousarray(cu, dtype=np.int64)
+    p = None if pos is None else np.ascontiguousarray(pos, dtype=np.int64)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(q), np.zeros_like(q)
+    lib(so).oracle_attn_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, d_o.ctypes.data,
+                                 cu.ctypes.data, len(cu) - 1, _ptr(p), T, h, d, scale, base,
+                                 dq.ctypes.data, dk.ctypes.data, dv.ctypes.data)
+    return dq, dk, dv
+
+
+def sample_head_slice(x, cu, i: int, a: int):
+    """Rows of sample i, head a of a packed [T, h, d] array, as [L_i, 1, d]."""
+    return x[int(cu[i]):int(cu[i + 1]), a:a + 1, :]
+
+
+def attn_fwd_pair(q, k, v, cu, pos, i: int, a: int, **kw):
+    """The oracle on one (sample, head) pair: exact because samples and heads are
+    independent in the definition.  Returns O [L, d], LSE [L]."""
+    sl = slice(int(cu[i]), int(cu[i + 1]))
+    L = sl.stop - sl.start
+    o, lse = attn_fwd(sample_head_slice(q, cu, i, a), sample_head_slice(k, cu, i, a),
+                      sample_head_slice(v, cu, i, a), np.array([0, L]), pos[sl], **kw)
+    return o[:, 0, :], lse[0]
+
+
+def attn_bwd_pair(q, k, v, d_o, cu, pos, i: int, a: int, **kw):
+    sl = slice(int(cu[i]), int(cu[i + 1]))
+    L = sl.stop - sl.start
+    dq, dk, dv = attn_bwd(sample_head_slice(q, cu, i, a), sample_head_slice(k, cu, i, a),
+                          sample_head_slice(v, cu, i, a), sample_head_slice(d_o, cu, i, a),
+                          np.array([0, L]), pos[sl], **kw)
+    return dq[:, 0, :], dk[:, 0, :], dv[:, 0, :]

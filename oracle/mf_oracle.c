@@ -1,0 +1,235 @@
+/*
+ * FP64 CPU oracle for packed native-resolution 2D-RoPE varlen attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and bench.py's
+ * cpu_baseline / reference leg load this library.  It shares no code, header,
+ * table or helper with the CUDA library and never calls it.
+ *
+ * What it computes, and where the pages define it:
+ *  - Packing: Mage-Flow (arXiv 2607.19064), rcap.io post, training-step listing
+ *    "native-resolution packed step" (pack(text_tokens + tokens, budget=50_000));
+ *    paperlayer.ai summary §3.2.1 "Model Architecture and Native Packing" (variable
+ *    length text and image sequences packed under a fixed token budget, each image
+ *    keeping its native latent grid, no padding, no buckets).
+ *  - Per-sample 2D RoPE: rcap.io post, same listing (per_sample_2d_rope(packed),
+ *    "native positions"); ai.thesatyajit.com explainer, "A backbone that doesn't
+ *    crop" (per-sample 2D rotary embeddings preserving each image's native layout).
+ *    The pages give no formula; the problem statement fixes it: image token k of an
+ *    H x W grid sits at (r, c) = (k div W, k mod W); text tokens at (0, 0); the first
+ *    half of head_dim rotates by r, the second half by c; within a half, the pair
+ *    (2j, 2j+1) rotates by theta = p * 10000^(-2j/(d/2)), j < d/4, with the usual
+ *    rotary sign (x, y) -> (x cos - y sin, x sin + y cos).
+ *  - Joint attention within a sample: paperlayer.ai §3.2.1 (concatenated text and
+ *    image tokens use joint self-attention; cross-modal interaction through
+ *    self-attention over the combined sequence), realised with variable-length
+ *    kernels (rcap.io post, "Native-resolution packing"): non-causal softmax
+ *    attention restricted to each sample's own tokens, scale 1/sqrt(d), sequence
+ *    order [text; image].  LSE is the natural-log logsumexp of the scaled logits.
+ *  - Backward: the training step of the rcap.io listing differentiates through
+ *    the attention; the gradient is the exact derivative of the definitions above
+ *    (softmax Jacobian and the transpose of the rotation, which is its inverse).
+ *
+ * Every loop follows the definition directly, one query row at a time, in double.
+ * No blocking, no fusion, no online softmax.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORACLE_OK = 0, ORACLE_ERR = 1 };
+
+/* ---------------------------------------------------------------- packing */
+/*
+ * specs[i] = {text_len, H, W}.  cu[0] = 0, cu[i+1] = cu[i] + text_len + H*W.
+ * Within sample i, tokens [cu[i], cu[i]+text_len) are text at (0,0); token
+ * cu[i]+text_len+k, 0 <= k < H*W, is image token k at (k div W, k mod W).
+ * pos is [T][2] = (r, c).  pos may be NULL (sizes only).
+ */
+int oracle_pack(const int64_t* specs, int64_t n, int64_t* cu, int64_t* pos) {
+  cu[0] = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t t = specs[3 * i], H = specs[3 * i + 1], W = specs[3 * i + 2];
+    if (t < 0 || H < 0 || W < 0) return ORACLE_ERR;
+    int64_t L = t + H * W;
+    if (pos) {
+      for (int64_t k = 0; k < t; ++k) {
+        pos[2 * (cu[i] + k)] = 0;
+        pos[2 * (cu[i] + k) + 1] = 0;
+      }
+      for (int64_t k = 0; k < H * W; ++k) {
+        pos[2 * (cu[i] + t + k)] = k / W;
+        pos[2 * (cu[i] + t + k) + 1] = k % W;
+      }
+    }
+    cu[i + 1] = cu[i] + L;
+  }
+  return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------- RoPE */
+/*
+ * Rotate one head vector v[d] of a token at position (r, c) by +theta
+ * (sign = +1) or -theta (sign = -1), writing out[d].
+ */
+static void rope_vec(const double* v, int64_t r, int64_t c, int64_t d, double base, int sign,
+                     double* out) {
+  int64_t half = d / 2, nfreq = d / 4;
+  for (int64_t h = 0; h < 2; ++h) {
+    double p = (h == 0) ? (double)r : (double)c;
+    for (int64_t j = 0; j < nfreq; ++j) {
+      double omega = pow(base, -2.0 * (double)j / (double)half);
+      double theta = sign * p * omega;
+      double x = v[h * half + 2 * j], y = v[h * half + 2 * j + 1];
+      out[h * half + 2 * j] = x * cos(theta) - y * sin(theta);
+      out[h * half + 2 * j + 1] = x * sin(theta) + y * cos(theta);
+    }
+  }
+}
+
+/* x, y: [T][heads][d]; pos [T][2]; sign +1 forward rotation, -1 inverse. */
+int oracle_rope2d(const double* x, const int64_t* pos, int64_t T, int64_t heads, int64_t d,
+                  double base, int sign, double* y) {
+  if (d % 4 != 0) return ORACLE_ERR;
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t a = 0; a < heads; ++a)
+      rope_vec(x + (t * heads + a) * d, pos[2 * t], pos[2 * t + 1], d, base, sign,
+               y + (t * heads + a) * d);
+  return ORACLE_OK;
+}
+
+/* ------------------------------------------------------ attention forward */
+/*
+ * Inputs un-rotated q, k, v [T][heads][d]; cu [n+1]; pos [T][2] or NULL (no
+ * rotation).  Outputs o [T][heads][d], lse [heads][T].
+ * For each sample i and head a, for each query row j of sample i:
+ *   S_jk = scale * <q'_j, k'_k> over the keys k of sample i only,
+ *   m_j = max_k S_jk, LSE_j = m_j + ln sum_k exp(S_jk - m_j),
+ *   O_j = sum_k exp(S_jk - LSE_j) v_k.
+ * q' = R(theta) q and k' = R(theta) k are formed first, exactly as defined above.
+ */
+int oracle_attn_fwd(const double* q, const double* k, const double* v, const int64_t* cu,
+                    int64_t n, const int64_t* pos, int64_t T, int64_t heads, int64_t d,
+                    double scale, double base, double* o, double* lse) {
+  double* qr = (double*)malloc(sizeof(double) * (size_t)(T * heads * d + 1));
+  double* kr = (double*)malloc(sizeof(double) * (size_t)(T * heads * d + 1));
+  if (!qr || !kr) { free(qr); free(kr); return ORACLE_ERR; }
+  if (pos) {
+    oracle_rope2d(q, pos, T, heads, d, base, +1, qr);
+    oracle_rope2d(k, pos, T, heads, d, base, +1, kr);
+  } else {
+    memcpy(qr, q, sizeof(double) * (size_t)(T * heads * d));
+    memcpy(kr, k, sizeof(double) * (size_t)(T * heads * d));
+  }
+  int64_t npairs = n * heads;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t pr = 0; pr < npairs; ++pr) {
+    int64_t i = pr / heads, a = pr % heads;
+    int64_t s0 = cu[i], L = cu[i + 1] - cu[i];
+    if (L <= 0) continue;
+    double* srow = (double*)malloc(sizeof(double) * (size_t)L);
+    for (int64_t j = 0; j < L; ++j) {
+      const double* qj = qr + ((s0 + j) * heads + a) * d;
+      double m = -INFINITY;
+      for (int64_t kk = 0; kk < L; ++kk) {
+        const double* kv = kr + ((s0 + kk) * heads + a) * d;
+        double acc = 0.0;
+        for (int64_t e = 0; e < d; ++e) acc += qj[e] * kv[e];
+        srow[kk] = scale * acc;
+        if (srow[kk] > m) m = srow[kk];
+      }
+      double l = 0.0;
+      for (int64_t kk = 0; kk < L; ++kk) l += exp(srow[kk] - m);
+      double lj = m + log(l);
+      lse[a * T + s0 + j] = lj;
+      double* oj = o + ((s0 + j) * heads + a) * d;
+      for (int64_t e = 0; e < d; ++e) oj[e] = 0.0;
+      for (int64_t kk = 0; kk < L; ++kk) {
+        double p = exp(srow[kk] - lj);
+        const double* vk = v + ((s0 + kk) * heads + a) * d;
+        for (int64_t e = 0; e < d; ++e) oj[e] += p * vk[e];
+      }
+    }
+    free(srow);
+  }
+  free(qr);
+  free(kr);
+  return ORACLE_OK;
+}
+
+/* ----------------------------------------------------- attention backward */
+/*
+ * Gradients of the forward above with respect to the un-rotated q, k and v, for
+ * the upstream gradient d_o [T][heads][d].  Per sample and head:
+ *   O, LSE recomputed as in the forward;  D_j = <dO_j, O_j>;
+ *   P_jk = exp(S_jk - LSE_j);  dV_k = sum_j P_jk dO_j;
+ *   dP_jk = <dO_j, v_k>;  dS_jk = P_jk (dP_jk - D_j);
+ *   dQ'_j = scale sum_k dS_jk k'_k;  dK'_k = scale sum_j dS_jk q'_j;
+ *   dQ = R(-theta) dQ',  dK = R(-theta) dK'  (R is orthogonal: R^T = R(-theta)).
+ */
+int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* d_o,
+                    const int64_t* cu, int64_t n, const int64_t* pos, int64_t T, int64_t heads,
+                    int64_t d, double scale, double base, double* dq, double* dk, double* dv) {
+  size_t N = (size_t)(T * heads * d);
+  double* qr = (double*)malloc(sizeof(double) * (N + 1));
+  double* kr = (double*)malloc(sizeof(double) * (N + 1));
+  double* o = (double*)malloc(sizeof(double) * (N + 1));
+  double* lse = (double*)malloc(sizeof(double) * (size_t)(heads * T + 1));
+  double* dqr = (double*)calloc(N + 1, sizeof(double));
+  double* dkr = (double*)calloc(N + 1, sizeof(double));
+  if (!qr || !kr || !o || !lse || !dqr || !dkr) {
+    free(qr); free(kr); free(o); free(lse); free(dqr); free(dkr);
+    return ORACLE_ERR;
+  }
+  oracle_attn_fwd(q, k, v, cu, n, pos, T, heads, d, scale, base, o, lse);
+  if (pos) {
+    oracle_rope2d(q, pos, T, heads, d, base, +1, qr);
+    oracle_rope2d(k, pos, T, heads, d, base, +1, kr);
+  } else {
+    memcpy(qr, q, sizeof(double) * N);
+    memcpy(kr, k, sizeof(double) * N);
+  }
+  memset(dv, 0, sizeof(double) * N);
+  int64_t npairs = n * heads;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t pr = 0; pr < npairs; ++pr) {
+    int64_t i = pr / heads, a = pr % heads;
+    int64_t s0 = cu[i], L = cu[i + 1] - cu[i];
+    if (L <= 0) continue;
+    double* prow = (double*)malloc(sizeof(double) * (size_t)L);
+    for (int64_t j = 0; j < L; ++j) {
+      int64_t rj = ((s0 + j) * heads + a) * d;
+      double Dj = 0.0;
+      for (int64_t e = 0; e < d; ++e) Dj += d_o[rj + e] * o[rj + e];
+      double lj = lse[a * T + s0 + j];
+      for (int64_t kk = 0; kk < L; ++kk) {
+        int64_t rk = ((s0 + kk) * heads + a) * d;
+        double acc = 0.0;
+        for (int64_t e = 0; e < d; ++e) acc += qr[rj + e] * kr[rk + e];
+        prow[kk] = exp(scale * acc - lj);
+      }
+      for (int64_t kk = 0; kk < L; ++kk) {
+        int64_t rk = ((s0 + kk) * heads + a) * d;
+        double dp = 0.0;
+        for (int64_t e = 0; e < d; ++e) dp += d_o[rj + e] * v[rk + e];
+        double ds = prow[kk] * (dp - Dj);
+        for (int64_t e = 0; e < d; ++e) {
+          dv[rk + e] += prow[kk] * d_o[rj + e];
+          dqr[rj + e] += scale * ds * kr[rk + e];
+          dkr[rk + e] += scale * ds * qr[rj + e];
+        }
+      }
+    }
+    free(prow);
+  }
+  if (pos) {
+    oracle_rope2d(dqr, pos, T, heads, d, base, -1, dq);
+    oracle_rope2d(dkr, pos, T, heads, d, base, -1, dk);
+  } else {
+    memcpy(dq, dqr, sizeof(double) * N);
+    memcpy(dk, dkr, sizeof(double) * N);
+  }
+  free(qr); free(kr); free(o); free(lse); free(dqr); free(dkr);
+  return ORACLE_OK;
+}

@@ -1,0 +1,275 @@
+"""Pins of the FP64 oracle against things other than itself.
+
+Each ``pin_*`` function raises AssertionError when the oracle (``so`` selects a
+build of it) disagrees with a hand-computed table, a closed form, a library
+routine on a special case, an invariant of the definition, or finite
+differences.  ``tests/test_oracle_pins.py`` runs them on the real oracle;
+``tests/test_oracle_mutants.py`` plants plausible mistakes in copies of the
+oracle source and checks that some pin fails for each.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _tiny_inputs(seed=0):
+    wl = synth.tiny(seed)
+    q, k, v, do = synth.make_inputs(wl, with_do=True)
+    f = synth.bf16_bits_to_f64
+    return wl, f(q), f(k), f(v), f(do)
+
+
+# ------------------------------------------------------------------ packing
+def pin_pack_golden(so=None):
+    for case in _golden("pack_cases.json")["cases"]:
+        cu, pos = oracle.pack(case["specs"], so=so)
+        assert cu.tolist() == case["cu"], (case["specs"], cu)
+        if "pos" in case:
+            assert pos.tolist() == case["pos"], (case["specs"], pos)
+        for t, rc in case.get("pos_spot", {}).items():
+            assert pos[int(t)].tolist() == rc, (t, pos[int(t)], rc)
+
+
+# --------------------------------------------------------------------- RoPE
+def pin_rope_golden(so=None):
+    fn = {"cos": math.cos, "sin": math.sin, "-sin": lambda a: -math.sin(a)}
+    for case in _golden("rope_d8.json")["cases"]:
+        x = np.zeros((1, 1, 8))
+        x[0, 0, case["unit"]] = 1.0
+        y = oracle.rope2d(x, np.array([case["pos"]]), so=so)[0, 0]
+        want = np.zeros(8)
+        for dim, (kind, ang) in case["out"].items():
+            want[int(dim)] = fn[kind](ang)
+        np.testing.assert_allclose(y, want, atol=1e-15, err_msg=str(case))
+
+
+def pin_rope_frequencies_d128(so=None):
+    """d = 128: pair j of the row half turns by r * 10000^(-j/32) (closed form
+    of 10000^(-2j/(d/2)) at d/2 = 64); checked at j = 0, 16 (10000^-0.5 = 0.01)
+    and 31, for r = 1, and for the column half with c = 1."""
+    for half, pos in ((0, [1, 0]), (1, [0, 1])):
+        for j, omega in ((0, 1.0), (16, 0.01), (31, 10000.0 ** (-31 / 32))):
+            x = np.zeros((1, 1, 128))
+            x[0, 0, 64 * half + 2 * j] = 1.0
+            y = oracle.rope2d(x, np.array([pos]), so=so)[0, 0]
+            assert abs(y[64 * half + 2 * j] - math.cos(omega)) < 1e-14
+            assert abs(y[64 * half + 2 * j + 1] - math.sin(omega)) < 1e-14
+            y[64 * half + 2 * j: 64 * half + 2 * j + 2] = 0
+            assert np.abs(y).max() == 0.0
+
+
+def pin_rope_identity_and_norm(so=None):
+    r = _rng(1)
+    x = r.standard_normal((50, 3, 64))
+    pos = np.zeros((50, 2), dtype=np.int64)
+    np.testing.assert_array_equal(oracle.rope2d(x, pos, so=so), x)
+    pos = r.integers(0, 128, size=(50, 2))
+    y = oracle.rope2d(x, pos, so=so)
+    nx = x[..., 0::2] ** 2 + x[..., 1::2] ** 2
+    ny = y[..., 0::2] ** 2 + y[..., 1::2] ** 2
+    np.testing.assert_allclose(ny, nx, rtol=0, atol=1e-12)
+    back = oracle.rope2d(y, pos, inverse=True, so=so)
+    np.testing.assert_allclose(back, x, rtol=0, atol=1e-12)
+
+
+def pin_rope_relative(so=None):
+    """<R(p1) q, R(p2) k> depends only on p1 - p2: shifting both positions by the
+    same (dr, dc) leaves the dot product unchanged."""
+    r = _rng(2)
+    for d in (64, 128):
+        q = r.standard_normal((20, 1, d))
+        k = r.standard_normal((20, 1, d))
+        p1 = r.integers(0, 100, size=(20, 2))
+        p2 = r.integers(0, 100, size=(20, 2))
+        shift = r.integers(-20, 20, size=(20, 2))
+        shift = np.maximum(shift, -np.minimum(p1, p2))
+        a = (oracle.rope2d(q, p1, so=so) * oracle.rope2d(k, p2, so=so)).sum(-1)
+        b = (oracle.rope2d(q, p1 + shift, so=so) * oracle.rope2d(k, p2 + shift, so=so)).sum(-1)
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-11)
+        # and it does depend on the offset (a rotation that ignored positions passes
+        # the shift test trivially)
+        c = (oracle.rope2d(q, p1 + 1, so=so) * oracle.rope2d(k, p2, so=so)).sum(-1)
+        assert np.abs(a - c).max() > 1e-3
+
+
+# ---------------------------------------------------------------- attention
+def _sdpa_per_sample(q, k, v, cu):
+    """torch.nn.functional.scaled_dot_product_attention (a library routine) run
+    on each sample alone, fp64 on the CPU; LSE from torch.logsumexp."""
+    T, h, d = q.shape
+    o = np.zeros_like(q)
+    lse = np.zeros((h, T))
+    for i in range(len(cu) - 1):
+        s, e = int(cu[i]), int(cu[i + 1])
+        if e == s:
+            continue
+        Q = torch.from_numpy(q[s:e]).permute(1, 0, 2)
+        K = torch.from_numpy(k[s:e]).permute(1, 0, 2)
+        V = torch.from_numpy(v[s:e]).permute(1, 0, 2)
+        o[s:e] = torch.nn.functional.scaled_dot_product_attention(Q, K, V).permute(1, 0, 2).numpy()
+        lse[:, s:e] = torch.logsumexp(torch.einsum("hqd,hkd->hqk", Q, K) / math.sqrt(d), -1).numpy()
+    return o, lse
+
+
+def pin_attn_vs_library(so=None):
+    """No rotation: the oracle equals per-sample torch SDPA; with rotation it equals
+    SDPA on the rotated inputs (RoPE itself pinned above)."""
+    wl, q, k, v, _ = _tiny_inputs()
+    cu, pos = oracle.pack(wl.specs)
+    o, lse = oracle.attn_fwd(q, k, v, cu, None, so=so)
+    o_ref, lse_ref = _sdpa_per_sample(q, k, v, cu)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+    o, lse = oracle.attn_fwd(q, k, v, cu, pos, so=so)
+    qr, kr = oracle.rope2d(q, pos), oracle.rope2d(k, pos)
+    o_ref, lse_ref = _sdpa_per_sample(qr, kr, v, cu)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def pin_attn_packed_equals_unpacked(so=None):
+    wl, q, k, v, _ = _tiny_inputs()
+    cu, pos = oracle.pack(wl.specs, so=so)
+    o, lse = oracle.attn_fwd(q, k, v, cu, pos, so=so)
+    for i in range(len(cu) - 1):
+        s, e = int(cu[i]), int(cu[i + 1])
+        oi, li = oracle.attn_fwd(q[s:e], k[s:e], v[s:e], np.array([0, e - s]), pos[s:e], so=so)
+        np.testing.assert_allclose(o[s:e], oi, rtol=0, atol=1e-15)
+        np.testing.assert_allclose(lse[:, s:e], li, rtol=0, atol=1e-15)
+
+
+def pin_attn_cross_sample_independence(so=None):
+    wl, q, k, v, _ = _tiny_inputs()
+    cu, pos = oracle.pack(wl.specs, so=so)
+    o, lse = oracle.attn_fwd(q, k, v, cu, pos, so=so)
+    s, e = int(cu[1]), int(cu[2])
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    r = _rng(3)
+    for x in (q2, k2, v2):
+        x[s:e] = r.standard_normal(x[s:e].shape) * 3
+    o2, lse2 = oracle.attn_fwd(q2, k2, v2, cu, pos, so=so)
+    keep = np.r_[0:s, e:len(q)]
+    assert np.array_equal(o[keep], o2[keep])
+    assert np.array_equal(lse[:, keep], lse2[:, keep])
+    assert np.abs(o[s:e] - o2[s:e]).max() > 1e-3
+
+
+def pin_attn_closed_forms(so=None):
+    wl, q, k, v, _ = _tiny_inputs()
+    cu, pos = oracle.pack(wl.specs, so=so)
+    T, h, d = q.shape
+    # V -> V + c_i (a constant vector per sample) gives O -> O + c_i
+    c = _rng(4).standard_normal((len(cu) - 1, h, d))
+    v2 = v.copy()
+    for i in range(len(cu) - 1):
+        v2[cu[i]:cu[i + 1]] += c[i]
+    o, _ = oracle.attn_fwd(q, k, v, cu, pos, so=so)
+    o2, _ = oracle.attn_fwd(q, k, v2, cu, pos, so=so)
+    for i in range(len(cu) - 1):
+        np.testing.assert_allclose(o2[cu[i]:cu[i + 1]] - o[cu[i]:cu[i + 1]],
+                                   np.broadcast_to(c[i], o[cu[i]:cu[i + 1]].shape), atol=1e-12)
+    # Q = 0: uniform weights, O = per-sample mean of V, LSE = ln L
+    o0, lse0 = oracle.attn_fwd(np.zeros_like(q), k, v, cu, pos, so=so)
+    for i in range(len(cu) - 1):
+        s, e = int(cu[i]), int(cu[i + 1])
+        np.testing.assert_allclose(o0[s:e], np.broadcast_to(v[s:e].mean(0), o0[s:e].shape), atol=1e-13)
+        np.testing.assert_allclose(lse0[:, s:e], math.log(e - s), atol=1e-13)
+    # L = 1 samples: O = V, LSE = <q, k> / sqrt(d) (one rotation on both sides)
+    specs = [(1, 0, 0), (0, 1, 1), (0, 3, 3)]
+    cu1, pos1 = oracle.pack(specs, so=so)
+    r = _rng(5)
+    q1, k1, v1 = (r.standard_normal((int(cu1[-1]), 2, 64)) for _ in range(3))
+    pos1 = pos1 + np.array([[5, 7], [2, 9]] + [[3, 4]] * 9)
+    o1, l1 = oracle.attn_fwd(q1, k1, v1, cu1, pos1, so=so)
+    for t in (0, 1):
+        np.testing.assert_allclose(o1[t], v1[t], atol=1e-15)
+        np.testing.assert_allclose(l1[:, t], (q1[t] * k1[t]).sum(-1) / 8.0, atol=1e-13)
+
+
+# ----------------------------------------------------------------- backward
+def pin_bwd_finite_differences(so=None, ncoord=240):
+    """Central differences of f = <dO, O(q, k, v)> (step 1e-6) at >= 200 random
+    coordinates of q, k and v, with rotation, on the tiny workload."""
+    wl, q, k, v, do = _tiny_inputs()
+    cu, pos = oracle.pack(wl.specs)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, cu, pos, so=so)
+    grads = {"q": dq, "k": dk, "v": dv}
+    base = {"q": q, "k": k, "v": v}
+
+    def f(xs):
+        o, _ = oracle.attn_fwd(xs["q"], xs["k"], xs["v"], cu, pos, so=so)
+        return float((o * do).sum())
+
+    r = _rng(6)
+    eps = 1e-6
+    worst = 0.0
+    for it in range(ncoord):
+        name = "qkv"[it % 3]
+        idx = tuple(int(r.integers(0, s)) for s in q.shape)
+        xs = {n: base[n] for n in base}
+        xp = base[name].copy(); xp[idx] += eps
+        xm = base[name].copy(); xm[idx] -= eps
+        xs[name] = xp; fp = f(xs)
+        xs[name] = xm; fm = f(xs)
+        fd = (fp - fm) / (2 * eps)
+        g = grads[name][idx]
+        err = abs(fd - g) / max(1.0, abs(g))
+        worst = max(worst, err)
+        assert err < 1e-6, (name, idx, fd, g)
+    return worst
+
+
+def pin_bwd_vs_library(so=None):
+    """No rotation: the oracle's gradients equal torch autograd through per-sample
+    SDPA in fp64."""
+    wl, q, k, v, do = _tiny_inputs()
+    cu, _ = oracle.pack(wl.specs)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, cu, None, so=so)
+    for i in range(len(cu) - 1):
+        s, e = int(cu[i]), int(cu[i + 1])
+        Q, K, V = (torch.from_numpy(x[s:e].copy()).permute(1, 0, 2).requires_grad_() for x in (q, k, v))
+        O = torch.nn.functional.scaled_dot_product_attention(Q, K, V)
+        O.backward(torch.from_numpy(do[s:e]).permute(1, 0, 2))
+        for g, t in ((dq, Q), (dk, K), (dv, V)):
+            np.testing.assert_allclose(g[s:e], t.grad.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def pin_bwd_invariants(so=None):
+    """Two consequences of the definition.  (1) Rows of P sum to one, so
+    sum_k dV_k = sum_j dO_j within each sample.  (2) Rows of dS sum to zero: in a
+    text-only sample (every token at (0,0), so no rotation), adding one vector c
+    to every key shifts each logit row by a constant; P, O, dV and dK are
+    unchanged and dQ moves by scale * c * sum_k dS_jk = 0."""
+    wl, q, k, v, do = _tiny_inputs()
+    cu, pos = oracle.pack(wl.specs)
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do, cu, pos, so=so)
+    for i in range(len(cu) - 1):
+        s, e = int(cu[i]), int(cu[i + 1])
+        np.testing.assert_allclose(dv[s:e].sum(0), do[s:e].sum(0), atol=1e-11)
+    r = _rng(7)
+    L, h, d = 40, 2, 64
+    cu1 = np.array([0, L]); pos1 = np.zeros((L, 2), dtype=np.int64)
+    q1, k1, v1, do1 = (r.standard_normal((L, h, d)) for _ in range(4))
+    g1 = oracle.attn_bwd(q1, k1, v1, do1, cu1, pos1, so=so)
+    g2 = oracle.attn_bwd(q1, k1 + r.standard_normal((1, h, d)), v1, do1, cu1, pos1, so=so)
+    for a, b in zip(g1, g2):
+        np.testing.assert_allclose(a, b, atol=1e-11)

@@ -1,0 +1,55 @@
+"""Plant plausible mistakes in copies of the oracle source (CPU only) and check
+that at least one pin fails for each: the pins would catch such a slip in the
+oracle itself."""
+import os
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "mf_oracle.c")
+
+# (name, exact source fragment, replacement)
+MUTANTS = [
+    ("rope_sign", "out[h * half + 2 * j] = x * cos(theta) - y * sin(theta);",
+     "out[h * half + 2 * j] = x * cos(theta) + y * sin(theta);"),
+    ("rope_freq_exponent", "pow(base, -2.0 * (double)j / (double)half)",
+     "pow(base, -1.0 * (double)j / (double)half)"),
+    ("rope_rows_cols_swapped", "double p = (h == 0) ? (double)r : (double)c;",
+     "double p = (h == 0) ? (double)c : (double)r;"),
+    ("pack_col_major_flatten", "pos[2 * (cu[i] + t + k) + 1] = k % W;",
+     "pos[2 * (cu[i] + t + k) + 1] = k / (H > 0 ? H : 1);"),
+    ("pack_one_based_rows", "pos[2 * (cu[i] + t + k)] = k / W;",
+     "pos[2 * (cu[i] + t + k)] = k / W + 1;"),
+    ("attn_no_scale", "srow[kk] = scale * acc;", "srow[kk] = acc;"),
+    ("attn_lse_without_max", "double lj = m + log(l);", "double lj = log(l);"),
+    ("attn_unnormalised", "double p = exp(srow[kk] - lj);", "double p = exp(srow[kk] - m);"),
+    ("bwd_missing_D", "double ds = prow[kk] * (dp - Dj);", "double ds = prow[kk] * dp;"),
+    ("bwd_dk_forward_rotation", "oracle_rope2d(dkr, pos, T, heads, d, base, -1, dk);",
+     "oracle_rope2d(dkr, pos, T, heads, d, base, +1, dk);"),
+    ("bwd_dq_forward_rotation", "oracle_rope2d(dqr, pos, T, heads, d, base, -1, dq);",
+     "oracle_rope2d(dqr, pos, T, heads, d, base, +1, dq);"),
+    ("bwd_dv_transposed", "dv[rk + e] += prow[kk] * d_o[rj + e];",
+     "dv[rj + e] += prow[kk] * d_o[rk + e];"),
+    ("bwd_dk_missing_scale", "dkr[rk + e] += scale * ds * qr[rj + e];",
+     "dkr[rk + e] += ds * qr[rj + e];"),
+    ("bwd_dq_unrotated_keys", "dqr[rj + e] += scale * ds * kr[rk + e];",
+     "dqr[rj + e] += scale * ds * k[rk + e];"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, tmp_path):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"fragment for {name} not found exactly once"
+    path = tmp_path / f"oracle_{name}.c"
+    path.write_text(src.replace(old, new))
+    so = oracle.compile_source(str(path), str(tmp_path / f"lib_{name}.so"))
+    failed = []
+    for pin in [n for n in dir(pins) if n.startswith("pin_")]:
+        try:
+            getattr(pins, pin)(so=so)
+        except (AssertionError, ValueError, IndexError):
+            failed.append(pin)
+    assert failed, f"planted mistake {name} passed every pin"
