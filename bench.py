@@ -1,0 +1,396 @@
+#!/usr/bin/env python
+"""Benchmark of the packed native-resolution 2D-RoPE varlen attention path.
+
+One step = the whole hot path over one pack: mf_pack (cu_seqlens + (r, c)
+tables), the forward (2D RoPE of Q/K + block-diagonal attention, O and LSE) and
+the backward (dQ, dK, dV with the RoPE transpose folded in), all through the C
+ABI.  The workload is the mixed-resolution training pack to a 50,000-token
+budget (latent grids {32x32, 48x64, 64x48, 64x64, 40x96, 96x40}, text U[32, 512],
+24 heads x 128, bf16 N(0,1), seeded).  Metric: attention TFLOP/s of the step,
+counting 4 * sum(L_i^2) * d * heads forward and 2.5x that backward.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Under torchrun each rank runs its own pack (seed = rank): replicas, no data-path
+collective (weak scaling); the timing is max over ranks.  Prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "packed 2D-RoPE varlen attention TFLOP/s fwd/bwd at 50k tokens; % BF16 peak"
+UNIT = "TFLOP/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixed_50k")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--budget", type=int, default=None,
+                    help="token budget of the packed workload (default 50,000)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def workload_desc(wl) -> str:
+    return (f"{wl.name}: seed-{wl.seed} pack of {len(wl.specs)} samples, T={wl.total}, "
+            f"max L={wl.max_len}, {wl.heads} heads x {wl.head_dim}, bf16 N(0,1)")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_burst": float(p["bf16_tflops"]), "bf16_sustained": float(p["bf16_tflops_sustained"]),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_burst": 1800.0, "bf16_sustained": 1400.0, "hbm_gbs": 6400.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------ CPU oracle leg
+def oracle_sample(wl, q, k, v, do, max_pairs):
+    """The first `max_pairs` (sample, head) pairs, smallest samples first, as a
+    sub-pack of one-head samples (exact: samples and heads are independent)."""
+    import oracle
+    cu, pos = oracle.pack(wl.specs)
+    L = np.diff(cu)
+    pairs = [(int(i), a) for i in np.argsort(L, kind="stable") for a in range(wl.heads)][:max_pairs]
+    f = synth.bf16_bits_to_f64
+    sl = lambda x, i, a: x[cu[i]:cu[i + 1], a:a + 1, :]  # noqa: E731
+    sub = [np.concatenate([f(sl(x, i, a)) for (i, a) in pairs], 0) for x in (q, k, v, do)]
+    lens = [int(L[i]) for (i, _) in pairs]
+    cu_s = np.concatenate([[0], np.cumsum(lens)])
+    pos_s = np.concatenate([pos[cu[i]:cu[i + 1]] for (i, _) in pairs], 0)
+    flops = 3.5 * 4.0 * sum(x * x for x in lens) * wl.head_dim
+    return sub, cu_s, pos_s, flops, pairs
+
+
+def run_oracle_step(sub, cu_s, pos_s):
+    import oracle
+    q, k, v, do = sub
+    oracle.attn_fwd(q, k, v, cu_s, pos_s)
+    oracle.attn_bwd(q, k, v, do, cu_s, pos_s)
+
+
+def cpu_baseline(wl, q, k, v, do, budget_s):
+    """The oracle as it stands on this host's cores: forward + backward of
+    (sample, head) pairs, smallest samples first, in batches of one pair per core,
+    until `budget_s` seconds have passed."""
+    cores = len(os.sched_getaffinity(0))
+    total_pairs = len(wl.specs) * wl.heads
+    done_flops, n_pairs, t0 = 0.0, 0, time.perf_counter()
+    while n_pairs < total_pairs and time.perf_counter() - t0 < budget_s:
+        take = min(total_pairs, n_pairs + cores)
+        sub, cu_s, pos_s, _, pairs = oracle_sample(wl, q, k, v, do, take)
+        # only the new pairs of this batch
+        sub_new, cu_new, pos_new, fl, _ = _slice_pairs(sub, cu_s, pos_s, n_pairs, take, wl.head_dim)
+        run_oracle_step(sub_new, cu_new, pos_new)
+        done_flops += fl
+        n_pairs = take
+    el = time.perf_counter() - t0
+    return {"value": done_flops / el / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"FP64 C oracle, forward + backward of {n_pairs} of {total_pairs} (sample, head) "
+                      f"pairs of the same pack, smallest samples first, {el:.1f} s wall, "
+                      f"OpenMP over pairs"}
+
+
+def _slice_pairs(sub, cu_s, pos_s, a, b, d):
+    s, e = int(cu_s[a]), int(cu_s[b])
+    lens = np.diff(cu_s[a:b + 1])
+    cu_new = np.concatenate([[0], np.cumsum(lens)])
+    return [x[s:e] for x in sub], cu_new, pos_s[s:e], 3.5 * 4.0 * float((lens ** 2).sum()) * d, None
+
+
+def reference_arm(args):
+    """The FP64 oracle timed as the reference arm, on this host's cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    wl = synth.workload(args.workload, args.seed, args.budget)
+    q, k, v, do = synth.make_inputs(wl, with_do=True)
+    cores = len(os.sched_getaffinity(0))
+    sub, cu_s, pos_s, flops, pairs = oracle_sample(wl, q, k, v, do, cores)
+    for _ in range(args.warmup):
+        run_oracle_step(sub, cu_s, pos_s)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run_oracle_step(sub, cu_s, pos_s)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    val = flops / (ms / 1e3) / 1e12
+    sample = (f"FP64 C oracle, forward + backward of {len(pairs)} (sample, head) pairs "
+              f"(smallest samples first) of the pack per step")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(wl), "sample": sample},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- GPU arm
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id):
+        self.bus_id = bus_id
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.bus_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        time.sleep(0.15)
+
+    def result(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+
+    import packed_resolution_diffusion_pack_b300 as mf
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    mf.load()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    wl = synth.workload(args.workload, args.seed + rank, args.budget)
+    q, k, v, do = synth.make_inputs(wl, with_do=True)
+    T, max_len = mf.pack_size(wl.specs)
+    n, h, d = len(wl.specs), wl.heads, wl.head_dim
+    pin = lambda b: synth.bits_to_torch(b).pin_memory()  # noqa: E731
+    hq, hk, hv, hdo = pin(q), pin(k), pin(v), pin(do)
+    qd, kd, vd, dod = (x.cuda() for x in (hq, hk, hv, hdo))
+    o = torch.empty_like(qd)
+    lse = torch.empty((h, T), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws_f = mf.workspace(T, n, h, d, False)
+    ws_b = mf.workspace(T, n, h, d, True)
+    cu = torch.empty(n + 1, dtype=torch.int32, device="cuda")
+    pos = torch.empty((T, 2), dtype=torch.int32, device="cuda")
+
+    def step(qd=qd, kd=kd, vd=vd, dod=dod):
+        mf.pack(wl.specs, cu=cu, pos=pos)
+        mf.varlen_attn_fwd(qd, kd, vd, cu, pos, max_len, o=o, lse=lse, ws=ws_f)
+        mf.varlen_attn_bwd(qd, kd, vd, o, lse, dod, cu, pos, max_len, dq=dq, dk=dk, dv=dv, ws=ws_b)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    mf.get_status(ws_f)
+    mf.get_status(ws_b)
+    barrier()
+
+    props = torch.cuda.get_device_properties(local)
+    bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    mf.timing_enable(True)
+    mf.timing_reset()
+    with ClockSampler(bus) as clk:
+        barrier()
+        ev0.record()
+        for _ in range(args.steps):
+            step()
+        ev1.record()
+        barrier()
+    clocks = clk.result()
+    kern = mf.timing_read()
+    mf.timing_enable(False)
+    mf.get_status(ws_f)
+    mf.get_status(ws_b)
+    ms = ev0.elapsed_time(ev1) / args.steps
+
+    flops_fwd, flops_bwd = wl.flops_fwd(), wl.flops_bwd()
+    t = torch.tensor([ms, flops_fwd + flops_bwd], dtype=torch.float64)
+    if world > 1:
+        tmax = t.clone()
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        tsum = t.clone()
+        dist.all_reduce(tsum, op=dist.ReduceOp.SUM)
+        ms_max, flops_all = float(tmax[0]), float(tsum[1])
+    else:
+        ms_max, flops_all = ms, float(t[1])
+    value = flops_all / (ms_max / 1e3) / 1e12
+
+    # ---- end to end through the public API with pinned host buffers
+    h_o = torch.empty_like(hq)
+    h_lse = torch.empty((h, T), dtype=torch.float32).pin_memory()
+    h_dq, h_dk, h_dv = (torch.empty_like(hq) for _ in range(3))
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        qq, kk, vv, dd = (x.to("cuda", non_blocking=True) for x in (hq, hk, hv, hdo))
+        step(qq, kk, vv, dd)
+        h_o.copy_(o, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        h_dq.copy_(dq, non_blocking=True)
+        h_dk.copy_(dk, non_blocking=True)
+        h_dv.copy_(dv, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    ev0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    ev1.record()
+    barrier()
+    ms_e2e = ev0.elapsed_time(ev1) / e2e_steps
+    if world > 1:
+        te = torch.tensor([ms_e2e], dtype=torch.float64)
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        ms_e2e = float(te[0])
+    elem = T * h * d
+    h2d = 4 * elem * 2
+    d2h = 4 * elem * 2 + h * T * 4
+
+    pk = peaks()
+    per_launch = {}
+    for name, (tot, cnt) in kern.items():
+        if cnt:
+            per_launch[name] = {"ms_per_launch": tot / cnt, "launches": cnt,
+                                "share": tot / max(1e-9, sum(x[0] for x in kern.values()))}
+    algo = {"attn_fwd": ("tensor", flops_fwd), "attn_bwd": ("tensor", flops_bwd),
+            "rope": ("hbm", 8.0 * T * h * d + 8.0 * T)}
+    for name, (bound, amount) in algo.items():
+        if name in per_launch:
+            pl = per_launch[name]
+            if bound == "tensor":
+                ach = amount / (pl["ms_per_launch"] / 1e3) / 1e12
+                pl.update(achieved_tflops=ach, frac_of_sustained=ach / pk["bf16_sustained"],
+                          frac_of_burst=ach / pk["bf16_burst"])
+            else:
+                ach = amount / (pl["ms_per_launch"] / 1e3) / 1e9
+                pl.update(achieved_gbs=ach, frac_of_hbm=ach / pk["hbm_gbs"])
+    dom = max(("attn_fwd", "attn_bwd"), key=lambda nm: kern[nm][0])
+    traffic = _recorded_traffic(dom)
+    ach = per_launch[dom]["achieved_tflops"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": pk["bf16_sustained"],
+                "unit": "TFLOP/s", "frac": ach / pk["bf16_sustained"], "traffic": traffic,
+                "peak_kind": f"{pk['source']} bf16 sustained (cuBLAS, seconds-long loop); "
+                             f"burst {pk['bf16_burst']} gives frac {ach / pk['bf16_burst']:.3f}"}
+    fwd_ms = per_launch["attn_fwd"]["ms_per_launch"]
+    bwd_ms = per_launch["attn_bwd"]["ms_per_launch"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(wl), "global_tokens": T * world,
+                   "step": "mf_pack + mf_varlen_attn_fwd (RoPE + attention) + mf_varlen_attn_bwd",
+                   "l2": "no flush: Q, K, V, dO alone are %.2f GB, far above the 126 MB L2" % (
+                       4 * elem * 2 / 1e9),
+                   "parallelism": "replicas: one pack per GPU, no data-path collective"},
+        "fwd_tflops": flops_fwd / (fwd_ms / 1e3) / 1e12,
+        "bwd_tflops": flops_bwd / (bwd_ms / 1e3) / 1e12,
+        "fwd_frac_of_peak": flops_fwd / (fwd_ms / 1e3) / 1e12 / pk["bf16_sustained"],
+        "bwd_frac_of_peak": flops_bwd / (bwd_ms / 1e3) / 1e12 / pk["bf16_sustained"],
+        "roofline": roofline,
+        "kernels": per_launch,
+        "gpu_launches": int(sum(x[1] for x in kern.values())),
+        "e2e": {"value": flops_all / (ms_e2e / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, q, k, v, do, args.cpu_budget_s)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def _recorded_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
+    summary was taken on the current kernel source (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "packed_resolution_diffusion_pack_b300", "csrc", rec["source"])
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return rec["bytes_per_launch"] if sha == rec.get("source_sha") else None
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

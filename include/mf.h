@@ -1,0 +1,199 @@
+/*
+ * mf.h -- C ABI of the packed native-resolution 2D-RoPE varlen attention library
+ * (libmf.so, sm_103a / B300).
+ *
+ * The operation is the joint self-attention of Mage-Flow's native-resolution
+ * MMDiT ("Mage-Flow: An Efficient Native-Resolution Foundation Model for Image
+ * Generation and Editing", arXiv 2607.19064):
+ *   - many samples, each a variable-length text sequence followed by a flattened
+ *     image-latent grid of any H x W, are packed into one token stream without
+ *     padding or resolution buckets (rcap.io post, training-step listing
+ *     "native-resolution packed step": pack(text_tokens + tokens, budget=50_000);
+ *     paperlayer.ai summary section 3.2.1 "Model Architecture and Native Packing");
+ *   - per-sample 2D rotary embeddings are applied to Q and K from each image
+ *     token's native (row, col) latent position (rcap.io post, same listing:
+ *     per_sample_2d_rope; ai.thesatyajit.com explainer, "A backbone that doesn't
+ *     crop");
+ *   - non-causal multi-head attention runs within each sample only, realised with
+ *     variable-length attention kernels (rcap.io post; paperlayer.ai section 3.2.1:
+ *     joint self-attention over the concatenated text and image tokens);
+ *   - packed classifier-free guidance is the same call with the conditional and
+ *     unconditional branches as two samples (paperlayer.ai section 3.2.1).
+ * The pages print no formula for the rotation; this library fixes it (and the
+ * oracle used to test it follows the same reading):
+ *   image token k of an H x W grid is at (r, c) = (k div W, k mod W), text tokens at
+ *   (0, 0); dims [0, d/2) rotate by r and [d/2, d) by c; within a half, the pair
+ *   (2j, 2j+1), j < d/4, rotates by theta = p * 10000^(-2j/(d/2)):
+ *   (x, y) -> (x cos theta - y sin theta, x sin theta + y cos theta).
+ *   Softmax scale defaults to 1/sqrt(d).  LSE is the natural-log logsumexp of the
+ *   scaled logits.
+ *
+ * Conventions for every call:
+ *   - Layout "THD": packed tensors are [T][heads][head_dim] bf16, row-major,
+ *     contiguous; LSE and the like are [heads][T] fp32.  cu_seqlens is int32[n+1]
+ *     with cu_seqlens[0] = 0, non-decreasing, cu_seqlens[n] = T.  pos is int32[T][2]
+ *     = (r, c).
+ *   - Pointers prefixed d_ and all tensor pointers are DEVICE pointers on the
+ *     current CUDA device; `specs` is a HOST pointer.  The caller owns every buffer;
+ *     the library allocates no device memory (workspaces are sized by
+ *     mf_attn_workspace_bytes and passed in).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Argument errors are detected on the host before any launch and
+ *     returned synchronously; launch failures return MF_ERR_CUDA.  Errors found on
+ *     the device (malformed cu_seqlens, a wait that ran out) are recorded in the
+ *     workspace and reported by mf_get_status.
+ *   - Tensor pointers must be 16-byte aligned; head_dim must be 64 or 128; T and
+ *     every index fit in int32 (T * heads * head_dim < 2^31 is not required, but
+ *     T < 2^31 is).  Anything else: MF_ERR_UNSUPPORTED / MF_ERR_OVERFLOW.
+ */
+#ifndef MF_H_
+#define MF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MF_OK = 0,
+  MF_ERR_INVALID_ARG = 1,  /* bad argument (negative size, NULL pointer, ...) */
+  MF_ERR_UNSUPPORTED = 2,  /* valid but not supported (head_dim, alignment, ...) */
+  MF_ERR_OVERFLOW = 3,     /* a size does not fit in int32 */
+  MF_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  MF_ERR_TIMEOUT = 5,      /* a device-side wait ran out (kernel gave up cleanly) */
+  MF_ERR_BAD_SEQLENS = 6   /* device-side check: cu_seqlens malformed or a sample > max_len */
+} mf_status;
+
+typedef uint16_t mf_bf16; /* bfloat16 storage */
+typedef void* mf_stream;  /* cudaStream_t */
+
+/* Human-readable name of a status code (static string). */
+const char* mf_status_string(mf_status s);
+
+/* Library version, e.g. 10000 for 1.0.0. */
+int32_t mf_version(void);
+
+/*
+ * Packing sizes (host only, no device work).
+ * specs: HOST int32[n][3] = {text_len, H_lat, W_lat} per sample, in pack order.
+ * Outputs: *total = T = sum_i (text_len_i + H_i * W_i); *max_len = max_i L_i
+ * (0 when n = 0).  Either output pointer may be NULL.
+ * Errors: MF_ERR_INVALID_ARG for n < 0, a NULL specs with n > 0, or a negative
+ * entry; MF_ERR_OVERFLOW when T or an H*W product exceeds INT32_MAX.
+ * Defined by: rcap.io post, training-step listing (pack(...)); paperlayer.ai 3.2.1.
+ */
+mf_status mf_pack_size(const int32_t* specs, int32_t n, int32_t* total, int32_t* max_len);
+
+/*
+ * Build the packed-stream tables on the device.
+ * specs: HOST int32[n][3] as above (read before the call returns).
+ * d_cu_seqlens: DEVICE int32[n+1] out: cu[0] = 0, cu[i+1] = cu[i] + L_i.
+ * d_pos: DEVICE int32[T][2] out: token cu[i] + k is text at (0,0) for k < text_len_i,
+ *   else image token m = k - text_len_i at (m div W_i, m mod W_i).  May be NULL.
+ * Zero-length samples are allowed.  Same errors as mf_pack_size, plus
+ * MF_ERR_INVALID_ARG for a NULL d_cu_seqlens and MF_ERR_UNSUPPORTED for a
+ * misaligned d_pos (needs 8-byte alignment).
+ * Defined by: rcap.io post, training-step listing; paperlayer.ai 3.2.1 (packing
+ * under a token budget, native latent grid kept, no padding).
+ */
+mf_status mf_pack(const int32_t* specs, int32_t n, int32_t* d_cu_seqlens, int32_t* d_pos,
+                  mf_stream stream);
+
+/*
+ * Standalone per-sample 2D RoPE on Q and K.
+ * q, k: DEVICE bf16 [T][heads][head_dim] in; q_out, k_out: DEVICE bf16 out, same
+ * layout (q_out == q and/or k_out == k is allowed: in place).  d_pos: DEVICE
+ * int32[T][2].  Computes q_out = R(theta(pos)) q, k_out = R(theta(pos)) k with the
+ * rotation defined at the top of this file, in fp32 with a correctly rounded
+ * (nearest-even) bf16 result.  q (with q_out) or k (with k_out) may be NULL to
+ * rotate only the other one.
+ * Errors: MF_ERR_INVALID_ARG (T < 0, heads < 1, NULL d_pos with T > 0);
+ * MF_ERR_UNSUPPORTED (head_dim not 64/128, misaligned pointer).
+ * Defined by: rcap.io post (per_sample_2d_rope, native positions); explainer
+ * "A backbone that doesn't crop".
+ */
+mf_status mf_rope2d_qk(const mf_bf16* q, const mf_bf16* k, mf_bf16* q_out, mf_bf16* k_out,
+                       const int32_t* d_pos, int32_t T, int32_t heads, int32_t head_dim,
+                       mf_stream stream);
+
+/*
+ * Workspace bytes needed by mf_varlen_attn_fwd (bwd = 0) or mf_varlen_attn_bwd
+ * (bwd = 1) for these sizes.  The workspace is a DEVICE buffer of at least that
+ * many bytes, 256-byte aligned, owned by the caller, not shared by concurrent
+ * calls; its contents need no initialisation.  Returns 0 on invalid sizes.
+ */
+size_t mf_attn_workspace_bytes(int32_t T, int32_t n, int32_t heads, int32_t head_dim, int32_t bwd);
+
+/*
+ * Varlen attention forward with per-sample 2D RoPE.
+ * q, k, v: DEVICE bf16 [T][heads][head_dim], un-rotated.
+ * d_cu_seqlens: DEVICE int32[n+1]; d_pos: DEVICE int32[T][2], or NULL for no
+ * rotation.  max_len: an upper bound on every L_i (checked on the device).
+ * softmax_scale <= 0 selects 1/sqrt(head_dim).
+ * o: DEVICE bf16 [T][heads][head_dim] out.  lse: DEVICE fp32 [heads][T] out
+ * (natural-log logsumexp of the scaled logits of each query row).
+ * ws / ws_bytes: workspace from mf_attn_workspace_bytes(T, n, heads, head_dim, 0).
+ * For each sample i and head a, and each query row j of sample i:
+ *   O_j = sum_k softmax_k(scale * <q'_j, k'_k>) v_k over the keys of sample i only,
+ * q' = R(theta) q, k' = R(theta) k.  Rows of zero-length samples do not exist; every
+ * output row belongs to exactly one sample and is written exactly once.
+ * Defined by: paperlayer.ai 3.2.1 (joint self-attention within the packed
+ * sequence), rcap.io post (varlen attention, per-sample 2D RoPE).
+ */
+mf_status mf_varlen_attn_fwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                             const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t n,
+                             int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
+                             float softmax_scale, mf_bf16* o, float* lse, void* ws,
+                             size_t ws_bytes, mf_stream stream);
+
+/*
+ * Varlen attention backward (gradients with respect to the UN-rotated q and k,
+ * i.e. the rotation's transpose R(-theta) is folded in).
+ * q, k, v, o, d_o: DEVICE bf16 [T][heads][head_dim]; lse: DEVICE fp32 [heads][T]
+ * from the forward.  Other arguments as in the forward.
+ * dq, dk, dv: DEVICE bf16 [T][heads][head_dim] out.
+ * ws / ws_bytes: workspace from mf_attn_workspace_bytes(T, n, heads, head_dim, 1)
+ * (holds the rotated Q/K, D = rowsum(dO * O) and the fp32 dQ accumulator).
+ * Per sample and head: P = exp(S - LSE), dV = P^T dO, dP = dO V^T,
+ * dS = P * (dP - D), dQ = R(-theta) scale dS K', dK = R(-theta) scale dS^T Q'.
+ * Defined by: the training step of the rcap.io listing (loss.backward through the
+ * attention); gradients are those of the forward above.
+ */
+mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                             const mf_bf16* o, const float* lse, const mf_bf16* d_o,
+                             const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t n,
+                             int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
+                             float softmax_scale, mf_bf16* dq, mf_bf16* dk, mf_bf16* dv,
+                             void* ws, size_t ws_bytes, mf_stream stream);
+
+/*
+ * Synchronise `stream` and report device-side errors recorded in `ws` by the last
+ * mf_varlen_attn_* call that used it: MF_ERR_BAD_SEQLENS, MF_ERR_TIMEOUT, or
+ * MF_ERR_CUDA if the stream itself failed; MF_OK otherwise.
+ */
+mf_status mf_get_status(void* ws, mf_stream stream);
+
+/*
+ * Optional per-kernel timing (instrumentation; no counterpart on the pages).
+ * When enabled, every kernel launch made by the calls above is bracketed by two
+ * CUDA events recorded on the call's stream (a few microseconds of host work per
+ * launch; nothing changes on the device path).  mf_timing_read synchronises on
+ * the recorded events and returns, for kernel `id`, the summed device time in
+ * milliseconds and the number of launches since the last reset.  Ids:
+ *   MF_K_PACK 0, MF_K_ROPE 1, MF_K_SCHEDULE 2, MF_K_ATTN_FWD 3, MF_K_BWD_PRE 4,
+ *   MF_K_ATTN_BWD 5, MF_K_DQ_POST 6.
+ * Process-wide state guarded by a mutex; not for use under stream capture.
+ */
+enum { MF_K_PACK = 0, MF_K_ROPE, MF_K_SCHEDULE, MF_K_ATTN_FWD, MF_K_BWD_PRE, MF_K_ATTN_BWD,
+       MF_K_DQ_POST, MF_K_COUNT };
+mf_status mf_timing_enable(int32_t on);
+mf_status mf_timing_reset(void);
+mf_status mf_timing_read(int32_t id, double* total_ms, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MF_H_ */

@@ -60,7 +60,9 @@ def lib(so: str | None = None):
         L.oracle_rope2d.argtypes = [p, p, i64, i64, i64, f64, i32, p]
         L.oracle_attn_fwd.argtypes = [p, p, p, p, i64, p, i64, i64, i64, f64, f64, p, p]
         L.oracle_attn_bwd.argtypes = [p, p, p, p, p, i64, p, i64, i64, i64, f64, f64, p, p, p]
-        for f in (L.oracle_pack, L.oracle_rope2d, L.oracle_attn_fwd, L.oracle_attn_bwd):
+        L.oracle_attn_fwd_rows.argtypes = [p, p, p, p, i64, p, i64, i64, i64, f64, f64, p, i64, p, p]
+        for f in (L.oracle_pack, L.oracle_rope2d, L.oracle_attn_fwd, L.oracle_attn_bwd,
+                  L.oracle_attn_fwd_rows):
             f.restype = ctypes.c_int
         _libs[key] = L
     return _libs[key]
@@ -111,6 +113,26 @@ def attn_fwd(q, k, v, cu, pos, scale=None, base: float = ROPE_BASE, so: str | No
     lib(so).oracle_attn_fwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, cu.ctypes.data,
                                  len(cu) - 1, _ptr(p), T, h, d, scale, base, o.ctypes.data,
                                  lse.ctypes.data)
+    return o, lse
+
+
+def attn_fwd_rows(q, k, v, cu, pos, rows, scale=None, base: float = ROPE_BASE,
+                  so: str | None = None):
+    """O and LSE of selected query rows only; rows = [(token, head), ...].
+    Returns (o_rows [m, d], lse_rows [m])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, h, d = q.shape
+    cu = np.ascontiguousarray(cu, dtype=np.int64)
+    p = None if pos is None else np.ascontiguousarray(pos, dtype=np.int64)
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 2))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = np.zeros((len(r), d))
+    lse = np.zeros(len(r))
+    rc = lib(so).oracle_attn_fwd_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, cu.ctypes.data,
+                                      len(cu) - 1, _ptr(p), T, h, d, scale, base, r.ctypes.data,
+                                      len(r), o.ctypes.data, lse.ctypes.data)
+    if rc != 0:
+        raise ValueError("row outside the pack")
     return o, lse
 
 

@@ -101,27 +101,61 @@ int oracle_rope2d(const double* x, const int64_t* pos, int64_t T, int64_t heads,
 
 /* ------------------------------------------------------ attention forward */
 /*
+ * One query row (token tj, head a) of sample [s0, s0+L), rotated inputs qr, kr:
+ *   S_k = scale * <q'_j, k'_k> over the keys k of the sample only,
+ *   m = max_k S_k, LSE = m + ln sum_k exp(S_k - m),  O_j = sum_k exp(S_k - LSE) v_k.
+ * srow is scratch of length L.
+ */
+static void attn_row(const double* qr, const double* kr, const double* v, int64_t s0, int64_t L,
+                     int64_t tj, int64_t a, int64_t heads, int64_t d, double scale, double* srow,
+                     double* oj, double* lse_j) {
+  const double* qj = qr + (tj * heads + a) * d;
+  double m = -INFINITY;
+  for (int64_t kk = 0; kk < L; ++kk) {
+    const double* kv = kr + ((s0 + kk) * heads + a) * d;
+    double acc = 0.0;
+    for (int64_t e = 0; e < d; ++e) acc += qj[e] * kv[e];
+    srow[kk] = scale * acc;
+    if (srow[kk] > m) m = srow[kk];
+  }
+  double l = 0.0;
+  for (int64_t kk = 0; kk < L; ++kk) l += exp(srow[kk] - m);
+  double lj = m + log(l);
+  *lse_j = lj;
+  for (int64_t e = 0; e < d; ++e) oj[e] = 0.0;
+  for (int64_t kk = 0; kk < L; ++kk) {
+    double p = exp(srow[kk] - lj);
+    const double* vk = v + ((s0 + kk) * heads + a) * d;
+    for (int64_t e = 0; e < d; ++e) oj[e] += p * vk[e];
+  }
+}
+
+static int rotate_qk(const double* q, const double* k, const int64_t* pos, int64_t T,
+                     int64_t heads, int64_t d, double base, double** qr, double** kr) {
+  *qr = (double*)malloc(sizeof(double) * (size_t)(T * heads * d + 1));
+  *kr = (double*)malloc(sizeof(double) * (size_t)(T * heads * d + 1));
+  if (!*qr || !*kr) { free(*qr); free(*kr); return ORACLE_ERR; }
+  if (pos) {
+    oracle_rope2d(q, pos, T, heads, d, base, +1, *qr);
+    oracle_rope2d(k, pos, T, heads, d, base, +1, *kr);
+  } else {
+    memcpy(*qr, q, sizeof(double) * (size_t)(T * heads * d));
+    memcpy(*kr, k, sizeof(double) * (size_t)(T * heads * d));
+  }
+  return ORACLE_OK;
+}
+
+/*
  * Inputs un-rotated q, k, v [T][heads][d]; cu [n+1]; pos [T][2] or NULL (no
- * rotation).  Outputs o [T][heads][d], lse [heads][T].
- * For each sample i and head a, for each query row j of sample i:
- *   S_jk = scale * <q'_j, k'_k> over the keys k of sample i only,
- *   m_j = max_k S_jk, LSE_j = m_j + ln sum_k exp(S_jk - m_j),
- *   O_j = sum_k exp(S_jk - LSE_j) v_k.
- * q' = R(theta) q and k' = R(theta) k are formed first, exactly as defined above.
+ * rotation).  Outputs o [T][heads][d], lse [heads][T]: every row of every sample
+ * and head, each by attn_row.  q' = R(theta) q and k' = R(theta) k are formed
+ * first, exactly as defined above.
  */
 int oracle_attn_fwd(const double* q, const double* k, const double* v, const int64_t* cu,
                     int64_t n, const int64_t* pos, int64_t T, int64_t heads, int64_t d,
                     double scale, double base, double* o, double* lse) {
-  double* qr = (double*)malloc(sizeof(double) * (size_t)(T * heads * d + 1));
-  double* kr = (double*)malloc(sizeof(double) * (size_t)(T * heads * d + 1));
-  if (!qr || !kr) { free(qr); free(kr); return ORACLE_ERR; }
-  if (pos) {
-    oracle_rope2d(q, pos, T, heads, d, base, +1, qr);
-    oracle_rope2d(k, pos, T, heads, d, base, +1, kr);
-  } else {
-    memcpy(qr, q, sizeof(double) * (size_t)(T * heads * d));
-    memcpy(kr, k, sizeof(double) * (size_t)(T * heads * d));
-  }
+  double *qr, *kr;
+  if (rotate_qk(q, k, pos, T, heads, d, base, &qr, &kr) != ORACLE_OK) return ORACLE_ERR;
   int64_t npairs = n * heads;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t pr = 0; pr < npairs; ++pr) {
@@ -129,33 +163,42 @@ int oracle_attn_fwd(const double* q, const double* k, const double* v, const int
     int64_t s0 = cu[i], L = cu[i + 1] - cu[i];
     if (L <= 0) continue;
     double* srow = (double*)malloc(sizeof(double) * (size_t)L);
-    for (int64_t j = 0; j < L; ++j) {
-      const double* qj = qr + ((s0 + j) * heads + a) * d;
-      double m = -INFINITY;
-      for (int64_t kk = 0; kk < L; ++kk) {
-        const double* kv = kr + ((s0 + kk) * heads + a) * d;
-        double acc = 0.0;
-        for (int64_t e = 0; e < d; ++e) acc += qj[e] * kv[e];
-        srow[kk] = scale * acc;
-        if (srow[kk] > m) m = srow[kk];
-      }
-      double l = 0.0;
-      for (int64_t kk = 0; kk < L; ++kk) l += exp(srow[kk] - m);
-      double lj = m + log(l);
-      lse[a * T + s0 + j] = lj;
-      double* oj = o + ((s0 + j) * heads + a) * d;
-      for (int64_t e = 0; e < d; ++e) oj[e] = 0.0;
-      for (int64_t kk = 0; kk < L; ++kk) {
-        double p = exp(srow[kk] - lj);
-        const double* vk = v + ((s0 + kk) * heads + a) * d;
-        for (int64_t e = 0; e < d; ++e) oj[e] += p * vk[e];
-      }
-    }
+    for (int64_t j = 0; j < L; ++j)
+      attn_row(qr, kr, v, s0, L, s0 + j, a, heads, d, scale, srow, o + ((s0 + j) * heads + a) * d,
+               lse + a * T + s0 + j);
     free(srow);
   }
   free(qr);
   free(kr);
   return ORACLE_OK;
+}
+
+/*
+ * The same definition restricted to m requested rows: rows[r] = (token, head).
+ * Writes o_rows [m][d] and lse_rows [m].  Rotation of q and k is applied to the
+ * whole input (as above) before the rows are evaluated.
+ */
+int oracle_attn_fwd_rows(const double* q, const double* k, const double* v, const int64_t* cu,
+                         int64_t n, const int64_t* pos, int64_t T, int64_t heads, int64_t d,
+                         double scale, double base, const int64_t* rows, int64_t m,
+                         double* o_rows, double* lse_rows) {
+  double *qr, *kr;
+  if (rotate_qk(q, k, pos, T, heads, d, base, &qr, &kr) != ORACLE_OK) return ORACLE_ERR;
+  int err = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < m; ++r) {
+    int64_t tj = rows[2 * r], a = rows[2 * r + 1];
+    int64_t i = 0;
+    while (i < n && cu[i + 1] <= tj) ++i; /* the sample holding token tj */
+    if (i >= n || tj < 0 || a < 0 || a >= heads) { err = ORACLE_ERR; continue; }
+    int64_t s0 = cu[i], L = cu[i + 1] - cu[i];
+    double* srow = (double*)malloc(sizeof(double) * (size_t)L);
+    attn_row(qr, kr, v, s0, L, tj, a, heads, d, scale, srow, o_rows + r * d, lse_rows + r);
+    free(srow);
+  }
+  free(qr);
+  free(kr);
+  return err;
 }
 
 /* ----------------------------------------------------- attention backward */
@@ -172,8 +215,8 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
                     const int64_t* cu, int64_t n, const int64_t* pos, int64_t T, int64_t heads,
                     int64_t d, double scale, double base, double* dq, double* dk, double* dv) {
   size_t N = (size_t)(T * heads * d);
-  double* qr = (double*)malloc(sizeof(double) * (N + 1));
-  double* kr = (double*)malloc(sizeof(double) * (N + 1));
+  double *qr = NULL, *kr = NULL;
+  if (rotate_qk(q, k, pos, T, heads, d, base, &qr, &kr) != ORACLE_OK) return ORACLE_ERR;
   double* o = (double*)malloc(sizeof(double) * (N + 1));
   double* lse = (double*)malloc(sizeof(double) * (size_t)(heads * T + 1));
   double* dqr = (double*)calloc(N + 1, sizeof(double));
@@ -183,13 +226,6 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
     return ORACLE_ERR;
   }
   oracle_attn_fwd(q, k, v, cu, n, pos, T, heads, d, scale, base, o, lse);
-  if (pos) {
-    oracle_rope2d(q, pos, T, heads, d, base, +1, qr);
-    oracle_rope2d(k, pos, T, heads, d, base, +1, kr);
-  } else {
-    memcpy(qr, q, sizeof(double) * N);
-    memcpy(kr, k, sizeof(double) * N);
-  }
   memset(dv, 0, sizeof(double) * N);
   int64_t npairs = n * heads;
 #pragma omp parallel for schedule(dynamic, 1)

@@ -1,0 +1,177 @@
+"""Packed native-resolution 2D-RoPE varlen attention on B300 (sm_103a).
+
+The hot path of Mage-Flow's native-resolution MMDiT joint attention: pack many
+[text; image-latent] samples into one token stream, rotate Q/K by each image
+token's native (row, col) latent position, and run block-diagonal (per-sample)
+attention forward and backward.  All compute runs in the hand-written CUDA
+kernels of ``libmf.so`` (C ABI: ``include/mf.h``); this module only marshals
+torch tensors (device memory, streams) into those calls.
+
+Tensors are "THD": ``[T, heads, head_dim]`` bf16, contiguous, on a CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._lib import MFError, STATUS_NAMES, check, library_path, load
+
+__all__ = [
+    "MFError", "STATUS_NAMES", "load", "library_path", "pack_size", "pack", "rope2d_qk",
+    "attn_workspace_bytes", "workspace", "varlen_attn_fwd", "varlen_attn_bwd", "get_status",
+]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _specs_array(specs):
+    flat = [int(x) for s in specs for x in s]
+    if len(flat) != 3 * len(specs):
+        raise ValueError("specs must be (text_len, H_lat, W_lat) triples")
+    return (ctypes.c_int32 * max(1, len(flat)))(*flat), len(specs)
+
+
+def _check_thd(name, t, T=None, heads=None, head_dim=None):
+    torch = _torch()
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+        raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor [T, heads, head_dim]")
+    if (T is not None and t.shape[0] != T) or (heads is not None and t.shape[1] != heads) or \
+            (head_dim is not None and t.shape[2] != head_dim):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected ({T}, {heads}, {head_dim})")
+
+
+def pack_size(specs):
+    """(T, max_len) of a pack of (text_len, H_lat, W_lat) samples (host only)."""
+    arr, n = _specs_array(specs)
+    T, mx = ctypes.c_int32(), ctypes.c_int32()
+    check(load().mf_pack_size(arr, n, ctypes.byref(T), ctypes.byref(mx)), "mf_pack_size")
+    return T.value, mx.value
+
+
+def pack(specs, device=None, stream=None, with_pos: bool = True, cu=None, pos=None):
+    """cu_seqlens int32 [n+1] and pos int32 [T, 2] built on the device by mf_pack
+    (into `cu` / `pos` when given)."""
+    torch = _torch()
+    arr, n = _specs_array(specs)
+    T, _ = pack_size(specs)
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if cu is None:
+        cu = torch.empty(n + 1, dtype=torch.int32, device=dev)
+    if pos is None and with_pos:
+        pos = torch.empty((T, 2), dtype=torch.int32, device=dev)
+    if cu.numel() != n + 1 or cu.dtype != torch.int32 or (pos is not None and pos.shape != (T, 2)):
+        raise ValueError("cu/pos buffers do not match the specs")
+    check(load().mf_pack(arr, n, _ptr(cu), _ptr(pos) if pos is not None and T > 0 else None,
+                         _stream_ptr(stream)), "mf_pack")
+    return cu, pos
+
+
+def rope2d_qk(q, k, pos, q_out=None, k_out=None, stream=None):
+    """Per-sample 2D RoPE of q and k (either may be None); returns (q_out, k_out)."""
+    torch = _torch()
+    ref = q if q is not None else k
+    _check_thd("q/k", ref)
+    T, h, d = ref.shape
+    if q is not None:
+        _check_thd("q", q, T, h, d)
+        q_out = torch.empty_like(q) if q_out is None else q_out
+        _check_thd("q_out", q_out, T, h, d)
+    if k is not None:
+        _check_thd("k", k, T, h, d)
+        k_out = torch.empty_like(k) if k_out is None else k_out
+        _check_thd("k_out", k_out, T, h, d)
+    check(load().mf_rope2d_qk(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _ptr(pos), T, h, d,
+                              _stream_ptr(stream)), "mf_rope2d_qk")
+    return q_out, k_out
+
+
+def attn_workspace_bytes(T, n, heads, head_dim, bwd: bool) -> int:
+    return int(load().mf_attn_workspace_bytes(T, n, heads, head_dim, 1 if bwd else 0))
+
+
+def workspace(T, n, heads, head_dim, bwd: bool, device=None):
+    """A device workspace of the size the library asks for (uint8 tensor)."""
+    torch = _torch()
+    nbytes = attn_workspace_bytes(T, n, heads, head_dim, bwd)
+    if nbytes == 0:
+        raise ValueError("invalid attention sizes")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def varlen_attn_fwd(q, k, v, cu_seqlens, pos, max_len, softmax_scale: float = 0.0, o=None,
+                    lse=None, ws=None, stream=None):
+    """Block-diagonal attention forward with per-sample 2D RoPE (pos=None: none).
+    Returns (o [T, h, d] bf16, lse [h, T] fp32)."""
+    torch = _torch()
+    _check_thd("q", q)
+    T, h, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        _check_thd(name, t, T, h, d)
+    n = cu_seqlens.numel() - 1
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((h, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = workspace(T, n, h, d, False, q.device) if ws is None else ws
+    check(load().mf_varlen_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(pos), n, T,
+                                    int(max_len), h, d, float(softmax_scale), _ptr(o), _ptr(lse),
+                                    _ptr(ws), ws.numel(), _stream_ptr(stream)),
+          "mf_varlen_attn_fwd")
+    return o, lse
+
+
+def varlen_attn_bwd(q, k, v, o, lse, d_o, cu_seqlens, pos, max_len, softmax_scale: float = 0.0,
+                    dq=None, dk=None, dv=None, ws=None, stream=None):
+    """Gradients (dq, dk, dv) with respect to the un-rotated q, k and v."""
+    torch = _torch()
+    _check_thd("q", q)
+    T, h, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("d_o", d_o)):
+        _check_thd(name, t, T, h, d)
+    n = cu_seqlens.numel() - 1
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = workspace(T, n, h, d, True, q.device) if ws is None else ws
+    check(load().mf_varlen_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
+                                    _ptr(cu_seqlens), _ptr(pos), n, T, int(max_len), h, d,
+                                    float(softmax_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                                    ws.numel(), _stream_ptr(stream)),
+          "mf_varlen_attn_bwd")
+    return dq, dk, dv
+
+
+def get_status(ws, stream=None) -> None:
+    """Synchronise and raise MFError if the last call on this workspace recorded a
+    device-side error (malformed cu_seqlens, a wait that ran out)."""
+    check(load().mf_get_status(_ptr(ws), _stream_ptr(stream)), "device status")
+
+
+def timing_enable(on: bool = True) -> None:
+    """Bracket every kernel launch of the library with CUDA events (opt-in)."""
+    check(load().mf_timing_enable(1 if on else 0), "mf_timing_enable")
+
+
+def timing_reset() -> None:
+    check(load().mf_timing_reset(), "mf_timing_reset")
+
+
+def timing_read() -> dict:
+    """{kernel name: (total device ms, launches)} since the last reset (syncs)."""
+    from ._lib import KERNELS
+    out = {}
+    for i, name in enumerate(KERNELS):
+        ms, n = ctypes.c_double(), ctypes.c_int64()
+        check(load().mf_timing_read(i, ctypes.byref(ms), ctypes.byref(n)), "mf_timing_read")
+        out[name] = (ms.value, n.value)
+    return out

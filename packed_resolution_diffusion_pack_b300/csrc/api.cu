@@ -1,0 +1,256 @@
+// C ABI (include/mf.h): argument validation, workspace layout and launch order.
+// The arithmetic is in the kernels of pack_rope.cu, attn_fwd.cu and attn_bwd.cu.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "../../include/mf.h"
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mf {
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+WsLayout ws_layout(int64_t T, int64_t n, int64_t heads, int64_t head_dim, bool bwd) {
+  WsLayout L;
+  size_t off = 0;
+  L.status = off;
+  off += 256;
+  L.order = off;
+  off += align_up(sizeof(int32_t) * static_cast<size_t>(n > 0 ? n : 1), 256);
+  L.prefix = off;
+  off += align_up(sizeof(int32_t) * static_cast<size_t>(n + 1), 256);
+  off = align_up(off, 1024);
+  const size_t elems = static_cast<size_t>(T) * heads * head_dim;
+  L.q16 = off;
+  off = align_up(off + 2 * elems, 1024);
+  L.k16 = off;
+  off = align_up(off + 2 * elems, 1024);
+  if (!bwd) {
+    L.v16 = off;
+    off = align_up(off + 2 * elems, 1024);
+  } else {
+    L.hmax = off;
+    off = align_up(off + 8 * static_cast<size_t>(heads), 1024);
+    L.delta = off;
+    off = align_up(off + 4 * static_cast<size_t>(heads) * T, 1024);
+    L.dq_acc = off;
+    off = align_up(off + 4 * elems, 1024);
+  }
+  L.total = off;
+  return L;
+}
+
+static bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// Shared validation of the attention calls.
+static mf_status check_attn(const void* const* ptrs, int nptr, const int32_t* cu, int32_t n,
+                            int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
+                            const void* ws, size_t ws_bytes, bool bwd) {
+  if (n < 0 || T < 0 || max_len < 0 || heads < 1 || cu == nullptr || ws == nullptr)
+    return MF_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
+  const int64_t items = (static_cast<int64_t>(T) / 128 + 1 + n) * heads;
+  if (items > INT32_MAX || static_cast<int64_t>(heads) * T > INT32_MAX) return MF_ERR_OVERFLOW;
+  for (int i = 0; i < nptr; ++i) {
+    if (T > 0 && ptrs[i] == nullptr) return MF_ERR_INVALID_ARG;
+    if (!aligned(ptrs[i], 16)) return MF_ERR_UNSUPPORTED;
+  }
+  if (!aligned(ws, 256)) return MF_ERR_UNSUPPORTED;
+  if (ws_bytes < ws_layout(T, n, heads, head_dim, bwd).total) return MF_ERR_INVALID_ARG;
+  return MF_OK;
+}
+
+static mf_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MF_OK : MF_ERR_CUDA; }
+
+}  // namespace mf
+
+using namespace mf;
+
+extern "C" {
+
+const char* mf_status_string(mf_status s) {
+  switch (s) {
+    case MF_OK: return "MF_OK";
+    case MF_ERR_INVALID_ARG: return "MF_ERR_INVALID_ARG";
+    case MF_ERR_UNSUPPORTED: return "MF_ERR_UNSUPPORTED";
+    case MF_ERR_OVERFLOW: return "MF_ERR_OVERFLOW";
+    case MF_ERR_CUDA: return "MF_ERR_CUDA";
+    case MF_ERR_TIMEOUT: return "MF_ERR_TIMEOUT";
+    case MF_ERR_BAD_SEQLENS: return "MF_ERR_BAD_SEQLENS";
+  }
+  return "MF_ERR_UNKNOWN";
+}
+
+int32_t mf_version(void) { return 10000; }
+
+mf_status mf_pack_size(const int32_t* specs, int32_t n, int32_t* total, int32_t* max_len) {
+  if (n < 0 || (n > 0 && specs == nullptr)) return MF_ERR_INVALID_ARG;
+  int64_t T = 0, mx = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t t = specs[3 * i], H = specs[3 * i + 1], W = specs[3 * i + 2];
+    if (t < 0 || H < 0 || W < 0) return MF_ERR_INVALID_ARG;
+    const int64_t L = t + H * W;
+    if (H * W > INT32_MAX || L > INT32_MAX) return MF_ERR_OVERFLOW;
+    T += L;
+    if (T > INT32_MAX) return MF_ERR_OVERFLOW;
+    if (L > mx) mx = L;
+  }
+  if (total) *total = static_cast<int32_t>(T);
+  if (max_len) *max_len = static_cast<int32_t>(mx);
+  return MF_OK;
+}
+
+mf_status mf_pack(const int32_t* specs, int32_t n, int32_t* d_cu_seqlens, int32_t* d_pos,
+                  mf_stream stream) {
+  int32_t T = 0;
+  const mf_status st = mf_pack_size(specs, n, &T, nullptr);
+  if (st != MF_OK) return st;
+  if (d_cu_seqlens == nullptr) return MF_ERR_INVALID_ARG;
+  if (d_pos != nullptr && !aligned(d_pos, 8)) return MF_ERR_UNSUPPORTED;
+  return cuda_status(
+      launch_pack(specs, n, d_cu_seqlens, d_pos, static_cast<cudaStream_t>(stream)));
+}
+
+mf_status mf_rope2d_qk(const mf_bf16* q, const mf_bf16* k, mf_bf16* q_out, mf_bf16* k_out,
+                       const int32_t* d_pos, int32_t T, int32_t heads, int32_t head_dim,
+                       mf_stream stream) {
+  if (T < 0 || heads < 1) return MF_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(heads) * head_dim * T / 8 > INT64_MAX / 2) return MF_ERR_OVERFLOW;
+  if (T == 0) return MF_OK;
+  if (d_pos == nullptr || (q == nullptr && k == nullptr)) return MF_ERR_INVALID_ARG;
+  if ((q == nullptr) != (q_out == nullptr) || (k == nullptr) != (k_out == nullptr))
+    return MF_ERR_INVALID_ARG;
+  const void* ps[4] = {q, k, q_out, k_out};
+  for (const void* ptr : ps)
+    if (ptr != nullptr && !aligned(ptr, 16)) return MF_ERR_UNSUPPORTED;
+  if (!aligned(d_pos, 8)) return MF_ERR_UNSUPPORTED;
+  return cuda_status(launch_rope(q, k, q_out, k_out, d_pos, T, heads, head_dim, 1.0f,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+size_t mf_attn_workspace_bytes(int32_t T, int32_t n, int32_t heads, int32_t head_dim,
+                               int32_t bwd) {
+  if (T < 0 || n < 0 || heads < 1 || (head_dim != 64 && head_dim != 128)) return 0;
+  return ws_layout(T, n, heads, head_dim, bwd != 0).total;
+}
+
+mf_status mf_varlen_attn_fwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                             const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t n,
+                             int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
+                             float softmax_scale, mf_bf16* o, float* lse, void* ws,
+                             size_t ws_bytes, mf_stream stream) {
+  const void* ptrs[5] = {q, k, v, o, lse};
+  mf_status st = check_attn(ptrs, 5, d_cu_seqlens, n, T, max_len, heads, head_dim, ws, ws_bytes,
+                            false);
+  if (st != MF_OK) return st;
+  if (d_pos != nullptr && !aligned(d_pos, 8)) return MF_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(T, n, heads, head_dim, false);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  auto* status = reinterpret_cast<uint32_t*>(w + L.status);
+  auto* order = reinterpret_cast<int32_t*>(w + L.order);
+  auto* prefix = reinterpret_cast<int32_t*>(w + L.prefix);
+  cudaError_t e =
+      launch_schedule(d_cu_seqlens, n, T, max_len, heads, 256, status, order, prefix, nullptr, 0, s);
+  if (e != cudaSuccess) return MF_ERR_CUDA;
+  if (T == 0) return MF_OK;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(head_dim));
+  // Q' = R q, K' = R k (R = I without positions) and V' = v, all fp16
+  auto* q16 = reinterpret_cast<uint16_t*>(w + L.q16);
+  auto* k16 = reinterpret_cast<uint16_t*>(w + L.k16);
+  auto* v16 = reinterpret_cast<uint16_t*>(w + L.v16);
+  e = launch_prep_f16(q, k, v, q16, k16, v16, d_pos, T, heads, head_dim, status, s);
+  if (e != cudaSuccess) return MF_ERR_CUDA;
+  AttnFwdArgs a;
+  a.q = q16;
+  a.k = k16;
+  a.v = v16;
+  a.cu = d_cu_seqlens;
+  a.order = order;
+  a.prefix = prefix;
+  a.status = status;
+  a.o = o;
+  a.lse = lse;
+  a.n = n;
+  a.T = T;
+  a.heads = heads;
+  a.head_dim = head_dim;
+  a.scale = scale;
+  return cuda_status(launch_attn_fwd(a, s));
+}
+
+mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                             const mf_bf16* o, const float* lse, const mf_bf16* d_o,
+                             const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t n,
+                             int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
+                             float softmax_scale, mf_bf16* dq, mf_bf16* dk, mf_bf16* dv,
+                             void* ws, size_t ws_bytes, mf_stream stream) {
+  const void* ptrs[9] = {q, k, v, o, lse, d_o, dq, dk, dv};
+  mf_status st = check_attn(ptrs, 9, d_cu_seqlens, n, T, max_len, heads, head_dim, ws, ws_bytes,
+                            true);
+  if (st != MF_OK) return st;
+  if (d_pos != nullptr && !aligned(d_pos, 8)) return MF_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(T, n, heads, head_dim, true);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  auto* status = reinterpret_cast<uint32_t*>(w + L.status);
+  auto* order = reinterpret_cast<int32_t*>(w + L.order);
+  auto* prefix = reinterpret_cast<int32_t*>(w + L.prefix);
+  auto* hmax = reinterpret_cast<float*>(w + L.hmax);
+  cudaError_t e = launch_schedule(d_cu_seqlens, n, T, max_len, heads, 128, status, order, prefix,
+                                  hmax, 2 * heads, s);
+  if (e != cudaSuccess) return MF_ERR_CUDA;
+  if (T == 0) return MF_OK;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(head_dim));
+  // Q' = R q, K' = R k in fp16, as in the forward (same logits as the LSE came from)
+  auto* q16 = reinterpret_cast<uint16_t*>(w + L.q16);
+  auto* k16 = reinterpret_cast<uint16_t*>(w + L.k16);
+  e = launch_prep_f16(q, k, nullptr, q16, k16, nullptr, d_pos, T, heads, head_dim, status, s);
+  if (e != cudaSuccess) return MF_ERR_CUDA;
+  AttnBwdArgs a;
+  a.q = q16;
+  a.k = k16;
+  a.v = v;
+  a.hmax = hmax;
+  a.o = o;
+  a.d_o = d_o;
+  a.lse = lse;
+  a.cu = d_cu_seqlens;
+  a.pos = d_pos;
+  a.order = order;
+  a.prefix = prefix;
+  a.status = status;
+  a.delta = reinterpret_cast<float*>(w + L.delta);
+  a.dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.n = n;
+  a.T = T;
+  a.heads = heads;
+  a.head_dim = head_dim;
+  a.scale = scale;
+  return cuda_status(launch_attn_bwd(a, s));
+}
+
+mf_status mf_get_status(void* ws, mf_stream stream) {
+  if (ws == nullptr) return MF_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MF_ERR_CUDA;
+  uint32_t flags = 0;
+  if (cudaMemcpy(&flags, ws, sizeof(flags), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MF_ERR_CUDA;
+  if (flags & kFlagBadSeqlens) return MF_ERR_BAD_SEQLENS;
+  if (flags & kFlagTimeout) return MF_ERR_TIMEOUT;
+  if (flags & kFlagFp16Range) return MF_ERR_OVERFLOW;
+  if (flags & kFlagSmemAlign) return MF_ERR_CUDA;
+  return MF_OK;
+}
+
+}  // extern "C"

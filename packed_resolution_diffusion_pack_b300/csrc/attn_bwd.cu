@@ -1,0 +1,655 @@
+// Block-diagonal attention backward with the RoPE transpose folded in, on
+// tcgen05 / TMEM / TMA.
+//
+// Gradient of the forward (Mage-Flow training step, rcap.io post listing:
+// the loss is back-propagated through the packed attention).  Per sample, head:
+//   D_j = <dO_j, O_j>,  P = exp(S - LSE),  dV = P^T dO,  dP = dO V^T,
+//   dS = P o (dP - D),  dQ' = scale dS K',  dK' = scale dS^T Q',
+//   dQ = R(-theta) dQ',  dK = R(-theta) dK'   (R orthogonal, R^T = R(-theta)).
+//
+// Kernels:
+//   bwd_pre_kernel   D = rowsum(dO o O) in fp32 ([h][T]); zeroes the fp32 dQ
+//                    accumulator rows.
+//   attn_bwd_kernel  one CTA = one sample, one head, one 128-key tile (K_j, V_j
+//                    resident in smem); loops over the sample's 128-row Q tiles:
+//       warp 8     TMA: K, V once; (Q_i, dO_i) through a 2-stage ring.
+//       warp 9     MMA (one thread): S^T = K Q_i^T, dP^T = V dO_i^T (SS);
+//                  dV += P^T dO_i (P^T from TMEM, TS); dK += dS^T Q_i and
+//                  dQ_i = dS K (SS, dS^T staged in smem, read K- and MN-major).
+//       warps 0-3  thread = key row: P^T = exp2(S^T scale log2e - LSE log2e),
+//                  P^T -> TMEM (bf16), dS^T = P^T (dP^T - D) -> smem (bf16);
+//                  epilogue dV -> bf16, dK -> scale, R(-theta), bf16.
+//       warps 4-7  thread = query row: dQ_i from TMEM, scaled, added into the
+//                  fp32 accumulator with vector atomics.
+//   dq_post_kernel   dQ = R(-theta) dq_acc -> bf16.
+// TMEM: S^T [0,128) (P^T bf16 over its first 64 columns), dP^T [128,256) reused
+// for dQ_i, dV [256,256+D), dK [256+D,256+2D).
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mf {
+
+struct WorkItemB {
+  int32_t sample, head, blk, start, len;
+};
+// Per-CTA scalars kept in the dynamic shared-memory region.
+struct CtaMiscB {
+  WorkItemB w;
+  int valid;
+  uint32_t tmem;
+  uint32_t abort;
+};
+__device__ __forceinline__ bool find_item_b(const int32_t* __restrict__ cu,
+                                            const int32_t* __restrict__ order,
+                                            const int32_t* __restrict__ prefix, int32_t n,
+                                            int32_t blk_rows, int32_t idx, WorkItemB& w) {
+  if (n <= 0 || idx >= prefix[n]) return false;
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= idx) lo = mid; else hi = mid - 1;
+  }
+  w.sample = order[lo];
+  w.start = cu[w.sample];
+  w.len = cu[w.sample + 1] - w.start;
+  const int32_t nb = (w.len + blk_rows - 1) / blk_rows;
+  const int32_t local = idx - prefix[lo];
+  w.head = local / nb;
+  w.blk = local - w.head * nb;
+  return true;
+}
+
+// ------------------------------------------------------------- preprocess
+// Rows are (token, head) pairs in THD order; 8 lanes per row, each covering D/8
+// elements.  Per row: D = <dO, O> -> delta[h][t]; the row of the fp32 dQ
+// accumulator zeroed; ||dO|| and ||v|| folded into per-head maxima (shared memory
+// per block, then one atomicMax per head: non-negative floats order like their
+// bit patterns).
+constexpr int kPreRowsPerBlock = 512;
+constexpr int kPreMaxHeads = 256;
+
+__device__ __forceinline__ void bf16x8_dot(const uint4& a, const uint4& b, float& acc) {
+  const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    acc = fmaf(__uint_as_float(wa[e] << 16), __uint_as_float(wb[e] << 16), acc);
+    acc = fmaf(__uint_as_float(wa[e] & 0xFFFF0000u), __uint_as_float(wb[e] & 0xFFFF0000u), acc);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ o,
+                                                      const uint4* __restrict__ d_o,
+                                                      const uint4* __restrict__ v,
+                                                      float* __restrict__ delta,
+                                                      float4* __restrict__ dq_acc,
+                                                      float* __restrict__ hmax, int64_t rows,
+                                                      int32_t T, int32_t heads) {
+  constexpr int V = D / 64;  // uint4 (8 bf16) per lane
+  __shared__ float s_max[2 * kPreMaxHeads];
+  const bool smem_max = heads <= kPreMaxHeads;
+  for (int i = threadIdx.x; i < 2 * kPreMaxHeads; i += blockDim.x) s_max[i] = 0.f;
+  __syncthreads();
+  const int sub = threadIdx.x & 7;
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kPreRowsPerBlock;
+  for (int it = 0; it < kPreRowsPerBlock; it += 32) {
+    const int64_t row = row0 + it + (threadIdx.x >> 3);
+    const bool ok = row < rows;
+    float acc = 0.f, ndo = 0.f, nv = 0.f;
+    if (ok) {
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        const int64_t idx = row * (D / 8) + sub * V + u;
+        const uint4 a = o[idx], b = d_o[idx], c = v[idx];
+        bf16x8_dot(a, b, acc);
+        bf16x8_dot(b, b, ndo);
+        bf16x8_dot(c, c, nv);
+      }
+#pragma unroll
+      for (int u = 0; u < 2 * V; ++u)
+        dq_acc[row * (D / 4) + sub * 2 * V + u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+      acc += __shfl_xor_sync(0xffffffffu, acc, m);
+      ndo += __shfl_xor_sync(0xffffffffu, ndo, m);
+      nv += __shfl_xor_sync(0xffffffffu, nv, m);
+    }
+    if (ok && sub == 0) {
+      const int64_t t = row / heads;
+      const int32_t a = static_cast<int32_t>(row - t * heads);
+      delta[static_cast<int64_t>(a) * T + t] = acc;
+      const unsigned bdo = __float_as_uint(sqrtf(ndo)), bv = __float_as_uint(sqrtf(nv));
+      if (smem_max) {
+        atomicMax(reinterpret_cast<unsigned*>(&s_max[a]), bdo);
+        atomicMax(reinterpret_cast<unsigned*>(&s_max[kPreMaxHeads + a]), bv);
+      } else {
+        atomicMax(reinterpret_cast<unsigned*>(&hmax[a]), bdo);
+        atomicMax(reinterpret_cast<unsigned*>(&hmax[heads + a]), bv);
+      }
+    }
+  }
+  __syncthreads();
+  if (smem_max) {
+    for (int i = threadIdx.x; i < heads; i += blockDim.x) {
+      if (s_max[i] > 0.f) atomicMax(reinterpret_cast<unsigned*>(&hmax[i]), __float_as_uint(s_max[i]));
+      if (s_max[kPreMaxHeads + i] > 0.f)
+        atomicMax(reinterpret_cast<unsigned*>(&hmax[heads + i]),
+                  __float_as_uint(s_max[kPreMaxHeads + i]));
+    }
+  }
+}
+
+// --------------------------------------------------------- dQ post-process
+// dq[t][a][:] = R(-theta(pos_t)) dq_acc[t][a][:]  (or a plain cast without pos).
+template <int D>
+__global__ void __launch_bounds__(256) dq_post_kernel(const float4* __restrict__ acc,
+                                                      uint2* __restrict__ dq,
+                                                      const int2* __restrict__ pos,
+                                                      int64_t rows, int32_t heads,
+                                                      const RopeFreqs f) {
+  // one thread per 4 consecutive elements = 2 rotary pairs
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t total = rows * (D / 4);
+  if (gid >= total) return;
+  const int64_t row = gid / (D / 4);
+  const int e4 = static_cast<int>(gid - row * (D / 4));
+  float4 x = acc[gid];
+  if (pos != nullptr) {
+    const int2 p = pos[row / heads];
+    float v[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int P = e4 * 2 + u;  // pair index in [0, D/2)
+      const float pp = static_cast<float>(P < D / 4 ? p.x : p.y);
+      float s, c;
+      rope_sincos(pp, f.omega[P % (D / 4)], f.omega_lo[P % (D / 4)], -1.f, &s, &c);
+      const float a = v[2 * u], b = v[2 * u + 1];
+      v[2 * u] = fmaf(a, c, -b * s);
+      v[2 * u + 1] = fmaf(a, s, b * c);
+    }
+    x = make_float4(v[0], v[1], v[2], v[3]);
+  }
+  dq[gid] = make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
+}
+
+// --------------------------------------------------------------- main kernel
+template <int D>
+struct BwdCfg {
+  static constexpr int BK = 128;           // keys per CTA
+  static constexpr int BQ = 128;           // queries per Q tile
+  static constexpr int CHUNK = 128 * 128;  // one 64-column chunk of a 128-row tile
+  static constexpr int TILE = 128 * D * 2;
+  static constexpr int NST = 2;            // (Q, dO) stages
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = TILE;
+  static constexpr int OFF_Q = 2 * TILE;              // [NST] Q tiles
+  static constexpr int OFF_DO = OFF_Q + NST * TILE;   // [NST] dO tiles
+  static constexpr int OFF_DS = OFF_DO + NST * TILE;  // dS^T 128 x 128 bf16 (2 chunks)
+  static constexpr int OFF_BAR = OFF_DS + 2 * CHUNK;
+  static constexpr int OFF_VEC = OFF_BAR + 256;       // [NST] x (lse, delta) x 128 fp32
+  static constexpr int OFF_MISC = OFF_VEC + NST * 1024;
+  static constexpr int SMEM = OFF_MISC + 64;
+  static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 256 + D;
+  // fp16 where Q', K' and the scaled dS meet; bf16 where the caller's V and dO do
+  // (gradient-sized values keep bf16's range there).
+  static constexpr uint32_t IDESC_S = idesc_f32acc(128, 128, kF16, 0, 0);    // S^T = K'Q'^T
+  static constexpr uint32_t IDESC_DK = idesc_f32acc(128, D, kF16, 0, 1);     // dK += dS^T Q'
+  static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, D, kF16, 1, 1);     // dQ = dS K'
+  static constexpr uint32_t IDESC_DP = idesc_f32acc(128, 128, kBF16, 0, 0);  // dP^T = V dO^T
+  static constexpr uint32_t IDESC_DV = idesc_f32acc(128, D, kBF16, 0, 1);    // dV += P^T dO
+};
+
+struct BwdParams {
+  const int32_t* cu;
+  const int32_t* order;
+  const int32_t* prefix;
+  const int32_t* pos;
+  const float* lse;
+  const float* delta;
+  uint32_t* status;
+  float* dq_acc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int32_t n, T, heads;
+  float scale, scale_log2;
+  RopeFreqs f;
+  // per-head max ||dO_j|| at [a], max ||v_k|| at [heads + a]: they bound
+  // |dS| <= |dP| + |D| <= 2 max||dO|| max||v||, which sets the power-of-two
+  // scale under which dS is staged in fp16 (undone in the dK / dQ epilogues)
+  const float* hmax;
+};
+
+// 2^e with e = floor(log2(2^15 / bound)) clamped to [-64, 64]: scaled |dS| stays
+// below 2^15 (fp16 max 65504) and small gradients keep fp16's precision.
+__device__ __forceinline__ float ds_scale_for(float max_do, float max_v) {
+  const float bound = 2.f * max_do * max_v;
+  if (!(bound > 0.f) || !(bound < 3.0e38f)) return 1.f;
+  int e = static_cast<int>(floorf(log2f(32768.f / bound)));
+  e = max(-64, min(64, e));
+  return exp2f(static_cast<float>(e));
+}
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using C = BwdCfg<D>;
+  // All shared memory is dynamic (no static __shared__), so its base is the
+  // start of the CTA's window: 1024-byte aligned, as the 128B-swizzled tiles need.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = smem_u32(smem_raw);
+  uint8_t* gbase = smem_raw;
+  CtaMiscB& misc = *reinterpret_cast<CtaMiscB*>(smem_raw + C::OFF_MISC);
+  WorkItemB& s_w = misc.w;
+  int& s_valid = misc.valid;
+  uint32_t& s_tmem = misc.tmem;
+  volatile uint32_t& s_abort = misc.abort;
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kFlagSmemAlign);
+    return;
+  }
+  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+  const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO, sDS = sbase + C::OFF_DS;
+  uint8_t* gDS = gbase + C::OFF_DS;
+  // per stage: lse (log2 domain) at [st*256, +128), delta at [st*256+128, +128)
+  float* vec = reinterpret_cast<float*>(gbase + C::OFF_VEC);
+  const uint32_t bars = sbase + C::OFF_BAR;
+  const uint32_t bar_kv = bars;
+  const uint32_t bar_full = bars + 8;                // [NST]
+  const uint32_t bar_empty = bar_full + 8 * C::NST;  // [NST]
+  const uint32_t bar_st = bar_empty + 8 * C::NST;
+  const uint32_t bar_dpt = bar_st + 8;
+  const uint32_t bar_ds = bar_dpt + 8;
+  const uint32_t bar_dq = bar_ds + 8;
+  const uint32_t bar_dq_empty = bar_dq + 8;
+  const uint32_t bar_done = bar_dq_empty + 8;
+  const uint32_t bar_drain = bar_done + 8;
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    s_valid = ((*p.status & kFlagBadSeqlens) == 0) &&
+              find_item_b(p.cu, p.order, p.prefix, p.n, C::BK, blockIdx.x, s_w);
+    if (s_valid) {
+      mbar_init(bar_kv, 1);
+      for (int i = 0; i < C::NST; ++i) {
+        mbar_init(bar_full + 8 * i, 32);  // the producer warp's 32 lanes (+ TMA bytes)
+        mbar_init(bar_empty + 8 * i, 1);
+      }
+      mbar_init(bar_st, 1);
+      mbar_init(bar_dpt, 1);
+      mbar_init(bar_ds, 128);
+      mbar_init(bar_dq, 1);
+      mbar_init(bar_dq_empty, 128);
+      mbar_init(bar_done, 1);
+      mbar_init(bar_drain, 1);
+      fence_mbar_init();
+    }
+  }
+  __syncthreads();
+  if (!s_valid) return;
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&s_tmem), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const WorkItemB w = s_w;
+  const int32_t k0 = w.blk * C::BK;                // first key (in sample)
+  const int32_t nq = (w.len + C::BQ - 1) / C::BQ;  // Q tiles
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    // Lane 0 issues the tile copies; all 32 lanes stage the Q tile's LSE (log2
+    // domain; +inf past the sample, so P = 0 there) and D (0 past the sample)
+    // into the stage's vectors and arrive on its full barrier.
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
+      for (int ch = 0; ch < D / 64; ++ch) {
+        tma_load_3d(sK + ch * C::CHUNK, &tm_k, bar_kv, ch * 64, w.head, w.start + k0);
+        tma_load_3d(sV + ch * C::CHUNK, &tm_v, bar_kv, ch * 64, w.head, w.start + k0);
+      }
+    }
+    __syncwarp();
+    int32_t issued = 0;
+    for (int32_t i = 0; i < nq; ++i) {
+      const int32_t st = i % C::NST, use = i / C::NST;
+      if (use > 0 &&
+          !__all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * st, (use - 1) & 1, &s_abort))) {
+        s_abort = 1;
+        if (lane == 0) atomicOr(p.status, kFlagTimeout);
+        break;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = static_cast<int>(lane) * 4 + u;
+        const int32_t qi = i * C::BQ + q;
+        const bool q_ok = qi < w.len;
+        const int64_t g = static_cast<int64_t>(w.head) * p.T + w.start + qi;
+        vec[st * 256 + q] = q_ok ? p.lse[g] * 1.4426950408889634f : INFINITY;
+        vec[st * 256 + 128 + q] = q_ok ? p.delta[g] : 0.f;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_full + 8 * st, 2 * C::TILE);
+        for (int ch = 0; ch < D / 64; ++ch) {
+          tma_load_3d(sQ + st * C::TILE + ch * C::CHUNK, &tm_q, bar_full + 8 * st, ch * 64,
+                      w.head, w.start + i * C::BQ);
+          tma_load_3d(sDO + st * C::TILE + ch * C::CHUNK, &tm_do, bar_full + 8 * st, ch * 64,
+                      w.head, w.start + i * C::BQ);
+        }
+      } else {
+        mbar_arrive(bar_full + 8 * st);
+      }
+      ++issued;
+    }
+    if (lane == 0) {
+      mbar_wait_drain(bar_kv, 0);
+      for (int32_t c = (issued > C::NST ? issued - C::NST : 0); c < issued; ++c)
+        mbar_wait_drain(bar_full + 8 * (c % C::NST), (c / C::NST) & 1);
+    }
+  } else if (warp == 9) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        const bool r = mbar_wait(bar, parity, &s_abort);
+        tc_fence_after();
+        return r;
+      };
+      auto desc_k = [](uint32_t base, int kk) {  // K-major operand, K-step kk of 16
+        return sdesc_sw128(base + (kk >> 2) * C::CHUNK + (kk & 3) * 32, 16, 1024);
+      };
+      auto desc_mn = [](uint32_t base, int kk) {  // MN-major operand, K-step kk of 16 rows
+        return sdesc_sw128(base + kk * 2048, C::CHUNK, 1024);
+      };
+      auto issue_st = [&](int32_t i) {  // S^T = K Q_i^T
+        const uint32_t q = sQ + (i % C::NST) * C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::COL_ST, desc_k(sK, kk), desc_k(q, kk), C::IDESC_S, kk > 0);
+        mma_commit(bar_st);
+      };
+      bool ok = wait(bar_kv, 0) && wait(bar_full, 0);
+      if (ok) issue_st(0);
+      for (int32_t i = 0; i < nq && ok; ++i) {
+        const int32_t st = i % C::NST;
+        const uint32_t q = sQ + st * C::TILE, dO = sDO + st * C::TILE;
+        if (i > 0 && !(ok = wait(bar_dq_empty, (i - 1) & 1))) break;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)  // dP^T = V dO_i^T
+          mma_ss(tmem + C::COL_DPT, desc_k(sV, kk), desc_k(dO, kk), C::IDESC_DP, kk > 0);
+        mma_commit(bar_dpt);
+        if (!(ok = wait(bar_ds, i & 1))) break;
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk)  // dV += P^T dO_i
+          mma_ts(tmem + C::COL_DV, tmem + C::COL_ST + kk * 8, desc_mn(dO, kk), C::IDESC_DV,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        if (i + 1 < nq) {
+          if (!(ok = wait(bar_full + 8 * ((i + 1) % C::NST), ((i + 1) / C::NST) & 1))) break;
+          issue_st(i + 1);
+        }
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T Q_i
+          mma_ss(tmem + C::COL_DK, desc_k(sDS, kk), desc_mn(q, kk), C::IDESC_DK,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ_i = dS K
+          mma_ss(tmem + C::COL_DPT, desc_mn(sDS, kk), desc_mn(sK, kk), C::IDESC_DQ, kk > 0);
+        mma_commit(bar_dq);
+        mma_commit(bar_empty + 8 * st);
+      }
+      if (ok) {
+        mma_commit(bar_done);
+      } else {
+        s_abort = 1;
+        atomicOr(p.status, kFlagTimeout);
+      }
+      mma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------ P / dS warpgroup (keys)
+    const uint32_t row = threadIdx.x;  // key row in the tile = TMEM lane
+    const uint32_t lane_off = ((warp & 3) * 32) << 16;
+    const uint32_t tST = tmem + lane_off + C::COL_ST;
+    const uint32_t tDPT = tmem + lane_off + C::COL_DPT;
+    const bool key_ok = k0 + static_cast<int32_t>(row) < w.len;
+    const float sl2 = p.scale_log2;
+    // dS is staged in fp16 as ds_mul * dS (a power of two; see ds_scale_for)
+    const float ds_mul = ds_scale_for(p.hmax[w.head], p.hmax[p.heads + w.head]);
+    float dsmax = 0.f;  // scaled |dS|: flag values outside the fp16 range
+    bool ok = true;
+    for (int32_t i = 0; i < nq; ++i) {
+      const int32_t st = i % C::NST;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_full + 8 * st, (i / C::NST) & 1, &s_abort) &&
+                                       mbar_wait(bar_st, i & 1, &s_abort) &&
+                                       mbar_wait(bar_dpt, i & 1, &s_abort));
+      if (!ok) break;
+      tc_fence_after();
+      const float* vl = vec + st * 256;
+      const float* vd = vl + 128;
+      // 32 queries at a time: P^T (bf16) goes to TMEM columns [16c, 16c+16), which
+      // hold S^T values already read; dS^T to smem, 128B-swizzled K-major:
+      // chunk = q / 64, 16-byte unit (q % 64) / 8 stored at unit ^ (row % 8).
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t rs[32], rd[32];
+        tmem_ld32(tST + c * 32, rs);
+        tmem_ld32(tDPT + c * 32, rd);
+        tmem_wait_ld();
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int q0 = c * 32 + 2 * u;
+          const float p0 = key_ok ? ex2_approx(fmaf(__uint_as_float(rs[2 * u]), sl2, -vl[q0])) : 0.f;
+          const float p1 =
+              key_ok ? ex2_approx(fmaf(__uint_as_float(rs[2 * u + 1]), sl2, -vl[q0 + 1])) : 0.f;
+          pp[u] = pack_bf16x2(p0, p1);
+          const float ds0 = p0 * ds_mul * (__uint_as_float(rd[2 * u]) - vd[q0]);
+          const float ds1 = p1 * ds_mul * (__uint_as_float(rd[2 * u + 1]) - vd[q0 + 1]);
+          dsmax = fmaxf(dsmax, fmaxf(fabsf(ds0), fabsf(ds1)));
+          pd[u] = pack_f16x2(ds0, ds1);
+        }
+        tmem_st16(tST + c * 16, pp);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int q = c * 32 + u * 8;  // first query of this 16-byte unit
+          const int chunk = q >> 6, unit = (q & 63) >> 3;
+          uint4* dst = reinterpret_cast<uint4*>(gDS + chunk * C::CHUNK + row * 128 +
+                                                ((unit ^ (row & 7)) << 4));
+          *dst = make_uint4(pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar_ds);
+    }
+    if (!(dsmax <= 65504.f)) atomicOr(p.status, kFlagFp16Range);
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, &s_abort));
+    if (ok) {
+      tc_fence_after();
+      const int64_t grow = (static_cast<int64_t>(w.start) + k0 + row) * p.heads + w.head;
+      const float dk_mul = p.scale / ds_mul;  // exact: ds_mul is a power of two
+      int32_t pr_ = 0, pc_ = 0;
+      if (key_ok && p.pos != nullptr) {
+        pr_ = p.pos[2 * (w.start + k0 + row)];
+        pc_ = p.pos[2 * (w.start + k0 + row) + 1];
+      }
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::COL_DV + cc * 32, r);
+        tmem_wait_ld();
+        if (key_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dv + grow * D + cc * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dst[u] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * u]), __uint_as_float(r[8 * u + 1])),
+                                pack_bf16x2(__uint_as_float(r[8 * u + 2]), __uint_as_float(r[8 * u + 3])),
+                                pack_bf16x2(__uint_as_float(r[8 * u + 4]), __uint_as_float(r[8 * u + 5])),
+                                pack_bf16x2(__uint_as_float(r[8 * u + 6]), __uint_as_float(r[8 * u + 7])));
+        }
+      }
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::COL_DK + cc * 32, r);
+        tmem_wait_ld();
+        if (key_ok) {
+          float v[32];
+#pragma unroll
+          for (int u = 0; u < 32; ++u) v[u] = __uint_as_float(r[u]) * dk_mul;
+          if (p.pos != nullptr) {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const int P = cc * 16 + u;  // pair index
+              const float pp = static_cast<float>(P < D / 4 ? pr_ : pc_);
+              float s, c;
+              rope_sincos(pp, p.f.omega[P % (D / 4)], p.f.omega_lo[P % (D / 4)], -1.f, &s, &c);
+              const float a = v[2 * u], b = v[2 * u + 1];
+              v[2 * u] = fmaf(a, c, -b * s);
+              v[2 * u + 1] = fmaf(a, s, b * c);
+            }
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.dk + grow * D + cc * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            dst[u] = make_uint4(pack_bf16x2(v[8 * u], v[8 * u + 1]),
+                                pack_bf16x2(v[8 * u + 2], v[8 * u + 3]),
+                                pack_bf16x2(v[8 * u + 4], v[8 * u + 5]),
+                                pack_bf16x2(v[8 * u + 6], v[8 * u + 7]));
+        }
+      }
+    } else {
+      s_abort = 1;
+      atomicOr(p.status, kFlagTimeout);
+    }
+  } else {
+    // --------------------------------------------------- dQ warpgroup (queries)
+    const uint32_t row = threadIdx.x & 127;  // query row in the Q tile = TMEM lane
+    const uint32_t lane_off = ((warp & 3) * 32) << 16;
+    // softmax scale over the power-of-two dS staging scale (exact division)
+    const float dq_mul = p.scale / ds_scale_for(p.hmax[w.head], p.hmax[p.heads + w.head]);
+    for (int32_t i = 0; i < nq; ++i) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, &s_abort));
+      if (!ok) {
+        s_abort = 1;
+        atomicOr(p.status, kFlagTimeout);
+        break;
+      }
+      tc_fence_after();
+      const int32_t qi = i * C::BQ + static_cast<int32_t>(row);
+      const bool q_ok = qi < w.len;
+      float4* dst = reinterpret_cast<float4*>(
+          p.dq_acc + ((static_cast<int64_t>(w.start) + qi) * p.heads + w.head) * D);
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::COL_DPT + cc * 32, r);
+        tmem_wait_ld();
+        if (q_ok) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            atomicAdd(dst + cc * 8 + u,
+                      make_float4(__uint_as_float(r[4 * u]) * dq_mul,
+                                  __uint_as_float(r[4 * u + 1]) * dq_mul,
+                                  __uint_as_float(r[4 * u + 2]) * dq_mul,
+                                  __uint_as_float(r[4 * u + 3]) * dq_mul));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_dq_empty);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
+  using C = BwdCfg<D>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int64_t rows = static_cast<int64_t>(a.T) * a.heads;
+  const RopeFreqs f = make_rope_freqs(D);
+  if (rows > 0) {
+    const int64_t blocks = (rows + kPreRowsPerBlock - 1) / kPreRowsPerBlock;
+    KernelTimer kt(MF_K_BWD_PRE, s);
+    bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        reinterpret_cast<const uint4*>(a.o), reinterpret_cast<const uint4*>(a.d_o),
+        reinterpret_cast<const uint4*>(a.v), a.delta, reinterpret_cast<float4*>(a.dq_acc), a.hmax,
+        rows, a.T, a.heads);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_thd(&tq, a.q, a.T, a.heads, D, 128, true) ||
+      !make_tmap_thd(&tk, a.k, a.T, a.heads, D, 128, true) ||
+      !make_tmap_thd(&tv, a.v, a.T, a.heads, D, 128) ||
+      !make_tmap_thd(&tdo, a.d_o, a.T, a.heads, D, 128))
+    return cudaErrorInvalidValue;
+  BwdParams p;
+  p.cu = a.cu;
+  p.order = a.order;
+  p.prefix = a.prefix;
+  p.pos = a.pos;
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.status = a.status;
+  p.dq_acc = a.dq_acc;
+  p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
+  p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
+  p.n = a.n;
+  p.T = a.T;
+  p.heads = a.heads;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.f = f;
+  p.hmax = a.hmax;
+  const int64_t blocks = (static_cast<int64_t>(a.T + C::BK - 1) / C::BK + a.n) * a.heads;
+  if (blocks > 0) {
+    {
+      KernelTimer kt(MF_K_ATTN_BWD, s);
+      attn_bwd_kernel<D><<<static_cast<unsigned>(blocks), 320, C::SMEM, s>>>(tq, tk, tv, tdo, p);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (rows > 0) {
+    const int64_t total = rows * (D / 4);
+    KernelTimer kt(MF_K_DQ_POST, s);
+    dq_post_kernel<D><<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(
+        reinterpret_cast<const float4*>(a.dq_acc), reinterpret_cast<uint2*>(a.dq),
+        reinterpret_cast<const int2*>(a.pos), rows, a.heads, f);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_attn_bwd(const AttnBwdArgs& a, cudaStream_t s) {
+  return a.head_dim == 128 ? launch_bwd_d<128>(a, s) : launch_bwd_d<64>(a, s);
+}
+
+}  // namespace mf

@@ -1,0 +1,535 @@
+// Block-diagonal (per-sample) non-causal attention forward on tcgen05 / TMEM / TMA.
+//
+// Operation: Mage-Flow joint self-attention over each packed sample (paperlayer.ai
+// summary 3.2.1 "Model Architecture and Native Packing"; rcap.io post, varlen
+// attention over the packed stream).  For each sample i, head a, query row j:
+//   O_j = sum_k softmax_k(scale <q'_j, k'_k>) v_k over the keys of sample i only,
+//   LSE_j = ln sum_k exp(scale <q'_j, k'_k>).
+//
+// Design (one CTA = one sample, one head, 256 query rows = two 128-row Q tiles):
+//   warp 8      TMA producer: Q tiles once, then K_j, V_j tiles through a ring
+//               of shared-memory slots (128B-swizzled, 64-column chunks).
+//   warp 9      MMA issuer (one thread): S_t = Q'_t K'_j^T (SS, into TMEM), then
+//               O_t += P_t V'_j with P_t read from TMEM (TS).  Q', K', V', P are
+//               fp16 (11 significant bits), accumulation fp32.  The two Q tiles
+//               ping-pong so the tensor core works on one while the other's
+//               softmax runs.
+//   warps 0-7   two softmax warpgroups, one per Q tile; thread = query row =
+//               TMEM lane.  Online softmax in base 2 with a lazy rescale of O
+//               (only when the running max grows by more than 2^8), P written
+//               back to TMEM as fp16 over the S columns.  Epilogue: O / l, LSE.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D).
+// Tiles never cross a sample: K/V tiles start at the sample's first token, key
+// columns past the sample end are masked to -inf, query rows past it not stored.
+// Every wait is bounded; a CTA that gives up records kFlagTimeout, lets its
+// in-flight copies and MMAs land, frees TMEM and exits.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mf {
+
+// ----------------------------------------------------------- tensor maps
+bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t T, int64_t heads,
+                   int64_t head_dim, int box_rows, bool f16) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encode == nullptr) {
+    cudaDriverEntryPointQueryResult qres;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &qres) != cudaSuccess ||
+        qres != cudaDriverEntryPointSuccess || fn == nullptr)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const int64_t rows = T > 0 ? T : 1;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim * 2),
+                           static_cast<cuuint64_t>(heads * head_dim * 2)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      3, const_cast<void*>(base), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------- scheduling
+// One block.  Validates cu_seqlens (cu[0] = 0, non-decreasing, cu[n] = T, every
+// L_i <= max_len), zeroes the status word, ranks samples longest first and writes
+// prefix[r] = work items of ranks < r, where a sample holds ceil(L/blk) * heads
+// items.  On a malformed cu_seqlens it records kFlagBadSeqlens and schedules no
+// work at all.
+constexpr int kRankLimit = 4096;  // larger n keeps pack order (no LPT ranking)
+
+__global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* __restrict__ cu,
+                                                        int32_t n, int32_t T, int32_t max_len,
+                                                        int32_t heads, int32_t blk,
+                                                        uint32_t* __restrict__ status,
+                                                        int32_t* __restrict__ order,
+                                                        int32_t* __restrict__ prefix,
+                                                        float* __restrict__ zero, int32_t nzero) {
+  __shared__ int s_bad;
+  __shared__ int64_t s_part[1024];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int i = tid; i < nzero; i += nt) zero[i] = 0.f;
+  if (tid == 0) s_bad = (cu[0] != 0 || cu[n] != T) ? 1 : 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += nt) {
+    const int32_t L = cu[i + 1] - cu[i];
+    if (L < 0 || L > max_len) s_bad = 1;
+  }
+  __syncthreads();
+  if (s_bad) {
+    for (int i = tid; i <= n; i += nt) prefix[i] = 0;
+    if (tid == 0) *status = kFlagBadSeqlens;
+    return;
+  }
+  if (tid == 0) *status = 0u;
+  if (n <= kRankLimit) {
+    for (int i = tid; i < n; i += nt) {
+      const int32_t Li = cu[i + 1] - cu[i];
+      int rank = 0;
+      for (int k = 0; k < n; ++k) {
+        const int32_t Lk = cu[k + 1] - cu[k];
+        rank += (Lk > Li) || (Lk == Li && k < i);
+      }
+      order[rank] = i;
+    }
+  } else {
+    for (int i = tid; i < n; i += nt) order[i] = i;
+  }
+  __syncthreads();
+  // chunked exclusive scan of items over ranks
+  const int per = (n + nt - 1) / nt;
+  const int b = tid * per, e = min(n, b + per);
+  int64_t sum = 0;
+  for (int r = b; r < e; ++r) {
+    const int i = order[r];
+    sum += static_cast<int64_t>((cu[i + 1] - cu[i] + blk - 1) / blk) * heads;
+  }
+  s_part[tid] = sum;
+  __syncthreads();
+  if (tid == 0) {
+    int64_t acc = 0;
+    for (int t = 0; t < nt; ++t) {
+      const int64_t v = s_part[t];
+      s_part[t] = acc;
+      acc += v;
+    }
+    prefix[n] = static_cast<int32_t>(acc);
+  }
+  __syncthreads();
+  int64_t acc = s_part[tid];
+  for (int r = b; r < e; ++r) {
+    prefix[r] = static_cast<int32_t>(acc);
+    const int i = order[r];
+    acc += static_cast<int64_t>((cu[i + 1] - cu[i] + blk - 1) / blk) * heads;
+  }
+}
+
+cudaError_t launch_schedule(const int32_t* d_cu, int32_t n, int32_t T, int32_t max_len,
+                            int32_t heads, int32_t blk, uint32_t* status, int32_t* order,
+                            int32_t* prefix, float* zero, int32_t nzero, cudaStream_t s) {
+  KernelTimer kt(MF_K_SCHEDULE, s);
+  schedule_kernel<<<1, 1024, 0, s>>>(d_cu, n, T, max_len, heads, blk, status, order, prefix, zero,
+                                     nzero);
+  return cudaGetLastError();
+}
+
+// Resolve the work item of this CTA: rank r with prefix[r] <= idx < prefix[r+1].
+struct WorkItem {
+  int32_t sample, head, blk, start, len;
+};
+// Per-CTA scalars kept in the dynamic shared-memory region.
+struct CtaMisc {
+  WorkItem w;
+  int valid;
+  uint32_t tmem;
+  uint32_t abort;
+};
+__device__ __forceinline__ bool find_item(const int32_t* __restrict__ cu,
+                                          const int32_t* __restrict__ order,
+                                          const int32_t* __restrict__ prefix, int32_t n,
+                                          int32_t blk_rows, int32_t idx, WorkItem& w) {
+  if (n <= 0 || idx >= prefix[n]) return false;
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= idx) lo = mid; else hi = mid - 1;
+  }
+  w.sample = order[lo];
+  w.start = cu[w.sample];
+  w.len = cu[w.sample + 1] - w.start;
+  const int32_t nb = (w.len + blk_rows - 1) / blk_rows;
+  const int32_t local = idx - prefix[lo];
+  w.head = local / nb;
+  w.blk = local - w.head * nb;
+  return true;
+}
+
+// ------------------------------------------------------------------ forward
+template <int D>
+struct FwdCfg {
+  static constexpr int BM = 128;                  // query rows per Q tile
+  static constexpr int BN = 128;                  // keys per K/V tile
+  static constexpr int CHUNK = 128 * 128;         // one 64-column chunk of a 128-row tile
+  static constexpr int TILE = BM * D * 2;         // bytes of one 128 x D bf16 tile
+  static constexpr int NSLOT = D == 128 ? 4 : 8;  // K/V ring slots
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = 2 * TILE;
+  static constexpr int OFF_BAR = OFF_KV + NSLOT * TILE;
+  static constexpr int OFF_MISC = OFF_BAR + 256;
+  static constexpr int SMEM = OFF_MISC + 64;
+  static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
+  // fp16 operands throughout: S = Q'K'^T and O += P V' (V' MN-major)
+  static constexpr uint32_t IDESC_S = idesc_f32acc(128, 128, kF16, 0, 0);
+  static constexpr uint32_t IDESC_PV = idesc_f32acc(128, D, kF16, 0, 1);
+};
+
+struct FwdParams {
+  const int32_t* cu;
+  const int32_t* order;
+  const int32_t* prefix;
+  uint32_t* status;
+  __nv_bfloat16* o;
+  float* lse;
+  int32_t n, T, heads;
+  float scale_log2;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = FwdCfg<D>;
+  // All shared memory is dynamic (no static __shared__), so its base is the
+  // start of the CTA's window: 1024-byte aligned, as the 128B-swizzled tiles need.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = smem_u32(smem_raw);
+  CtaMisc& misc = *reinterpret_cast<CtaMisc*>(smem_raw + C::OFF_MISC);
+  WorkItem& s_w = misc.w;
+  int& s_valid = misc.valid;
+  uint32_t& s_tmem = misc.tmem;
+  volatile uint32_t& s_abort = misc.abort;
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kFlagSmemAlign);
+    return;
+  }
+  const uint32_t sQ = sbase + C::OFF_Q;
+  const uint32_t sKV = sbase + C::OFF_KV;
+  const uint32_t bars = sbase + C::OFF_BAR;
+  // barrier addresses (8 bytes each)
+  const uint32_t bar_q = bars;
+  const uint32_t bar_full = bars + 8;                     // [NSLOT]
+  const uint32_t bar_empty = bar_full + 8 * C::NSLOT;     // [NSLOT]
+  const uint32_t bar_s = bar_empty + 8 * C::NSLOT;        // [2]
+  const uint32_t bar_p = bar_s + 16;                      // [2]
+  const uint32_t bar_o = bar_p + 16;                      // [2]
+  const uint32_t bar_drain = bar_o + 16;
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    s_valid = ((*p.status & kFlagBadSeqlens) == 0) &&
+              find_item(p.cu, p.order, p.prefix, p.n, 2 * C::BM, blockIdx.x, s_w);
+    if (s_valid) {
+      mbar_init(bar_q, 1);
+      for (int i = 0; i < C::NSLOT; ++i) {
+        mbar_init(bar_full + 8 * i, 1);
+        mbar_init(bar_empty + 8 * i, 1);
+      }
+      mbar_init(bar_s, 1);
+      mbar_init(bar_s + 8, 1);
+      mbar_init(bar_p, 128);
+      mbar_init(bar_p + 8, 128);
+      mbar_init(bar_o, 1);
+      mbar_init(bar_o + 8, 1);
+      mbar_init(bar_drain, 1);
+      fence_mbar_init();
+    }
+  }
+  __syncthreads();
+  if (!s_valid) return;
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&s_tmem), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  const WorkItem w = s_w;
+  const int32_t q0 = w.blk * 2 * C::BM;            // first query row (in sample)
+  const bool has1 = q0 + C::BM < w.len;             // second Q tile holds rows
+  const int32_t nkv = (w.len + C::BN - 1) / C::BN;  // K/V tiles
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(bar_q, (has1 ? 2 : 1) * C::TILE);
+      for (int t = 0; t < (has1 ? 2 : 1); ++t)
+        for (int ch = 0; ch < D / 64; ++ch)
+          tma_load_3d(sQ + t * C::TILE + ch * C::CHUNK, &tm_q, bar_q, ch * 64, w.head,
+                      w.start + q0 + t * C::BM);
+      int32_t issued = 0;
+      bool ok = true;
+      for (int32_t j = 0; j < nkv && ok; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int32_t c = 2 * j + kv;
+          const int32_t slot = c % C::NSLOT, use = c / C::NSLOT;
+          if (use > 0 && !mbar_wait(bar_empty + 8 * slot, (use - 1) & 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar_full + 8 * slot, C::TILE);
+          for (int ch = 0; ch < D / 64; ++ch)
+            tma_load_3d(sKV + slot * C::TILE + ch * C::CHUNK, kv ? &tm_v : &tm_k,
+                        bar_full + 8 * slot, ch * 64, w.head, w.start + j * C::BN);
+          ++issued;
+        }
+      }
+      if (!ok) {
+        s_abort = 1;
+        atomicOr(p.status, kFlagTimeout);
+      }
+      // let every issued copy land before the CTA can exit
+      mbar_wait_drain(bar_q, 0);
+      for (int32_t c = (issued > C::NSLOT ? issued - C::NSLOT : 0); c < issued; ++c)
+        mbar_wait_drain(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1);
+    }
+  } else if (warp == 9) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(bar_q, 0, &s_abort);
+      tc_fence_after();
+      auto kv_wait = [&](int32_t c) -> bool {
+        const bool r = mbar_wait(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1, &s_abort);
+        tc_fence_after();
+        return r;
+      };
+      auto issue_s = [&](int t, int32_t j) {
+        const uint32_t a0 = sQ + t * C::TILE;
+        const uint32_t b0 = sKV + ((2 * j) % C::NSLOT) * C::TILE;
+        const uint32_t d = tmem + (t ? C::S_COL1 : C::S_COL0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
+          mma_ss(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), C::IDESC_S,
+                 kk > 0);
+        }
+        mma_commit(bar_s + 8 * t);
+      };
+      auto issue_pv = [&](int t, int32_t j) {
+        const uint32_t b0 = sKV + ((2 * j + 1) % C::NSLOT) * C::TILE;
+        const uint32_t d = tmem + (t ? C::O_COL1 : C::O_COL0);
+        const uint32_t a = tmem + (t ? C::S_COL1 : C::S_COL0);
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_ts(d, a + kk * 8, sdesc_sw128(b0 + kk * 2048, C::CHUNK, 1024), C::IDESC_PV,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+      };
+      if (ok) ok = kv_wait(0);
+      if (ok) {
+        issue_s(0, 0);
+        if (has1) issue_s(1, 0);
+        mma_commit(bar_empty + 8 * (0 % C::NSLOT));
+      }
+      for (int32_t j = 0; j < nkv && ok; ++j) {
+        ok = mbar_wait(bar_p, j & 1, &s_abort) && kv_wait(2 * j + 1);
+        if (!ok) break;
+        issue_pv(0, j);
+        const bool more = j + 1 < nkv;
+        if (more) {
+          if (!(ok = kv_wait(2 * j + 2))) break;
+          issue_s(0, j + 1);
+        }
+        if (has1) {
+          if (!(ok = mbar_wait(bar_p + 8, j & 1, &s_abort))) break;
+          tc_fence_after();
+          issue_pv(1, j);
+        }
+        mma_commit(bar_empty + 8 * ((2 * j + 1) % C::NSLOT));
+        if (more) {
+          if (has1) issue_s(1, j + 1);
+          mma_commit(bar_empty + 8 * ((2 * j + 2) % C::NSLOT));
+        }
+      }
+      if (ok) {
+        mma_commit(bar_o);
+        if (has1) mma_commit(bar_o + 8);
+      } else {
+        s_abort = 1;
+        atomicOr(p.status, kFlagTimeout);
+      }
+      // every MMA issued so far must finish before TMEM is released
+      mma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0);
+    }
+  } else {
+    // ---------------------------------------------------- softmax warpgroups
+    const int t = warp >> 2;  // Q tile of this warpgroup
+    if (t == 0 || has1) {
+      const uint32_t row = threadIdx.x & 127;
+      const uint32_t lane_off = ((warp & 3) * 32) << 16;
+      const uint32_t tS = tmem + lane_off + (t ? C::S_COL1 : C::S_COL0);
+      const uint32_t tO = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
+      const int32_t qrow = q0 + t * C::BM + static_cast<int32_t>(row);
+      const float sl2 = p.scale_log2;
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int32_t j = 0; j < nkv; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_s + 8 * t, j & 1, &s_abort));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tS + c * 32, r);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) s[c * 32 + u] = r[u];
+        }
+        tmem_wait_ld();
+        const int32_t nvalid = w.len - j * C::BN;
+        if (nvalid < C::BN) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= nvalid) s[c] = __float_as_uint(-INFINITY);
+        }
+        float mx = __uint_as_float(s[0]);
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+        const float m_new = fmaxf(m, mx * sl2);
+        if (j == 0) {
+          m = m_new;
+        } else {
+          const bool need = m_new > m + 8.f;
+          if (__any_sync(0xffffffffu, need)) {
+            const float f = need ? ex2_approx(m - m_new) : 1.f;
+            if (need) {
+              l *= f;
+              m = m_new;
+            }
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t r[32];
+              tmem_ld32(tO + cc * 32, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * f);
+              tmem_st32(tO + cc * 32, r);
+            }
+            tmem_wait_st();
+          }
+        }
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(s[c * 32 + 2 * u]), sl2, -m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(s[c * 32 + 2 * u + 1]), sl2, -m));
+            sum += p0 + p1;
+            pk[u] = pack_f16x2(p0, p1);
+          }
+          tmem_st16(tS + c * 16, pk);
+        }
+        l += sum;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_p + 8 * t);
+      }
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_o + 8 * t, 0, &s_abort));
+      if (ok) {
+        tc_fence_after();
+        const bool store = qrow < w.len;
+        const float inv = 1.f / l;
+        __nv_bfloat16* orow =
+            p.o + (static_cast<int64_t>(w.start + qrow) * p.heads + w.head) * D;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(tO + cc * 32, r);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            pk[u] = pack_bf16x2(__uint_as_float(r[2 * u]) * inv, __uint_as_float(r[2 * u + 1]) * inv);
+          if (store) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
+        }
+        if (store)
+          p.lse[static_cast<int64_t>(w.head) * p.T + w.start + qrow] =
+              (m + log2f(l)) * 0.69314718055994530942f;
+      } else {
+        s_abort = 1;
+        atomicOr(p.status, kFlagTimeout);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+static cudaError_t launch_fwd_d(const AttnFwdArgs& a, cudaStream_t s) {
+  using C = FwdCfg<D>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_thd(&tq, a.q, a.T, a.heads, D, 128, true) ||
+      !make_tmap_thd(&tk, a.k, a.T, a.heads, D, 128, true) ||
+      !make_tmap_thd(&tv, a.v, a.T, a.heads, D, 128, true))
+    return cudaErrorInvalidValue;
+  FwdParams p;
+  p.cu = a.cu;
+  p.order = a.order;
+  p.prefix = a.prefix;
+  p.status = a.status;
+  p.o = reinterpret_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.n = a.n;
+  p.T = a.T;
+  p.heads = a.heads;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  const int64_t blocks = (static_cast<int64_t>(a.T + 2 * C::BM - 1) / (2 * C::BM) + a.n) * a.heads;
+  if (blocks <= 0) return cudaSuccess;
+  {
+    KernelTimer kt(MF_K_ATTN_FWD, s);
+    attn_fwd_kernel<D><<<static_cast<unsigned>(blocks), 320, C::SMEM, s>>>(tq, tk, tv, p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_fwd(const AttnFwdArgs& a, cudaStream_t s) {
+  return a.head_dim == 128 ? launch_fwd_d<128>(a, s) : launch_fwd_d<64>(a, s);
+}
+
+}  // namespace mf

@@ -1,0 +1,135 @@
+// Shared internal definitions of the CUDA library: workspace layout, kernel
+// launch declarations and host helpers.  Not part of the public ABI (mf.h).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mf.h"
+
+namespace mf {
+
+constexpr double kRopeBase = 10000.0;
+constexpr int kMaxFreq = 32;  // d/4 for head_dim 128
+
+// Rotary frequencies omega_j = base^(-2j/(d/2)), j < d/4, computed on the host in
+// double and split into fp32 hi + lo parts (passed by value to the kernels), so a
+// kernel can form theta = p * omega to ~2^-40 relative before taking sin/cos.
+struct RopeFreqs {
+  float omega[kMaxFreq];
+  float omega_lo[kMaxFreq];
+};
+RopeFreqs make_rope_freqs(int head_dim);
+
+// sin and cos of theta = sign * p * omega (p a small integer as float): the fp32
+// product's rounding error is recovered exactly with an FMA and added, together
+// with p * omega_lo, as a first-order correction to sincosf(theta_hi).
+__device__ __forceinline__ void rope_sincos(float p, float w_hi, float w_lo, float sign,
+                                            float* s, float* c) {
+  const float th = p * w_hi;
+  const float err = fmaf(p, w_hi, -th) + p * w_lo;
+  float s0, c0;
+  sincosf(sign * th, &s0, &c0);
+  const float e = sign * err;
+  *s = fmaf(e, c0, s0);
+  *c = fmaf(-e, s0, c0);
+}
+
+// --------------------------------------------------------- workspace layout
+// [0, 256)            device status word (uint32, flags kFlag*)
+// [256, +sched)       schedule: int32 order[n], int32 prefix[n+1]
+// then 1024-aligned:  q16, k16  fp16 [T][h][d]  (rotated Q', K')
+// fwd only:           v16 fp16 [T][h][d]
+// bwd only:           hmax fp32 [2][h] (per-head max ||dO_j||, max ||v_k||),
+//                     delta fp32 [h][T], dq_acc fp32 [T][h][d]
+struct WsLayout {
+  size_t status = 0;
+  size_t order = 0, prefix = 0;
+  size_t q16 = 0, k16 = 0, v16 = 0;
+  size_t hmax = 0, delta = 0, dq_acc = 0;
+  size_t total = 0;
+};
+WsLayout ws_layout(int64_t T, int64_t n, int64_t heads, int64_t head_dim, bool bwd);
+
+// ---------------------------------------------------------------- launches
+cudaError_t launch_pack(const int32_t* specs, int32_t n, int32_t* d_cu, int32_t* d_pos,
+                        cudaStream_t s);
+// bf16 in, bf16 out (the standalone mf_rope2d_qk).
+cudaError_t launch_rope(const uint16_t* q, const uint16_t* k, uint16_t* q_out, uint16_t* k_out,
+                        const int32_t* d_pos, int32_t T, int32_t heads, int32_t head_dim,
+                        float sign, cudaStream_t s);
+// bf16 in, fp16 out: the attention's operands Q' = R q, K' = R k (R the identity
+// when d_pos is null) and, when v is given, V' = v converted.  fp16 carries 3 more
+// mantissa bits than bf16 at the same tensor-core rate.  Sets kFlagFp16Range in
+// *status if a value leaves the fp16 range.  Any of q/k/v may be null.
+cudaError_t launch_prep_f16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                            uint16_t* q_out, uint16_t* k_out, uint16_t* v_out,
+                            const int32_t* d_pos, int32_t T, int32_t heads, int32_t head_dim,
+                            uint32_t* status, cudaStream_t s);
+// Builds the longest-first work list (items of `blk` rows per sample and head)
+// and validates cu_seqlens; zeroes the status word first, and `nzero` floats at
+// `zero` (may be null).
+cudaError_t launch_schedule(const int32_t* d_cu, int32_t n, int32_t T, int32_t max_len,
+                            int32_t heads, int32_t blk, uint32_t* status, int32_t* order,
+                            int32_t* prefix, float* zero, int32_t nzero, cudaStream_t s);
+
+struct AttnFwdArgs {
+  const uint16_t* q;  // fp16 Q' (rotated)
+  const uint16_t* k;  // fp16 K' (rotated)
+  const uint16_t* v;  // fp16 V'
+  const int32_t* cu;
+  const int32_t* order;
+  const int32_t* prefix;
+  uint32_t* status;
+  uint16_t* o;  // bf16
+  float* lse;
+  int32_t n, T, heads, head_dim;
+  float scale;
+};
+cudaError_t launch_attn_fwd(const AttnFwdArgs& a, cudaStream_t s);
+
+struct AttnBwdArgs {
+  const uint16_t* q;    // fp16 Q' (rotated)
+  const uint16_t* k;    // fp16 K' (rotated)
+  const uint16_t* v;    // bf16 (caller's)
+  const uint16_t* o;    // bf16
+  const uint16_t* d_o;  // bf16
+  const float* lse;
+  const int32_t* cu;
+  const int32_t* pos;  // may be null
+  const int32_t* order;
+  const int32_t* prefix;
+  uint32_t* status;
+  float* hmax;    // [2][h]: max ||dO_j||, max ||v_k|| per head (zeroed by the schedule)
+  float* delta;   // [h][T]
+  float* dq_acc;  // [T][h][d]
+  uint16_t* dq;
+  uint16_t* dk;
+  uint16_t* dv;
+  int32_t n, T, heads, head_dim;
+  float scale;
+};
+cudaError_t launch_attn_bwd(const AttnBwdArgs& a, cudaStream_t s);
+
+// RAII bracket of one kernel launch for the opt-in timing (mf_timing_*): records
+// an event on `s` when built and another when destroyed; no-op when disabled.
+class KernelTimer {
+ public:
+  KernelTimer(int id, cudaStream_t s);
+  ~KernelTimer();
+  KernelTimer(const KernelTimer&) = delete;
+  KernelTimer& operator=(const KernelTimer&) = delete;
+
+ private:
+  int id_;
+  cudaStream_t s_;
+  void* a_ = nullptr;
+};
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+// Element type bf16, or fp16 when `f16` (same size and layout).
+bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t T, int64_t heads,
+                   int64_t head_dim, int box_rows, bool f16 = false);
+
+}  // namespace mf

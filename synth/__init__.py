@@ -228,7 +228,11 @@ def extreme_aspect(seed: int = 0, budget: int = TOKEN_BUDGET) -> Workload:
 WORKLOADS = {f.__name__: f for f in (tiny, single_1024, mixed_50k, cfg_2048, extreme_aspect)}
 
 
-def workload(name: str, seed: int = 0) -> Workload:
+def workload(name: str, seed: int = 0, budget: int | None = None) -> Workload:
+    """A named workload; `budget` overrides the 50,000-token budget of the two
+    budget-packed workloads (used for smaller profiling captures)."""
+    if budget is not None and name in ("mixed_50k", "extreme_aspect"):
+        return WORKLOADS[name](seed, budget=budget)
     return WORKLOADS[name](seed)
 
 

@@ -273,3 +273,16 @@ def pin_bwd_invariants(so=None):
     g2 = oracle.attn_bwd(q1, k1 + r.standard_normal((1, h, d)), v1, do1, cu1, pos1, so=so)
     for a, b in zip(g1, g2):
         np.testing.assert_allclose(a, b, atol=1e-11)
+
+
+def pin_fwd_rows_match_full(so=None):
+    """The row-subset entry gives the same rows as the full forward (it is the
+    same definition restricted to those rows)."""
+    wl, q, k, v, _ = _tiny_inputs()
+    cu, pos = oracle.pack(wl.specs)
+    o, lse = oracle.attn_fwd(q, k, v, cu, pos, so=so)
+    rows = [(0, 0), (28, 1), (29, 0), (99, 1), (134, 0), (100, 1)]
+    orow, lrow = oracle.attn_fwd_rows(q, k, v, cu, pos, rows, so=so)
+    for r, (t, a) in enumerate(rows):
+        np.testing.assert_array_equal(orow[r], o[t, a])
+        assert lrow[r] == lse[a, t]

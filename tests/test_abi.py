@@ -1,0 +1,95 @@
+"""The C-ABI library without a GPU: it builds for sm_103a, loads, exports every
+function include/mf.h declares, and rejects bad arguments on the host before any
+device work (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import packed_resolution_diffusion_pack_b300 as mf
+from packed_resolution_diffusion_pack_b300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "mf.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mf_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol():
+    lib = mf.load()
+    names = _declared()
+    assert len(names) >= 9
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings_and_version():
+    lib = mf.load()
+    for code, name in _lib.STATUS_NAMES.items():
+        assert lib.mf_status_string(code).decode() == name
+    assert lib.mf_version() == 10000
+
+
+def test_pack_size_host():
+    assert mf.pack_size([(5, 4, 6), (7, 8, 8), (3, 2, 16)]) == (135, 71)
+    assert mf.pack_size([]) == (0, 0)
+    assert mf.pack_size([(0, 0, 0), (3, 0, 5)]) == (3, 3)
+
+
+@pytest.mark.parametrize("specs,code", [
+    ([(1, 2, 3), (-1, 2, 2)], 1),
+    ([(1, -2, 3)], 1),
+    ([(0, 65536, 65536)], 3),
+    ([(2 ** 31 - 1, 0, 0), (1, 0, 0)], 3),
+])
+def test_pack_size_errors(specs, code):
+    with pytest.raises(mf.MFError) as ei:
+        mf.pack_size(specs)
+    assert ei.value.status == code
+
+
+def _fwd(lib, q=16, k=16, v=16, o=16, lse=16, cu=16, n=1, T=8, max_len=8, h=1, d=64, ws=256,
+         ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = lib.mf_attn_workspace_bytes(T, n, h, d, 0)
+    p = ctypes.c_void_p
+    return lib.mf_varlen_attn_fwd(p(q), p(k), p(v), p(cu), None, n, T, max_len, h, d, 0.0, p(o),
+                                  p(lse), p(ws), ws_bytes, None)
+
+
+def test_attn_argument_errors_on_host():
+    lib = mf.load()
+    # fake, never dereferenced addresses: every case must be rejected before launch
+    base = 1 << 20
+    a = dict(q=base, k=base + 4096, v=base + 8192, o=base + 12288, lse=base + 16384,
+             cu=base + 20480, ws=base + 24576)
+    assert _fwd(lib, **a, d=96) == 2           # head_dim unsupported
+    assert _fwd(lib, **{**a, "q": base + 8}) == 2  # misaligned tensor
+    assert _fwd(lib, **{**a, "ws": base + 64}) == 2  # misaligned workspace
+    assert _fwd(lib, **a, ws_bytes=16) == 1    # workspace too small
+    assert _fwd(lib, **a, n=-1) == 1
+    assert _fwd(lib, **a, h=0) == 1
+    assert _fwd(lib, **{**a, "cu": 0}) == 1
+    assert _fwd(lib, **{**a, "q": 0}) == 1
+    assert _fwd(lib, **a, T=2 ** 30, h=64) == 3  # heads * T overflows int32
+    assert lib.mf_attn_workspace_bytes(10, 1, 1, 96, 0) == 0
+    assert lib.mf_attn_workspace_bytes(10, 1, 2, 128, 1) > lib.mf_attn_workspace_bytes(10, 1, 2, 128, 0)
+
+
+def test_rope_argument_errors_on_host():
+    lib = mf.load()
+    p = ctypes.c_void_p
+    assert lib.mf_rope2d_qk(p(1 << 20), None, p(1 << 21), None, p(1 << 22), 4, 2, 80, None) == 2
+    assert lib.mf_rope2d_qk(p(1 << 20), None, None, None, p(1 << 22), 4, 2, 64, None) == 1
+    assert lib.mf_rope2d_qk(p(1 << 20), None, p(1 << 21), None, None, 4, 2, 64, None) == 1
+    assert lib.mf_rope2d_qk(p((1 << 20) + 2), None, p(1 << 21), None, p(1 << 22), 4, 2, 64, None) == 2
+    assert lib.mf_rope2d_qk(None, None, None, None, None, 0, 2, 64, None) == 0  # nothing to do
+
+
+def test_get_status_rejects_null():
+    assert mf.load().mf_get_status(None, None) == 1
