@@ -145,36 +145,43 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
 }
 
 // --------------------------------------------------------- dQ post-process
-// dq[t][a][:] = R(-theta(pos_t)) dq_acc[t][a][:]  (or a plain cast without pos).
+// dq[t][a][:] = R(-theta(pos_t)) dq_acc[t][a][:] (a plain cast without pos).  One
+// block handles kPostTok tokens: their (cos, sin) per rotary pair are formed once
+// in shared memory and shared by all heads; then 16-byte fp32 chunks (2 pairs) of
+// every head stream through it.
+constexpr int kPostTok = 4;
+
 template <int D>
 __global__ void __launch_bounds__(256) dq_post_kernel(const float4* __restrict__ acc,
                                                       uint2* __restrict__ dq,
-                                                      const int2* __restrict__ pos,
-                                                      int64_t rows, int32_t heads,
-                                                      const RopeFreqs f) {
-  // one thread per 4 consecutive elements = 2 rotary pairs
-  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t total = rows * (D / 4);
-  if (gid >= total) return;
-  const int64_t row = gid / (D / 4);
-  const int e4 = static_cast<int>(gid - row * (D / 4));
-  float4 x = acc[gid];
-  if (pos != nullptr) {
-    const int2 p = pos[row / heads];
-    float v[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int P = e4 * 2 + u;  // pair index in [0, D/2)
-      const float pp = static_cast<float>(P < D / 4 ? p.x : p.y);
-      float s, c;
-      rope_sincos(pp, f.omega[P % (D / 4)], f.omega_lo[P % (D / 4)], -1.f, &s, &c);
-      const float a = v[2 * u], b = v[2 * u + 1];
-      v[2 * u] = fmaf(a, c, -b * s);
-      v[2 * u + 1] = fmaf(a, s, b * c);
+                                                      const int2* __restrict__ pos, int32_t T,
+                                                      int32_t heads, const RopeFreqs f) {
+  constexpr int NP = D / 2, NF = D / 4;
+  __shared__ float2 cs[kPostTok][NP];
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kPostTok;
+  for (int i = threadIdx.x; i < kPostTok * NP; i += blockDim.x) {
+    const int tt = i / NP, P = i % NP;
+    float c = 1.f, sn = 0.f;
+    if (t0 + tt < T && pos != nullptr) {
+      const int2 p = pos[t0 + tt];
+      const float pp = static_cast<float>(P < NF ? p.x : p.y);
+      rope_sincos(pp, f.omega[P % NF], f.omega_lo[P % NF], -1.f, &sn, &c);
     }
-    x = make_float4(v[0], v[1], v[2], v[3]);
+    cs[tt][P] = make_float2(c, sn);
   }
-  dq[gid] = make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
+  __syncthreads();
+  constexpr int CPR = D / 4;  // float4 chunks per head vector
+  const int per_tok = heads * CPR;
+  const int ntok = static_cast<int>(T - t0 < kPostTok ? T - t0 : kPostTok);
+  for (int i = threadIdx.x; i < ntok * per_tok; i += blockDim.x) {
+    const int tt = i / per_tok, ch = i % per_tok;
+    const int64_t idx = (t0 + tt) * per_tok + ch;
+    const float4 x = acc[idx];
+    const int P0 = (ch % CPR) * 2;
+    const float2 r0 = cs[tt][P0], r1 = cs[tt][P0 + 1];
+    dq[idx] = make_uint2(pack_bf16x2(fmaf(x.x, r0.x, -x.y * r0.y), fmaf(x.x, r0.y, x.y * r0.x)),
+                         pack_bf16x2(fmaf(x.z, r1.x, -x.w * r1.y), fmaf(x.z, r1.y, x.w * r1.x)));
+  }
 }
 
 // --------------------------------------------------------------- main kernel
@@ -638,11 +645,10 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   if (rows > 0) {
-    const int64_t total = rows * (D / 4);
     KernelTimer kt(MF_K_DQ_POST, s);
-    dq_post_kernel<D><<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(
+    dq_post_kernel<D><<<static_cast<unsigned>((a.T + kPostTok - 1) / kPostTok), 256, 0, s>>>(
         reinterpret_cast<const float4*>(a.dq_acc), reinterpret_cast<uint2*>(a.dq),
-        reinterpret_cast<const int2*>(a.pos), rows, a.heads, f);
+        reinterpret_cast<const int2*>(a.pos), a.T, a.heads, f);
     return cudaGetLastError();
   }
   return cudaSuccess;
