@@ -169,6 +169,40 @@ mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
                              void* ws, size_t ws_bytes, mf_stream stream);
 
 /*
+ * Varlen attention forward that allocates nothing and takes no workspace.
+ * (The pages have no counterpart to this call: it is for callers of this library.)
+ * Some callers cannot allocate device memory: a plugin inside a framework that
+ * owns the device allocator and hands it only inputs and outputs, or a
+ * latency-critical loop where cudaMalloc / cudaFree, which can synchronise the
+ * device, are not allowed.  This entry point computes exactly what
+ * mf_varlen_attn_fwd computes, with the same arguments minus ws / ws_bytes; its
+ * scratch is one fixed device array inside the library, MF_NOALLOC_SCRATCH_BYTES
+ * bytes, which every GPU that loads the library holds until the process exits.
+ *  - Limits: n <= MF_NOALLOC_MAX_SAMPLES and T * heads * head_dim <=
+ *    MF_NOALLOC_MAX_ELEMS; larger problems return MF_ERR_UNSUPPORTED before any
+ *    launch (use mf_varlen_attn_fwd with a caller workspace for them).
+ *  - The first call on each device looks up the array's device address once
+ *    (cudaGetSymbolAddress, with that device current); make that first call before
+ *    any stream capture.  Later calls only reuse the cached address.
+ *  - Every call shares the one array, which keeps the previous call's contents;
+ *    the forward rewrites everything it reads from it (status word, work list,
+ *    fp16 operand copies), so no clearing is needed between calls.  Calls that
+ *    overlap on the GPU (concurrent streams, other threads) race on the array:
+ *    serialise them.
+ *  - mf_get_status cannot be used for this call (it has no workspace argument);
+ *    device-side errors are not reported back.
+ * No device memory is allocated by this call or by the library on its behalf.
+ */
+#define MF_NOALLOC_MAX_ELEMS 4194304LL   /* T * heads * head_dim */
+#define MF_NOALLOC_MAX_SAMPLES 4096
+#define MF_NOALLOC_SCRATCH_BYTES 25199616ULL
+mf_status mf_varlen_attn_fwd_noalloc(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                     const int32_t* d_cu_seqlens, const int32_t* d_pos,
+                                     int32_t n, int32_t T, int32_t max_len, int32_t heads,
+                                     int32_t head_dim, float softmax_scale, mf_bf16* o,
+                                     float* lse, mf_stream stream);
+
+/*
  * Synchronise `stream` and report device-side errors recorded in `ws` by the last
  * mf_varlen_attn_* call that used it: MF_ERR_BAD_SEQLENS, MF_ERR_TIMEOUT, or
  * MF_ERR_CUDA if the stream itself failed; MF_OK otherwise.

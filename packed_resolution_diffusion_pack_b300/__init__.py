@@ -151,6 +151,27 @@ def varlen_attn_bwd(q, k, v, o, lse, d_o, cu_seqlens, pos, max_len, softmax_scal
     return dq, dk, dv
 
 
+def varlen_attn_fwd_noalloc(q, k, v, cu_seqlens, pos, max_len, softmax_scale: float = 0.0,
+                            o=None, lse=None, stream=None):
+    """The forward without a workspace, for callers that cannot allocate device
+    memory (e.g. a plugin handed only its inputs and outputs): its scratch is a
+    fixed array inside the library (limits MF_NOALLOC_* in mf.h).  Pass `o` and
+    `lse` to keep this call itself free of allocations."""
+    torch = _torch()
+    _check_thd("q", q)
+    T, h, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        _check_thd(name, t, T, h, d)
+    n = cu_seqlens.numel() - 1
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((h, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    check(load().mf_varlen_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(pos),
+                                            n, T, int(max_len), h, d, float(softmax_scale), _ptr(o),
+                                            _ptr(lse), _stream_ptr(stream)),
+          "mf_varlen_attn_fwd_noalloc")
+    return o, lse
+
+
 def get_status(ws, stream=None) -> None:
     """Synchronise and raise MFError if the last call on this workspace recorded a
     device-side error (malformed cu_seqlens, a wait that ran out)."""

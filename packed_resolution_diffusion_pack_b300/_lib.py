@@ -33,6 +33,8 @@ SIGNATURES = {
                                           _p, _p, _p, _sz, _p]),
     "mf_varlen_attn_bwd": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32,
                                           _i32, _f32, _p, _p, _p, _p, _sz, _p]),
+    "mf_varlen_attn_fwd_noalloc": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32,
+                                                  _i32, _f32, _p, _p, _p]),
     "mf_get_status": (ctypes.c_int, [_p, _p]),
     "mf_timing_enable": (ctypes.c_int, [_i32]),
     "mf_timing_reset": (ctypes.c_int, []),
