@@ -185,30 +185,56 @@ __global__ void __launch_bounds__(256) dq_post_kernel(const float4* __restrict__
 }
 
 // --------------------------------------------------------------- main kernel
+// One CTA = one sample, one head, one 128-key tile (K', V resident in smem); it
+// walks the sample's queries in 64-row tiles i.  Per tile (b = i % 2):
+//   S^T_i  = K' Q'_i^T        M=128 keys, N=64, K=d   SS fp16   -> TMEM ST[b]
+//   dP^T_i = V dO_i^T         M=128 keys, N=64, K=d   SS bf16   -> TMEM DPT
+//   P^T_i  = exp2(S^T scale log2e - LSE log2e) (bf16 -> ST[b] columns [0,32))
+//   dS^T_i = P^T (dP^T - D) * ds_mul           (fp16 -> smem DS[b])
+//   dV    += P^T_i dO_i       M=128 keys, N=d, K=64   TS bf16
+//   dK    += dS^T_i Q'_i      M=128 keys, N=d, K=64   SS fp16
+//   dQ^T_i = K'^T dS^T_i      M=128 (d),  N=64, K=128 SS fp16   -> TMEM DQT
+// dQ is produced transposed (TMEM lane = head-dim index, column = query), so the
+// warps that add it into the fp32 accumulator write 32 consecutive floats of one
+// query row per instruction.  S^T is double-buffered and dP^T_{i+1}, S^T_{i+2}
+// are issued before the tile-i GEMMs that need the P/dS warpgroup, so that
+// warpgroup's exp/dS work overlaps the tensor core.
+//   warp 8     TMA: K', V once; (Q'_i, dO_i) through an NST-stage ring, with
+//              the tile's LSE (log2 domain) and D staged beside them.
+//   warp 9     MMA issuer (one thread).
+//   warps 0-3  thread = key row: P^T, dS^T; epilogue dV, dK (scale, R(-theta)).
+//   warps 4-7  thread = head-dim row of dQ^T: fp32 atomics into dq_acc.
+// At d = 64 the dQ^T GEMM is padded to M = 128 with a zero smem chunk (its rows
+// 64-127 are ignored).
 template <int D>
 struct BwdCfg {
-  static constexpr int BK = 128;           // keys per CTA
-  static constexpr int BQ = 128;           // queries per Q tile
-  static constexpr int CHUNK = 128 * 128;  // one 64-column chunk of a 128-row tile
-  static constexpr int TILE = 128 * D * 2;
-  static constexpr int NST = 2;            // (Q, dO) stages
+  static constexpr int BK = 128;                // keys per CTA
+  static constexpr int BQ = 64;                 // queries per tile
+  static constexpr int NST = 3;                 // (Q', dO) stages
+  static constexpr int KCHUNK = 128 * 128;      // 64-column chunk of a 128-row tile
+  static constexpr int QCHUNK = 64 * 128;       // 64-column chunk of a 64-row tile
+  static constexpr int KTILE = 128 * D * 2;     // K' or V tile
+  static constexpr int QTILE = 64 * D * 2;      // Q' or dO tile
+  static constexpr int DSTILE = 128 * 64 * 2;   // dS^T tile (one chunk)
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = TILE;
-  static constexpr int OFF_Q = 2 * TILE;              // [NST] Q tiles
-  static constexpr int OFF_DO = OFF_Q + NST * TILE;   // [NST] dO tiles
-  static constexpr int OFF_DS = OFF_DO + NST * TILE;  // dS^T 128 x 128 bf16 (2 chunks)
-  static constexpr int OFF_BAR = OFF_DS + 2 * CHUNK;
-  static constexpr int OFF_VEC = OFF_BAR + 256;       // [NST] x (lse, delta) x 128 fp32
-  static constexpr int OFF_MISC = OFF_VEC + NST * 1024;
+  static constexpr int OFF_V = KTILE;
+  static constexpr int OFF_Z = 2 * KTILE;                         // zero chunk (d = 64)
+  static constexpr int OFF_Q = OFF_Z + (D == 64 ? KCHUNK : 0);    // [NST]
+  static constexpr int OFF_DO = OFF_Q + NST * QTILE;              // [NST]
+  static constexpr int OFF_DS = OFF_DO + NST * QTILE;             // [2]
+  static constexpr int OFF_VEC = OFF_DS + 2 * DSTILE;             // [NST] x (lse, D) x 64
+  static constexpr int OFF_BAR = OFF_VEC + NST * 512;
+  static constexpr int OFF_MISC = OFF_BAR + 256;
   static constexpr int SMEM = OFF_MISC + 64;
-  static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 256 + D;
+  static constexpr uint32_t COL_ST0 = 0, COL_ST1 = 64, COL_DPT = 128, COL_DQT = 192;
+  static constexpr uint32_t COL_DV = 256, COL_DK = 256 + D;
   // fp16 where Q', K' and the scaled dS meet; bf16 where the caller's V and dO do
   // (gradient-sized values keep bf16's range there).
-  static constexpr uint32_t IDESC_S = idesc_f32acc(128, 128, kF16, 0, 0);    // S^T = K'Q'^T
-  static constexpr uint32_t IDESC_DK = idesc_f32acc(128, D, kF16, 0, 1);     // dK += dS^T Q'
-  static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, D, kF16, 1, 1);     // dQ = dS K'
-  static constexpr uint32_t IDESC_DP = idesc_f32acc(128, 128, kBF16, 0, 0);  // dP^T = V dO^T
-  static constexpr uint32_t IDESC_DV = idesc_f32acc(128, D, kBF16, 0, 1);    // dV += P^T dO
+  static constexpr uint32_t IDESC_S = idesc_f32acc(128, 64, kF16, 0, 0);     // S^T
+  static constexpr uint32_t IDESC_DP = idesc_f32acc(128, 64, kBF16, 0, 0);   // dP^T
+  static constexpr uint32_t IDESC_DV = idesc_f32acc(128, D, kBF16, 0, 1);    // dV
+  static constexpr uint32_t IDESC_DK = idesc_f32acc(128, D, kF16, 0, 1);     // dK
+  static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, 64, kF16, 1, 1);    // dQ^T
 };
 
 struct BwdParams {
@@ -262,18 +288,17 @@ __global__ void __launch_bounds__(320, 1)
     if (threadIdx.x == 0) atomicOr(p.status, kFlagSmemAlign);
     return;
   }
-  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sZ = sbase + C::OFF_Z;
   const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO, sDS = sbase + C::OFF_DS;
-  uint8_t* gDS = gbase + C::OFF_DS;
-  // per stage: lse (log2 domain) at [st*256, +128), delta at [st*256+128, +128)
+  // per stage: lse (log2 domain) at [st*128, +64), D at [st*128+64, +64)
   float* vec = reinterpret_cast<float*>(gbase + C::OFF_VEC);
   const uint32_t bars = sbase + C::OFF_BAR;
   const uint32_t bar_kv = bars;
   const uint32_t bar_full = bars + 8;                // [NST]
   const uint32_t bar_empty = bar_full + 8 * C::NST;  // [NST]
-  const uint32_t bar_st = bar_empty + 8 * C::NST;
-  const uint32_t bar_dpt = bar_st + 8;
-  const uint32_t bar_ds = bar_dpt + 8;
+  const uint32_t bar_st = bar_empty + 8 * C::NST;    // [2]
+  const uint32_t bar_dp = bar_st + 16;
+  const uint32_t bar_ds = bar_dp + 8;
   const uint32_t bar_dq = bar_ds + 8;
   const uint32_t bar_dq_empty = bar_dq + 8;
   const uint32_t bar_done = bar_dq_empty + 8;
@@ -291,7 +316,8 @@ __global__ void __launch_bounds__(320, 1)
         mbar_init(bar_empty + 8 * i, 1);
       }
       mbar_init(bar_st, 1);
-      mbar_init(bar_dpt, 1);
+      mbar_init(bar_st + 8, 1);
+      mbar_init(bar_dp, 1);
       mbar_init(bar_ds, 128);
       mbar_init(bar_dq, 1);
       mbar_init(bar_dq_empty, 128);
@@ -299,6 +325,11 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bar_drain, 1);
       fence_mbar_init();
     }
+  }
+  if (D == 64) {  // zero chunk padding the dQ^T GEMM to M = 128
+    uint4* z = reinterpret_cast<uint4*>(gbase + C::OFF_Z);
+    for (int i = threadIdx.x; i < C::KCHUNK / 16; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
   }
   __syncthreads();
   if (!s_valid) return;
@@ -312,22 +343,22 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = s_tmem;
   const WorkItemB w = s_w;
   const int32_t k0 = w.blk * C::BK;                // first key (in sample)
-  const int32_t nq = (w.len + C::BQ - 1) / C::BQ;  // Q tiles
+  const int32_t nq = (w.len + C::BQ - 1) / C::BQ;  // query tiles
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    // Lane 0 issues the tile copies; all 32 lanes stage the Q tile's LSE (log2
+    // Lane 0 issues the tile copies; all 32 lanes stage the tile's LSE (log2
     // domain; +inf past the sample, so P = 0 there) and D (0 past the sample)
-    // into the stage's vectors and arrive on its full barrier.
+    // and arrive on its full barrier.
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
+      mbar_arrive_expect_tx(bar_kv, 2 * C::KTILE);
       for (int ch = 0; ch < D / 64; ++ch) {
-        tma_load_3d(sK + ch * C::CHUNK, &tm_k, bar_kv, ch * 64, w.head, w.start + k0);
-        tma_load_3d(sV + ch * C::CHUNK, &tm_v, bar_kv, ch * 64, w.head, w.start + k0);
+        tma_load_3d(sK + ch * C::KCHUNK, &tm_k, bar_kv, ch * 64, w.head, w.start + k0);
+        tma_load_3d(sV + ch * C::KCHUNK, &tm_v, bar_kv, ch * 64, w.head, w.start + k0);
       }
     }
     __syncwarp();
@@ -341,20 +372,20 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int q = static_cast<int>(lane) * 4 + u;
+      for (int u = 0; u < 2; ++u) {
+        const int q = static_cast<int>(lane) * 2 + u;
         const int32_t qi = i * C::BQ + q;
         const bool q_ok = qi < w.len;
         const int64_t g = static_cast<int64_t>(w.head) * p.T + w.start + qi;
-        vec[st * 256 + q] = q_ok ? p.lse[g] * 1.4426950408889634f : INFINITY;
-        vec[st * 256 + 128 + q] = q_ok ? p.delta[g] : 0.f;
+        vec[st * 128 + q] = q_ok ? p.lse[g] * 1.4426950408889634f : INFINITY;
+        vec[st * 128 + 64 + q] = q_ok ? p.delta[g] : 0.f;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar_full + 8 * st, 2 * C::TILE);
+        mbar_arrive_expect_tx(bar_full + 8 * st, 2 * C::QTILE);
         for (int ch = 0; ch < D / 64; ++ch) {
-          tma_load_3d(sQ + st * C::TILE + ch * C::CHUNK, &tm_q, bar_full + 8 * st, ch * 64,
+          tma_load_3d(sQ + st * C::QTILE + ch * C::QCHUNK, &tm_q, bar_full + 8 * st, ch * 64,
                       w.head, w.start + i * C::BQ);
-          tma_load_3d(sDO + st * C::TILE + ch * C::CHUNK, &tm_do, bar_full + 8 * st, ch * 64,
+          tma_load_3d(sDO + st * C::QTILE + ch * C::QCHUNK, &tm_do, bar_full + 8 * st, ch * 64,
                       w.head, w.start + i * C::BQ);
         }
       } else {
@@ -375,47 +406,69 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         return r;
       };
-      auto desc_k = [](uint32_t base, int kk) {  // K-major operand, K-step kk of 16
-        return sdesc_sw128(base + (kk >> 2) * C::CHUNK + (kk & 3) * 32, 16, 1024);
+      // K-major operand, K-step kk of 16 elements; `chunk` = bytes per 64-col chunk
+      auto desc_k = [](uint32_t base, int kk, uint32_t chunk) {
+        return sdesc_sw128(base + (kk >> 2) * chunk + (kk & 3) * 32, 16, 1024);
       };
-      auto desc_mn = [](uint32_t base, int kk) {  // MN-major operand, K-step kk of 16 rows
-        return sdesc_sw128(base + kk * 2048, C::CHUNK, 1024);
+      // MN-major operand, K-step kk of 16 rows; `lbo` = bytes between 64-wide atoms
+      auto desc_mn = [](uint32_t base, int kk, uint32_t lbo) {
+        return sdesc_sw128(base + kk * 2048, lbo, 1024);
       };
-      auto issue_st = [&](int32_t i) {  // S^T = K Q_i^T
-        const uint32_t q = sQ + (i % C::NST) * C::TILE;
+      auto full = [&](int32_t i) {
+        return wait(bar_full + 8 * (i % C::NST), (i / C::NST) & 1);
+      };
+      auto issue_st = [&](int32_t i) {  // S^T_i = K' Q'_i^T -> ST[i % 2]
+        const uint32_t q = sQ + (i % C::NST) * C::QTILE;
+        const uint32_t d = tmem + ((i & 1) ? C::COL_ST1 : C::COL_ST0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::COL_ST, desc_k(sK, kk), desc_k(q, kk), C::IDESC_S, kk > 0);
-        mma_commit(bar_st);
+          mma_ss(d, desc_k(sK, kk, C::KCHUNK), desc_k(q, kk, C::QCHUNK), C::IDESC_S, kk > 0);
+        mma_commit(bar_st + 8 * (i & 1));
       };
-      bool ok = wait(bar_kv, 0) && wait(bar_full, 0);
-      if (ok) issue_st(0);
+      auto issue_dp = [&](int32_t i) {  // dP^T_i = V dO_i^T -> DPT
+        const uint32_t o = sDO + (i % C::NST) * C::QTILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::COL_DPT, desc_k(sV, kk, C::KCHUNK), desc_k(o, kk, C::QCHUNK),
+                 C::IDESC_DP, kk > 0);
+        mma_commit(bar_dp);
+      };
+      bool ok = wait(bar_kv, 0) && full(0);
+      if (ok) {
+        issue_st(0);
+        issue_dp(0);
+        if (nq > 1) {
+          ok = full(1);
+          if (ok) issue_st(1);
+        }
+      }
       for (int32_t i = 0; i < nq && ok; ++i) {
         const int32_t st = i % C::NST;
-        const uint32_t q = sQ + st * C::TILE, dO = sDO + st * C::TILE;
+        const uint32_t q = sQ + st * C::QTILE, o = sDO + st * C::QTILE;
+        const uint32_t stb = tmem + ((i & 1) ? C::COL_ST1 : C::COL_ST0);
+        const uint32_t ds = sDS + (i & 1) * C::DSTILE;
+        if (!(ok = wait(bar_ds, i & 1))) break;  // P^T_i in TMEM, dS^T_i in smem
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk)  // dV += P^T_i dO_i
+          mma_ts(tmem + C::COL_DV, stb + kk * 8, desc_mn(o, kk, C::QCHUNK), C::IDESC_DV,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T_i Q'_i
+          mma_ss(tmem + C::COL_DK, desc_k(ds, kk, C::DSTILE), desc_mn(q, kk, C::QCHUNK),
+                 C::IDESC_DK, (i > 0 || kk > 0) ? 1u : 0u);
+        if (i + 1 < nq) issue_dp(i + 1);  // DPT was read before bar_ds(i)
         if (i > 0 && !(ok = wait(bar_dq_empty, (i - 1) & 1))) break;
+        const uint32_t lbo_a = D == 128 ? static_cast<uint32_t>(C::KCHUNK) : (sZ - sK);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)  // dP^T = V dO_i^T
-          mma_ss(tmem + C::COL_DPT, desc_k(sV, kk), desc_k(dO, kk), C::IDESC_DP, kk > 0);
-        mma_commit(bar_dpt);
-        if (!(ok = wait(bar_ds, i & 1))) break;
-#pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)  // dV += P^T dO_i
-          mma_ts(tmem + C::COL_DV, tmem + C::COL_ST + kk * 8, desc_mn(dO, kk), C::IDESC_DV,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        if (i + 1 < nq) {
-          if (!(ok = wait(bar_full + 8 * ((i + 1) % C::NST), ((i + 1) / C::NST) & 1))) break;
-          issue_st(i + 1);
-        }
-#pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T Q_i
-          mma_ss(tmem + C::COL_DK, desc_k(sDS, kk), desc_mn(q, kk), C::IDESC_DK,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ_i = dS K
-          mma_ss(tmem + C::COL_DPT, desc_mn(sDS, kk), desc_mn(sK, kk), C::IDESC_DQ, kk > 0);
+        for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ^T_i = K'^T dS^T_i
+          mma_ss(tmem + C::COL_DQT, desc_mn(sK, kk, lbo_a), desc_mn(ds, kk, C::DSTILE),
+                 C::IDESC_DQ, kk > 0);
         mma_commit(bar_dq);
-        mma_commit(bar_empty + 8 * st);
+        mma_commit(bar_empty + 8 * st);  // Q'_i, dO_i no longer read
+        if (i + 2 < nq) {  // ST[i % 2] is free once dV_i (issued above) has read P^T_i
+          if (!(ok = full(i + 2))) break;
+          issue_st(i + 2);
+        }
       }
       if (ok) {
         mma_commit(bar_done);
@@ -430,7 +483,6 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------ P / dS warpgroup (keys)
     const uint32_t row = threadIdx.x;  // key row in the tile = TMEM lane
     const uint32_t lane_off = ((warp & 3) * 32) << 16;
-    const uint32_t tST = tmem + lane_off + C::COL_ST;
     const uint32_t tDPT = tmem + lane_off + C::COL_DPT;
     const bool key_ok = k0 + static_cast<int32_t>(row) < w.len;
     const float sl2 = p.scale_log2;
@@ -440,42 +492,54 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     for (int32_t i = 0; i < nq; ++i) {
       const int32_t st = i % C::NST;
+      const uint32_t tST = tmem + lane_off + ((i & 1) ? C::COL_ST1 : C::COL_ST0);
+      uint8_t* gds = gbase + C::OFF_DS + (i & 1) * C::DSTILE;
       ok = __all_sync(0xffffffffu, mbar_wait(bar_full + 8 * st, (i / C::NST) & 1, &s_abort) &&
-                                       mbar_wait(bar_st, i & 1, &s_abort) &&
-                                       mbar_wait(bar_dpt, i & 1, &s_abort));
+                                       mbar_wait(bar_st + 8 * (i & 1), (i >> 1) & 1, &s_abort));
       if (!ok) break;
       tc_fence_after();
-      const float* vl = vec + st * 256;
-      const float* vd = vl + 128;
-      // 32 queries at a time: P^T (bf16) goes to TMEM columns [16c, 16c+16), which
-      // hold S^T values already read; dS^T to smem, 128B-swizzled K-major:
-      // chunk = q / 64, 16-byte unit (q % 64) / 8 stored at unit ^ (row % 8).
+      const float* vl = vec + st * 128;
+      const float* vd = vl + 64;
+      // P^T: 64 queries; bf16 into ST columns [0, 32) (S^T values already read)
+      float pr[64];
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tST, r0);
+        tmem_ld32(tST + 32, r1);
+        tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t rs[32], rd[32];
-        tmem_ld32(tST + c * 32, rs);
+        for (int c = 0; c < 32; ++c) {
+          pr[c] = key_ok ? ex2_approx(fmaf(__uint_as_float(r0[c]), sl2, -vl[c])) : 0.f;
+          pr[32 + c] = key_ok ? ex2_approx(fmaf(__uint_as_float(r1[c]), sl2, -vl[32 + c])) : 0.f;
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) pk[u] = pack_bf16x2(pr[2 * u], pr[2 * u + 1]);
+        tmem_st32(tST, pk);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dp, i & 1, &s_abort));
+      if (!ok) break;
+      tc_fence_after();
+      // dS^T row -> smem DS[i % 2], 128B-swizzled K-major [key][query]: 16-byte
+      // unit u (queries 8u..8u+7) stored at u ^ (row % 8)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t rd[32];
         tmem_ld32(tDPT + c * 32, rd);
         tmem_wait_ld();
-        uint32_t pp[16], pd[16];
+        uint32_t pd[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int q0 = c * 32 + 2 * u;
-          const float p0 = key_ok ? ex2_approx(fmaf(__uint_as_float(rs[2 * u]), sl2, -vl[q0])) : 0.f;
-          const float p1 =
-              key_ok ? ex2_approx(fmaf(__uint_as_float(rs[2 * u + 1]), sl2, -vl[q0 + 1])) : 0.f;
-          pp[u] = pack_bf16x2(p0, p1);
-          const float ds0 = p0 * ds_mul * (__uint_as_float(rd[2 * u]) - vd[q0]);
-          const float ds1 = p1 * ds_mul * (__uint_as_float(rd[2 * u + 1]) - vd[q0 + 1]);
+          const float ds0 = pr[q0] * ds_mul * (__uint_as_float(rd[2 * u]) - vd[q0]);
+          const float ds1 = pr[q0 + 1] * ds_mul * (__uint_as_float(rd[2 * u + 1]) - vd[q0 + 1]);
           dsmax = fmaxf(dsmax, fmaxf(fabsf(ds0), fabsf(ds1)));
           pd[u] = pack_f16x2(ds0, ds1);
         }
-        tmem_st16(tST + c * 16, pp);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int q = c * 32 + u * 8;  // first query of this 16-byte unit
-          const int chunk = q >> 6, unit = (q & 63) >> 3;
-          uint4* dst = reinterpret_cast<uint4*>(gDS + chunk * C::CHUNK + row * 128 +
-                                                ((unit ^ (row & 7)) << 4));
+          const int unit = c * 4 + u;
+          uint4* dst = reinterpret_cast<uint4*>(gds + row * 128 + ((unit ^ (row & 7)) << 4));
           *dst = make_uint4(pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
         }
       }
@@ -545,11 +609,14 @@ __global__ void __launch_bounds__(320, 1)
       atomicOr(p.status, kFlagTimeout);
     }
   } else {
-    // --------------------------------------------------- dQ warpgroup (queries)
-    const uint32_t row = threadIdx.x & 127;  // query row in the Q tile = TMEM lane
+    // ------------------------------------------ dQ^T warpgroup (head-dim rows)
+    const uint32_t e = threadIdx.x & 127;  // head-dim index = TMEM lane of dQ^T
     const uint32_t lane_off = ((warp & 3) * 32) << 16;
+    const bool e_ok = e < static_cast<uint32_t>(D);
     // softmax scale over the power-of-two dS staging scale (exact division)
     const float dq_mul = p.scale / ds_scale_for(p.hmax[w.head], p.hmax[p.heads + w.head]);
+    float* col0 = p.dq_acc + (static_cast<int64_t>(w.start) * p.heads + w.head) * D + e;
+    const int64_t qstride = static_cast<int64_t>(p.heads) * D;
     for (int32_t i = 0; i < nq; ++i) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, &s_abort));
       if (!ok) {
@@ -558,27 +625,23 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       tc_fence_after();
-      const int32_t qi = i * C::BQ + static_cast<int32_t>(row);
-      const bool q_ok = qi < w.len;
-      float4* dst = reinterpret_cast<float4*>(
-          p.dq_acc + ((static_cast<int64_t>(w.start) + qi) * p.heads + w.head) * D);
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + C::COL_DPT + cc * 32, r);
-        tmem_wait_ld();
-        if (q_ok) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            atomicAdd(dst + cc * 8 + u,
-                      make_float4(__uint_as_float(r[4 * u]) * dq_mul,
-                                  __uint_as_float(r[4 * u + 1]) * dq_mul,
-                                  __uint_as_float(r[4 * u + 2]) * dq_mul,
-                                  __uint_as_float(r[4 * u + 3]) * dq_mul));
-        }
-      }
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tmem + lane_off + C::COL_DQT, r0);
+      tmem_ld32(tmem + lane_off + C::COL_DQT + 32, r1);
+      tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar_dq_empty);
+      const int32_t nvalid = min(C::BQ, w.len - i * C::BQ);
+      if (e_ok) {
+        float* dst = col0 + static_cast<int64_t>(i) * C::BQ * qstride;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c < nvalid) atomicAdd(dst + c * qstride, __uint_as_float(r0[c]) * dq_mul);
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (32 + c < nvalid)
+            atomicAdd(dst + (32 + c) * qstride, __uint_as_float(r1[c]) * dq_mul);
+      }
     }
   }
   tc_fence_before();
@@ -612,10 +675,10 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   CUtensorMap tq, tk, tv, tdo;
-  if (!make_tmap_thd(&tq, a.q, a.T, a.heads, D, 128, true) ||
-      !make_tmap_thd(&tk, a.k, a.T, a.heads, D, 128, true) ||
-      !make_tmap_thd(&tv, a.v, a.T, a.heads, D, 128) ||
-      !make_tmap_thd(&tdo, a.d_o, a.T, a.heads, D, 128))
+  if (!make_tmap_thd(&tq, a.q, a.T, a.heads, D, C::BQ, true) ||
+      !make_tmap_thd(&tk, a.k, a.T, a.heads, D, C::BK, true) ||
+      !make_tmap_thd(&tv, a.v, a.T, a.heads, D, C::BK) ||
+      !make_tmap_thd(&tdo, a.d_o, a.T, a.heads, D, C::BQ))
     return cudaErrorInvalidValue;
   BwdParams p;
   p.cu = a.cu;
