@@ -65,10 +65,11 @@ __device__ __forceinline__ bool find_item_b(const int32_t* __restrict__ cu,
 
 // ------------------------------------------------------------- preprocess
 // Rows are (token, head) pairs in THD order; 8 lanes per row, each covering D/8
-// elements.  Per row: D = <dO, O> -> delta[h][t]; the row of the fp32 dQ
-// accumulator zeroed; ||dO|| and ||v|| folded into per-head maxima (shared memory
-// per block, then one atomicMax per head: non-negative floats order like their
-// bit patterns).
+// elements.  Per row: D = <dO, O> -> delta[h][t]; LSE * log2 e -> lse2[h][t]; the
+// row of the fp32 dQ accumulator zeroed; ||dO|| and ||v|| folded into per-head
+// maxima (shared memory per block, then one atomicMax per head: non-negative
+// floats order like their bit patterns).  Block 0 also writes the pad rows
+// (64 x +inf as LSE, 64 x 0 as D) that stand in for query rows past a sample.
 constexpr int kPreRowsPerBlock = 512;
 constexpr int kPreMaxHeads = 256;
 
@@ -85,7 +86,10 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ o,
                                                       const uint4* __restrict__ d_o,
                                                       const uint4* __restrict__ v,
+                                                      const float* __restrict__ lse,
+                                                      float* __restrict__ lse2,
                                                       float* __restrict__ delta,
+                                                      float* __restrict__ pad,
                                                       float4* __restrict__ dq_acc,
                                                       float* __restrict__ hmax, int64_t rows,
                                                       int32_t T, int32_t heads) {
@@ -93,6 +97,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
   __shared__ float s_max[2 * kPreMaxHeads];
   const bool smem_max = heads <= kPreMaxHeads;
   for (int i = threadIdx.x; i < 2 * kPreMaxHeads; i += blockDim.x) s_max[i] = 0.f;
+  if (blockIdx.x == 0 && threadIdx.x < 128) pad[threadIdx.x] = threadIdx.x < 64 ? INFINITY : 0.f;
   __syncthreads();
   const int sub = threadIdx.x & 7;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kPreRowsPerBlock;
@@ -122,7 +127,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
     if (ok && sub == 0) {
       const int64_t t = row / heads;
       const int32_t a = static_cast<int32_t>(row - t * heads);
-      delta[static_cast<int64_t>(a) * T + t] = acc;
+      const int64_t g = static_cast<int64_t>(a) * T + t;
+      delta[g] = acc;
+      lse2[g] = lse[g] * 1.4426950408889634f;
       const unsigned bdo = __float_as_uint(sqrtf(ndo)), bv = __float_as_uint(sqrtf(nv));
       if (smem_max) {
         atomicMax(reinterpret_cast<unsigned*>(&s_max[a]), bdo);
@@ -194,16 +201,20 @@ __global__ void __launch_bounds__(256) dq_post_kernel(const float4* __restrict__
 //   dV    += P^T_i dO_i       M=128 keys, N=d, K=64   TS bf16
 //   dK    += dS^T_i Q'_i      M=128 keys, N=d, K=64   SS fp16
 //   dQ^T_i = K'^T dS^T_i      M=128 (d),  N=64, K=128 SS fp16   -> TMEM DQT
-// dQ is produced transposed (TMEM lane = head-dim index, column = query), so the
-// warps that add it into the fp32 accumulator write 32 consecutive floats of one
-// query row per instruction.  S^T is double-buffered and dP^T_{i+1}, S^T_{i+2}
-// are issued before the tile-i GEMMs that need the P/dS warpgroup, so that
-// warpgroup's exp/dS work overlaps the tensor core.
-//   warp 8     TMA: K', V once; (Q'_i, dO_i) through an NST-stage ring, with
-//              the tile's LSE (log2 domain) and D staged beside them.
+// dQ is produced transposed (TMEM lane = head-dim index, column = query): the
+// warps that drain it write a [query][d] fp32 tile to shared memory with
+// conflict-free stores, and one thread adds the tile into the fp32 accumulator
+// with a TMA reduce-add (rows past the sample are zero, so they add nothing).
+// S^T is double-buffered; the (Q', dO) stage of tile i is released as soon as
+// dV_i and dK_i (its last readers) are issued, and dP^T_{i+1} and S^T_{i+2} are
+// issued ahead of the GEMMs that need the P/dS warpgroup, so that warpgroup's
+// exp/dS work overlaps the tensor core.
+//   warp 8     TMA: K', V once; (Q'_i, dO_i) through an NST-stage ring; the
+//              lanes copy the tile's LSE * log2 e and D rows beside them with
+//              cp.async (pad rows past the sample), all on the stage barrier.
 //   warp 9     MMA issuer (one thread).
 //   warps 0-3  thread = key row: P^T, dS^T; epilogue dV, dK (scale, R(-theta)).
-//   warps 4-7  thread = head-dim row of dQ^T: fp32 atomics into dq_acc.
+//   warps 4-7  thread = head-dim row of dQ^T: smem tile + TMA reduce-add.
 // At d = 64 the dQ^T GEMM is padded to M = 128 with a zero smem chunk (its rows
 // 64-127 are ignored).
 template <int D>
@@ -216,13 +227,15 @@ struct BwdCfg {
   static constexpr int KTILE = 128 * D * 2;     // K' or V tile
   static constexpr int QTILE = 64 * D * 2;      // Q' or dO tile
   static constexpr int DSTILE = 128 * 64 * 2;   // dS^T tile (one chunk)
+  static constexpr int DQTILE = BQ * D * 4;     // fp32 dQ staging tile [query][d]
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KTILE;
   static constexpr int OFF_Z = 2 * KTILE;                         // zero chunk (d = 64)
   static constexpr int OFF_Q = OFF_Z + (D == 64 ? KCHUNK : 0);    // [NST]
   static constexpr int OFF_DO = OFF_Q + NST * QTILE;              // [NST]
   static constexpr int OFF_DS = OFF_DO + NST * QTILE;             // [2]
-  static constexpr int OFF_VEC = OFF_DS + 2 * DSTILE;             // [NST] x (lse, D) x 64
+  static constexpr int OFF_DQ = OFF_DS + 2 * DSTILE;
+  static constexpr int OFF_VEC = OFF_DQ + DQTILE;                 // [NST] x (lse2, D) x 64
   static constexpr int OFF_BAR = OFF_VEC + NST * 512;
   static constexpr int OFF_MISC = OFF_BAR + 256;
   static constexpr int SMEM = OFF_MISC + 64;
@@ -236,16 +249,17 @@ struct BwdCfg {
   static constexpr uint32_t IDESC_DK = idesc_f32acc(128, D, kF16, 0, 1);     // dK
   static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, 64, kF16, 1, 1);    // dQ^T
 };
+static_assert(BwdCfg<128>::SMEM <= 232448, "backward shared memory over the per-CTA limit");
 
 struct BwdParams {
   const int32_t* cu;
   const int32_t* order;
   const int32_t* prefix;
   const int32_t* pos;
-  const float* lse;
+  const float* lse2;
   const float* delta;
+  const float* pad;
   uint32_t* status;
-  float* dq_acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int32_t n, T, heads;
@@ -272,7 +286,8 @@ __global__ void __launch_bounds__(320, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using C = BwdCfg<D>;
   // All shared memory is dynamic (no static __shared__), so its base is the
   // start of the CTA's window: 1024-byte aligned, as the 128B-swizzled tiles need.
@@ -290,8 +305,9 @@ __global__ void __launch_bounds__(320, 1)
   }
   const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sZ = sbase + C::OFF_Z;
   const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO, sDS = sbase + C::OFF_DS;
-  // per stage: lse (log2 domain) at [st*128, +64), D at [st*128+64, +64)
-  float* vec = reinterpret_cast<float*>(gbase + C::OFF_VEC);
+  const uint32_t sDQ = sbase + C::OFF_DQ, sVEC = sbase + C::OFF_VEC;
+  // per stage: lse2 at [st*128, +64), D at [st*128+64, +64)
+  const float* vec = reinterpret_cast<const float*>(gbase + C::OFF_VEC);
   const uint32_t bars = sbase + C::OFF_BAR;
   const uint32_t bar_kv = bars;
   const uint32_t bar_full = bars + 8;                // [NST]
@@ -312,7 +328,8 @@ __global__ void __launch_bounds__(320, 1)
     if (s_valid) {
       mbar_init(bar_kv, 1);
       for (int i = 0; i < C::NST; ++i) {
-        mbar_init(bar_full + 8 * i, 32);  // the producer warp's 32 lanes (+ TMA bytes)
+        // 32 cp.async arrivals (LSE / D rows) + the TMA issuer's expect-tx arrival
+        mbar_init(bar_full + 8 * i, 33);
         mbar_init(bar_empty + 8 * i, 1);
       }
       mbar_init(bar_st, 1);
@@ -347,9 +364,6 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
-    // Lane 0 issues the tile copies; all 32 lanes stage the tile's LSE (log2
-    // domain; +inf past the sample, so P = 0 there) and D (0 past the sample)
-    // and arrive on its full barrier.
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -362,6 +376,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     __syncwarp();
+    const int64_t gbase_row = static_cast<int64_t>(w.head) * p.T + w.start;
     int32_t issued = 0;
     for (int32_t i = 0; i < nq; ++i) {
       const int32_t st = i % C::NST, use = i / C::NST;
@@ -371,15 +386,6 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0) atomicOr(p.status, kFlagTimeout);
         break;
       }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int q = static_cast<int>(lane) * 2 + u;
-        const int32_t qi = i * C::BQ + q;
-        const bool q_ok = qi < w.len;
-        const int64_t g = static_cast<int64_t>(w.head) * p.T + w.start + qi;
-        vec[st * 128 + q] = q_ok ? p.lse[g] * 1.4426950408889634f : INFINITY;
-        vec[st * 128 + 64 + q] = q_ok ? p.delta[g] : 0.f;
-      }
       if (lane == 0) {
         mbar_arrive_expect_tx(bar_full + 8 * st, 2 * C::QTILE);
         for (int ch = 0; ch < D / 64; ++ch) {
@@ -388,9 +394,16 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_3d(sDO + st * C::QTILE + ch * C::QCHUNK, &tm_do, bar_full + 8 * st, ch * 64,
                       w.head, w.start + i * C::BQ);
         }
-      } else {
-        mbar_arrive(bar_full + 8 * st);
       }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = static_cast<int>(lane) * 2 + u;
+        const int32_t qi = i * C::BQ + q;
+        const bool q_ok = qi < w.len;
+        cp_async_4(sVEC + st * 512 + q * 4, q_ok ? p.lse2 + gbase_row + qi : p.pad + q);
+        cp_async_4(sVEC + st * 512 + 256 + q * 4, q_ok ? p.delta + gbase_row + qi : p.pad + 64 + q);
+      }
+      cp_async_arrive_noinc(bar_full + 8 * st);
       ++issued;
     }
     if (lane == 0) {
@@ -456,7 +469,8 @@ __global__ void __launch_bounds__(320, 1)
         for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T_i Q'_i
           mma_ss(tmem + C::COL_DK, desc_k(ds, kk, C::DSTILE), desc_mn(q, kk, C::QCHUNK),
                  C::IDESC_DK, (i > 0 || kk > 0) ? 1u : 0u);
-        if (i + 1 < nq) issue_dp(i + 1);  // DPT was read before bar_ds(i)
+        mma_commit(bar_empty + 8 * st);  // Q'_i, dO_i no longer read
+        if (i + 1 < nq) issue_dp(i + 1);  // DPT was read before bar_ds(i); stage i+1 landed
         if (i > 0 && !(ok = wait(bar_dq_empty, (i - 1) & 1))) break;
         const uint32_t lbo_a = D == 128 ? static_cast<uint32_t>(C::KCHUNK) : (sZ - sK);
 #pragma unroll
@@ -464,7 +478,6 @@ __global__ void __launch_bounds__(320, 1)
           mma_ss(tmem + C::COL_DQT, desc_mn(sK, kk, lbo_a), desc_mn(ds, kk, C::DSTILE),
                  C::IDESC_DQ, kk > 0);
         mma_commit(bar_dq);
-        mma_commit(bar_empty + 8 * st);  // Q'_i, dO_i no longer read
         if (i + 2 < nq) {  // ST[i % 2] is free once dV_i (issued above) has read P^T_i
           if (!(ok = full(i + 2))) break;
           issue_st(i + 2);
@@ -498,19 +511,33 @@ __global__ void __launch_bounds__(320, 1)
                                        mbar_wait(bar_st + 8 * (i & 1), (i >> 1) & 1, &s_abort));
       if (!ok) break;
       tc_fence_after();
-      const float* vl = vec + st * 128;
-      const float* vd = vl + 64;
-      // P^T: 64 queries; bf16 into ST columns [0, 32) (S^T values already read)
+      const float4* vl4 = reinterpret_cast<const float4*>(vec + st * 128);
+      const float4* vd4 = vl4 + 16;
+      // P^T: 64 queries; bf16 into ST columns [0, 32) (S^T values already read).
+      // Key rows past the sample get P = 0 (their S^T holds another sample's keys).
       float pr[64];
       {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tST, r0);
-        tmem_ld32(tST + 32, r1);
-        tmem_wait_ld();
+        uint32_t r[64];
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tST, r0);
+          tmem_ld32(tST + 32, r1);
+          tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          pr[c] = key_ok ? ex2_approx(fmaf(__uint_as_float(r0[c]), sl2, -vl[c])) : 0.f;
-          pr[32 + c] = key_ok ? ex2_approx(fmaf(__uint_as_float(r1[c]), sl2, -vl[32 + c])) : 0.f;
+          for (int c = 0; c < 32; ++c) {
+            r[c] = r0[c];
+            r[32 + c] = r1[c];
+          }
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l = vl4[c4];
+          const float ls[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float e = ex2_approx(fmaf(__uint_as_float(r[4 * c4 + u]), sl2, -ls[u]));
+            pr[4 * c4 + u] = key_ok ? e : 0.f;
+          }
         }
         uint32_t pk[32];
 #pragma unroll
@@ -529,12 +556,18 @@ __global__ void __launch_bounds__(320, 1)
         tmem_wait_ld();
         uint32_t pd[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int q0 = c * 32 + 2 * u;
-          const float ds0 = pr[q0] * ds_mul * (__uint_as_float(rd[2 * u]) - vd[q0]);
-          const float ds1 = pr[q0 + 1] * ds_mul * (__uint_as_float(rd[2 * u + 1]) - vd[q0 + 1]);
-          dsmax = fmaxf(dsmax, fmaxf(fabsf(ds0), fabsf(ds1)));
-          pd[u] = pack_f16x2(ds0, ds1);
+        for (int u4 = 0; u4 < 8; ++u4) {
+          const float4 dd = vd4[c * 8 + u4];
+          const float ds[4] = {dd.x, dd.y, dd.z, dd.w};
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int q0 = c * 32 + u4 * 4 + 2 * h;
+            const float ds0 = pr[q0] * ds_mul * (__uint_as_float(rd[u4 * 4 + 2 * h]) - ds[2 * h]);
+            const float ds1 =
+                pr[q0 + 1] * ds_mul * (__uint_as_float(rd[u4 * 4 + 2 * h + 1]) - ds[2 * h + 1]);
+            dsmax = fmaxf(dsmax, fmaxf(fabsf(ds0), fabsf(ds1)));
+            pd[u4 * 2 + h] = pack_f16x2(ds0, ds1);
+          }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -610,39 +643,53 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     // ------------------------------------------ dQ^T warpgroup (head-dim rows)
+    // Per tile: dQ^T from TMEM (thread e = head-dim index), scaled, written as
+    // a [query][d] fp32 tile (rows past the sample = 0) to the staging buffer;
+    // one thread adds the tile into the accumulator with a TMA reduce-add.  The
+    // four warps agree on every step with a barrier-reduction, so a wait that
+    // ran out in one of them stops all of them at the same point.
     const uint32_t e = threadIdx.x & 127;  // head-dim index = TMEM lane of dQ^T
     const uint32_t lane_off = ((warp & 3) * 32) << 16;
     const bool e_ok = e < static_cast<uint32_t>(D);
+    const bool leader = threadIdx.x == 128;
     // softmax scale over the power-of-two dS staging scale (exact division)
     const float dq_mul = p.scale / ds_scale_for(p.hmax[w.head], p.hmax[p.heads + w.head]);
-    float* col0 = p.dq_acc + (static_cast<int64_t>(w.start) * p.heads + w.head) * D + e;
-    const int64_t qstride = static_cast<int64_t>(p.heads) * D;
+    float* stage = reinterpret_cast<float*>(gbase + C::OFF_DQ);
+    if (leader) tma_prefetch_desc(&tm_dq);
     for (int32_t i = 0; i < nq; ++i) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, &s_abort));
-      if (!ok) {
+      uint32_t r0[32], r1[32];
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32(tmem + lane_off + C::COL_DQT, r0);
+        tmem_ld32(tmem + lane_off + C::COL_DQT + 32, r1);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar_dq_empty);
+      }
+      if (leader) bulk_wait_read_all();  // the previous tile's reduce has read the buffer
+      if (named_bar_or(1, 128, !ok)) {
         s_abort = 1;
-        atomicOr(p.status, kFlagTimeout);
+        if (lane == 0) atomicOr(p.status, kFlagTimeout);
         break;
       }
-      tc_fence_after();
-      uint32_t r0[32], r1[32];
-      tmem_ld32(tmem + lane_off + C::COL_DQT, r0);
-      tmem_ld32(tmem + lane_off + C::COL_DQT + 32, r1);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar_dq_empty);
       const int32_t nvalid = min(C::BQ, w.len - i * C::BQ);
       if (e_ok) {
-        float* dst = col0 + static_cast<int64_t>(i) * C::BQ * qstride;
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          if (c < nvalid) atomicAdd(dst + c * qstride, __uint_as_float(r0[c]) * dq_mul);
+          stage[c * D + e] = c < nvalid ? __uint_as_float(r0[c]) * dq_mul : 0.f;
 #pragma unroll
         for (int c = 0; c < 32; ++c)
-          if (32 + c < nvalid)
-            atomicAdd(dst + (32 + c) * qstride, __uint_as_float(r1[c]) * dq_mul);
+          stage[(32 + c) * D + e] = 32 + c < nvalid ? __uint_as_float(r1[c]) * dq_mul : 0.f;
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (leader) {
+        tma_reduce_add_3d(&tm_dq, sDQ, 0, w.head, w.start + i * C::BQ);
+        bulk_commit_group();
       }
     }
+    if (leader) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -669,26 +716,27 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
     KernelTimer kt(MF_K_BWD_PRE, s);
     bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         reinterpret_cast<const uint4*>(a.o), reinterpret_cast<const uint4*>(a.d_o),
-        reinterpret_cast<const uint4*>(a.v), a.delta, reinterpret_cast<float4*>(a.dq_acc), a.hmax,
-        rows, a.T, a.heads);
+        reinterpret_cast<const uint4*>(a.v), a.lse, a.lse2, a.delta, a.pad,
+        reinterpret_cast<float4*>(a.dq_acc), a.hmax, rows, a.T, a.heads);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_tmap_thd(&tq, a.q, a.T, a.heads, D, C::BQ, true) ||
       !make_tmap_thd(&tk, a.k, a.T, a.heads, D, C::BK, true) ||
       !make_tmap_thd(&tv, a.v, a.T, a.heads, D, C::BK) ||
-      !make_tmap_thd(&tdo, a.d_o, a.T, a.heads, D, C::BQ))
+      !make_tmap_thd(&tdo, a.d_o, a.T, a.heads, D, C::BQ) ||
+      !make_tmap_f32_thd(&tdq, a.dq_acc, a.T, a.heads, D, C::BQ))
     return cudaErrorInvalidValue;
   BwdParams p;
   p.cu = a.cu;
   p.order = a.order;
   p.prefix = a.prefix;
   p.pos = a.pos;
-  p.lse = a.lse;
+  p.lse2 = a.lse2;
   p.delta = a.delta;
+  p.pad = a.pad;
   p.status = a.status;
-  p.dq_acc = a.dq_acc;
   p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
   p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
   p.n = a.n;
@@ -702,7 +750,7 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
   if (blocks > 0) {
     {
       KernelTimer kt(MF_K_ATTN_BWD, s);
-      attn_bwd_kernel<D><<<static_cast<unsigned>(blocks), 320, C::SMEM, s>>>(tq, tk, tv, tdo, p);
+      attn_bwd_kernel<D><<<static_cast<unsigned>(blocks), 320, C::SMEM, s>>>(tq, tk, tv, tdo, tdq, p);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

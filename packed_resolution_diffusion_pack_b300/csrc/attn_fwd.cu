@@ -34,8 +34,7 @@
 namespace mf {
 
 // ----------------------------------------------------------- tensor maps
-bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t T, int64_t heads,
-                   int64_t head_dim, int box_rows, bool f16) {
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (encode == nullptr) {
     cudaDriverEntryPointQueryResult qres;
@@ -43,9 +42,16 @@ bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t T, int64_t heads,
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
                                          &qres) != cudaSuccess ||
         qres != cudaDriverEntryPointSuccess || fn == nullptr)
-      return false;
+      return nullptr;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
+  return encode;
+}
+
+bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t T, int64_t heads,
+                   int64_t head_dim, int box_rows, bool f16) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+  if (encode == nullptr) return false;
   const int64_t rows = T > 0 ? T : 1;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(heads),
                         static_cast<cuuint64_t>(rows)};
@@ -57,6 +63,24 @@ bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t T, int64_t heads,
                       3, const_cast<void*>(base), dims,
                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_f32_thd(CUtensorMap* map, const void* base, int64_t T, int64_t heads,
+                       int64_t head_dim, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+  if (encode == nullptr) return false;
+  const int64_t rows = T > 0 ? T : 1;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim * 4),
+                           static_cast<cuuint64_t>(heads * head_dim * 4)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(head_dim), 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
