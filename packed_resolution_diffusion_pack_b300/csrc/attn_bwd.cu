@@ -419,30 +419,37 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         return r;
       };
+      // Shared-memory descriptors: one base per operand buffer, then the start
+      // address field (16-byte units, bits 0-13) advanced by a small offset.
       // K-major operand, K-step kk of 16 elements; `chunk` = bytes per 64-col chunk
-      auto desc_k = [](uint32_t base, int kk, uint32_t chunk) {
-        return sdesc_sw128(base + (kk >> 2) * chunk + (kk & 3) * 32, 16, 1024);
+      auto kofs = [](int kk, uint32_t chunk) -> uint64_t {
+        return ((kk >> 2) * chunk + (kk & 3) * 32) >> 4;
       };
-      // MN-major operand, K-step kk of 16 rows; `lbo` = bytes between 64-wide atoms
-      auto desc_mn = [](uint32_t base, int kk, uint32_t lbo) {
-        return sdesc_sw128(base + kk * 2048, lbo, 1024);
-      };
+      // MN-major operand, K-step kk of 16 rows
+      auto mofs = [](int kk) -> uint64_t { return (kk * 2048) >> 4; };
+      const uint32_t lbo_a = D == 128 ? static_cast<uint32_t>(C::KCHUNK) : (sZ - sK);
+      const uint64_t dK_k = sdesc_sw128(sK, 16, 1024), dV_k = sdesc_sw128(sV, 16, 1024);
+      const uint64_t dK_m = sdesc_sw128(sK, lbo_a, 1024);
+      const uint64_t dQ_k0 = sdesc_sw128(sQ, 16, 1024), dQ_m0 = sdesc_sw128(sQ, C::QCHUNK, 1024);
+      const uint64_t dO_k0 = sdesc_sw128(sDO, 16, 1024), dO_m0 = sdesc_sw128(sDO, C::QCHUNK, 1024);
+      const uint64_t dS_k0 = sdesc_sw128(sDS, 16, 1024), dS_m0 = sdesc_sw128(sDS, C::DSTILE, 1024);
+      constexpr uint64_t kStage = C::QTILE >> 4, kDsBuf = C::DSTILE >> 4;
       auto full = [&](int32_t i) {
         return wait(bar_full + 8 * (i % C::NST), (i / C::NST) & 1);
       };
       auto issue_st = [&](int32_t i) {  // S^T_i = K' Q'_i^T -> ST[i % 2]
-        const uint32_t q = sQ + (i % C::NST) * C::QTILE;
+        const uint64_t q = dQ_k0 + (i % C::NST) * kStage;
         const uint32_t d = tmem + ((i & 1) ? C::COL_ST1 : C::COL_ST0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(d, desc_k(sK, kk, C::KCHUNK), desc_k(q, kk, C::QCHUNK), C::IDESC_S, kk > 0);
+          mma_ss(d, dK_k + kofs(kk, C::KCHUNK), q + kofs(kk, C::QCHUNK), C::IDESC_S, kk > 0);
         mma_commit(bar_st + 8 * (i & 1));
       };
       auto issue_dp = [&](int32_t i) {  // dP^T_i = V dO_i^T -> DPT
-        const uint32_t o = sDO + (i % C::NST) * C::QTILE;
+        const uint64_t o = dO_k0 + (i % C::NST) * kStage;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::COL_DPT, desc_k(sV, kk, C::KCHUNK), desc_k(o, kk, C::QCHUNK),
+          mma_ss(tmem + C::COL_DPT, dV_k + kofs(kk, C::KCHUNK), o + kofs(kk, C::QCHUNK),
                  C::IDESC_DP, kk > 0);
         mma_commit(bar_dp);
       };
@@ -457,26 +464,24 @@ __global__ void __launch_bounds__(320, 1)
       }
       for (int32_t i = 0; i < nq && ok; ++i) {
         const int32_t st = i % C::NST;
-        const uint32_t q = sQ + st * C::QTILE, o = sDO + st * C::QTILE;
+        const uint64_t q_m = dQ_m0 + st * kStage, o_m = dO_m0 + st * kStage;
+        const uint64_t ds_k = dS_k0 + (i & 1) * kDsBuf, ds_m = dS_m0 + (i & 1) * kDsBuf;
         const uint32_t stb = tmem + ((i & 1) ? C::COL_ST1 : C::COL_ST0);
-        const uint32_t ds = sDS + (i & 1) * C::DSTILE;
         if (!(ok = wait(bar_ds, i & 1))) break;  // P^T_i in TMEM, dS^T_i in smem
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)  // dV += P^T_i dO_i
-          mma_ts(tmem + C::COL_DV, stb + kk * 8, desc_mn(o, kk, C::QCHUNK), C::IDESC_DV,
+          mma_ts(tmem + C::COL_DV, stb + kk * 8, o_m + mofs(kk), C::IDESC_DV,
                  (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T_i Q'_i
-          mma_ss(tmem + C::COL_DK, desc_k(ds, kk, C::DSTILE), desc_mn(q, kk, C::QCHUNK),
-                 C::IDESC_DK, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ss(tmem + C::COL_DK, ds_k + kofs(kk, C::DSTILE), q_m + mofs(kk), C::IDESC_DK,
+                 (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar_empty + 8 * st);  // Q'_i, dO_i no longer read
         if (i + 1 < nq) issue_dp(i + 1);  // DPT was read before bar_ds(i); stage i+1 landed
         if (i > 0 && !(ok = wait(bar_dq_empty, (i - 1) & 1))) break;
-        const uint32_t lbo_a = D == 128 ? static_cast<uint32_t>(C::KCHUNK) : (sZ - sK);
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ^T_i = K'^T dS^T_i
-          mma_ss(tmem + C::COL_DQT, desc_mn(sK, kk, lbo_a), desc_mn(ds, kk, C::DSTILE),
-                 C::IDESC_DQ, kk > 0);
+          mma_ss(tmem + C::COL_DQT, dK_m + mofs(kk), ds_m + mofs(kk), C::IDESC_DQ, kk > 0);
         mma_commit(bar_dq);
         if (i + 2 < nq) {  // ST[i % 2] is free once dV_i (issued above) has read P^T_i
           if (!(ok = full(i + 2))) break;
@@ -583,59 +588,74 @@ __global__ void __launch_bounds__(320, 1)
     }
     if (!(dsmax <= 65504.f)) atomicOr(p.status, kFlagFp16Range);
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, &s_abort));
-    if (ok) {
+    // the four warps agree (a warp whose wait ran out skips the epilogue, and so
+    // must every other: the epilogue has a barrier among them)
+    const bool all_ok = !named_bar_or(2, 128, !ok);
+    if (all_ok) {
       tc_fence_after();
-      const int64_t grow = (static_cast<int64_t>(w.start) + k0 + row) * p.heads + w.head;
-      const float dk_mul = p.scale / ds_mul;  // exact: ds_mul is a power of two
-      int32_t pr_ = 0, pc_ = 0;
-      if (key_ok && p.pos != nullptr) {
-        pr_ = p.pos[2 * (w.start + k0 + row)];
-        pc_ = p.pos[2 * (w.start + k0 + row) + 1];
-      }
+      // dV and dK rows (bf16) are staged in the (now idle) Q' / dO stage buffers
+      // as [128 keys][D] with 16-byte units XOR-swizzled by row, then written
+      // out by all four warps with coalesced row stores.
+      constexpr int UNITS = D / 8;  // 16-byte units per row
+      uint8_t* sdv = gbase + C::OFF_Q;
+      uint8_t* sdk = gbase + C::OFF_DO;
+      auto put = [&](uint8_t* base, int unit, uint4 val) {
+        *reinterpret_cast<uint4*>(base + row * (D * 2) + ((unit ^ (row % UNITS)) << 4)) = val;
+      };
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t r[32];
         tmem_ld32(tmem + lane_off + C::COL_DV + cc * 32, r);
         tmem_wait_ld();
-        if (key_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(p.dv + grow * D + cc * 32);
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            dst[u] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * u]), __uint_as_float(r[8 * u + 1])),
-                                pack_bf16x2(__uint_as_float(r[8 * u + 2]), __uint_as_float(r[8 * u + 3])),
-                                pack_bf16x2(__uint_as_float(r[8 * u + 4]), __uint_as_float(r[8 * u + 5])),
-                                pack_bf16x2(__uint_as_float(r[8 * u + 6]), __uint_as_float(r[8 * u + 7])));
-        }
+        for (int u = 0; u < 4; ++u)
+          put(sdv, cc * 4 + u,
+              make_uint4(pack_bf16x2(__uint_as_float(r[8 * u]), __uint_as_float(r[8 * u + 1])),
+                         pack_bf16x2(__uint_as_float(r[8 * u + 2]), __uint_as_float(r[8 * u + 3])),
+                         pack_bf16x2(__uint_as_float(r[8 * u + 4]), __uint_as_float(r[8 * u + 5])),
+                         pack_bf16x2(__uint_as_float(r[8 * u + 6]), __uint_as_float(r[8 * u + 7]))));
+      }
+      const float dk_mul = p.scale / ds_mul;  // exact: ds_mul is a power of two
+      float pr_ = 0.f, pc_ = 0.f;
+      if (key_ok && p.pos != nullptr) {
+        pr_ = static_cast<float>(p.pos[2 * (w.start + k0 + row)]);
+        pc_ = static_cast<float>(p.pos[2 * (w.start + k0 + row) + 1]);
       }
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t r[32];
         tmem_ld32(tmem + lane_off + C::COL_DK + cc * 32, r);
         tmem_wait_ld();
-        if (key_ok) {
-          float v[32];
+        float v[32];
 #pragma unroll
-          for (int u = 0; u < 32; ++u) v[u] = __uint_as_float(r[u]) * dk_mul;
-          if (p.pos != nullptr) {
+        for (int u = 0; u < 32; ++u) v[u] = __uint_as_float(r[u]) * dk_mul;
+        if (p.pos != nullptr) {
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const int P = cc * 16 + u;  // pair index
-              const float pp = static_cast<float>(P < D / 4 ? pr_ : pc_);
-              float s, c;
-              rope_sincos(pp, p.f.omega[P % (D / 4)], p.f.omega_lo[P % (D / 4)], -1.f, &s, &c);
-              const float a = v[2 * u], b = v[2 * u + 1];
-              v[2 * u] = fmaf(a, c, -b * s);
-              v[2 * u + 1] = fmaf(a, s, b * c);
-            }
+          for (int u = 0; u < 16; ++u) {
+            const int P = cc * 16 + u;  // pair index
+            float sn, cs;
+            rope_sincos_fast(P < D / 4 ? pr_ : pc_, p.f.omega[P % (D / 4)],
+                             p.f.omega_lo[P % (D / 4)], -1.f, &sn, &cs);
+            const float a = v[2 * u], b = v[2 * u + 1];
+            v[2 * u] = fmaf(a, cs, -b * sn);
+            v[2 * u + 1] = fmaf(a, sn, b * cs);
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.dk + grow * D + cc * 32);
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            dst[u] = make_uint4(pack_bf16x2(v[8 * u], v[8 * u + 1]),
-                                pack_bf16x2(v[8 * u + 2], v[8 * u + 3]),
-                                pack_bf16x2(v[8 * u + 4], v[8 * u + 5]),
-                                pack_bf16x2(v[8 * u + 6], v[8 * u + 7]));
         }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          put(sdk, cc * 4 + u,
+              make_uint4(pack_bf16x2(v[8 * u], v[8 * u + 1]), pack_bf16x2(v[8 * u + 2], v[8 * u + 3]),
+                         pack_bf16x2(v[8 * u + 4], v[8 * u + 5]),
+                         pack_bf16x2(v[8 * u + 6], v[8 * u + 7])));
+      }
+      named_bar_sync(2, 128);
+      const int32_t nrows = min(C::BK, w.len - k0);
+      const int u = static_cast<int>(row) % UNITS;
+      for (int r = static_cast<int>(row) / UNITS; r < nrows; r += 128 / UNITS) {
+        const int64_t g = ((static_cast<int64_t>(w.start) + k0 + r) * p.heads + w.head) * D + u * 8;
+        const int off = r * (D * 2) + ((u ^ (r % UNITS)) << 4);
+        *reinterpret_cast<uint4*>(p.dv + g) = *reinterpret_cast<const uint4*>(sdv + off);
+        *reinterpret_cast<uint4*>(p.dk + g) = *reinterpret_cast<const uint4*>(sdk + off);
       }
     } else {
       s_abort = 1;

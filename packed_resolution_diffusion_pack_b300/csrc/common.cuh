@@ -36,6 +36,35 @@ __device__ __forceinline__ void rope_sincos(float p, float w_hi, float w_lo, flo
   *c = fmaf(-e, s0, c0);
 }
 
+// The same angle with a cheaper evaluation, for epilogues that rotate many
+// values per thread: theta = p * omega as above (hi part + first-order error),
+// Cody-Waite reduction of the hi part by pi/2 with a three-part constant (the
+// first two parts carry 12 trailing zero bits, so k * part is exact for
+// |k| < 2^12), then the hardware sine / cosine approximations on
+// |r| <= pi/4 (absolute error ~2^-21 there) and the quadrant's sign swap.
+__device__ __forceinline__ void rope_sincos_fast(float p, float w_hi, float w_lo, float sign,
+                                                 float* s, float* c) {
+  constexpr float kPio2Hi = 1.5703125f;                 // 0x1.92p+0
+  constexpr float kPio2Mid = 4.837512969970703e-04f;    // 0x1.fb4p-12
+  constexpr float kPio2Lo = 7.549790126404332e-08f;     // 0x1.4442d2p-24
+  constexpr float kTwoOverPi = 0.6366197466850281f;
+  const float th = p * w_hi;
+  const float err = fmaf(p, w_hi, -th) + p * w_lo;
+  const float k = rintf(th * kTwoOverPi);
+  float r = fmaf(-k, kPio2Hi, th);
+  r = fmaf(-k, kPio2Mid, r);
+  r = fmaf(-k, kPio2Lo, r);
+  r += err;
+  const float s0 = __sinf(r), c0 = __cosf(r);
+  const int q = static_cast<int>(k) & 3;
+  float ss = (q & 1) ? c0 : s0;
+  float cc = (q & 1) ? s0 : c0;
+  if (q == 1 || q == 2) cc = -cc;
+  if (q >= 2) ss = -ss;
+  *s = sign * ss;
+  *c = cc;
+}
+
 // --------------------------------------------------------- workspace layout
 // [0, 256)            device status word (uint32, flags kFlag*)
 // [256, +sched)       schedule: int32 order[n], int32 prefix[n+1]
