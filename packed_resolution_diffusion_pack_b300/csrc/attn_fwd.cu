@@ -6,7 +6,8 @@
 //   O_j = sum_k softmax_k(scale <q'_j, k'_k>) v_k over the keys of sample i only,
 //   LSE_j = ln sum_k exp(scale <q'_j, k'_k>).
 //
-// Design (one CTA = one sample, one head, 256 query rows = two 128-row Q tiles):
+// Design (one CTA = one sample, one head, 256 query rows = two 128-row Q tiles;
+// three warpgroups, registers moved from the third to the first two):
 //   warp 8      TMA producer: Q tiles once, then K_j, V_j tiles through a ring
 //               of shared-memory slots (128B-swizzled, 64-column chunks).
 //   warp 9      MMA issuer (one thread): S_t = Q'_t K'_j^T (SS, into TMEM), then
@@ -14,10 +15,15 @@
 //               fp16 (11 significant bits), accumulation fp32.  The two Q tiles
 //               ping-pong so the tensor core works on one while the other's
 //               softmax runs.
+//   warps 10-11 idle (they complete the third warpgroup).
 //   warps 0-7   two softmax warpgroups, one per Q tile; thread = query row =
-//               TMEM lane.  Online softmax in base 2 with a lazy rescale of O
-//               (only when the running max grows by more than 2^8), P written
-//               back to TMEM as fp16 over the S columns.  Epilogue: O / l, LSE.
+//               TMEM lane.  Online softmax in base 2: row max by a tree of
+//               three-input maxima, packed two-lane FMAs and adds around the
+//               exponentials, a lazy rescale
+//               of O (only when the running max grows by more than 2^8), P
+//               written back to TMEM as fp16 over the S columns.  Epilogue: O / l
+//               staged in the tile's Q buffer, written out with coalesced row
+//               stores; LSE.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D).
 // Tiles never cross a sample: K/V tiles start at the sample's first token, key
 // columns past the sample end are masked to -inf, query rows past it not stored.
@@ -200,6 +206,15 @@ __device__ __forceinline__ bool find_item(const int32_t* __restrict__ cu,
 }
 
 // ------------------------------------------------------------------ forward
+// Three warpgroups: softmax (warps 0-3, 4-7) and producer / MMA / idle (8-11).
+// Launched at 168 registers a thread (384 x 168 = 64,512); the third warpgroup
+// drops to 88 and the softmax warpgroups rise to 208: 128 x 88 + 256 x 208 =
+// 64,512, exactly the launch total.
+constexpr int kFwdThreads = 384;
+constexpr uint32_t kFwdRegsLow = 88, kFwdRegsHigh = 208;
+static_assert(128 * kFwdRegsLow + 256 * kFwdRegsHigh <= kFwdThreads * 168,
+              "forward register split exceeds the launch total");
+
 template <int D>
 struct FwdCfg {
   static constexpr int BM = 128;                  // query rows per Q tile
@@ -230,7 +245,7 @@ struct FwdParams {
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -297,112 +312,119 @@ __global__ void __launch_bounds__(320, 1)
   const bool has1 = q0 + C::BM < w.len;             // second Q tile holds rows
   const int32_t nkv = (w.len + C::BN - 1) / C::BN;  // K/V tiles
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar_q, (has1 ? 2 : 1) * C::TILE);
-      for (int t = 0; t < (has1 ? 2 : 1); ++t)
-        for (int ch = 0; ch < D / 64; ++ch)
-          tma_load_3d(sQ + t * C::TILE + ch * C::CHUNK, &tm_q, bar_q, ch * 64, w.head,
-                      w.start + q0 + t * C::BM);
-      int32_t issued = 0;
-      bool ok = true;
-      for (int32_t j = 0; j < nkv && ok; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const int32_t c = 2 * j + kv;
-          const int32_t slot = c % C::NSLOT, use = c / C::NSLOT;
-          if (use > 0 && !mbar_wait(bar_empty + 8 * slot, (use - 1) & 1, &s_abort)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar_full + 8 * slot, C::TILE);
+  if (warp >= 8) {
+    warpgroup_reg_dealloc<kFwdRegsLow>();
+    if (warp == 8) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        mbar_arrive_expect_tx(bar_q, (has1 ? 2 : 1) * C::TILE);
+        for (int t = 0; t < (has1 ? 2 : 1); ++t)
           for (int ch = 0; ch < D / 64; ++ch)
-            tma_load_3d(sKV + slot * C::TILE + ch * C::CHUNK, kv ? &tm_v : &tm_k,
-                        bar_full + 8 * slot, ch * 64, w.head, w.start + j * C::BN);
-          ++issued;
+            tma_load_3d(sQ + t * C::TILE + ch * C::CHUNK, &tm_q, bar_q, ch * 64, w.head,
+                        w.start + q0 + t * C::BM);
+        int32_t issued = 0;
+        bool ok = true;
+        for (int32_t j = 0; j < nkv && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const int32_t c = 2 * j + kv;
+            const int32_t slot = c % C::NSLOT, use = c / C::NSLOT;
+            if (use > 0 && !mbar_wait(bar_empty + 8 * slot, (use - 1) & 1, &s_abort)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar_full + 8 * slot, C::TILE);
+            for (int ch = 0; ch < D / 64; ++ch)
+              tma_load_3d(sKV + slot * C::TILE + ch * C::CHUNK, kv ? &tm_v : &tm_k,
+                          bar_full + 8 * slot, ch * 64, w.head, w.start + j * C::BN);
+            ++issued;
+          }
         }
+        if (!ok) {
+          s_abort = 1;
+          atomicOr(p.status, kFlagTimeout);
+        }
+        // let every issued copy land before the CTA can exit
+        mbar_wait_drain(bar_q, 0);
+        for (int32_t c = (issued > C::NSLOT ? issued - C::NSLOT : 0); c < issued; ++c)
+          mbar_wait_drain(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1);
       }
-      if (!ok) {
-        s_abort = 1;
-        atomicOr(p.status, kFlagTimeout);
-      }
-      // let every issued copy land before the CTA can exit
-      mbar_wait_drain(bar_q, 0);
-      for (int32_t c = (issued > C::NSLOT ? issued - C::NSLOT : 0); c < issued; ++c)
-        mbar_wait_drain(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1);
-    }
-  } else if (warp == 9) {
-    // -------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      bool ok = mbar_wait(bar_q, 0, &s_abort);
-      tc_fence_after();
-      auto kv_wait = [&](int32_t c) -> bool {
-        const bool r = mbar_wait(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1, &s_abort);
+    } else if (warp == 9) {
+      // -------------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        bool ok = mbar_wait(bar_q, 0, &s_abort);
         tc_fence_after();
-        return r;
-      };
-      auto issue_s = [&](int t, int32_t j) {
-        const uint32_t a0 = sQ + t * C::TILE;
-        const uint32_t b0 = sKV + ((2 * j) % C::NSLOT) * C::TILE;
-        const uint32_t d = tmem + (t ? C::S_COL1 : C::S_COL0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK + (kk & 3) * 32;
-          mma_ss(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), C::IDESC_S,
-                 kk > 0);
-        }
-        mma_commit(bar_s + 8 * t);
-      };
-      auto issue_pv = [&](int t, int32_t j) {
-        const uint32_t b0 = sKV + ((2 * j + 1) % C::NSLOT) * C::TILE;
-        const uint32_t d = tmem + (t ? C::O_COL1 : C::O_COL0);
-        const uint32_t a = tmem + (t ? C::S_COL1 : C::S_COL0);
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ts(d, a + kk * 8, sdesc_sw128(b0 + kk * 2048, C::CHUNK, 1024), C::IDESC_PV,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-      };
-      if (ok) ok = kv_wait(0);
-      if (ok) {
-        issue_s(0, 0);
-        if (has1) issue_s(1, 0);
-        mma_commit(bar_empty + 8 * (0 % C::NSLOT));
-      }
-      for (int32_t j = 0; j < nkv && ok; ++j) {
-        ok = mbar_wait(bar_p, j & 1, &s_abort) && kv_wait(2 * j + 1);
-        if (!ok) break;
-        issue_pv(0, j);
-        const bool more = j + 1 < nkv;
-        if (more) {
-          if (!(ok = kv_wait(2 * j + 2))) break;
-          issue_s(0, j + 1);
-        }
-        if (has1) {
-          if (!(ok = mbar_wait(bar_p + 8, j & 1, &s_abort))) break;
+        auto kv_wait = [&](int32_t c) -> bool {
+          const bool r = mbar_wait(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1, &s_abort);
           tc_fence_after();
-          issue_pv(1, j);
+          return r;
+        };
+        // Shared-memory descriptors: one base per buffer, then the start-address
+        // field (16-byte units) advanced by constant offsets.
+        const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
+        const uint64_t dkv_k = sdesc_sw128(sKV, 16, 1024);          // K-major (K tiles)
+        const uint64_t dkv_m = sdesc_sw128(sKV, C::CHUNK, 1024);    // MN-major (V tiles)
+        constexpr uint64_t kTile = C::TILE >> 4;
+        auto kofs = [](int kk) -> uint64_t { return ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4; };
+        auto issue_s = [&](int t, int32_t j) {
+          const uint64_t a0 = dq0 + t * kTile;
+          const uint64_t b0 = dkv_k + ((2 * j) % C::NSLOT) * kTile;
+          const uint32_t d = tmem + (t ? C::S_COL1 : C::S_COL0);
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(d, a0 + kofs(kk), b0 + kofs(kk), C::IDESC_S, kk > 0);
+          mma_commit(bar_s + 8 * t);
+        };
+        auto issue_pv = [&](int t, int32_t j) {
+          const uint64_t b0 = dkv_m + ((2 * j + 1) % C::NSLOT) * kTile;
+          const uint32_t d = tmem + (t ? C::O_COL1 : C::O_COL0);
+          const uint32_t a = tmem + (t ? C::S_COL1 : C::S_COL0);
+  #pragma unroll
+          for (int kk = 0; kk < C::BN / 16; ++kk)
+            mma_ts(d, a + kk * 8, b0 + ((kk * 2048) >> 4), C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        };
+        if (ok) ok = kv_wait(0);
+        if (ok) {
+          issue_s(0, 0);
+          if (has1) issue_s(1, 0);
+          mma_commit(bar_empty + 8 * (0 % C::NSLOT));
         }
-        mma_commit(bar_empty + 8 * ((2 * j + 1) % C::NSLOT));
-        if (more) {
-          if (has1) issue_s(1, j + 1);
-          mma_commit(bar_empty + 8 * ((2 * j + 2) % C::NSLOT));
+        for (int32_t j = 0; j < nkv && ok; ++j) {
+          ok = mbar_wait(bar_p, j & 1, &s_abort) && kv_wait(2 * j + 1);
+          if (!ok) break;
+          issue_pv(0, j);
+          const bool more = j + 1 < nkv;
+          if (more) {
+            if (!(ok = kv_wait(2 * j + 2))) break;
+            issue_s(0, j + 1);
+          }
+          if (has1) {
+            if (!(ok = mbar_wait(bar_p + 8, j & 1, &s_abort))) break;
+            tc_fence_after();
+            issue_pv(1, j);
+          }
+          mma_commit(bar_empty + 8 * ((2 * j + 1) % C::NSLOT));
+          if (more) {
+            if (has1) issue_s(1, j + 1);
+            mma_commit(bar_empty + 8 * ((2 * j + 2) % C::NSLOT));
+          }
         }
+        if (ok) {
+          mma_commit(bar_o);
+          if (has1) mma_commit(bar_o + 8);
+        } else {
+          s_abort = 1;
+          atomicOr(p.status, kFlagTimeout);
+        }
+        // every MMA issued so far must finish before TMEM is released
+        mma_commit(bar_drain);
+        mbar_wait_drain(bar_drain, 0);
       }
-      if (ok) {
-        mma_commit(bar_o);
-        if (has1) mma_commit(bar_o + 8);
-      } else {
-        s_abort = 1;
-        atomicOr(p.status, kFlagTimeout);
-      }
-      // every MMA issued so far must finish before TMEM is released
-      mma_commit(bar_drain);
-      mbar_wait_drain(bar_drain, 0);
     }
   } else {
+    warpgroup_reg_alloc<kFwdRegsHigh>();
     // ---------------------------------------------------- softmax warpgroups
     const int t = warp >> 2;  // Q tile of this warpgroup
     if (t == 0 || has1) {
@@ -433,9 +455,21 @@ __global__ void __launch_bounds__(320, 1)
           for (int c = 0; c < 128; ++c)
             if (c >= nvalid) s[c] = __float_as_uint(-INFINITY);
         }
-        float mx = __uint_as_float(s[0]);
+        // row max: a tree of three-input maxima (depth 4 instead of a 127-long chain)
+        float mx;
+        {
+          float m0[16];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t* v = s + 8 * i;
+            m0[i] = fmax3(fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2])),
+                          fmax3(__uint_as_float(v[3]), __uint_as_float(v[4]), __uint_as_float(v[5])),
+                          fmaxf(__uint_as_float(v[6]), __uint_as_float(v[7])));
+          }
+          mx = fmax3(fmax3(fmax3(m0[0], m0[1], m0[2]), fmax3(m0[3], m0[4], m0[5]),
+                           fmax3(m0[6], m0[7], m0[8])),
+                     fmax3(m0[9], m0[10], m0[11]), fmax3(m0[12], m0[13], fmaxf(m0[14], m0[15])));
+        }
         const float m_new = fmaxf(m, mx * sl2);
         if (j == 0) {
           m = m_new;
@@ -459,50 +493,73 @@ __global__ void __launch_bounds__(320, 1)
             tmem_wait_st();
           }
         }
-        float sum = 0.f;
+        // P = 2^(s scale log2e - m), two columns per packed FMA; two packed sums
+        const uint64_t sl2x2 = f32x2_pack(sl2, sl2), negm2 = f32x2_pack(-m, -m);
+        uint64_t sum2[2] = {f32x2_pack(0.f, 0.f), f32x2_pack(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(s[c * 32 + 2 * u]), sl2, -m));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(s[c * 32 + 2 * u + 1]), sl2, -m));
-            sum += p0 + p1;
+            const uint64_t x = f32x2_fma(f32x2_pack(__uint_as_float(s[c * 32 + 2 * u]),
+                                                    __uint_as_float(s[c * 32 + 2 * u + 1])),
+                                         sl2x2, negm2);
+            float x0, x1;
+            f32x2_unpack(x, x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            sum2[u & 1] = f32x2_add(sum2[u & 1], f32x2_pack(p0, p1));
             pk[u] = pack_f16x2(p0, p1);
           }
           tmem_st16(tS + c * 16, pk);
         }
+        float sa, sb, sc, sd;
+        f32x2_unpack(sum2[0], sa, sb);
+        f32x2_unpack(sum2[1], sc, sd);
+        const float sum = (sa + sb) + (sc + sd);
         l += sum;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar_p + 8 * t);
       }
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_o + 8 * t, 0, &s_abort));
-      if (ok) {
+      // the warpgroup's four warps agree before the epilogue's barrier
+      const bool all_ok = !(t ? named_bar_or(2, 128, !ok) : named_bar_or(1, 128, !ok));
+      if (all_ok) {
         tc_fence_after();
-        const bool store = qrow < w.len;
+        // O rows (bf16) staged in this tile's Q buffer (idle once every MMA is
+        // done) as [128 rows][D], 16-byte units XOR-swizzled by row, then written
+        // out with coalesced row stores by the warpgroup
+        constexpr int UNITS = D / 8;
+        uint8_t* so = smem_raw + C::OFF_Q + t * C::TILE;
         const float inv = 1.f / l;
-        __nv_bfloat16* orow =
-            p.o + (static_cast<int64_t>(w.start + qrow) * p.heads + w.head) * D;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t r[32];
           tmem_ld32(tO + cc * 32, r);
           tmem_wait_ld();
-          uint32_t pk[16];
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
-            pk[u] = pack_bf16x2(__uint_as_float(r[2 * u]) * inv, __uint_as_float(r[2 * u + 1]) * inv);
-          if (store) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          for (int u = 0; u < 4; ++u) {
+            const uint4 val = make_uint4(
+                pack_bf16x2(__uint_as_float(r[8 * u]) * inv, __uint_as_float(r[8 * u + 1]) * inv),
+                pack_bf16x2(__uint_as_float(r[8 * u + 2]) * inv, __uint_as_float(r[8 * u + 3]) * inv),
+                pack_bf16x2(__uint_as_float(r[8 * u + 4]) * inv, __uint_as_float(r[8 * u + 5]) * inv),
+                pack_bf16x2(__uint_as_float(r[8 * u + 6]) * inv, __uint_as_float(r[8 * u + 7]) * inv));
+            const int unit = cc * 4 + u;
+            *reinterpret_cast<uint4*>(so + row * (D * 2) + ((unit ^ (row % UNITS)) << 4)) = val;
           }
         }
-        if (store)
+        if (qrow < w.len)
           p.lse[static_cast<int64_t>(w.head) * p.T + w.start + qrow] =
               (m + log2f(l)) * 0.69314718055994530942f;
+        if (t) named_bar_sync(2, 128); else named_bar_sync(1, 128);
+        const int32_t r0 = q0 + t * C::BM;  // first query row of the tile (in sample)
+        const int32_t nrows = min(C::BM, w.len - r0);
+        const int u = static_cast<int>(row) % UNITS;
+        for (int r = static_cast<int>(row) / UNITS; r < nrows; r += 128 / UNITS) {
+          const int64_t g = ((static_cast<int64_t>(w.start) + r0 + r) * p.heads + w.head) * D + u * 8;
+          *reinterpret_cast<uint4*>(p.o + g) =
+              *reinterpret_cast<const uint4*>(so + r * (D * 2) + ((u ^ (r % UNITS)) << 4));
+        }
       } else {
         s_abort = 1;
         atomicOr(p.status, kFlagTimeout);
@@ -547,7 +604,7 @@ static cudaError_t launch_fwd_d(const AttnFwdArgs& a, cudaStream_t s) {
   if (blocks <= 0) return cudaSuccess;
   {
     KernelTimer kt(MF_K_ATTN_FWD, s);
-    attn_fwd_kernel<D><<<static_cast<unsigned>(blocks), 320, C::SMEM, s>>>(tq, tk, tv, p);
+    attn_fwd_kernel<D><<<static_cast<unsigned>(blocks), kFwdThreads, C::SMEM, s>>>(tq, tk, tv, p);
   }
   return cudaGetLastError();
 }
