@@ -36,7 +36,7 @@ WsLayout ws_layout(int64_t T, int64_t n, int64_t heads, int64_t head_dim, bool b
     off = align_up(off + 8 * static_cast<size_t>(heads), 256);
     L.pad = off;
     off = align_up(off + 4 * 128, 1024);
-    L.lse2 = off;
+    L.nlse2 = off;
     off = align_up(off + 4 * static_cast<size_t>(heads) * T, 1024);
     L.delta = off;
     off = align_up(off + 4 * static_cast<size_t>(heads) * T, 1024);
@@ -231,7 +231,7 @@ mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
   a.prefix = prefix;
   a.status = status;
   a.pad = reinterpret_cast<float*>(w + L.pad);
-  a.lse2 = reinterpret_cast<float*>(w + L.lse2);
+  a.nlse2 = reinterpret_cast<float*>(w + L.nlse2);
   a.delta = reinterpret_cast<float*>(w + L.delta);
   a.dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
   a.dq = dq;

@@ -65,11 +65,12 @@ __device__ __forceinline__ bool find_item_b(const int32_t* __restrict__ cu,
 
 // ------------------------------------------------------------- preprocess
 // Rows are (token, head) pairs in THD order; 8 lanes per row, each covering D/8
-// elements.  Per row: D = <dO, O> -> delta[h][t]; LSE * log2 e -> lse2[h][t]; the
+// elements.  Per row: D = <dO, O> -> delta[h][t]; -LSE * log2 e -> nlse2[h][t]; the
 // row of the fp32 dQ accumulator zeroed; ||dO|| and ||v|| folded into per-head
 // maxima (shared memory per block, then one atomicMax per head: non-negative
 // floats order like their bit patterns).  Block 0 also writes the pad rows
-// (64 x +inf as LSE, 64 x 0 as D) that stand in for query rows past a sample.
+// (64 x -inf as -LSE log2 e, 64 x 0 as D) that stand in for query rows past a
+// sample (they make P = 0 there).
 constexpr int kPreRowsPerBlock = 512;
 constexpr int kPreMaxHeads = 256;
 
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
                                                       const uint4* __restrict__ d_o,
                                                       const uint4* __restrict__ v,
                                                       const float* __restrict__ lse,
-                                                      float* __restrict__ lse2,
+                                                      float* __restrict__ nlse2,
                                                       float* __restrict__ delta,
                                                       float* __restrict__ pad,
                                                       float4* __restrict__ dq_acc,
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
   __shared__ float s_max[2 * kPreMaxHeads];
   const bool smem_max = heads <= kPreMaxHeads;
   for (int i = threadIdx.x; i < 2 * kPreMaxHeads; i += blockDim.x) s_max[i] = 0.f;
-  if (blockIdx.x == 0 && threadIdx.x < 128) pad[threadIdx.x] = threadIdx.x < 64 ? INFINITY : 0.f;
+  if (blockIdx.x == 0 && threadIdx.x < 128) pad[threadIdx.x] = threadIdx.x < 64 ? -INFINITY : 0.f;
   __syncthreads();
   const int sub = threadIdx.x & 7;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kPreRowsPerBlock;
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
       const int32_t a = static_cast<int32_t>(row - t * heads);
       const int64_t g = static_cast<int64_t>(a) * T + t;
       delta[g] = acc;
-      lse2[g] = lse[g] * 1.4426950408889634f;
+      nlse2[g] = lse[g] * -1.4426950408889634f;
       const unsigned bdo = __float_as_uint(sqrtf(ndo)), bv = __float_as_uint(sqrtf(nv));
       if (smem_max) {
         atomicMax(reinterpret_cast<unsigned*>(&s_max[a]), bdo);
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(256) dq_post_kernel(const float4* __restrict__
 //   S^T_i  = K' Q'_i^T        M=128 keys, N=64, K=d   SS fp16   -> TMEM ST[b]
 //   dP^T_i = V dO_i^T         M=128 keys, N=64, K=d   SS bf16   -> TMEM DPT
 //   P^T_i  = exp2(S^T scale log2e - LSE log2e) (bf16 -> ST[b] columns [0,32))
+//            (the preprocess stores -LSE log2e, so this is one packed FMA per pair)
 //   dS^T_i = P^T (dP^T - D) * ds_mul           (fp16 -> smem DS[b])
 //   dV    += P^T_i dO_i       M=128 keys, N=d, K=64   TS bf16
 //   dK    += dS^T_i Q'_i      M=128 keys, N=d, K=64   SS fp16
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(256) dq_post_kernel(const float4* __restrict__
 // issued ahead of the GEMMs that need the P/dS warpgroup, so that warpgroup's
 // exp/dS work overlaps the tensor core.
 //   warp 8     TMA: K', V once; (Q'_i, dO_i) through an NST-stage ring; the
-//              lanes copy the tile's LSE * log2 e and D rows beside them with
+//              lanes copy the tile's -LSE * log2 e and D rows beside them with
 //              cp.async (pad rows past the sample), all on the stage barrier.
 //   warp 9     MMA issuer (one thread).
 //   warps 0-3  thread = key row: P^T, dS^T; epilogue dV, dK (scale, R(-theta)).
@@ -235,7 +237,7 @@ struct BwdCfg {
   static constexpr int OFF_DO = OFF_Q + NST * QTILE;              // [NST]
   static constexpr int OFF_DS = OFF_DO + NST * QTILE;             // [2]
   static constexpr int OFF_DQ = OFF_DS + 2 * DSTILE;
-  static constexpr int OFF_VEC = OFF_DQ + DQTILE;                 // [NST] x (lse2, D) x 64
+  static constexpr int OFF_VEC = OFF_DQ + DQTILE;                 // [NST] x (-LSE log2e, D) x 64
   static constexpr int OFF_BAR = OFF_VEC + NST * 512;
   static constexpr int OFF_MISC = OFF_BAR + 256;
   static constexpr int SMEM = OFF_MISC + 64;
@@ -256,7 +258,7 @@ struct BwdParams {
   const int32_t* order;
   const int32_t* prefix;
   const int32_t* pos;
-  const float* lse2;
+  const float* nlse2;
   const float* delta;
   const float* pad;
   uint32_t* status;
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sZ = sbase + C::OFF_Z;
   const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO, sDS = sbase + C::OFF_DS;
   const uint32_t sDQ = sbase + C::OFF_DQ, sVEC = sbase + C::OFF_VEC;
-  // per stage: lse2 at [st*128, +64), D at [st*128+64, +64)
+  // per stage: -LSE log2 e at [st*128, +64), D at [st*128+64, +64)
   const float* vec = reinterpret_cast<const float*>(gbase + C::OFF_VEC);
   const uint32_t bars = sbase + C::OFF_BAR;
   const uint32_t bar_kv = bars;
@@ -400,7 +402,7 @@ __global__ void __launch_bounds__(320, 1)
         const int q = static_cast<int>(lane) * 2 + u;
         const int32_t qi = i * C::BQ + q;
         const bool q_ok = qi < w.len;
-        cp_async_4(sVEC + st * 512 + q * 4, q_ok ? p.lse2 + gbase_row + qi : p.pad + q);
+        cp_async_4(sVEC + st * 512 + q * 4, q_ok ? p.nlse2 + gbase_row + qi : p.pad + q);
         cp_async_4(sVEC + st * 512 + 256 + q * 4, q_ok ? p.delta + gbase_row + qi : p.pad + 64 + q);
       }
       cp_async_arrive_noinc(bar_full + 8 * st);
@@ -516,11 +518,12 @@ __global__ void __launch_bounds__(320, 1)
                                        mbar_wait(bar_st + 8 * (i & 1), (i >> 1) & 1, &s_abort));
       if (!ok) break;
       tc_fence_after();
-      const float4* vl4 = reinterpret_cast<const float4*>(vec + st * 128);
-      const float4* vd4 = vl4 + 16;
-      // P^T: 64 queries; bf16 into ST columns [0, 32) (S^T values already read).
-      // Key rows past the sample get P = 0 (their S^T holds another sample's keys).
-      float pr[64];
+      const float4* vl4 = reinterpret_cast<const float4*>(vec + st * 128);  // -LSE log2 e
+      const float4* vd4 = vl4 + 16;                                           // D
+      // P^T: 64 queries, two per packed FMA; bf16 into ST columns [0, 32) (S^T
+      // values already read).  Key rows past the sample get P = 0 (their S^T
+      // holds another sample's keys).
+      uint64_t pr2[32];
       {
         uint32_t r[64];
         {
@@ -534,26 +537,36 @@ __global__ void __launch_bounds__(320, 1)
             r[32 + c] = r1[c];
           }
         }
+        const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
 #pragma unroll
         for (int c4 = 0; c4 < 16; ++c4) {
           const float4 l = vl4[c4];
-          const float ls[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float e = ex2_approx(fmaf(__uint_as_float(r[4 * c4 + u]), sl2, -ls[u]));
-            pr[4 * c4 + u] = key_ok ? e : 0.f;
+          for (int h = 0; h < 2; ++h) {
+            const uint64_t x = f32x2_fma(f32x2_pack(__uint_as_float(r[4 * c4 + 2 * h]),
+                                                    __uint_as_float(r[4 * c4 + 2 * h + 1])),
+                                         sl2x2, h ? f32x2_pack(l.z, l.w) : f32x2_pack(l.x, l.y));
+            float x0, x1;
+            f32x2_unpack(x, x0, x1);
+            pr2[2 * c4 + h] = key_ok ? f32x2_pack(ex2_approx(x0), ex2_approx(x1)) : 0ull;
           }
         }
         uint32_t pk[32];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) pk[u] = pack_bf16x2(pr[2 * u], pr[2 * u + 1]);
+        for (int u = 0; u < 32; ++u) {
+          float a, b;
+          f32x2_unpack(pr2[u], a, b);
+          pk[u] = pack_bf16x2(a, b);
+        }
         tmem_st32(tST, pk);
       }
       ok = __all_sync(0xffffffffu, mbar_wait(bar_dp, i & 1, &s_abort));
       if (!ok) break;
       tc_fence_after();
-      // dS^T row -> smem DS[i % 2], 128B-swizzled K-major [key][query]: 16-byte
-      // unit u (queries 8u..8u+7) stored at u ^ (row % 8)
+      // dS^T = P^T (dP^T - D) ds_mul, two queries per packed op; row -> smem
+      // DS[i % 2], 128B-swizzled K-major [key][query]: 16-byte unit u (queries
+      // 8u..8u+7) stored at u ^ (row % 8)
+      const uint64_t dsm2 = f32x2_pack(ds_mul, ds_mul);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t rd[32];
@@ -563,14 +576,15 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int u4 = 0; u4 < 8; ++u4) {
           const float4 dd = vd4[c * 8 + u4];
-          const float ds[4] = {dd.x, dd.y, dd.z, dd.w};
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int q0 = c * 32 + u4 * 4 + 2 * h;
-            const float ds0 = pr[q0] * ds_mul * (__uint_as_float(rd[u4 * 4 + 2 * h]) - ds[2 * h]);
-            const float ds1 =
-                pr[q0 + 1] * ds_mul * (__uint_as_float(rd[u4 * 4 + 2 * h + 1]) - ds[2 * h + 1]);
-            dsmax = fmaxf(dsmax, fmaxf(fabsf(ds0), fabsf(ds1)));
+            const uint64_t t2 = f32x2_sub(f32x2_pack(__uint_as_float(rd[u4 * 4 + 2 * h]),
+                                                     __uint_as_float(rd[u4 * 4 + 2 * h + 1])),
+                                          h ? f32x2_pack(dd.z, dd.w) : f32x2_pack(dd.x, dd.y));
+            const uint64_t ds2 = f32x2_mul(f32x2_mul(pr2[c * 16 + u4 * 2 + h], dsm2), t2);
+            float ds0, ds1;
+            f32x2_unpack(ds2, ds0, ds1);
+            dsmax = fmax3(dsmax, fabsf(ds0), fabsf(ds1));
             pd[u4 * 2 + h] = pack_f16x2(ds0, ds1);
           }
         }
@@ -736,7 +750,7 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
     KernelTimer kt(MF_K_BWD_PRE, s);
     bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         reinterpret_cast<const uint4*>(a.o), reinterpret_cast<const uint4*>(a.d_o),
-        reinterpret_cast<const uint4*>(a.v), a.lse, a.lse2, a.delta, a.pad,
+        reinterpret_cast<const uint4*>(a.v), a.lse, a.nlse2, a.delta, a.pad,
         reinterpret_cast<float4*>(a.dq_acc), a.hmax, rows, a.T, a.heads);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -753,7 +767,7 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
   p.order = a.order;
   p.prefix = a.prefix;
   p.pos = a.pos;
-  p.lse2 = a.lse2;
+  p.nlse2 = a.nlse2;
   p.delta = a.delta;
   p.pad = a.pad;
   p.status = a.status;

@@ -71,14 +71,14 @@ __device__ __forceinline__ void rope_sincos_fast(float p, float w_hi, float w_lo
 // then 1024-aligned:  q16, k16  fp16 [T][h][d]  (rotated Q', K')
 // fwd only:           v16 fp16 [T][h][d]
 // bwd only:           hmax fp32 [2][h] (per-head max ||dO_j||, max ||v_k||),
-//                     pad fp32 [128] (64 x +inf, 64 x 0: LSE / D of rows past a
-//                     sample), lse2 fp32 [h][T] (LSE * log2 e), delta fp32 [h][T],
+//                     pad fp32 [128] (64 x -inf, 64 x 0: -LSE log2 e / D of rows
+//                     past a sample), nlse2 fp32 [h][T] (-LSE * log2 e), delta fp32 [h][T],
 //                     dq_acc fp32 [T][h][d]
 struct WsLayout {
   size_t status = 0;
   size_t order = 0, prefix = 0;
   size_t q16 = 0, k16 = 0, v16 = 0;
-  size_t hmax = 0, pad = 0, lse2 = 0, delta = 0, dq_acc = 0;
+  size_t hmax = 0, pad = 0, nlse2 = 0, delta = 0, dq_acc = 0;
   size_t total = 0;
 };
 WsLayout ws_layout(int64_t T, int64_t n, int64_t heads, int64_t head_dim, bool bwd);
@@ -133,8 +133,8 @@ struct AttnBwdArgs {
   const int32_t* prefix;
   uint32_t* status;
   float* hmax;    // [2][h]: max ||dO_j||, max ||v_k|| per head (zeroed by the schedule)
-  float* pad;     // [128]: 64 x +inf then 64 x 0 (written by the preprocess)
-  float* lse2;    // [h][T]: LSE * log2 e (written by the preprocess)
+  float* pad;     // [128]: 64 x -inf then 64 x 0 (written by the preprocess)
+  float* nlse2;   // [h][T]: -LSE * log2 e (written by the preprocess)
   float* delta;   // [h][T]
   float* dq_acc;  // [T][h][d]
   uint16_t* dq;
