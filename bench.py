@@ -379,23 +379,25 @@ def gpu_arm(args):
 
 
 def _recorded_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
-    summary was taken on the current kernel source (else None)."""
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/dram_mixed_50k.md, lines `traffic <kernel> <source> <sha16> <bytes>`),
+    if that summary was taken on the current kernel source (else None)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    path = os.path.join(ROOT, "profiles", "dram_mixed_50k.md")
     try:
-        with open(path) as f:
-            rec = json.load(f).get(kernel)
-    except (OSError, ValueError):
-        return None
-    if not rec:
-        return None
-    src = os.path.join(ROOT, "packed_resolution_diffusion_pack_b300", "csrc", rec["source"])
-    try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        lines = open(path).read().splitlines()
     except OSError:
         return None
-    return rec["bytes_per_launch"] if sha == rec.get("source_sha") else None
+    for line in lines:
+        parts = line.split()
+        if len(parts) == 5 and parts[0] == "traffic" and parts[1] == kernel:
+            src = os.path.join(ROOT, "packed_resolution_diffusion_pack_b300", "csrc", parts[2])
+            try:
+                sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+            except OSError:
+                return None
+            return int(parts[4]) if sha == parts[3] else None
+    return None
 
 
 def main():
