@@ -1,4 +1,5 @@
-"""FP64 CPU oracle for packed native-resolution 2D-RoPE varlen attention.
+"""FP64 CPU oracle for packed native-resolution 2D-RoPE varlen attention and its
+neighbours (packed-CFG Euler step, adaptive LayerNorm, gated residual).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
 ``bench.py``'s cpu_baseline / reference leg may import this package.  The product
@@ -61,8 +62,12 @@ def lib(so: str | None = None):
         L.oracle_attn_fwd.argtypes = [p, p, p, p, i64, p, i64, i64, i64, f64, f64, p, p]
         L.oracle_attn_bwd.argtypes = [p, p, p, p, p, i64, p, i64, i64, i64, f64, f64, p, p, p]
         L.oracle_attn_fwd_rows.argtypes = [p, p, p, p, i64, p, i64, i64, i64, f64, f64, p, i64, p, p]
+        L.oracle_cfg_euler.argtypes = [p, p, i64, i64, f64, f64, p, p]
+        L.oracle_adaln.argtypes = [p, p, i64, i64, p, p, f64, p]
+        L.oracle_gated_residual.argtypes = [p, p, p, i64, i64, p, p]
         for f in (L.oracle_pack, L.oracle_rope2d, L.oracle_attn_fwd, L.oracle_attn_bwd,
-                  L.oracle_attn_fwd_rows):
+                  L.oracle_attn_fwd_rows, L.oracle_cfg_euler, L.oracle_adaln,
+                  L.oracle_gated_residual):
             f.restype = ctypes.c_int
         _libs[key] = L
     return _libs[key]
@@ -148,6 +153,42 @@ def attn_bwd(q, k, v, d_o, cu, pos, scale=None, base: float = ROPE_BASE, so: str
                                  cu.ctypes.data, len(cu) - 1, _ptr(p), T, h, d, scale, base,
                                  dq.ctypes.data, dk.ctypes.data, dv.ctypes.data)
     return dq, dk, dv
+
+
+def cfg_euler(v, specs, guidance: float, dt: float, z, so: str | None = None):
+    """One packed-CFG rectified-flow Euler step: z + dt * (v_u + g (v_c - v_u)) on
+    each (cond, uncond) pair's image rows.  v [T, C], z [N, C] (float64);
+    specs = [(text_len, H, W)] * 2 pairs, cond then uncond per pair."""
+    v, z = _f64(v), _f64(z)
+    s = np.ascontiguousarray(np.asarray(specs, dtype=np.int64).reshape(-1, 3))
+    if s.shape[0] % 2:
+        raise ValueError("specs must hold (cond, uncond) pairs")
+    out = np.empty_like(z)
+    rc = lib(so).oracle_cfg_euler(v.ctypes.data, s.ctypes.data, s.shape[0] // 2, v.shape[1],
+                                  float(guidance), float(dt), z.ctypes.data, out.ctypes.data)
+    if rc != 0:
+        raise ValueError("a pair's two samples have different image grids")
+    return out
+
+
+def adaln(x, cu, shift, scale, eps: float = 1e-6, so: str | None = None):
+    """LN(x) * (1 + scale_s) + shift_s per token of sample s; x [T, Dm] (float64)."""
+    x, shift, scale = _f64(x), _f64(shift), _f64(scale)
+    cu = np.ascontiguousarray(cu, dtype=np.int64)
+    y = np.empty_like(x)
+    lib(so).oracle_adaln(x.ctypes.data, cu.ctypes.data, len(cu) - 1, x.shape[1],
+                         shift.ctypes.data, scale.ctypes.data, float(eps), y.ctypes.data)
+    return y
+
+
+def gated_residual(x, h, cu, gate, so: str | None = None):
+    """x + gate_s * h per token of sample s; x, h [T, Dm] (float64)."""
+    x, h, gate = _f64(x), _f64(h), _f64(gate)
+    cu = np.ascontiguousarray(cu, dtype=np.int64)
+    out = np.empty_like(x)
+    lib(so).oracle_gated_residual(x.ctypes.data, h.ctypes.data, cu.ctypes.data, len(cu) - 1,
+                                  x.shape[1], gate.ctypes.data, out.ctypes.data)
+    return out
 
 
 def sample_head_slice(x, cu, i: int, a: int):

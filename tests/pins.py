@@ -286,3 +286,140 @@ def pin_fwd_rows_match_full(so=None):
     for r, (t, a) in enumerate(rows):
         np.testing.assert_array_equal(orow[r], o[t, a])
         assert lrow[r] == lse[a, t]
+
+
+# ------------------------------------------------- packed CFG + Euler step
+def pin_cfg_euler_golden(so=None):
+    for case in _golden("cfg_euler.json")["cases"]:
+        out = oracle.cfg_euler(np.array(case["v"], float), case["specs"], case["g"], case["dt"],
+                               np.array(case["z"], float), so=so)
+        assert np.array_equal(out, np.array(case["z_out"])), out
+
+
+def _cfg_pack(rng, grids, texts, C):
+    specs = []
+    for (H, W), (tc, tu) in zip(grids, texts):
+        specs += [(tc, H, W), (tu, H, W)]
+    cu, _ = oracle.pack(specs)
+    return specs, cu, rng.standard_normal((int(cu[-1]), C))
+
+
+def pin_cfg_euler_straight_line(so=None):
+    """On a straight rectified-flow path z_t = (1 - t) z0 + t eps with both branches
+    predicting the exact velocity z0 - eps, one Euler step from t to t - dt lands
+    exactly on z_{t-dt} for any guidance scale (pins the step's sign and the velocity
+    convention against the pages' objective)."""
+    rng = _rng(11)
+    C = 8
+    specs, cu, v = _cfg_pack(rng, [(3, 5), (2, 2)], [(4, 1), (0, 6)], C)
+    N = 15 + 4
+    z0, eps = rng.standard_normal((N, C)), rng.standard_normal((N, C))
+    vel = z0 - eps
+    row = 0
+    for p in range(2):
+        tc, H, W = specs[2 * p]
+        tu = specs[2 * p + 1][0]
+        n = H * W
+        v[cu[2 * p] + tc: cu[2 * p] + tc + n] = vel[row:row + n]
+        v[cu[2 * p + 1] + tu: cu[2 * p + 1] + tu + n] = vel[row:row + n]
+        row += n
+    t, dt = 0.7, 0.25
+    for g in (0.0, 1.0, 4.5):
+        out = oracle.cfg_euler(v, specs, g, dt, (1 - t) * z0 + t * eps, so=so)
+        want = (1 - (t - dt)) * z0 + (t - dt) * eps
+        assert np.abs(out - want).max() < 1e-12, (g, np.abs(out - want).max())
+
+
+def pin_cfg_euler_branch_limits(so=None):
+    """g = 0 follows the unconditional branch and g = 1 the conditional one, each
+    read from its own sample's image rows (past its own text)."""
+    rng = _rng(12)
+    C = 4
+    specs, cu, v = _cfg_pack(rng, [(2, 3)], [(5, 2)], C)
+    z = rng.standard_normal((6, C))
+    dt = 0.125
+    vc = v[cu[0] + 5: cu[0] + 11]
+    vu = v[cu[1] + 2: cu[1] + 8]
+    # vu + (vc - vu) is vc up to one rounding of each operation
+    assert np.abs(oracle.cfg_euler(v, specs, 1.0, dt, z, so=so) - (z + dt * vc)).max() < 1e-14
+    assert np.array_equal(oracle.cfg_euler(v, specs, 0.0, dt, z, so=so), z + dt * vu)
+    assert np.array_equal(oracle.cfg_euler(v, specs, 2.0, 0.0, z, so=so), z)
+
+
+def pin_cfg_euler_pairs_independent(so=None):
+    rng = _rng(13)
+    C = 4
+    specs, cu, v = _cfg_pack(rng, [(2, 3), (4, 1), (1, 1)], [(5, 2), (0, 3), (2, 2)], C)
+    z = rng.standard_normal((6 + 4 + 1, C))
+    full = oracle.cfg_euler(v, specs, 2.5, 0.3, z, so=so)
+    row = 0
+    for p in range(3):
+        H, W = specs[2 * p][1], specs[2 * p][2]
+        part = oracle.cfg_euler(v[cu[2 * p]:cu[2 * p + 2]], specs[2 * p:2 * p + 2], 2.5, 0.3,
+                                z[row:row + H * W], so=so)
+        assert np.array_equal(part, full[row:row + H * W]), p
+        row += H * W
+
+
+# ------------------------------------------ adaptive LayerNorm, gated residual
+def _adaln_pack(rng, lens, Dm):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    return cu, rng.standard_normal((int(cu[-1]), Dm)) * 3.0 + 0.5
+
+
+def pin_adaln_vs_library(so=None):
+    """With zero modulation the block is plain LayerNorm without affine parameters:
+    torch's layer_norm in float64."""
+    rng = _rng(21)
+    Dm, eps = 48, 1e-6
+    cu, x = _adaln_pack(rng, [3, 0, 7, 1], Dm)
+    z = np.zeros((4, Dm))
+    y = oracle.adaln(x, cu, z, z, eps, so=so)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (Dm,), eps=eps).numpy()
+    assert np.abs(y - ref).max() < 1e-12, np.abs(y - ref).max()
+
+
+def pin_adaln_variance_closed_form(so=None):
+    """Each normalised row has mean 0 and variance var / (var + eps)."""
+    rng = _rng(22)
+    Dm, eps = 64, 0.25
+    cu, x = _adaln_pack(rng, [5, 3], Dm)
+    z = np.zeros((2, Dm))
+    y = oracle.adaln(x, cu, z, z, eps, so=so)
+    var = x.var(axis=1)
+    assert np.abs(y.mean(axis=1)).max() < 1e-12
+    assert np.abs(y.var(axis=1) - var / (var + eps)).max() < 1e-12
+
+
+def pin_adaln_modulation_per_sample(so=None):
+    """A constant row (small dyadic values, so its sum and mean are exact)
+    normalises to exactly 0, so its output is its own sample's shift; a row with a
+    +1/-1 pattern gets (1 + scale) times it."""
+    rng = _rng(23)
+    Dm = 16
+    cu = np.array([0, 2, 2, 5], dtype=np.int64)
+    x = np.repeat(rng.integers(-16, 16, size=(5, 1)) / 4.0, Dm, axis=1)
+    shift, scale = rng.standard_normal((3, Dm)), rng.standard_normal((3, Dm))
+    y = oracle.adaln(x, cu, shift, scale, 1e-6, so=so)
+    for s in range(3):
+        for t in range(cu[s], cu[s + 1]):
+            assert np.array_equal(y[t], shift[s]), (s, t)
+    alt = np.tile([1.0, -1.0], Dm // 2)[None, :].repeat(5, 0)
+    y = oracle.adaln(alt, cu, np.zeros((3, Dm)), scale, 0.0, so=so)
+    for s in range(3):
+        for t in range(cu[s], cu[s + 1]):
+            assert np.abs(y[t] - alt[t] * (1 + scale[s])).max() < 1e-15, (s, t)
+
+
+def pin_gated_residual(so=None):
+    rng = _rng(24)
+    Dm = 8
+    cu, x = _adaln_pack(rng, [2, 4, 1], Dm)
+    h = rng.standard_normal(x.shape)
+    zero = np.zeros((3, Dm))
+    assert np.array_equal(oracle.gated_residual(x, h, cu, zero, so=so), x)
+    gate = rng.standard_normal((3, Dm))
+    out = oracle.gated_residual(x, np.ones_like(x), cu, gate, so=so)
+    for s in range(3):
+        for t in range(cu[s], cu[s + 1]):
+            assert np.array_equal(out[t], x[t] + gate[s]), (s, t)

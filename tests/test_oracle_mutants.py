@@ -36,6 +36,18 @@ MUTANTS = [
      "dkr[rk + e] += ds * qr[rj + e];"),
     ("bwd_dq_unrotated_keys", "dqr[rj + e] += scale * ds * kr[rk + e];",
      "dqr[rj + e] += scale * ds * k[rk + e];"),
+    ("cfg_branches_swapped", "const double vg = vu + g * (vc - vu);",
+     "const double vg = vc + g * (vu - vc);"),
+    ("cfg_no_text_offset", "const int64_t img_c = start + sc[0];",
+     "const int64_t img_c = start;"),
+    ("cfg_step_sign", "z_in[(zrow + k) * C + e] + dt * vg;", "z_in[(zrow + k) * C + e] - dt * vg;"),
+    ("adaln_unbiased_variance", "var /= (double)Dm;", "var /= (double)(Dm - 1);"),
+    ("adaln_scale_without_one", "* (1.0 + scale[s * Dm + e]) + shift[s * Dm + e];",
+     "* scale[s * Dm + e] + shift[s * Dm + e];"),
+    ("adaln_first_sample_shift", "* (1.0 + scale[s * Dm + e]) + shift[s * Dm + e];",
+     "* (1.0 + scale[s * Dm + e]) + shift[e];"),
+    ("gated_first_sample_gate", "out[t * Dm + e] = x[t * Dm + e] + gate[s * Dm + e] * h[t * Dm + e];",
+     "out[t * Dm + e] = x[t * Dm + e] + gate[e] * h[t * Dm + e];"),
 ]
 
 
