@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--budget", type=int, default=None,
                     help="token budget of the packed workload (default 50,000)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the timing of the attention's memory-bound neighbours")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     return ap.parse_args()
 
@@ -368,6 +370,8 @@ def gpu_arm(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks,
     }
+    if not args.no_extras:
+        line["extras"] = neighbours(mf, wl, pk["hbm_gbs"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, q, k, v, do, args.cpu_budget_s)
     if rank == 0:
@@ -376,6 +380,53 @@ def gpu_arm(args):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def neighbours(mf, wl, hbm_gbs, reps=20):
+    """Device time and HBM throughput of the memory-bound neighbours of the
+    attention, outside the timed step: the adaptive LayerNorm modulation and the
+    gated residual on this pack's [T, heads x head_dim] activations, and the
+    packed-CFG Euler step on 32 2048^2 (cond, uncond) pairs with 64 latent
+    channels (every working set is above the 126 MB L2).  Algorithmic bytes: adaLN reads x and writes y (4 T Dm); the gated
+    residual reads x, h and writes out (6 T Dm); the CFG step reads both branches'
+    bf16 image rows and reads and writes the fp32 latent (12 N C)."""
+    import torch
+    T, Dm, n = wl.total, wl.heads * wl.head_dim, len(wl.specs)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(wl.lengths)]), dtype=torch.int32, device="cuda")
+    x = synth.bits_to_torch(synth.normal_bf16_bits(wl.seed, 32, (T, Dm))).cuda()
+    h = synth.bits_to_torch(synth.normal_bf16_bits(wl.seed, 35, (T, Dm))).cuda()
+    vec = synth.bits_to_torch(synth.normal_bf16_bits(wl.seed, 33, (n, Dm))).cuda()
+    y = torch.empty_like(x)
+    specs = [(512, 128, 128), (64, 128, 128)] * 32
+    Tc, _ = mf.pack_size(specs)
+    C = 64
+    v = synth.bits_to_torch(synth.normal_bf16_bits(wl.seed, 30, (Tc, C))).cuda()
+    N = 32 * 128 * 128
+    z = torch.zeros((N, C), dtype=torch.float32, device="cuda")
+    cases = {
+        "adaln_modulate": (lambda: mf.adaln_modulate(x, cu, vec, vec, 1e-6, y=y), 4.0 * T * Dm,
+                           f"T={T}, Dm={Dm}, bf16"),
+        "gated_residual": (lambda: mf.gated_residual(x, h, cu, vec, out=y), 6.0 * T * Dm,
+                           f"T={T}, Dm={Dm}, bf16"),
+        "cfg_euler_step": (lambda: mf.cfg_euler_step(v, specs, 4.0, 0.05, z), 12.0 * N * C,
+                           f"32 pairs of 2048^2 (16384 image tokens each), C={C}"),
+    }
+    out = {}
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for name, (fn, nbytes, shape) in cases.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ev0.record()
+        for _ in range(reps):
+            fn()
+        ev1.record()
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / reps
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"ms": ms, "achieved_gbs": gbs, "frac_of_hbm": gbs / hbm_gbs, "shape": shape,
+                     "bytes": nbytes}
+    return out
 
 
 def _recorded_traffic(kernel):

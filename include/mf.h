@@ -203,6 +203,59 @@ mf_status mf_varlen_attn_fwd_noalloc(const mf_bf16* q, const mf_bf16* k, const m
                                      float* lse, mf_stream stream);
 
 /*
+ * Packed classifier-free guidance followed by one rectified-flow Euler step.
+ * The conditional and unconditional branches of each image are two samples of
+ * one packed forward pass (paperlayer.ai summary 3.2.1 "Model Architecture and
+ * Native Packing"; hyper.ai summary "Experiment": the denoising trajectory is
+ * unchanged).  The pages give the flow-matching objective (hyper.ai "Method":
+ * z_t = (1 - t) z + t eps, the network regresses z - eps), so a step from t to
+ * t - dt is z <- z + dt v; they print no guidance formula, and the standard
+ * v = v_u + g (v_c - v_u) is used.
+ * v: DEVICE bf16 [T][C], the model's packed output for 2 * pairs samples laid out
+ *    as mf_pack lays out `specs` (T = the pack's total).
+ * specs: HOST int32 [2 * pairs][3] = {text_len, H, W}: pair p is samples 2p (cond)
+ *    and 2p + 1 (uncond), which must have the same H and W.
+ * z: DEVICE fp32 [N][C], N = sum_p H_p * W_p: each pair's image latent rows in pair
+ *    order, updated in place: z[row] += dt * (v_u[row] + g (v_c[row] - v_u[row]))
+ *    with v_c / v_u the pair's image-token rows of v (after each sample's text).
+ * Arithmetic in fp32.  C must be a positive multiple of 8 and v, z 16-byte
+ * aligned (else MF_ERR_UNSUPPORTED); negative entries, a pair whose grids differ
+ * or a NULL pointer with work to do: MF_ERR_INVALID_ARG; totals beyond int32:
+ * MF_ERR_OVERFLOW.
+ */
+mf_status mf_cfg_euler_step(const mf_bf16* v, const int32_t* specs, int32_t pairs, int32_t C,
+                            float guidance, float dt, float* z, mf_stream stream);
+
+/*
+ * Adaptive LayerNorm modulation of a packed batch (the input side of the fused
+ * Transformer chain of paperlayer.ai summary 3.3 "Training Infrastructure":
+ * adaptive normalization, rotary embeddings and gated residual updates).  The
+ * pages print no formula; the DiT-style block is used: for every token t of
+ * sample s (by d_cu_seqlens),
+ *   y_t = (x_t - mean_t) / sqrt(var_t + eps) * (1 + scale_s) + shift_s,
+ * mean and biased variance over the Dm features, no affine parameters.
+ * x, y: DEVICE bf16 [T][Dm] (y == x allowed); shift, scale: DEVICE bf16 [n][Dm];
+ * d_cu_seqlens: DEVICE int32 [n+1] as for the attention.  fp32 arithmetic.
+ * Dm must be a multiple of 8 and at most 4096, pointers 16-byte aligned (else
+ * MF_ERR_UNSUPPORTED); n = 0 with T > 0, eps < 0 or NULL pointers:
+ * MF_ERR_INVALID_ARG.  A malformed cu_seqlens gives wrong rows, never an
+ * out-of-range access (every row maps to a sample index in [0, n)).
+ */
+mf_status mf_adaln_modulate(const mf_bf16* x, const int32_t* d_cu_seqlens, int32_t n, int32_t T,
+                            int32_t Dm, const mf_bf16* shift, const mf_bf16* scale, float eps,
+                            mf_bf16* y, mf_stream stream);
+
+/*
+ * Gated residual update of a packed batch (output side of the same fused chain):
+ * out_t = x_t + gate_s * h_t for every token t of sample s.  x, h, out: DEVICE bf16
+ * [T][Dm] (out may alias x or h); gate: DEVICE bf16 [n][Dm].  fp32 arithmetic.
+ * Same shape rules and errors as mf_adaln_modulate (any Dm multiple of 8).
+ */
+mf_status mf_gated_residual(const mf_bf16* x, const mf_bf16* h, const int32_t* d_cu_seqlens,
+                            int32_t n, int32_t T, int32_t Dm, const mf_bf16* gate, mf_bf16* out,
+                            mf_stream stream);
+
+/*
  * Synchronise `stream` and report device-side errors recorded in `ws` by the last
  * mf_varlen_attn_* call that used it: MF_ERR_BAD_SEQLENS, MF_ERR_TIMEOUT, or
  * MF_ERR_CUDA if the stream itself failed; MF_OK otherwise.
@@ -217,11 +270,12 @@ mf_status mf_get_status(void* ws, mf_stream stream);
  * the recorded events and returns, for kernel `id`, the summed device time in
  * milliseconds and the number of launches since the last reset.  Ids:
  *   MF_K_PACK 0, MF_K_ROPE 1, MF_K_SCHEDULE 2, MF_K_ATTN_FWD 3, MF_K_BWD_PRE 4,
- *   MF_K_ATTN_BWD 5, MF_K_DQ_POST 6.
+ *   MF_K_ATTN_BWD 5, MF_K_DQ_POST 6, MF_K_CFG_EULER 7, MF_K_ADALN 8,
+ *   MF_K_GATED_RESIDUAL 9.
  * Process-wide state guarded by a mutex; not for use under stream capture.
  */
 enum { MF_K_PACK = 0, MF_K_ROPE, MF_K_SCHEDULE, MF_K_ATTN_FWD, MF_K_BWD_PRE, MF_K_ATTN_BWD,
-       MF_K_DQ_POST, MF_K_COUNT };
+       MF_K_DQ_POST, MF_K_CFG_EULER, MF_K_ADALN, MF_K_GATED_RESIDUAL, MF_K_COUNT };
 mf_status mf_timing_enable(int32_t on);
 mf_status mf_timing_reset(void);
 mf_status mf_timing_read(int32_t id, double* total_ms, int64_t* launches);

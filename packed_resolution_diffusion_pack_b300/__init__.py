@@ -18,6 +18,7 @@ from ._lib import MFError, STATUS_NAMES, check, library_path, load
 __all__ = [
     "MFError", "STATUS_NAMES", "load", "library_path", "pack_size", "pack", "rope2d_qk",
     "attn_workspace_bytes", "workspace", "varlen_attn_fwd", "varlen_attn_bwd", "get_status",
+    "cfg_euler_step", "adaln_modulate", "gated_residual",
 ]
 
 
@@ -170,6 +171,67 @@ def varlen_attn_fwd_noalloc(q, k, v, cu_seqlens, pos, max_len, softmax_scale: fl
                                             _ptr(lse), _stream_ptr(stream)),
           "mf_varlen_attn_fwd_noalloc")
     return o, lse
+
+
+def cfg_euler_step(v, specs, guidance: float, dt: float, z, stream=None):
+    """One packed-CFG rectified-flow Euler step, in place on z (fp32 [N, C]):
+    z += dt * (v_u + guidance (v_c - v_u)) over each (cond, uncond) pair's image
+    rows of the packed model output v (bf16 [T, C]).  specs: (text_len, H, W) of
+    the 2 * pairs samples, cond then uncond per pair."""
+    torch = _torch()
+    if v.dtype != torch.bfloat16 or v.dim() != 2 or not v.is_cuda or not v.is_contiguous():
+        raise ValueError("v must be a contiguous CUDA bf16 tensor [T, C]")
+    if z.dtype != torch.float32 or z.dim() != 2 or not z.is_cuda or not z.is_contiguous():
+        raise ValueError("z must be a contiguous CUDA fp32 tensor [N, C]")
+    arr, n = _specs_array(specs)
+    if n % 2:
+        raise ValueError("specs must hold (cond, uncond) pairs")
+    T, _ = pack_size(specs)
+    N = sum(int(s[1]) * int(s[2]) for s in specs[0::2])
+    C = v.shape[1]
+    if v.shape[0] != T or z.shape != (N, C):
+        raise ValueError(f"v {tuple(v.shape)} / z {tuple(z.shape)} do not match the specs ({T}, {N}, {C})")
+    check(load().mf_cfg_euler_step(_ptr(v), arr, n // 2, C, float(guidance), float(dt), _ptr(z),
+                                   _stream_ptr(stream)), "mf_cfg_euler_step")
+    return z
+
+
+def _check_rows(name, t, T=None, Dm=None):
+    torch = _torch()
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 2:
+        raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor [rows, Dm]")
+    if (T is not None and t.shape[0] != T) or (Dm is not None and t.shape[1] != Dm):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected ({T}, {Dm})")
+
+
+def adaln_modulate(x, cu_seqlens, shift, scale, eps: float = 1e-6, y=None, stream=None):
+    """LN(x) (1 + scale_s) + shift_s for every token of sample s (bf16 [T, Dm])."""
+    torch = _torch()
+    _check_rows("x", x)
+    T, Dm = x.shape
+    n = cu_seqlens.numel() - 1
+    _check_rows("shift", shift, n, Dm)
+    _check_rows("scale", scale, n, Dm)
+    y = torch.empty_like(x) if y is None else y
+    _check_rows("y", y, T, Dm)
+    check(load().mf_adaln_modulate(_ptr(x), _ptr(cu_seqlens), n, T, Dm, _ptr(shift), _ptr(scale),
+                                   float(eps), _ptr(y), _stream_ptr(stream)), "mf_adaln_modulate")
+    return y
+
+
+def gated_residual(x, h, cu_seqlens, gate, out=None, stream=None):
+    """x + gate_s * h for every token of sample s (bf16 [T, Dm])."""
+    torch = _torch()
+    _check_rows("x", x)
+    T, Dm = x.shape
+    n = cu_seqlens.numel() - 1
+    _check_rows("h", h, T, Dm)
+    _check_rows("gate", gate, n, Dm)
+    out = torch.empty_like(x) if out is None else out
+    _check_rows("out", out, T, Dm)
+    check(load().mf_gated_residual(_ptr(x), _ptr(h), _ptr(cu_seqlens), n, T, Dm, _ptr(gate),
+                                   _ptr(out), _stream_ptr(stream)), "mf_gated_residual")
+    return out
 
 
 def get_status(ws, stream=None) -> None:

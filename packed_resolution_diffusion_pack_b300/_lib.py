@@ -35,6 +35,9 @@ SIGNATURES = {
                                           _i32, _f32, _p, _p, _p, _p, _sz, _p]),
     "mf_varlen_attn_fwd_noalloc": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32,
                                                   _i32, _f32, _p, _p, _p]),
+    "mf_cfg_euler_step": (ctypes.c_int, [_p, _p, _i32, _i32, _f32, _f32, _p, _p]),
+    "mf_adaln_modulate": (ctypes.c_int, [_p, _p, _i32, _i32, _i32, _p, _p, _f32, _p, _p]),
+    "mf_gated_residual": (ctypes.c_int, [_p, _p, _p, _i32, _i32, _i32, _p, _p, _p]),
     "mf_get_status": (ctypes.c_int, [_p, _p]),
     "mf_timing_enable": (ctypes.c_int, [_i32]),
     "mf_timing_reset": (ctypes.c_int, []),
@@ -42,7 +45,8 @@ SIGNATURES = {
 }
 
 # kernel ids of the opt-in timing (mf.h MF_K_*)
-KERNELS = ["pack", "rope", "schedule", "attn_fwd", "bwd_pre", "attn_bwd", "dq_post"]
+KERNELS = ["pack", "rope", "schedule", "attn_fwd", "bwd_pre", "attn_bwd", "dq_post", "cfg_euler",
+           "adaln", "gated_residual"]
 
 
 class MFError(RuntimeError):

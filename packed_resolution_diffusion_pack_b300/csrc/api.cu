@@ -245,6 +245,64 @@ mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
   return cuda_status(launch_attn_bwd(a, s));
 }
 
+mf_status mf_cfg_euler_step(const mf_bf16* v, const int32_t* specs, int32_t pairs, int32_t C,
+                            float guidance, float dt, float* z, mf_stream stream) {
+  if (pairs < 0 || C <= 0 || (pairs > 0 && specs == nullptr)) return MF_ERR_INVALID_ARG;
+  if (C % 8 != 0) return MF_ERR_UNSUPPORTED;
+  int64_t T = 0, N = 0;
+  for (int32_t p = 0; p < pairs; ++p) {
+    const int32_t* sc = specs + 6 * p;
+    const int32_t* su = sc + 3;
+    for (int i = 0; i < 6; ++i)
+      if (sc[i] < 0) return MF_ERR_INVALID_ARG;
+    if (sc[1] != su[1] || sc[2] != su[2]) return MF_ERR_INVALID_ARG;
+    const int64_t n_img = static_cast<int64_t>(sc[1]) * sc[2];
+    T += static_cast<int64_t>(sc[0]) + su[0] + 2 * n_img;
+    N += n_img;
+  }
+  if (T > INT32_MAX || N > INT32_MAX || T * (C / 8) > INT64_MAX / 16) return MF_ERR_OVERFLOW;
+  if (N == 0) return MF_OK;
+  if (v == nullptr || z == nullptr) return MF_ERR_INVALID_ARG;
+  if (!aligned(v, 16) || !aligned(z, 16)) return MF_ERR_UNSUPPORTED;
+  return cuda_status(launch_cfg_euler(v, specs, pairs, C, guidance, dt, z,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+// Shared checks of the row-wise packed neighbours.
+static mf_status check_rows(const void* const* ptrs, int nptr, const int32_t* cu, int32_t n,
+                            int32_t T, int32_t Dm, int32_t max_dm) {
+  if (n < 0 || T < 0 || Dm <= 0 || (T > 0 && n == 0)) return MF_ERR_INVALID_ARG;
+  if (Dm % 8 != 0 || Dm > max_dm) return MF_ERR_UNSUPPORTED;
+  if (T == 0) return MF_OK;
+  if (cu == nullptr) return MF_ERR_INVALID_ARG;
+  for (int i = 0; i < nptr; ++i) {
+    if (ptrs[i] == nullptr) return MF_ERR_INVALID_ARG;
+    if (!aligned(ptrs[i], 16)) return MF_ERR_UNSUPPORTED;
+  }
+  return MF_OK;
+}
+
+mf_status mf_adaln_modulate(const mf_bf16* x, const int32_t* d_cu_seqlens, int32_t n, int32_t T,
+                            int32_t Dm, const mf_bf16* shift, const mf_bf16* scale, float eps,
+                            mf_bf16* y, mf_stream stream) {
+  const void* ptrs[4] = {x, shift, scale, y};
+  const mf_status st = check_rows(ptrs, 4, d_cu_seqlens, n, T, Dm, 4096);
+  if (st != MF_OK) return st;
+  if (!(eps >= 0.f)) return MF_ERR_INVALID_ARG;
+  return cuda_status(launch_adaln(x, d_cu_seqlens, n, T, Dm, shift, scale, eps, y,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+mf_status mf_gated_residual(const mf_bf16* x, const mf_bf16* h, const int32_t* d_cu_seqlens,
+                            int32_t n, int32_t T, int32_t Dm, const mf_bf16* gate, mf_bf16* out,
+                            mf_stream stream) {
+  const void* ptrs[4] = {x, h, gate, out};
+  const mf_status st = check_rows(ptrs, 4, d_cu_seqlens, n, T, Dm, INT32_MAX);
+  if (st != MF_OK) return st;
+  return cuda_status(launch_gated_residual(x, h, d_cu_seqlens, n, T, Dm, gate, out,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 mf_status mf_get_status(void* ws, mf_stream stream) {
   if (ws == nullptr) return MF_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

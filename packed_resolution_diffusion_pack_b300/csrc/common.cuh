@@ -145,6 +145,16 @@ struct AttnBwdArgs {
 };
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, cudaStream_t s);
 
+// Neighbours of the attention (neighbors.cu).  specs: host [2 * pairs][3].
+cudaError_t launch_cfg_euler(const uint16_t* v, const int32_t* specs, int32_t pairs, int32_t C,
+                             float g, float dt, float* z, cudaStream_t s);
+cudaError_t launch_adaln(const uint16_t* x, const int32_t* cu, int32_t n, int32_t T, int32_t Dm,
+                         const uint16_t* shift, const uint16_t* scale, float eps, uint16_t* y,
+                         cudaStream_t s);
+cudaError_t launch_gated_residual(const uint16_t* x, const uint16_t* h, const int32_t* cu,
+                                  int32_t n, int32_t T, int32_t Dm, const uint16_t* gate,
+                                  uint16_t* out, cudaStream_t s);
+
 // RAII bracket of one kernel launch for the opt-in timing (mf_timing_*): records
 // an event on `s` when built and another when destroyed; no-op when disabled.
 class KernelTimer {

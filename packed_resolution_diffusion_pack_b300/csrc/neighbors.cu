@@ -1,0 +1,289 @@
+// Memory-bound neighbours of the packed attention: the packed-CFG rectified-flow
+// Euler step, the adaptive LayerNorm modulation that feeds the QKV projection and
+// the gated residual after the attention's output projection.
+//
+// Packed CFG (paperlayer.ai summary 3.2.1; hyper.ai "Experiment"): the
+// conditional and unconditional branches are two samples of one packed pass; per
+// pair, v = v_u + g (v_c - v_u) over the image rows, then one rectified-flow Euler
+// step z <- z + dt v (hyper.ai "Method": z_t = (1 - t) z + t eps, the network
+// regresses z - eps).
+// Adaptive LayerNorm and gated residual (paperlayer.ai summary 3.3: the
+// Transformer-side fused chain of adaptive normalization, rotary embeddings and
+// gated residual updates): per sample s, y = LN(x) (1 + scale_s) + shift_s and
+// out = x + gate_s h, every token using its own sample's vectors (cu_seqlens).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace mf {
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+// Sample holding row t: the last s in [0, n) with cu[s] <= t (zero-length samples
+// share a start; the last of them is the one that holds t).  Always in [0, n).
+__device__ __forceinline__ int32_t sample_of(const int32_t* __restrict__ cu, int32_t n, int32_t t) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------- CFG Euler step
+constexpr int kCfgChunk = 256;  // pairs per launch (kernel parameter space)
+
+struct CfgChunk {
+  int32_t count;
+  int32_t z_begin;                // first latent row of the chunk
+  int32_t z_end;                  // one past its last latent row
+  int32_t z_start[kCfgChunk];     // first latent row of each pair
+  int32_t img_c[kCfgChunk];       // first image token of the conditional sample
+  int32_t img_u[kCfgChunk];       // first image token of the unconditional sample
+};
+
+// One thread = 8 channels of one latent row.
+__global__ void __launch_bounds__(256) cfg_euler_kernel(const __grid_constant__ CfgChunk c,
+                                                        const uint4* __restrict__ v,
+                                                        float4* __restrict__ z, int32_t C8,
+                                                        float g, float dt) {
+  __shared__ int32_t s_zs[kCfgChunk];
+  for (int i = threadIdx.x; i < c.count; i += blockDim.x) s_zs[i] = c.z_start[i];
+  __syncthreads();
+  const int64_t nrow = c.z_end - c.z_begin;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       idx < nrow * C8; idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int32_t row = c.z_begin + static_cast<int32_t>(idx / C8);
+    const int32_t grp = static_cast<int32_t>(idx % C8);
+    int lo = 0, hi = c.count - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_zs[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    const int32_t k = row - s_zs[lo];
+    float vc[8], vu[8];
+    bf16x8_to_f32(v[static_cast<int64_t>(c.img_c[lo] + k) * C8 + grp], vc);
+    bf16x8_to_f32(v[static_cast<int64_t>(c.img_u[lo] + k) * C8 + grp], vu);
+    float4* zp = z + (static_cast<int64_t>(row) * C8 + grp) * 2;
+    float4 a = zp[0], b = zp[1];
+    float zz[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) zz[e] = fmaf(dt, fmaf(g, vc[e] - vu[e], vu[e]), zz[e]);
+    zp[0] = make_float4(zz[0], zz[1], zz[2], zz[3]);
+    zp[1] = make_float4(zz[4], zz[5], zz[6], zz[7]);
+  }
+}
+
+cudaError_t launch_cfg_euler(const uint16_t* v, const int32_t* specs, int32_t pairs, int32_t C,
+                             float g, float dt, float* z, cudaStream_t s) {
+  int64_t tok = 0, zrow = 0;
+  for (int32_t first = 0; first < pairs; first += kCfgChunk) {
+    CfgChunk c{};
+    c.count = pairs - first < kCfgChunk ? pairs - first : kCfgChunk;
+    c.z_begin = static_cast<int32_t>(zrow);
+    for (int i = 0; i < c.count; ++i) {
+      const int32_t* sc = specs + 6 * (first + i);
+      const int32_t* su = sc + 3;
+      const int64_t n_img = static_cast<int64_t>(sc[1]) * sc[2];
+      c.z_start[i] = static_cast<int32_t>(zrow);
+      c.img_c[i] = static_cast<int32_t>(tok + sc[0]);
+      const int64_t Lc = sc[0] + n_img;
+      c.img_u[i] = static_cast<int32_t>(tok + Lc + su[0]);
+      tok += Lc + su[0] + n_img;
+      zrow += n_img;
+    }
+    c.z_end = static_cast<int32_t>(zrow);
+    const int64_t work = static_cast<int64_t>(c.z_end - c.z_begin) * (C / 8);
+    if (work == 0) continue;
+    const int64_t want = (work + 255) / 256;
+    const int blocks = static_cast<int>(want < 148 * 16 ? want : 148 * 16);
+    KernelTimer kt(MF_K_CFG_EULER, s);
+    cfg_euler_kernel<<<blocks, 256, 0, s>>>(c, reinterpret_cast<const uint4*>(v),
+                                            reinterpret_cast<float4*>(z), C / 8, g, dt);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// --------------------------------------------- adaptive LayerNorm, residual
+constexpr int kRowWarps = 8;        // rows (warps) per block
+constexpr int kCuSmem = 2048;       // cu_seqlens entries cached in shared memory
+
+// Sample of row t from the block's cached cu_seqlens (or global memory when the
+// pack has more samples than the cache holds).
+struct CuView {
+  const int32_t* g;
+  const int32_t* s;  // shared copy, or null
+  int32_t n;
+  __device__ __forceinline__ int32_t sample(int32_t t) const {
+    if (s == nullptr) return sample_of(g, n, t);
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  }
+};
+__device__ __forceinline__ CuView cache_cu(const int32_t* __restrict__ cu, int32_t n,
+                                           int32_t* smem) {
+  const bool fits = n + 1 <= kCuSmem;
+  if (fits)
+    for (int i = threadIdx.x; i <= n; i += blockDim.x) smem[i] = cu[i];
+  __syncthreads();
+  return CuView{cu, fits ? smem : nullptr, n};
+}
+
+// One warp = one row of Dm = 256 * NCH features at most (NCH 16-byte chunks per
+// lane); the row stays in registers between the mean, the variance (a second
+// pass over the registers) and the modulation.
+template <int NCH>
+__global__ void __launch_bounds__(32 * kRowWarps, 2) adaln_kernel(
+    const uint4* __restrict__ x, const int32_t* __restrict__ cu, int32_t n, int32_t T,
+    int32_t D8, const uint4* __restrict__ shift, const uint4* __restrict__ scale, float eps,
+    uint4* __restrict__ y) {
+  __shared__ int32_t s_cu[kCuSmem];
+  const CuView cv = cache_cu(cu, n, s_cu);
+  const int lane = threadIdx.x & 31;
+  const float inv_dm = 1.f / static_cast<float>(D8 * 8);
+  for (int32_t t = blockIdx.x * kRowWarps + (threadIdx.x >> 5); t < T;
+       t += gridDim.x * kRowWarps) {
+    const int64_t base = static_cast<int64_t>(t) * D8;
+    uint4 xv[NCH];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const int ch = lane + 32 * i;
+      xv[i] = ch < D8 ? x[base + ch] : make_uint4(0, 0, 0, 0);
+    }
+    const int64_t mbase = static_cast<int64_t>(cv.sample(t)) * D8;
+    // sums as independent per-chunk partials (short dependency chains)
+    float part[NCH];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      float f[8];
+      bf16x8_to_f32(xv[i], f);
+      part[i] = ((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]));
+    }
+#pragma unroll
+    for (int w = 1; w < NCH; w <<= 1)
+#pragma unroll
+      for (int i = 0; i + w < NCH; i += 2 * w) part[i] += part[i + w];
+    float sum = part[0];
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
+    const float mean = sum * inv_dm;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      float f[8];
+      bf16x8_to_f32(xv[i], f);
+      float a = 0.f, b = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        a = fmaf(f[e] - mean, f[e] - mean, a);
+        b = fmaf(f[e + 1] - mean, f[e + 1] - mean, b);
+      }
+      part[i] = lane + 32 * i < D8 ? a + b : 0.f;
+    }
+#pragma unroll
+    for (int w = 1; w < NCH; w <<= 1)
+#pragma unroll
+      for (int i = 0; i + w < NCH; i += 2 * w) part[i] += part[i + w];
+    float sq = part[0];
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, m);
+    const float rstd = rsqrtf(sq * inv_dm + eps);
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+      const int ch = lane + 32 * i;
+      if (ch < D8) {
+        float f[8], sh[8], sc[8];
+        bf16x8_to_f32(xv[i], f);
+        bf16x8_to_f32(__ldg(shift + mbase + ch), sh);
+        bf16x8_to_f32(__ldg(scale + mbase + ch), sc);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = fmaf((f[e] - mean) * rstd, 1.f + sc[e], sh[e]);
+        y[base + ch] = f32_to_bf16x8(f);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(32 * kRowWarps) gated_residual_kernel(
+    const uint4* __restrict__ x, const uint4* __restrict__ h, const int32_t* __restrict__ cu,
+    int32_t n, int32_t T, int32_t D8, const uint4* __restrict__ gate, uint4* __restrict__ out) {
+  __shared__ int32_t s_cu[kCuSmem];
+  const CuView cv = cache_cu(cu, n, s_cu);
+  const int lane = threadIdx.x & 31;
+  for (int32_t t = blockIdx.x * kRowWarps + (threadIdx.x >> 5); t < T;
+       t += gridDim.x * kRowWarps) {
+    const int64_t base = static_cast<int64_t>(t) * D8;
+    const int64_t gbase = static_cast<int64_t>(cv.sample(t)) * D8;
+    for (int ch = lane; ch < D8; ch += 32) {
+      float a[8], b[8], gg[8];
+      bf16x8_to_f32(x[base + ch], a);
+      bf16x8_to_f32(h[base + ch], b);
+      bf16x8_to_f32(__ldg(gate + gbase + ch), gg);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a[e] = fmaf(gg[e], b[e], a[e]);
+      out[base + ch] = f32_to_bf16x8(a);
+    }
+  }
+}
+
+// Grid of a row kernel: every block resident at once (SMs x blocks per SM from
+// the occupancy calculator), each striding over rows, capped by the row count.
+template <typename K>
+static int row_blocks(K kernel, int32_t T) {
+  int dev = 0, sms = 148, per_sm = 1;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 32 * kRowWarps, 0) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t want = (static_cast<int64_t>(T) + kRowWarps - 1) / kRowWarps;
+  const int64_t full = static_cast<int64_t>(sms) * per_sm;
+  return static_cast<int>(want < full ? want : full);
+}
+
+cudaError_t launch_adaln(const uint16_t* x, const int32_t* cu, int32_t n, int32_t T, int32_t Dm,
+                         const uint16_t* shift, const uint16_t* scale, float eps, uint16_t* y,
+                         cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int nch = (Dm / 8 + 31) / 32;  // 16-byte chunks per lane (Dm <= 4096: at most 16)
+  auto* kern = nch <= 4 ? adaln_kernel<4> : nch <= 8 ? adaln_kernel<8>
+             : nch <= 12 ? adaln_kernel<12> : adaln_kernel<16>;
+  KernelTimer kt(MF_K_ADALN, s);
+  kern<<<row_blocks(kern, T), 32 * kRowWarps, 0, s>>>(
+      reinterpret_cast<const uint4*>(x), cu, n, T, Dm / 8, reinterpret_cast<const uint4*>(shift),
+      reinterpret_cast<const uint4*>(scale), eps, reinterpret_cast<uint4*>(y));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gated_residual(const uint16_t* x, const uint16_t* h, const int32_t* cu,
+                                  int32_t n, int32_t T, int32_t Dm, const uint16_t* gate,
+                                  uint16_t* out, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  KernelTimer kt(MF_K_GATED_RESIDUAL, s);
+  const int64_t want = (static_cast<int64_t>(T) + kRowWarps - 1) / kRowWarps;
+  gated_residual_kernel<<<static_cast<unsigned>(want < 148 * 32 ? want : 148 * 32), 32 * kRowWarps,
+                          0, s>>>(
+      reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(h), cu, n, T, Dm / 8,
+      reinterpret_cast<const uint4*>(gate), reinterpret_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace mf

@@ -93,3 +93,34 @@ def test_rope_argument_errors_on_host():
 
 def test_get_status_rejects_null():
     assert mf.load().mf_get_status(None, None) == 1
+
+
+def test_neighbour_argument_errors_on_host():
+    lib = mf.load()
+    p = ctypes.c_void_p
+    spec = lambda rows: (ctypes.c_int32 * (3 * len(rows)))(*[x for r in rows for x in r])  # noqa: E731
+    good = spec([(1, 2, 3), (4, 2, 3)])
+    base = 1 << 20
+    # CFG step: every case rejected (or empty) before any launch
+    assert lib.mf_cfg_euler_step(p(base), good, 1, 12, 2.0, 0.1, p(base + 4096), None) == 2  # C % 8
+    assert lib.mf_cfg_euler_step(p(base), good, -1, 8, 2.0, 0.1, p(base + 4096), None) == 1
+    assert lib.mf_cfg_euler_step(p(base), spec([(1, 2, 3), (4, 3, 2)]), 1, 8, 2.0, 0.1,
+                                 p(base + 4096), None) == 1  # grids differ
+    assert lib.mf_cfg_euler_step(p(base), spec([(1, 2, 3), (-4, 2, 3)]), 1, 8, 2.0, 0.1,
+                                 p(base + 4096), None) == 1
+    assert lib.mf_cfg_euler_step(p(base + 8), good, 1, 8, 2.0, 0.1, p(base + 4096), None) == 2
+    assert lib.mf_cfg_euler_step(None, good, 1, 8, 2.0, 0.1, p(base + 4096), None) == 1
+    assert lib.mf_cfg_euler_step(None, spec([(1, 0, 3), (4, 0, 3)]), 1, 8, 2.0, 0.1, None, None) == 0
+    # adaptive LayerNorm / gated residual
+    x, s1, s2, y = p(base), p(base + 4096), p(base + 8192), p(base + 12288)
+    cu = p(base + 16384)
+    assert lib.mf_adaln_modulate(x, cu, 2, 10, 4104, s1, s2, 1e-6, y, None) == 2  # Dm > 4096
+    assert lib.mf_adaln_modulate(x, cu, 2, 10, 12, s1, s2, 1e-6, y, None) == 2    # Dm % 8
+    assert lib.mf_adaln_modulate(x, cu, 0, 10, 64, s1, s2, 1e-6, y, None) == 1    # no samples
+    assert lib.mf_adaln_modulate(x, cu, 2, 10, 64, s1, s2, -1.0, y, None) == 1    # eps < 0
+    assert lib.mf_adaln_modulate(p(base + 4), cu, 2, 10, 64, s1, s2, 1e-6, y, None) == 2
+    assert lib.mf_adaln_modulate(x, None, 2, 10, 64, s1, s2, 1e-6, y, None) == 1
+    assert lib.mf_adaln_modulate(None, None, 0, 0, 64, None, None, 1e-6, None, None) == 0
+    assert lib.mf_gated_residual(x, s1, cu, 2, 10, 60, s2, y, None) == 2
+    assert lib.mf_gated_residual(x, None, cu, 2, 10, 64, s2, y, None) == 1
+    assert lib.mf_gated_residual(x, s1, cu, -1, 10, 64, s2, y, None) == 1
