@@ -1,5 +1,6 @@
 """FP64 CPU oracle for packed native-resolution 2D-RoPE varlen attention and its
-neighbours (packed-CFG Euler step, adaptive LayerNorm, gated residual).
+neighbours (frame-aware 3D RoPE for editing packs, packed-CFG Euler step,
+adaptive LayerNorm, gated residual).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
 ``bench.py``'s cpu_baseline / reference leg may import this package.  The product
@@ -63,11 +64,13 @@ def lib(so: str | None = None):
         L.oracle_attn_bwd.argtypes = [p, p, p, p, p, i64, p, i64, i64, i64, f64, f64, p, p, p]
         L.oracle_attn_fwd_rows.argtypes = [p, p, p, p, i64, p, i64, i64, i64, f64, f64, p, i64, p, p]
         L.oracle_cfg_euler.argtypes = [p, p, i64, i64, f64, f64, p, p]
+        L.oracle_pack3d.argtypes = [p, i64, p, p]
+        L.oracle_rope3d.argtypes = [p, p, i64, i64, i64, f64, i32, p]
         L.oracle_adaln.argtypes = [p, p, i64, i64, p, p, f64, p]
         L.oracle_gated_residual.argtypes = [p, p, p, i64, i64, p, p]
         for f in (L.oracle_pack, L.oracle_rope2d, L.oracle_attn_fwd, L.oracle_attn_bwd,
                   L.oracle_attn_fwd_rows, L.oracle_cfg_euler, L.oracle_adaln,
-                  L.oracle_gated_residual):
+                  L.oracle_gated_residual, L.oracle_pack3d, L.oracle_rope3d):
             f.restype = ctypes.c_int
         _libs[key] = L
     return _libs[key]
@@ -153,6 +156,49 @@ def attn_bwd(q, k, v, d_o, cu, pos, scale=None, base: float = ROPE_BASE, so: str
                                  cu.ctypes.data, len(cu) - 1, _ptr(p), T, h, d, scale, base,
                                  dq.ctypes.data, dk.ctypes.data, dv.ctypes.data)
     return dq, dk, dv
+
+
+def pack3d(specs, so: str | None = None):
+    """Editing packs: (cu_seqlens int64[n+1], pos int64[T, 3] = (frame, row, col)) for
+    specs [(text_len, Hs, Ws, Ht, Wt)], each sample [text; source; target]."""
+    s = np.ascontiguousarray(np.asarray(specs, dtype=np.int64).reshape(-1, 5))
+    n = s.shape[0]
+    cu = np.zeros(n + 1, dtype=np.int64)
+    if lib(so).oracle_pack3d(s.ctypes.data, n, cu.ctypes.data, None) != 0:
+        raise ValueError("negative spec entry")
+    pos = np.zeros((int(cu[-1]), 3), dtype=np.int64)
+    lib(so).oracle_pack3d(s.ctypes.data, n, cu.ctypes.data, pos.ctypes.data)
+    return cu, pos
+
+
+def rope3d(x, pos, inverse: bool = False, base: float = ROPE_BASE, so: str | None = None):
+    """Frame-aware 3D rotation R(+theta) x (or R(-theta) x); x [T, heads, d] float64,
+    pos [T, 3]."""
+    x = _f64(x)
+    T, h, d = x.shape
+    y = np.empty_like(x)
+    p = np.ascontiguousarray(pos, dtype=np.int64)
+    if lib(so).oracle_rope3d(x.ctypes.data, p.ctypes.data, T, h, d, base,
+                             -1 if inverse else 1, y.ctypes.data) != 0:
+        raise ValueError("head_dim must be a multiple of 16")
+    return y
+
+
+def attn_fwd3d(q, k, v, cu, pos3, scale=None, base: float = ROPE_BASE, so: str | None = None):
+    """Attention of an editing pack: the attention above on q' = R3 q, k' = R3 k
+    (the definition written out: rotate, then attend without rotation)."""
+    return attn_fwd(rope3d(q, pos3, base=base, so=so), rope3d(k, pos3, base=base, so=so), v, cu,
+                    None, scale=scale, so=so)
+
+
+def attn_bwd3d(q, k, v, d_o, cu, pos3, scale=None, base: float = ROPE_BASE,
+               so: str | None = None):
+    """Gradients of attn_fwd3d with respect to the un-rotated q, k, v: the gradients
+    with respect to q', k' taken back through the rotation's transpose R3(-theta)."""
+    dqr, dkr, dv = attn_bwd(rope3d(q, pos3, base=base, so=so), rope3d(k, pos3, base=base, so=so),
+                            v, d_o, cu, None, scale=scale, so=so)
+    return (rope3d(dqr, pos3, inverse=True, base=base, so=so),
+            rope3d(dkr, pos3, inverse=True, base=base, so=so), dv)
 
 
 def cfg_euler(v, specs, guidance: float, dt: float, z, so: str | None = None):

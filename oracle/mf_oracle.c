@@ -350,3 +350,81 @@ int oracle_gated_residual(const double* x, const double* h, const int64_t* cu, i
         out[t * Dm + e] = x[t * Dm + e] + gate[s * Dm + e] * h[t * Dm + e];
   return ORACLE_OK;
 }
+
+/* ------------------------------------ frame-aware 3D packing and RoPE */
+/*
+ * Editing packs (hyper.ai summary "Method": for editing the 2D rotary embedding is
+ * extended with a frame dimension that tells source and target visual tokens
+ * apart; paperlayer.ai summary 3.2.2: editing concatenates the text conditioning
+ * with the source-image latents and the noisy target latents).  Reading taken
+ * (the pages give no layout or frequencies): sample i is [text; source grid;
+ * target grid], specs[i] = {text_len, Hs, Ws, Ht, Wt}; pos is [T][3] = (f, r, c):
+ * text (0, 0, 0), source token k at (0, k div Ws, k mod Ws), target token k at
+ * (1, k div Wt, k mod Wt).
+ */
+int oracle_pack3d(const int64_t* specs, int64_t n, int64_t* cu, int64_t* pos) {
+  cu[0] = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t* s = specs + 5 * i;
+    for (int q = 0; q < 5; ++q)
+      if (s[q] < 0) return ORACLE_ERR;
+    const int64_t t = s[0], Hs = s[1], Ws = s[2], Ht = s[3], Wt = s[4];
+    const int64_t L = t + Hs * Ws + Ht * Wt;
+    if (pos) {
+      int64_t tok = cu[i];
+      for (int64_t k = 0; k < t; ++k, ++tok) {
+        pos[3 * tok] = 0;
+        pos[3 * tok + 1] = 0;
+        pos[3 * tok + 2] = 0;
+      }
+      for (int64_t k = 0; k < Hs * Ws; ++k, ++tok) {
+        pos[3 * tok] = 0;
+        pos[3 * tok + 1] = k / Ws;
+        pos[3 * tok + 2] = k % Ws;
+      }
+      for (int64_t k = 0; k < Ht * Wt; ++k, ++tok) {
+        pos[3 * tok] = 1;
+        pos[3 * tok + 1] = k / Wt;
+        pos[3 * tok + 2] = k % Wt;
+      }
+    }
+    cu[i + 1] = cu[i] + L;
+  }
+  return ORACLE_OK;
+}
+
+/*
+ * 3D rotation of one head vector.  Reading taken: head_dim is split into three
+ * contiguous slices, frame [0, d/4), row [d/4, 5d/8), column [5d/8, d) (for
+ * d = 128: 16, 24 and 24 rotary pairs); within a slice of width w, the pair
+ * (2j, 2j+1) of the slice rotates by p * base^(-2j / w), p the token's
+ * coordinate on that axis -- the per-axis rule of the 2D embedding with the slice
+ * width in place of d/2.
+ */
+static void rope3_vec(const double* v, const int64_t* p3, int64_t d, double base, int sign,
+                      double* out) {
+  const int64_t width[3] = {d / 4, 3 * d / 8, 3 * d / 8};
+  int64_t off = 0;
+  for (int a = 0; a < 3; ++a) {
+    const double p = (double)p3[a];
+    for (int64_t j = 0; j < width[a] / 2; ++j) {
+      const double omega = pow(base, -2.0 * (double)j / (double)width[a]);
+      const double theta = sign * p * omega;
+      const double x = v[off + 2 * j], y = v[off + 2 * j + 1];
+      out[off + 2 * j] = x * cos(theta) - y * sin(theta);
+      out[off + 2 * j + 1] = x * sin(theta) + y * cos(theta);
+    }
+    off += width[a];
+  }
+}
+
+/* x, y: [T][heads][d] with d a multiple of 16; pos [T][3]; sign +1 / -1. */
+int oracle_rope3d(const double* x, const int64_t* pos, int64_t T, int64_t heads, int64_t d,
+                  double base, int sign, double* y) {
+  if (d % 16 != 0) return ORACLE_ERR;
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t a = 0; a < heads; ++a)
+      rope3_vec(x + (t * heads + a) * d, pos + 3 * t, d, base, sign, y + (t * heads + a) * d);
+  return ORACLE_OK;
+}

@@ -423,3 +423,71 @@ def pin_gated_residual(so=None):
     for s in range(3):
         for t in range(cu[s], cu[s + 1]):
             assert np.array_equal(out[t], x[t] + gate[s]), (s, t)
+
+
+# ------------------------------------------- frame-aware 3D RoPE (editing)
+def pin_pack3d_golden(so=None):
+    for case in _golden("pack3d_cases.json")["cases"]:
+        cu, pos = oracle.pack3d(case["specs"], so=so)
+        assert cu.tolist() == case["cu"], (case["specs"], cu)
+        assert pos.tolist() == case["pos"], (case["specs"], pos)
+
+
+def pin_rope3d_golden(so=None):
+    fn = {"cos": math.cos, "sin": math.sin, "-sin": lambda a: -math.sin(a)}
+    for case in _golden("rope3d_d16.json")["cases"]:
+        x = np.zeros((1, 1, 16))
+        x[0, 0, case["unit"]] = 1.0
+        y = oracle.rope3d(x, np.array([case["pos"]]), so=so)[0, 0]
+        want = np.zeros(16)
+        for dim, (kind, ang) in case["out"].items():
+            want[int(dim)] = fn[kind](ang)
+        assert np.abs(y - want).max() < 1e-14, (case, y)
+
+
+def pin_rope3d_norm_identity_inverse(so=None):
+    rng = _rng(31)
+    x = rng.standard_normal((7, 3, 64))
+    pos = rng.integers(0, 100, size=(7, 3))
+    y = oracle.rope3d(x, pos, so=so)
+    pairs = lambda a: np.hypot(a[..., 0::2], a[..., 1::2])  # noqa: E731
+    assert np.abs(pairs(y) - pairs(x)).max() < 1e-12
+    assert np.abs(oracle.rope3d(y, pos, inverse=True, so=so) - x).max() < 1e-12
+    assert np.array_equal(oracle.rope3d(x, np.zeros((7, 3), dtype=np.int64), so=so), x)
+
+
+def pin_rope3d_relative(so=None):
+    """<R(p1) q, R(p2) k> depends only on p1 - p2 along all three axes, and does
+    depend on the frame offset (source and target tokens at one grid position are
+    told apart)."""
+    rng = _rng(32)
+    q, k = rng.standard_normal((1, 1, 32)), rng.standard_normal((1, 1, 32))
+    dot = lambda p1, p2: float((oracle.rope3d(q, np.array([p1]), so=so) *  # noqa: E731
+                                oracle.rope3d(k, np.array([p2]), so=so)).sum())
+    base = dot([1, 5, 9], [0, 2, 4])
+    for sh in ([0, 3, 1], [2, 0, 0], [5, 7, 11]):
+        s = np.array(sh)
+        assert abs(dot(np.array([1, 5, 9]) + s, np.array([0, 2, 4]) + s) - base) < 1e-12, sh
+    assert abs(dot([1, 3, 3], [0, 3, 3]) - dot([0, 3, 3], [0, 3, 3])) > 1e-3
+
+
+def pin_attn3d_bwd_finite_differences(so=None):
+    """Central differences of <dO, O(q, k, v)> for an editing pack with 3D rotation
+    (relative error < 1e-6 at sampled coordinates of q, k and v)."""
+    rng = _rng(33)
+    specs = [(3, 2, 3, 2, 3), (2, 1, 4, 2, 2)]
+    cu, pos = oracle.pack3d(specs, so=so)
+    T, h, d = int(cu[-1]), 2, 16
+    q, k, v, do = (rng.standard_normal((T, h, d)) for _ in range(4))
+    dq, dk, dv = oracle.attn_bwd3d(q, k, v, do, cu, pos, so=so)
+    f = lambda q_, k_, v_: float((oracle.attn_fwd3d(q_, k_, v_, cu, pos, so=so)[0] * do).sum())  # noqa: E731
+    eps = 1e-6
+    for which, g in ((0, dq), (1, dk), (2, dv)):
+        for _ in range(20):
+            idx = (int(rng.integers(T)), int(rng.integers(h)), int(rng.integers(d)))
+            args_p = [q.copy(), k.copy(), v.copy()]
+            args_m = [q.copy(), k.copy(), v.copy()]
+            args_p[which][idx] += eps
+            args_m[which][idx] -= eps
+            num = (f(*args_p) - f(*args_m)) / (2 * eps)
+            assert abs(num - g[idx]) <= 1e-6 * max(1.0, abs(num)), (which, idx, num, g[idx])

@@ -46,6 +46,14 @@ MUTANTS = [
      "* scale[s * Dm + e] + shift[s * Dm + e];"),
     ("adaln_first_sample_shift", "* (1.0 + scale[s * Dm + e]) + shift[s * Dm + e];",
      "* (1.0 + scale[s * Dm + e]) + shift[e];"),
+    ("pack3d_target_frame_zero", "        pos[3 * tok] = 1;", "        pos[3 * tok] = 0;"),
+    ("pack3d_source_col_major", "pos[3 * tok + 2] = k % Ws;", "pos[3 * tok + 2] = k / (Hs > 0 ? Hs : 1);"),
+    ("rope3d_frame_slice_d8", "const int64_t width[3] = {d / 4, 3 * d / 8, 3 * d / 8};",
+     "const int64_t width[3] = {d / 8, 7 * d / 16, 7 * d / 16};"),
+    ("rope3d_freq_over_d", "pow(base, -2.0 * (double)j / (double)width[a])",
+     "pow(base, -2.0 * (double)j / (double)d)"),
+    ("rope3d_sign", "out[off + 2 * j] = x * cos(theta) - y * sin(theta);",
+     "out[off + 2 * j] = x * cos(theta) + y * sin(theta);"),
     ("gated_first_sample_gate", "out[t * Dm + e] = x[t * Dm + e] + gate[s * Dm + e] * h[t * Dm + e];",
      "out[t * Dm + e] = x[t * Dm + e] + gate[e] * h[t * Dm + e];"),
 ]
