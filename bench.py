@@ -74,7 +74,7 @@ def oracle_sample(wl, q, k, v, do, max_pairs):
     """The first `max_pairs` (sample, head) pairs, smallest samples first, as a
     sub-pack of one-head samples (exact: samples and heads are independent)."""
     import oracle
-    cu, pos = oracle.pack(wl.specs)
+    cu, pos = oracle.pack3d(wl.specs) if wl.edit else oracle.pack(wl.specs)
     L = np.diff(cu)
     pairs = [(int(i), a) for i in np.argsort(L, kind="stable") for a in range(wl.heads)][:max_pairs]
     f = synth.bf16_bits_to_f64
@@ -90,8 +90,12 @@ def oracle_sample(wl, q, k, v, do, max_pairs):
 def run_oracle_step(sub, cu_s, pos_s):
     import oracle
     q, k, v, do = sub
-    oracle.attn_fwd(q, k, v, cu_s, pos_s)
-    oracle.attn_bwd(q, k, v, do, cu_s, pos_s)
+    if pos_s.shape[1] == 3:  # editing pack: frame-aware 3D positions
+        oracle.attn_fwd3d(q, k, v, cu_s, pos_s)
+        oracle.attn_bwd3d(q, k, v, do, cu_s, pos_s)
+    else:
+        oracle.attn_fwd(q, k, v, cu_s, pos_s)
+        oracle.attn_bwd(q, k, v, do, cu_s, pos_s)
 
 
 def cpu_baseline(wl, q, k, v, do, budget_s):
@@ -224,7 +228,7 @@ def gpu_arm(args):
 
     wl = synth.workload(args.workload, args.seed + rank, args.budget)
     q, k, v, do = synth.make_inputs(wl, with_do=True)
-    T, max_len = mf.pack_size(wl.specs)
+    T, max_len = mf.pack3d_size(wl.specs) if wl.edit else mf.pack_size(wl.specs)
     n, h, d = len(wl.specs), wl.heads, wl.head_dim
     pin = lambda b: synth.bits_to_torch(b).pin_memory()  # noqa: E731
     hq, hk, hv, hdo = pin(q), pin(k), pin(v), pin(do)
@@ -235,10 +239,11 @@ def gpu_arm(args):
     ws_f = mf.workspace(T, n, h, d, False)
     ws_b = mf.workspace(T, n, h, d, True)
     cu = torch.empty(n + 1, dtype=torch.int32, device="cuda")
-    pos = torch.empty((T, 2), dtype=torch.int32, device="cuda")
+    pos = torch.empty((T, 3 if wl.edit else 2), dtype=torch.int32, device="cuda")
+    packer = mf.pack3d if wl.edit else mf.pack
 
     def step(qd=qd, kd=kd, vd=vd, dod=dod):
-        mf.pack(wl.specs, cu=cu, pos=pos)
+        packer(wl.specs, cu=cu, pos=pos)
         mf.varlen_attn_fwd(qd, kd, vd, cu, pos, max_len, o=o, lse=lse, ws=ws_f)
         mf.varlen_attn_bwd(qd, kd, vd, o, lse, dod, cu, pos, max_len, dq=dq, dk=dk, dv=dv, ws=ws_b)
 

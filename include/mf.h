@@ -169,6 +169,46 @@ mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
                              void* ws, size_t ws_bytes, mf_stream stream);
 
 /*
+ * Frame-aware 3D positions for editing packs.  The pages say that editing
+ * extends the 2D rotary embedding with a frame dimension that tells source and
+ * target visual tokens apart (hyper.ai summary "Method"; paperlayer.ai summary
+ * 3.2.1), and that editing concatenates the text conditioning with the source
+ * latents and the noisy target latents (paperlayer.ai summary 3.2.2).  They give
+ * no layout or frequencies; this library's reading:
+ *   - sample i is [text; source grid Hs x Ws; target grid Ht x Wt];
+ *   - positions are (f, r, c): text (0, 0, 0), source token m at
+ *     (0, m div Ws, m mod Ws), target token m at (1, m div Wt, m mod Wt);
+ *   - head_dim splits into contiguous frame, row and column slices of d/4, 3d/8 and
+ *     3d/8 dims (16, 24, 24 rotary pairs at d = 128); within a slice of width w the
+ *     pair (2j, 2j+1) of the slice rotates by p * 10000^(-2j / w), p the token's
+ *     coordinate on that axis, with the sign of the 2D rotation.
+ * specs: HOST int32 [n][5] = {text_len, Hs, Ws, Ht, Wt}.
+ */
+mf_status mf_pack3d_size(const int32_t* specs, int32_t n, int32_t* total, int32_t* max_len);
+/* d_cu_seqlens: DEVICE int32 [n+1]; d_pos3: DEVICE int32 [T][3] (may be NULL), 4-byte
+ * aligned.  Errors as mf_pack. */
+mf_status mf_pack3d(const int32_t* specs, int32_t n, int32_t* d_cu_seqlens, int32_t* d_pos3,
+                    mf_stream stream);
+/* Standalone 3D rotation of q and k (as mf_rope2d_qk, with d_pos3 [T][3]). */
+mf_status mf_rope3d_qk(const mf_bf16* q, const mf_bf16* k, mf_bf16* q_out, mf_bf16* k_out,
+                       const int32_t* d_pos3, int32_t T, int32_t heads, int32_t head_dim,
+                       mf_stream stream);
+/* The attention forward and backward of an editing pack: exactly mf_varlen_attn_fwd
+ * and mf_varlen_attn_bwd with q' = R3 q, k' = R3 k (d_pos3 [T][3], not NULL) and the
+ * gradients taken back through R3's transpose.  Same workspaces, shapes and errors. */
+mf_status mf_varlen_attn_fwd_3d(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                const int32_t* d_cu_seqlens, const int32_t* d_pos3, int32_t n,
+                                int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
+                                float softmax_scale, mf_bf16* o, float* lse, void* ws,
+                                size_t ws_bytes, mf_stream stream);
+mf_status mf_varlen_attn_bwd_3d(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                const mf_bf16* o, const float* lse, const mf_bf16* d_o,
+                                const int32_t* d_cu_seqlens, const int32_t* d_pos3, int32_t n,
+                                int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
+                                float softmax_scale, mf_bf16* dq, mf_bf16* dk, mf_bf16* dv,
+                                void* ws, size_t ws_bytes, mf_stream stream);
+
+/*
  * Varlen attention forward that allocates nothing and takes no workspace.
  * (The pages have no counterpart to this call: it is for callers of this library.)
  * Some callers cannot allocate device memory: a plugin inside a framework that

@@ -18,7 +18,7 @@ from ._lib import MFError, STATUS_NAMES, check, library_path, load
 __all__ = [
     "MFError", "STATUS_NAMES", "load", "library_path", "pack_size", "pack", "rope2d_qk",
     "attn_workspace_bytes", "workspace", "varlen_attn_fwd", "varlen_attn_bwd", "get_status",
-    "cfg_euler_step", "adaln_modulate", "gated_residual",
+    "cfg_euler_step", "adaln_modulate", "gated_residual", "pack3d_size", "pack3d", "rope3d_qk",
 ]
 
 
@@ -79,6 +79,54 @@ def pack(specs, device=None, stream=None, with_pos: bool = True, cu=None, pos=No
     return cu, pos
 
 
+def _specs5_array(specs):
+    flat = [int(x) for s in specs for x in s]
+    if len(flat) != 5 * len(specs):
+        raise ValueError("editing specs must be (text_len, Hs, Ws, Ht, Wt) tuples")
+    return (ctypes.c_int32 * max(1, len(flat)))(*flat), len(specs)
+
+
+def pack3d_size(specs):
+    """(T, max_len) of an editing pack of (text_len, Hs, Ws, Ht, Wt) samples."""
+    arr, n = _specs5_array(specs)
+    T, mx = ctypes.c_int32(), ctypes.c_int32()
+    check(load().mf_pack3d_size(arr, n, ctypes.byref(T), ctypes.byref(mx)), "mf_pack3d_size")
+    return T.value, mx.value
+
+
+def pack3d(specs, device=None, stream=None, cu=None, pos=None):
+    """cu_seqlens int32 [n+1] and pos int32 [T, 3] = (frame, row, col) of an editing
+    pack [text; source; target] built on the device by mf_pack3d."""
+    torch = _torch()
+    arr, n = _specs5_array(specs)
+    T, _ = pack3d_size(specs)
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    cu = torch.empty(n + 1, dtype=torch.int32, device=dev) if cu is None else cu
+    pos = torch.empty((T, 3), dtype=torch.int32, device=dev) if pos is None else pos
+    if cu.numel() != n + 1 or pos.shape != (T, 3):
+        raise ValueError("cu/pos buffers do not match the specs")
+    check(load().mf_pack3d(arr, n, _ptr(cu), _ptr(pos) if T > 0 else None, _stream_ptr(stream)),
+          "mf_pack3d")
+    return cu, pos
+
+
+def rope3d_qk(q, k, pos3, q_out=None, k_out=None, stream=None):
+    """Frame-aware 3D RoPE of q and k (either may be None); returns (q_out, k_out)."""
+    torch = _torch()
+    ref = q if q is not None else k
+    _check_thd("q/k", ref)
+    T, h, d = ref.shape
+    if q is not None:
+        q_out = torch.empty_like(q) if q_out is None else q_out
+        _check_thd("q_out", q_out, T, h, d)
+    if k is not None:
+        k_out = torch.empty_like(k) if k_out is None else k_out
+        _check_thd("k_out", k_out, T, h, d)
+    check(load().mf_rope3d_qk(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _ptr(pos3), T, h, d,
+                              _stream_ptr(stream)), "mf_rope3d_qk")
+    return q_out, k_out
+
+
 def rope2d_qk(q, k, pos, q_out=None, k_out=None, stream=None):
     """Per-sample 2D RoPE of q and k (either may be None); returns (q_out, k_out)."""
     torch = _torch()
@@ -111,9 +159,19 @@ def workspace(T, n, heads, head_dim, bwd: bool, device=None):
     return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
 
 
+def _is_3d(pos) -> bool:
+    """Positions with three coordinates per token select the editing-pack entry points."""
+    if pos is None:
+        return False
+    if pos.dim() != 2 or pos.shape[1] not in (2, 3) or pos.dtype != _torch().int32:
+        raise ValueError("pos must be an int32 tensor [T, 2] or [T, 3]")
+    return pos.shape[1] == 3
+
+
 def varlen_attn_fwd(q, k, v, cu_seqlens, pos, max_len, softmax_scale: float = 0.0, o=None,
                     lse=None, ws=None, stream=None):
-    """Block-diagonal attention forward with per-sample 2D RoPE (pos=None: none).
+    """Block-diagonal attention forward with per-sample 2D RoPE (pos [T, 2]; None:
+    no rotation) or, for editing packs, the frame-aware 3D RoPE (pos [T, 3]).
     Returns (o [T, h, d] bf16, lse [h, T] fp32)."""
     torch = _torch()
     _check_thd("q", q)
@@ -124,10 +182,10 @@ def varlen_attn_fwd(q, k, v, cu_seqlens, pos, max_len, softmax_scale: float = 0.
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((h, T), dtype=torch.float32, device=q.device) if lse is None else lse
     ws = workspace(T, n, h, d, False, q.device) if ws is None else ws
-    check(load().mf_varlen_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(pos), n, T,
-                                    int(max_len), h, d, float(softmax_scale), _ptr(o), _ptr(lse),
-                                    _ptr(ws), ws.numel(), _stream_ptr(stream)),
-          "mf_varlen_attn_fwd")
+    fn = "mf_varlen_attn_fwd_3d" if _is_3d(pos) else "mf_varlen_attn_fwd"
+    check(getattr(load(), fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(pos), n, T,
+                              int(max_len), h, d, float(softmax_scale), _ptr(o), _ptr(lse),
+                              _ptr(ws), ws.numel(), _stream_ptr(stream)), fn)
     return o, lse
 
 
@@ -144,11 +202,11 @@ def varlen_attn_bwd(q, k, v, o, lse, d_o, cu_seqlens, pos, max_len, softmax_scal
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     ws = workspace(T, n, h, d, True, q.device) if ws is None else ws
-    check(load().mf_varlen_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
-                                    _ptr(cu_seqlens), _ptr(pos), n, T, int(max_len), h, d,
-                                    float(softmax_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
-                                    ws.numel(), _stream_ptr(stream)),
-          "mf_varlen_attn_bwd")
+    fn = "mf_varlen_attn_bwd_3d" if _is_3d(pos) else "mf_varlen_attn_bwd"
+    check(getattr(load(), fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
+                              _ptr(cu_seqlens), _ptr(pos), n, T, int(max_len), h, d,
+                              float(softmax_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                              ws.numel(), _stream_ptr(stream)), fn)
     return dq, dk, dv
 
 

@@ -35,6 +35,13 @@ SIGNATURES = {
                                           _i32, _f32, _p, _p, _p, _p, _sz, _p]),
     "mf_varlen_attn_fwd_noalloc": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32,
                                                   _i32, _f32, _p, _p, _p]),
+    "mf_pack3d_size": (ctypes.c_int, [_p, _i32, _p, _p]),
+    "mf_pack3d": (ctypes.c_int, [_p, _i32, _p, _p, _p]),
+    "mf_rope3d_qk": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _p]),
+    "mf_varlen_attn_fwd_3d": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32,
+                                             _f32, _p, _p, _p, _sz, _p]),
+    "mf_varlen_attn_bwd_3d": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32,
+                                             _i32, _i32, _f32, _p, _p, _p, _p, _sz, _p]),
     "mf_cfg_euler_step": (ctypes.c_int, [_p, _p, _i32, _i32, _f32, _f32, _p, _p]),
     "mf_adaln_modulate": (ctypes.c_int, [_p, _p, _i32, _i32, _i32, _p, _p, _f32, _p, _p]),
     "mf_gated_residual": (ctypes.c_int, [_p, _p, _p, _i32, _i32, _i32, _p, _p, _p]),

@@ -134,7 +134,7 @@ mf_status mf_rope2d_qk(const mf_bf16* q, const mf_bf16* k, mf_bf16* q_out, mf_bf
   for (const void* ptr : ps)
     if (ptr != nullptr && !aligned(ptr, 16)) return MF_ERR_UNSUPPORTED;
   if (!aligned(d_pos, 8)) return MF_ERR_UNSUPPORTED;
-  return cuda_status(launch_rope(q, k, q_out, k_out, d_pos, T, heads, head_dim, 1.0f,
+  return cuda_status(launch_rope(q, k, q_out, k_out, d_pos, 2, T, heads, head_dim, 1.0f,
                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -144,16 +144,22 @@ size_t mf_attn_workspace_bytes(int32_t T, int32_t n, int32_t heads, int32_t head
   return ws_layout(T, n, heads, head_dim, bwd != 0).total;
 }
 
-mf_status mf_varlen_attn_fwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
-                             const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t n,
-                             int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
-                             float softmax_scale, mf_bf16* o, float* lse, void* ws,
-                             size_t ws_bytes, mf_stream stream) {
+}  // extern "C"
+
+namespace mf {
+
+// The forward for positions of `naxes` coordinates per token (2: native-resolution
+// packs, 3: editing packs); only the fp16 rotation pre-pass depends on it.
+static mf_status attn_fwd_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                               const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t naxes,
+                               int32_t n, int32_t T, int32_t max_len, int32_t heads,
+                               int32_t head_dim, float softmax_scale, mf_bf16* o, float* lse,
+                               void* ws, size_t ws_bytes, mf_stream stream) {
   const void* ptrs[5] = {q, k, v, o, lse};
   mf_status st = check_attn(ptrs, 5, d_cu_seqlens, n, T, max_len, heads, head_dim, ws, ws_bytes,
                             false);
   if (st != MF_OK) return st;
-  if (d_pos != nullptr && !aligned(d_pos, 8)) return MF_ERR_UNSUPPORTED;
+  if (d_pos != nullptr && !aligned(d_pos, 4)) return MF_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const WsLayout L = ws_layout(T, n, heads, head_dim, false);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -169,7 +175,7 @@ mf_status mf_varlen_attn_fwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
   auto* q16 = reinterpret_cast<uint16_t*>(w + L.q16);
   auto* k16 = reinterpret_cast<uint16_t*>(w + L.k16);
   auto* v16 = reinterpret_cast<uint16_t*>(w + L.v16);
-  e = launch_prep_f16(q, k, v, q16, k16, v16, d_pos, T, heads, head_dim, status, s);
+  e = launch_prep_f16(q, k, v, q16, k16, v16, d_pos, naxes, T, heads, head_dim, status, s);
   if (e != cudaSuccess) return MF_ERR_CUDA;
   AttnFwdArgs a;
   a.q = q16;
@@ -189,17 +195,17 @@ mf_status mf_varlen_attn_fwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
   return cuda_status(launch_attn_fwd(a, s));
 }
 
-mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
-                             const mf_bf16* o, const float* lse, const mf_bf16* d_o,
-                             const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t n,
-                             int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
-                             float softmax_scale, mf_bf16* dq, mf_bf16* dk, mf_bf16* dv,
-                             void* ws, size_t ws_bytes, mf_stream stream) {
+static mf_status attn_bwd_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                               const mf_bf16* o, const float* lse, const mf_bf16* d_o,
+                               const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t naxes,
+                               int32_t n, int32_t T, int32_t max_len, int32_t heads,
+                               int32_t head_dim, float softmax_scale, mf_bf16* dq, mf_bf16* dk,
+                               mf_bf16* dv, void* ws, size_t ws_bytes, mf_stream stream) {
   const void* ptrs[9] = {q, k, v, o, lse, d_o, dq, dk, dv};
   mf_status st = check_attn(ptrs, 9, d_cu_seqlens, n, T, max_len, heads, head_dim, ws, ws_bytes,
                             true);
   if (st != MF_OK) return st;
-  if (d_pos != nullptr && !aligned(d_pos, 8)) return MF_ERR_UNSUPPORTED;
+  if (d_pos != nullptr && !aligned(d_pos, 4)) return MF_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const WsLayout L = ws_layout(T, n, heads, head_dim, true);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -215,7 +221,8 @@ mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
   // Q' = R q, K' = R k in fp16, as in the forward (same logits as the LSE came from)
   auto* q16 = reinterpret_cast<uint16_t*>(w + L.q16);
   auto* k16 = reinterpret_cast<uint16_t*>(w + L.k16);
-  e = launch_prep_f16(q, k, nullptr, q16, k16, nullptr, d_pos, T, heads, head_dim, status, s);
+  e = launch_prep_f16(q, k, nullptr, q16, k16, nullptr, d_pos, naxes, T, heads, head_dim, status,
+                      s);
   if (e != cudaSuccess) return MF_ERR_CUDA;
   AttnBwdArgs a;
   a.q = q16;
@@ -227,6 +234,7 @@ mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
   a.lse = lse;
   a.cu = d_cu_seqlens;
   a.pos = d_pos;
+  a.naxes = naxes;
   a.order = order;
   a.prefix = prefix;
   a.status = status;
@@ -243,6 +251,97 @@ mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
   a.head_dim = head_dim;
   a.scale = scale;
   return cuda_status(launch_attn_bwd(a, s));
+}
+
+}  // namespace mf
+
+extern "C" {
+
+mf_status mf_varlen_attn_fwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                             const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t n,
+                             int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
+                             float softmax_scale, mf_bf16* o, float* lse, void* ws,
+                             size_t ws_bytes, mf_stream stream) {
+  return attn_fwd_impl(q, k, v, d_cu_seqlens, d_pos, 2, n, T, max_len, heads, head_dim,
+                       softmax_scale, o, lse, ws, ws_bytes, stream);
+}
+
+mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                             const mf_bf16* o, const float* lse, const mf_bf16* d_o,
+                             const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t n,
+                             int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
+                             float softmax_scale, mf_bf16* dq, mf_bf16* dk, mf_bf16* dv,
+                             void* ws, size_t ws_bytes, mf_stream stream) {
+  return attn_bwd_impl(q, k, v, o, lse, d_o, d_cu_seqlens, d_pos, 2, n, T, max_len, heads,
+                       head_dim, softmax_scale, dq, dk, dv, ws, ws_bytes, stream);
+}
+
+mf_status mf_varlen_attn_fwd_3d(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                const int32_t* d_cu_seqlens, const int32_t* d_pos3, int32_t n,
+                                int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
+                                float softmax_scale, mf_bf16* o, float* lse, void* ws,
+                                size_t ws_bytes, mf_stream stream) {
+  if (d_pos3 == nullptr) return MF_ERR_INVALID_ARG;
+  return attn_fwd_impl(q, k, v, d_cu_seqlens, d_pos3, 3, n, T, max_len, heads, head_dim,
+                       softmax_scale, o, lse, ws, ws_bytes, stream);
+}
+
+mf_status mf_varlen_attn_bwd_3d(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                const mf_bf16* o, const float* lse, const mf_bf16* d_o,
+                                const int32_t* d_cu_seqlens, const int32_t* d_pos3, int32_t n,
+                                int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
+                                float softmax_scale, mf_bf16* dq, mf_bf16* dk, mf_bf16* dv,
+                                void* ws, size_t ws_bytes, mf_stream stream) {
+  if (d_pos3 == nullptr) return MF_ERR_INVALID_ARG;
+  return attn_bwd_impl(q, k, v, o, lse, d_o, d_cu_seqlens, d_pos3, 3, n, T, max_len, heads,
+                       head_dim, softmax_scale, dq, dk, dv, ws, ws_bytes, stream);
+}
+
+mf_status mf_pack3d_size(const int32_t* specs, int32_t n, int32_t* total, int32_t* max_len) {
+  if (n < 0 || (n > 0 && specs == nullptr)) return MF_ERR_INVALID_ARG;
+  int64_t T = 0, mx = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t* sp = specs + 5 * i;
+    for (int q = 0; q < 5; ++q)
+      if (sp[q] < 0) return MF_ERR_INVALID_ARG;
+    const int64_t src = static_cast<int64_t>(sp[1]) * sp[2];
+    const int64_t tgt = static_cast<int64_t>(sp[3]) * sp[4];
+    const int64_t L = sp[0] + src + tgt;
+    if (src > INT32_MAX || tgt > INT32_MAX || L > INT32_MAX) return MF_ERR_OVERFLOW;
+    T += L;
+    if (T > INT32_MAX) return MF_ERR_OVERFLOW;
+    if (L > mx) mx = L;
+  }
+  if (total) *total = static_cast<int32_t>(T);
+  if (max_len) *max_len = static_cast<int32_t>(mx);
+  return MF_OK;
+}
+
+mf_status mf_pack3d(const int32_t* specs, int32_t n, int32_t* d_cu_seqlens, int32_t* d_pos3,
+                    mf_stream stream) {
+  const mf_status st = mf_pack3d_size(specs, n, nullptr, nullptr);
+  if (st != MF_OK) return st;
+  if (d_cu_seqlens == nullptr) return MF_ERR_INVALID_ARG;
+  if (d_pos3 != nullptr && !aligned(d_pos3, 4)) return MF_ERR_UNSUPPORTED;
+  return cuda_status(
+      launch_pack3d(specs, n, d_cu_seqlens, d_pos3, static_cast<cudaStream_t>(stream)));
+}
+
+mf_status mf_rope3d_qk(const mf_bf16* q, const mf_bf16* k, mf_bf16* q_out, mf_bf16* k_out,
+                       const int32_t* d_pos3, int32_t T, int32_t heads, int32_t head_dim,
+                       mf_stream stream) {
+  if (T < 0 || heads < 1) return MF_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return MF_ERR_UNSUPPORTED;
+  if (T == 0) return MF_OK;
+  if (d_pos3 == nullptr || (q == nullptr && k == nullptr)) return MF_ERR_INVALID_ARG;
+  if ((q == nullptr) != (q_out == nullptr) || (k == nullptr) != (k_out == nullptr))
+    return MF_ERR_INVALID_ARG;
+  const void* ps[4] = {q, k, q_out, k_out};
+  for (const void* ptr : ps)
+    if (ptr != nullptr && !aligned(ptr, 16)) return MF_ERR_UNSUPPORTED;
+  if (!aligned(d_pos3, 4)) return MF_ERR_UNSUPPORTED;
+  return cuda_status(launch_rope(q, k, q_out, k_out, d_pos3, 3, T, heads, head_dim, 1.0f,
+                                 static_cast<cudaStream_t>(stream)));
 }
 
 mf_status mf_cfg_euler_step(const mf_bf16* v, const int32_t* specs, int32_t pairs, int32_t C,

@@ -162,18 +162,18 @@ constexpr int kPostTok = 4;
 template <int D>
 __global__ void __launch_bounds__(256) dq_post_kernel(const float4* __restrict__ acc,
                                                       uint2* __restrict__ dq,
-                                                      const int2* __restrict__ pos, int32_t T,
-                                                      int32_t heads, const RopeFreqs f) {
-  constexpr int NP = D / 2, NF = D / 4;
+                                                      const int32_t* __restrict__ pos, int32_t T,
+                                                      int32_t heads,
+                                                      const __grid_constant__ RopeFreqs f) {
+  constexpr int NP = D / 2;
   __shared__ float2 cs[kPostTok][NP];
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kPostTok;
   for (int i = threadIdx.x; i < kPostTok * NP; i += blockDim.x) {
     const int tt = i / NP, P = i % NP;
     float c = 1.f, sn = 0.f;
     if (t0 + tt < T && pos != nullptr) {
-      const int2 p = pos[t0 + tt];
-      const float pp = static_cast<float>(P < NF ? p.x : p.y);
-      rope_sincos(pp, f.omega[P % NF], f.omega_lo[P % NF], -1.f, &sn, &c);
+      const float pp = static_cast<float>(pos[(t0 + tt) * f.naxes + f.axis[P]]);
+      rope_sincos(pp, f.omega[P], f.omega_lo[P], -1.f, &sn, &c);
     }
     cs[tt][P] = make_float2(c, sn);
   }
@@ -630,10 +630,13 @@ __global__ void __launch_bounds__(320, 1)
                          pack_bf16x2(__uint_as_float(r[8 * u + 6]), __uint_as_float(r[8 * u + 7]))));
       }
       const float dk_mul = p.scale / ds_mul;  // exact: ds_mul is a power of two
-      float pr_ = 0.f, pc_ = 0.f;
+      // the key row's position coordinates (2 or 3 of them)
+      float pv0 = 0.f, pv1 = 0.f, pv2 = 0.f;
       if (key_ok && p.pos != nullptr) {
-        pr_ = static_cast<float>(p.pos[2 * (w.start + k0 + row)]);
-        pc_ = static_cast<float>(p.pos[2 * (w.start + k0 + row) + 1]);
+        const int32_t* pp = p.pos + static_cast<int64_t>(w.start + k0 + row) * p.f.naxes;
+        pv0 = static_cast<float>(pp[0]);
+        pv1 = static_cast<float>(pp[1]);
+        if (p.f.naxes == 3) pv2 = static_cast<float>(pp[2]);
       }
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -648,8 +651,9 @@ __global__ void __launch_bounds__(320, 1)
           for (int u = 0; u < 16; ++u) {
             const int P = cc * 16 + u;  // pair index
             float sn, cs;
-            rope_sincos_fast(P < D / 4 ? pr_ : pc_, p.f.omega[P % (D / 4)],
-                             p.f.omega_lo[P % (D / 4)], -1.f, &sn, &cs);
+            const int ax = p.f.axis[P];
+            rope_sincos_fast(ax == 0 ? pv0 : ax == 1 ? pv1 : pv2, p.f.omega[P],
+                             p.f.omega_lo[P], -1.f, &sn, &cs);
             const float a = v[2 * u], b = v[2 * u + 1];
             v[2 * u] = fmaf(a, cs, -b * sn);
             v[2 * u + 1] = fmaf(a, sn, b * cs);
@@ -744,7 +748,7 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
     attr_done = true;
   }
   const int64_t rows = static_cast<int64_t>(a.T) * a.heads;
-  const RopeFreqs f = make_rope_freqs(D);
+  const RopeFreqs f = make_rope_freqs(D, a.naxes);
   if (rows > 0) {
     const int64_t blocks = (rows + kPreRowsPerBlock - 1) / kPreRowsPerBlock;
     KernelTimer kt(MF_K_BWD_PRE, s);
@@ -793,7 +797,7 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
     KernelTimer kt(MF_K_DQ_POST, s);
     dq_post_kernel<D><<<static_cast<unsigned>((a.T + kPostTok - 1) / kPostTok), 256, 0, s>>>(
         reinterpret_cast<const float4*>(a.dq_acc), reinterpret_cast<uint2*>(a.dq),
-        reinterpret_cast<const int2*>(a.pos), a.T, a.heads, f);
+        a.pos, a.T, a.heads, f);
     return cudaGetLastError();
   }
   return cudaSuccess;

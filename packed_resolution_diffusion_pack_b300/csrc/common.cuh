@@ -11,16 +11,24 @@
 namespace mf {
 
 constexpr double kRopeBase = 10000.0;
-constexpr int kMaxFreq = 32;  // d/4 for head_dim 128
+constexpr int kMaxPairs = 64;  // rotary pairs (d/2) for head_dim 128
 
-// Rotary frequencies omega_j = base^(-2j/(d/2)), j < d/4, computed on the host in
-// double and split into fp32 hi + lo parts (passed by value to the kernels), so a
-// kernel can form theta = p * omega to ~2^-40 relative before taking sin/cos.
+// Rotary angle of every pair of a head vector: pair P (dims 2P, 2P+1) rotates by
+// theta = pos[axis[P]] * omega[P], pos being the token's naxes coordinates.  omega
+// is computed on the host in double and split into fp32 hi + lo parts, so a kernel
+// can form theta to ~2^-40 relative before taking sin/cos.
+//  naxes = 2 (native-resolution packs): pos = (r, c); pairs [0, d/4) rotate by r,
+//    [d/4, d/2) by c, pair j of a half with omega = base^(-2j/(d/2)).
+//  naxes = 3 (editing packs): pos = (f, r, c); the frame, row and column slices
+//    are d/4, 3d/8 and 3d/8 dims wide; pair j of a slice of width w has
+//    omega = base^(-2j/w).
 struct RopeFreqs {
-  float omega[kMaxFreq];
-  float omega_lo[kMaxFreq];
+  float omega[kMaxPairs];
+  float omega_lo[kMaxPairs];
+  int8_t axis[kMaxPairs];
+  int32_t naxes;
 };
-RopeFreqs make_rope_freqs(int head_dim);
+RopeFreqs make_rope_freqs(int head_dim, int naxes);
 
 // sin and cos of theta = sign * p * omega (p a small integer as float): the fp32
 // product's rounding error is recovered exactly with an FMA and added, together
@@ -86,18 +94,22 @@ WsLayout ws_layout(int64_t T, int64_t n, int64_t heads, int64_t head_dim, bool b
 // ---------------------------------------------------------------- launches
 cudaError_t launch_pack(const int32_t* specs, int32_t n, int32_t* d_cu, int32_t* d_pos,
                         cudaStream_t s);
-// bf16 in, bf16 out (the standalone mf_rope2d_qk).
+// Editing packs: specs [n][5] = {text, Hs, Ws, Ht, Wt}; pos [T][3] = (f, r, c).
+cudaError_t launch_pack3d(const int32_t* specs, int32_t n, int32_t* d_cu, int32_t* d_pos,
+                          cudaStream_t s);
+// bf16 in, bf16 out (the standalone mf_rope2d_qk / mf_rope3d_qk); pos has naxes
+// coordinates per token.
 cudaError_t launch_rope(const uint16_t* q, const uint16_t* k, uint16_t* q_out, uint16_t* k_out,
-                        const int32_t* d_pos, int32_t T, int32_t heads, int32_t head_dim,
-                        float sign, cudaStream_t s);
+                        const int32_t* d_pos, int32_t naxes, int32_t T, int32_t heads,
+                        int32_t head_dim, float sign, cudaStream_t s);
 // bf16 in, fp16 out: the attention's operands Q' = R q, K' = R k (R the identity
 // when d_pos is null) and, when v is given, V' = v converted.  fp16 carries 3 more
 // mantissa bits than bf16 at the same tensor-core rate.  Sets kFlagFp16Range in
 // *status if a value leaves the fp16 range.  Any of q/k/v may be null.
 cudaError_t launch_prep_f16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                             uint16_t* q_out, uint16_t* k_out, uint16_t* v_out,
-                            const int32_t* d_pos, int32_t T, int32_t heads, int32_t head_dim,
-                            uint32_t* status, cudaStream_t s);
+                            const int32_t* d_pos, int32_t naxes, int32_t T, int32_t heads,
+                            int32_t head_dim, uint32_t* status, cudaStream_t s);
 // Builds the longest-first work list (items of `blk` rows per sample and head)
 // and validates cu_seqlens; zeroes the status word first, and `nzero` floats at
 // `zero` (may be null).
@@ -128,7 +140,8 @@ struct AttnBwdArgs {
   const uint16_t* d_o;  // bf16
   const float* lse;
   const int32_t* cu;
-  const int32_t* pos;  // may be null
+  const int32_t* pos;  // may be null; naxes coordinates per token
+  int32_t naxes;       // 2 or 3
   const int32_t* order;
   const int32_t* prefix;
   uint32_t* status;

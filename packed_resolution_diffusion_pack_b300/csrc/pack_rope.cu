@@ -16,13 +16,24 @@
 
 namespace mf {
 
-RopeFreqs make_rope_freqs(int head_dim) {
+RopeFreqs make_rope_freqs(int head_dim, int naxes) {
   RopeFreqs f{};
-  const int nfreq = head_dim / 4, half = head_dim / 2;
-  for (int j = 0; j < nfreq && j < kMaxFreq; ++j) {
-    const double w = std::pow(kRopeBase, -2.0 * j / static_cast<double>(half));
-    f.omega[j] = static_cast<float>(w);
-    f.omega_lo[j] = static_cast<float>(w - static_cast<double>(f.omega[j]));
+  f.naxes = naxes;
+  // slice widths (dims) per axis
+  int width[3] = {head_dim / 2, head_dim / 2, 0};
+  if (naxes == 3) {
+    width[0] = head_dim / 4;
+    width[1] = 3 * head_dim / 8;
+    width[2] = 3 * head_dim / 8;
+  }
+  int P = 0;
+  for (int a = 0; a < naxes; ++a) {
+    for (int j = 0; j < width[a] / 2 && P < kMaxPairs; ++j, ++P) {
+      const double w = std::pow(kRopeBase, -2.0 * j / static_cast<double>(width[a]));
+      f.omega[P] = static_cast<float>(w);
+      f.omega_lo[P] = static_cast<float>(w - static_cast<double>(f.omega[P]));
+      f.axis[P] = static_cast<int8_t>(a);
+    }
   }
   return f;
 }
@@ -104,6 +115,88 @@ cudaError_t launch_pack(const int32_t* specs, int32_t n, int32_t* d_cu, int32_t*
   return cudaSuccess;
 }
 
+// ------------------------------------------------------- editing packs (3D)
+// Sample i is [text; source grid; target grid] (specs {text, Hs, Ws, Ht, Wt}):
+// text tokens at (0, 0, 0), source token m at (0, m div Ws, m mod Ws), target
+// token m at (1, m div Wt, m mod Wt).
+struct Pack3Chunk {
+  int32_t first, count, tok_begin, tok_end, last;
+  int32_t start[kPackChunk];
+  int32_t text[kPackChunk];
+  int32_t src_n[kPackChunk];   // Hs * Ws
+  int32_t src_w[kPackChunk];
+  int32_t tgt_w[kPackChunk];
+};
+
+__global__ void __launch_bounds__(256) pack3_kernel(const __grid_constant__ Pack3Chunk c,
+                                                    int32_t* __restrict__ cu,
+                                                    int32_t* __restrict__ pos) {
+  __shared__ int32_t s_start[kPackChunk];
+  for (int i = threadIdx.x; i < c.count; i += blockDim.x) s_start[i] = c.start[i];
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < c.count; i += blockDim.x) cu[c.first + i] = s_start[i];
+    if (c.last && threadIdx.x == 0) cu[c.first + c.count] = c.tok_end;
+  }
+  if (pos == nullptr) return;
+  const int64_t t = static_cast<int64_t>(c.tok_begin) + blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= c.tok_end) return;
+  int lo = 0, hi = c.count - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_start[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int32_t k = static_cast<int32_t>(t) - s_start[lo];
+  int32_t f = 0, r = 0, col = 0;
+  if (k >= c.text[lo]) {
+    int32_t m = k - c.text[lo];
+    int32_t W = c.src_w[lo];
+    if (m >= c.src_n[lo]) {
+      m -= c.src_n[lo];
+      W = c.tgt_w[lo];
+      f = 1;
+    }
+    r = m / W;
+    col = m - r * W;
+  }
+  pos[3 * t] = f;
+  pos[3 * t + 1] = r;
+  pos[3 * t + 2] = col;
+}
+
+cudaError_t launch_pack3d(const int32_t* specs, int32_t n, int32_t* d_cu, int32_t* d_pos,
+                          cudaStream_t s) {
+  int64_t start = 0;
+  for (int32_t first = 0; first < n || (n == 0 && first == 0); first += kPackChunk) {
+    Pack3Chunk c{};
+    c.first = first;
+    c.count = n - first < kPackChunk ? n - first : kPackChunk;
+    c.tok_begin = static_cast<int32_t>(start);
+    for (int i = 0; i < c.count; ++i) {
+      const int32_t* sp = specs + 5 * (first + i);
+      c.start[i] = static_cast<int32_t>(start);
+      c.text[i] = sp[0];
+      c.src_n[i] = sp[1] * sp[2];
+      c.src_w[i] = sp[2];
+      c.tgt_w[i] = sp[4];
+      start += static_cast<int64_t>(sp[0]) + static_cast<int64_t>(sp[1]) * sp[2] +
+               static_cast<int64_t>(sp[3]) * sp[4];
+    }
+    c.tok_end = static_cast<int32_t>(start);
+    c.last = (first + c.count >= n) ? 1 : 0;
+    const int64_t ntok = c.tok_end - c.tok_begin;
+    const int blocks = static_cast<int>(ntok > 0 ? (ntok + 255) / 256 : 1);
+    {
+      KernelTimer kt(MF_K_PACK, s);
+      pack3_kernel<<<blocks, 256, 0, s>>>(c, d_cu, d_pos);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (n == 0) break;
+  }
+  return cudaSuccess;
+}
+
 // --------------------------------------------------------------------- RoPE
 // One block handles kRopeTok tokens: all heads of q and k (rotated) and of v
 // (converted only).  Phase 1 builds the (cos, sin) of every rotary pair of those
@@ -120,20 +213,19 @@ __global__ void __launch_bounds__(256) rope_kernel(const uint4* __restrict__ q,
                                                    uint4* __restrict__ q_out,
                                                    uint4* __restrict__ k_out,
                                                    uint4* __restrict__ v_out,
-                                                   const int2* __restrict__ pos, int32_t T,
-                                                   int32_t heads, const RopeFreqs f,
+                                                   const int32_t* __restrict__ pos, int32_t T,
+                                                   int32_t heads,
+                                                   const __grid_constant__ RopeFreqs f,
                                                    float sign, uint32_t* status) {
   constexpr int NP = D / 2;  // rotary pairs per head vector
-  constexpr int NF = D / 4;  // frequencies per half
   __shared__ float2 cs[kRopeTok][NP];
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRopeTok;
   for (int i = threadIdx.x; i < kRopeTok * NP; i += blockDim.x) {
     const int tt = i / NP, P = i % NP;
     float c = 1.f, s = 0.f;
     if (t0 + tt < T && pos != nullptr) {
-      const int2 p = pos[t0 + tt];
-      const float pp = static_cast<float>(P < NF ? p.x : p.y);
-      rope_sincos(pp, f.omega[P % NF], f.omega_lo[P % NF], sign, &s, &c);
+      const float pp = static_cast<float>(pos[(t0 + tt) * f.naxes + f.axis[P]]);
+      rope_sincos(pp, f.omega[P], f.omega_lo[P], sign, &s, &c);
     }
     cs[tt][P] = make_float2(c, s);
   }
@@ -179,14 +271,14 @@ __global__ void __launch_bounds__(256) rope_kernel(const uint4* __restrict__ q,
 template <bool F16_OUT>
 static cudaError_t launch_rope_t(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                  uint16_t* q_out, uint16_t* k_out, uint16_t* v_out,
-                                 const int32_t* d_pos, int32_t T, int32_t heads,
+                                 const int32_t* d_pos, int32_t naxes, int32_t T, int32_t heads,
                                  int32_t head_dim, float sign, uint32_t* status, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  const RopeFreqs f = make_rope_freqs(head_dim);
+  const RopeFreqs f = make_rope_freqs(head_dim, naxes);
   const int blocks = (T + kRopeTok - 1) / kRopeTok;
   auto in = [](const uint16_t* x) { return reinterpret_cast<const uint4*>(x); };
   auto out = [](uint16_t* x) { return reinterpret_cast<uint4*>(x); };
-  auto p = reinterpret_cast<const int2*>(d_pos);
+  const int32_t* p = d_pos;
   KernelTimer kt(MF_K_ROPE, s);
   if (head_dim == 128)
     rope_kernel<128, F16_OUT><<<blocks, 256, 0, s>>>(in(q), in(k), in(v), out(q_out), out(k_out),
@@ -198,18 +290,18 @@ static cudaError_t launch_rope_t(const uint16_t* q, const uint16_t* k, const uin
 }
 
 cudaError_t launch_rope(const uint16_t* q, const uint16_t* k, uint16_t* q_out, uint16_t* k_out,
-                        const int32_t* d_pos, int32_t T, int32_t heads, int32_t head_dim,
-                        float sign, cudaStream_t s) {
-  return launch_rope_t<false>(q, k, nullptr, q_out, k_out, nullptr, d_pos, T, heads, head_dim,
-                              sign, nullptr, s);
+                        const int32_t* d_pos, int32_t naxes, int32_t T, int32_t heads,
+                        int32_t head_dim, float sign, cudaStream_t s) {
+  return launch_rope_t<false>(q, k, nullptr, q_out, k_out, nullptr, d_pos, naxes, T, heads,
+                              head_dim, sign, nullptr, s);
 }
 
 cudaError_t launch_prep_f16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                             uint16_t* q_out, uint16_t* k_out, uint16_t* v_out,
-                            const int32_t* d_pos, int32_t T, int32_t heads, int32_t head_dim,
-                            uint32_t* status, cudaStream_t s) {
-  return launch_rope_t<true>(q, k, v, q_out, k_out, v_out, d_pos, T, heads, head_dim, 1.0f,
-                             status, s);
+                            const int32_t* d_pos, int32_t naxes, int32_t T, int32_t heads,
+                            int32_t head_dim, uint32_t* status, cudaStream_t s) {
+  return launch_rope_t<true>(q, k, v, q_out, k_out, v_out, d_pos, naxes, T, heads, head_dim,
+                             1.0f, status, s);
 }
 
 }  // namespace mf

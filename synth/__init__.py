@@ -19,6 +19,14 @@ Workloads (the pages' workload shapes; the pages' own data are proprietary):
                   fillers up to 50,000 tokens, t ~ U[64, 512]; 24 x 128;
                   Q/K/V = bf16(s * N(0,1)) with s ~ U(0.5, 2) per tensor and head;
                   forward + backward
+  edit_tiny       editing pack (text, source grid, target grid):
+                  (5, 2x3, 2x3), (3, 4x2, 3x3), (0, 1x1, 1x1); 2 heads x 64
+  edit_50k        editing pack: one latent grid per sample from the mixed set,
+                  used for both the source and the target image, text U[32, 512],
+                  appended until the next sample would exceed 50,000 tokens;
+                  24 x 128; forward + backward
+Editing specs are (text_len, Hs, Ws, Ht, Wt) and the sample is [text; source;
+target].
 """
 from __future__ import annotations
 
@@ -162,8 +170,13 @@ class Workload:
     note: str = ""
 
     @property
+    def edit(self) -> bool:
+        """Editing pack: specs are (text_len, Hs, Ws, Ht, Wt)."""
+        return bool(self.specs) and len(self.specs[0]) == 5
+
+    @property
     def lengths(self):
-        return [t + h * w for (t, h, w) in self.specs]
+        return [s[0] + s[1] * s[2] + (s[3] * s[4] if len(s) == 5 else 0) for s in self.specs]
 
     @property
     def total(self):
@@ -225,13 +238,34 @@ def extreme_aspect(seed: int = 0, budget: int = TOKEN_BUDGET) -> Workload:
     return Workload("extreme_aspect", specs, 24, 128, seed, True, head_scale=True)
 
 
-WORKLOADS = {f.__name__: f for f in (tiny, single_1024, mixed_50k, cfg_2048, extreme_aspect)}
+def edit_tiny(seed: int = 0) -> Workload:
+    return Workload("edit_tiny", [(5, 2, 3, 2, 3), (3, 4, 2, 3, 3), (0, 1, 1, 1, 1)], 2, 64, seed,
+                    True)
+
+
+def edit_50k(seed: int = 0, budget: int = TOKEN_BUDGET) -> Workload:
+    specs, total, k = [], 0, 0
+    while True:
+        g = int(randint(seed, STREAM_SPECS + 300, k + 1, 0, len(MIXED_GRIDS) - 1)[k])
+        t = int(randint(seed, STREAM_SPECS + 400, k + 1, 32, 512)[k])
+        H, W = MIXED_GRIDS[g]
+        L = t + 2 * H * W
+        if total + L > budget:
+            break
+        specs.append((t, H, W, H, W))
+        total += L
+        k += 1
+    return Workload("edit_50k", specs, 24, 128, seed, True)
+
+
+WORKLOADS = {f.__name__: f for f in (tiny, single_1024, mixed_50k, cfg_2048, extreme_aspect,
+                                     edit_tiny, edit_50k)}
 
 
 def workload(name: str, seed: int = 0, budget: int | None = None) -> Workload:
     """A named workload; `budget` overrides the 50,000-token budget of the two
     budget-packed workloads (used for smaller profiling captures)."""
-    if budget is not None and name in ("mixed_50k", "extreme_aspect"):
+    if budget is not None and name in ("mixed_50k", "extreme_aspect", "edit_50k"):
         return WORKLOADS[name](seed, budget=budget)
     return WORKLOADS[name](seed)
 

@@ -124,3 +124,21 @@ def test_neighbour_argument_errors_on_host():
     assert lib.mf_gated_residual(x, s1, cu, 2, 10, 60, s2, y, None) == 2
     assert lib.mf_gated_residual(x, None, cu, 2, 10, 64, s2, y, None) == 1
     assert lib.mf_gated_residual(x, s1, cu, -1, 10, 64, s2, y, None) == 1
+
+
+def test_pack3d_size_host():
+    assert mf.pack3d_size([(2, 1, 2, 2, 1)]) == (6, 6)
+    assert mf.pack3d_size([]) == (0, 0)
+    with pytest.raises(mf.MFError) as ei:
+        mf.pack3d_size([(1, 2, 3, -1, 1)])
+    assert ei.value.status == 1
+    with pytest.raises(mf.MFError) as ei:
+        mf.pack3d_size([(0, 65536, 65536, 0, 0)])
+    assert ei.value.status == 3
+    lib = mf.load()
+    p = ctypes.c_void_p
+    assert lib.mf_rope3d_qk(p(1 << 20), None, p(1 << 21), None, p(1 << 22), 4, 2, 80, None) == 2
+    assert lib.mf_rope3d_qk(p(1 << 20), None, p(1 << 21), None, None, 4, 2, 64, None) == 1
+    assert lib.mf_varlen_attn_fwd_3d(p(1 << 20), p(1 << 21), p(1 << 22), p(1 << 23), None, 1, 8, 8,
+                                     1, 64, 0.0, p(1 << 24), p(1 << 25), p(1 << 26), 1 << 20,
+                                     None) == 1  # 3D positions are required
