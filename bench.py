@@ -159,6 +159,27 @@ def reference_arm(args):
 
 
 # --------------------------------------------------------------- GPU arm
+def rank_workload(name: str, seed: int, rank: int, budget=None):
+    """The pack a rank processes: its own seeded draw of the workload (seed + rank).
+    Ranks share no data, so the path needs no collective (weak scaling)."""
+    return synth.workload(name, seed + rank, budget)
+
+
+def reduce_over_ranks(ms: float, flops: float, world: int):
+    """(max over ranks of the step time, sum over ranks of the work): the
+    whole-job throughput is the second over the first.  Host-side gloo / NCCL
+    all-reduces of two scalars; nothing on the data path."""
+    if world <= 1:
+        return ms, flops
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms, flops], dtype=torch.float64)
+    tmax, tsum = t.clone(), t.clone()
+    dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+    dist.all_reduce(tsum, op=dist.ReduceOp.SUM)
+    return float(tmax[0]), float(tsum[1])
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -226,7 +247,7 @@ def gpu_arm(args):
         if world > 1:
             dist.barrier()
 
-    wl = synth.workload(args.workload, args.seed + rank, args.budget)
+    wl = rank_workload(args.workload, args.seed, rank, args.budget)
     q, k, v, do = synth.make_inputs(wl, with_do=True)
     T, max_len = mf.pack3d_size(wl.specs) if wl.edit else mf.pack_size(wl.specs)
     n, h, d = len(wl.specs), wl.heads, wl.head_dim
@@ -273,15 +294,7 @@ def gpu_arm(args):
     ms = ev0.elapsed_time(ev1) / args.steps
 
     flops_fwd, flops_bwd = wl.flops_fwd(), wl.flops_bwd()
-    t = torch.tensor([ms, flops_fwd + flops_bwd], dtype=torch.float64)
-    if world > 1:
-        tmax = t.clone()
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        tsum = t.clone()
-        dist.all_reduce(tsum, op=dist.ReduceOp.SUM)
-        ms_max, flops_all = float(tmax[0]), float(tsum[1])
-    else:
-        ms_max, flops_all = ms, float(t[1])
+    ms_max, flops_all = reduce_over_ranks(ms, flops_fwd + flops_bwd, world)
     value = flops_all / (ms_max / 1e3) / 1e12
 
     # ---- end to end through the public API with pinned host buffers
@@ -306,11 +319,7 @@ def gpu_arm(args):
         e2e_step()
     ev1.record()
     barrier()
-    ms_e2e = ev0.elapsed_time(ev1) / e2e_steps
-    if world > 1:
-        te = torch.tensor([ms_e2e], dtype=torch.float64)
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        ms_e2e = float(te[0])
+    ms_e2e, _ = reduce_over_ranks(ev0.elapsed_time(ev1) / e2e_steps, 0.0, world)
     elem = T * h * d
     h2d = 4 * elem * 2
     d2h = 4 * elem * 2 + h * T * 4
