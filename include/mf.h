@@ -276,7 +276,7 @@ mf_status mf_cfg_euler_step(const mf_bf16* v, const int32_t* specs, int32_t pair
  * mean and biased variance over the Dm features, no affine parameters.
  * x, y: DEVICE bf16 [T][Dm] (y == x allowed); shift, scale: DEVICE bf16 [n][Dm];
  * d_cu_seqlens: DEVICE int32 [n+1] as for the attention.  fp32 arithmetic.
- * Dm must be a multiple of 8 and at most 4096, pointers 16-byte aligned (else
+ * Dm must be a multiple of 8 and pointers 16-byte aligned (else
  * MF_ERR_UNSUPPORTED); n = 0 with T > 0, eps < 0 or NULL pointers:
  * MF_ERR_INVALID_ARG.  A malformed cu_seqlens gives wrong rows, never an
  * out-of-range access (every row maps to a sample index in [0, n)).
@@ -289,7 +289,7 @@ mf_status mf_adaln_modulate(const mf_bf16* x, const int32_t* d_cu_seqlens, int32
  * Gated residual update of a packed batch (output side of the same fused chain):
  * out_t = x_t + gate_s * h_t for every token t of sample s.  x, h, out: DEVICE bf16
  * [T][Dm] (out may alias x or h); gate: DEVICE bf16 [n][Dm].  fp32 arithmetic.
- * Same shape rules and errors as mf_adaln_modulate (any Dm multiple of 8).
+ * Same shape rules and errors as mf_adaln_modulate.
  */
 mf_status mf_gated_residual(const mf_bf16* x, const mf_bf16* h, const int32_t* d_cu_seqlens,
                             int32_t n, int32_t T, int32_t Dm, const mf_bf16* gate, mf_bf16* out,

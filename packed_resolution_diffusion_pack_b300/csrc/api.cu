@@ -385,7 +385,7 @@ mf_status mf_adaln_modulate(const mf_bf16* x, const int32_t* d_cu_seqlens, int32
                             int32_t Dm, const mf_bf16* shift, const mf_bf16* scale, float eps,
                             mf_bf16* y, mf_stream stream) {
   const void* ptrs[4] = {x, shift, scale, y};
-  const mf_status st = check_rows(ptrs, 4, d_cu_seqlens, n, T, Dm, 4096);
+  const mf_status st = check_rows(ptrs, 4, d_cu_seqlens, n, T, Dm, INT32_MAX);
   if (st != MF_OK) return st;
   if (!(eps >= 0.f)) return MF_ERR_INVALID_ARG;
   return cuda_status(launch_adaln(x, d_cu_seqlens, n, T, Dm, shift, scale, eps, y,

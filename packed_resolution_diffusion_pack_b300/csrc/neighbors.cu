@@ -147,11 +147,26 @@ __device__ __forceinline__ CuView cache_cu(const int32_t* __restrict__ cu, int32
   return CuView{cu, fits ? smem : nullptr, n};
 }
 
-// One warp = one row of Dm = 256 * NCH features at most (NCH 16-byte chunks per
-// lane); the row stays in registers between the mean, the variance (a second
-// pass over the registers) and the modulation.
-template <int NCH>
-__global__ void __launch_bounds__(32 * kRowWarps, 2) adaln_kernel(
+// Running mean / sum of squared deviations (count n) merged with another
+// partial (Chan, Golub and LeVeque's pairwise update; stable in fp32).
+__device__ __forceinline__ void merge_stats(float& n, float& mean, float& m2, float nb,
+                                            float meanb, float m2b) {
+  const float nn = n + nb;
+  if (nb > 0.f) {
+    const float d = meanb - mean;
+    const float w = nb / nn;
+    mean = fmaf(d, w, mean);
+    m2 = m2 + m2b + d * d * n * w;
+    n = nn;
+  }
+}
+
+// One warp = one row.  Pass 1 streams the row once: every 16-byte chunk's exact
+// mean and sum of squared deviations are merged into the lane's running
+// statistics, then the 32 lanes merge theirs with shuffles.  Pass 2 reads the row
+// again (from L1 / L2: HBM sees it once) and writes the modulated result.  Few
+// registers per thread keep many rows in flight.
+__global__ void __launch_bounds__(32 * kRowWarps) adaln_kernel(
     const uint4* __restrict__ x, const int32_t* __restrict__ cu, int32_t n, int32_t T,
     int32_t D8, const uint4* __restrict__ shift, const uint4* __restrict__ scale, float eps,
     uint4* __restrict__ y) {
@@ -162,61 +177,44 @@ __global__ void __launch_bounds__(32 * kRowWarps, 2) adaln_kernel(
   for (int32_t t = blockIdx.x * kRowWarps + (threadIdx.x >> 5); t < T;
        t += gridDim.x * kRowWarps) {
     const int64_t base = static_cast<int64_t>(t) * D8;
-    uint4 xv[NCH];
-#pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-      const int ch = lane + 32 * i;
-      xv[i] = ch < D8 ? x[base + ch] : make_uint4(0, 0, 0, 0);
-    }
     const int64_t mbase = static_cast<int64_t>(cv.sample(t)) * D8;
-    // sums as independent per-chunk partials (short dependency chains)
-    float part[NCH];
-#pragma unroll
-    for (int i = 0; i < NCH; ++i) {
+    float cnt = 0.f, mean = 0.f, m2 = 0.f;
+#pragma unroll 4
+    for (int ch = lane; ch < D8; ch += 32) {
       float f[8];
-      bf16x8_to_f32(xv[i], f);
-      part[i] = ((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]));
-    }
-#pragma unroll
-    for (int w = 1; w < NCH; w <<= 1)
-#pragma unroll
-      for (int i = 0; i + w < NCH; i += 2 * w) part[i] += part[i + w];
-    float sum = part[0];
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, m);
-    const float mean = sum * inv_dm;
-#pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-      float f[8];
-      bf16x8_to_f32(xv[i], f);
+      bf16x8_to_f32(__ldg(x + base + ch), f);
+      const float cm = (((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]))) * 0.125f;
       float a = 0.f, b = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
-        a = fmaf(f[e] - mean, f[e] - mean, a);
-        b = fmaf(f[e + 1] - mean, f[e + 1] - mean, b);
+        a = fmaf(f[e] - cm, f[e] - cm, a);
+        b = fmaf(f[e + 1] - cm, f[e + 1] - cm, b);
       }
-      part[i] = lane + 32 * i < D8 ? a + b : 0.f;
+      merge_stats(cnt, mean, m2, 8.f, cm, a + b);
     }
 #pragma unroll
-    for (int w = 1; w < NCH; w <<= 1)
-#pragma unroll
-      for (int i = 0; i + w < NCH; i += 2 * w) part[i] += part[i + w];
-    float sq = part[0];
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, m);
-    const float rstd = rsqrtf(sq * inv_dm + eps);
-#pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-      const int ch = lane + 32 * i;
-      if (ch < D8) {
-        float f[8], sh[8], sc[8];
-        bf16x8_to_f32(xv[i], f);
-        bf16x8_to_f32(__ldg(shift + mbase + ch), sh);
-        bf16x8_to_f32(__ldg(scale + mbase + ch), sc);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = fmaf((f[e] - mean) * rstd, 1.f + sc[e], sh[e]);
-        y[base + ch] = f32_to_bf16x8(f);
+    for (int m = 16; m > 0; m >>= 1) {
+      const float nb = __shfl_xor_sync(0xffffffffu, cnt, m);
+      const float mb = __shfl_xor_sync(0xffffffffu, mean, m);
+      const float qb = __shfl_xor_sync(0xffffffffu, m2, m);
+      if (cnt == 0.f) {
+        cnt = nb;
+        mean = mb;
+        m2 = qb;
+      } else {
+        merge_stats(cnt, mean, m2, nb, mb, qb);
       }
+    }
+    const float rstd = rsqrtf(m2 * inv_dm + eps);
+#pragma unroll 4
+    for (int ch = lane; ch < D8; ch += 32) {
+      float f[8], sh[8], sc[8];
+      bf16x8_to_f32(__ldg(x + base + ch), f);
+      bf16x8_to_f32(__ldg(shift + mbase + ch), sh);
+      bf16x8_to_f32(__ldg(scale + mbase + ch), sc);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = fmaf((f[e] - mean) * rstd, 1.f + sc[e], sh[e]);
+      y[base + ch] = f32_to_bf16x8(f);
     }
   }
 }
@@ -263,11 +261,8 @@ cudaError_t launch_adaln(const uint16_t* x, const int32_t* cu, int32_t n, int32_
                          const uint16_t* shift, const uint16_t* scale, float eps, uint16_t* y,
                          cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int nch = (Dm / 8 + 31) / 32;  // 16-byte chunks per lane (Dm <= 4096: at most 16)
-  auto* kern = nch <= 4 ? adaln_kernel<4> : nch <= 8 ? adaln_kernel<8>
-             : nch <= 12 ? adaln_kernel<12> : adaln_kernel<16>;
   KernelTimer kt(MF_K_ADALN, s);
-  kern<<<row_blocks(kern, T), 32 * kRowWarps, 0, s>>>(
+  adaln_kernel<<<row_blocks(adaln_kernel, T), 32 * kRowWarps, 0, s>>>(
       reinterpret_cast<const uint4*>(x), cu, n, T, Dm / 8, reinterpret_cast<const uint4*>(shift),
       reinterpret_cast<const uint4*>(scale), eps, reinterpret_cast<uint4*>(y));
   return cudaGetLastError();

@@ -6,7 +6,8 @@ residual.
 Tolerances, derived from the kernels' arithmetic:
   CFG step (fp32 out): fmaf(dt, fmaf(g, v_c - v_u, v_u), z) rounds twice (v_c - v_u of
       two bf16 values is exact in fp32), so |err| <= 2^-22 (|z'| + |dt| (|v_u| + |g| |v_c - v_u|)).
-  adaLN (bf16 out): fp32 mean / variance / rsqrt, then one bf16 rounding:
+  adaLN (bf16 out): fp32 streamed mean / variance (chunk statistics merged
+      pairwise) and rsqrt, then one bf16 rounding:
       |err| <= 1 bf16 ulp of the result + 1e-4.
   gated residual (bf16 out): one fp32 FMA, then one bf16 rounding: |err| <= 1 bf16 ulp.
 """
@@ -89,6 +90,7 @@ ROW_CASES = {
     "tiny_pack_dm64": (synth.tiny().lengths, 64),
     "zero_length_samples_dm8": ([3, 0, 5, 0, 0, 1], 8),
     "one_row_dm4096": ([1], 4096),
+    "wide_rows_dm6144": ([3, 2], 6144),
     "ragged_dm1032": ([17, 1, 64, 5], 1032),
     "mixed_50k_dm3072": (synth.mixed_50k().lengths, 3072),
 }
