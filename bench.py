@@ -257,21 +257,22 @@ def gpu_arm(args):
     o = torch.empty_like(qd)
     lse = torch.empty((h, T), dtype=torch.float32, device="cuda")
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    ws_f = mf.workspace(T, n, h, d, False)
-    ws_b = mf.workspace(T, n, h, d, True)
+    # one workspace for forward and backward: the backward reuses the forward's
+    # rotated fp16 operands (mf_varlen_attn_bwd_after_fwd)
+    ws = mf.workspace(T, n, h, d, True)
     cu = torch.empty(n + 1, dtype=torch.int32, device="cuda")
     pos = torch.empty((T, 3 if wl.edit else 2), dtype=torch.int32, device="cuda")
     packer = mf.pack3d if wl.edit else mf.pack
 
     def step(qd=qd, kd=kd, vd=vd, dod=dod):
         packer(wl.specs, cu=cu, pos=pos)
-        mf.varlen_attn_fwd(qd, kd, vd, cu, pos, max_len, o=o, lse=lse, ws=ws_f)
-        mf.varlen_attn_bwd(qd, kd, vd, o, lse, dod, cu, pos, max_len, dq=dq, dk=dk, dv=dv, ws=ws_b)
+        mf.varlen_attn_fwd(qd, kd, vd, cu, pos, max_len, o=o, lse=lse, ws=ws)
+        mf.varlen_attn_bwd(qd, kd, vd, o, lse, dod, cu, pos, max_len, dq=dq, dk=dk, dv=dv, ws=ws,
+                           after_fwd=True)
 
     for _ in range(max(args.warmup, 3)):
         step()
-    mf.get_status(ws_f)
-    mf.get_status(ws_b)
+    mf.get_status(ws)
     barrier()
 
     props = torch.cuda.get_device_properties(local)
@@ -289,8 +290,7 @@ def gpu_arm(args):
     clocks = clk.result()
     kern = mf.timing_read()
     mf.timing_enable(False)
-    mf.get_status(ws_f)
-    mf.get_status(ws_b)
+    mf.get_status(ws)
     ms = ev0.elapsed_time(ev1) / args.steps
 
     flops_fwd, flops_bwd = wl.flops_fwd(), wl.flops_bwd()
@@ -333,10 +333,10 @@ def gpu_arm(args):
         qq, kk, vv, dd = dev_in[b]
         out = dev_out[b]
         packer(wl.specs, cu=cu, pos=pos, stream=s_comp)
-        mf.varlen_attn_fwd(qq, kk, vv, cu, pos, max_len, o=out["o"], lse=out["lse"], ws=ws_f,
+        mf.varlen_attn_fwd(qq, kk, vv, cu, pos, max_len, o=out["o"], lse=out["lse"], ws=ws,
                            stream=s_comp)
         mf.varlen_attn_bwd(qq, kk, vv, out["o"], out["lse"], dd, cu, pos, max_len, dq=out["dq"],
-                           dk=out["dk"], dv=out["dv"], ws=ws_b, stream=s_comp)
+                           dk=out["dk"], dv=out["dv"], ws=ws, stream=s_comp, after_fwd=True)
         ev_comp[b].record(s_comp)
         s_down.wait_event(ev_comp[b])
         with torch.cuda.stream(s_down):
@@ -353,8 +353,7 @@ def gpu_arm(args):
         e2e_step(i)
     e1.record(s_down)
     barrier()
-    mf.get_status(ws_f, s_comp)
-    mf.get_status(ws_b, s_comp)
+    mf.get_status(ws, s_comp)
     ms_e2e, _ = reduce_over_ranks(e0.elapsed_time(e1) / e2e_steps, 0.0, world)
     elem = T * h * d
     h2d = 4 * elem * 2
@@ -373,11 +372,11 @@ def gpu_arm(args):
     peak_name = (f"{pk['source']} bf16 " + ("burst (cuBLAS 8192^3, SM clock at max under our "
                  "load)" if full_clock else "sustained (cuBLAS, seconds-long loop)"))
     # algorithmic work per launch: FLOPs for the attention kernels, bytes for the
-    # memory-bound ones (rope: average of the forward launch, which rotates Q, K and
-    # converts V, and the backward launch, Q and K only)
+    # memory-bound ones (rope: the forward's pre-pass reads q, k, v bf16 and writes
+    # Q', K', V' fp16; the backward reuses them)
     elems = float(T * h * d)
     algo = {"attn_fwd": ("tensor", flops_fwd), "attn_bwd": ("tensor", flops_bwd),
-            "rope": ("hbm", 10.0 * elems + 8.0 * T),
+            "rope": ("hbm", 12.0 * elems + 8.0 * T),
             "bwd_pre": ("hbm", 10.0 * elems + 4.0 * h * T),
             "dq_post": ("hbm", 6.0 * elems + 8.0 * T)}
     for name, (bound, amount) in algo.items():
@@ -404,7 +403,8 @@ def gpu_arm(args):
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(wl), "global_tokens": T * world,
-                   "step": "mf_pack + mf_varlen_attn_fwd (RoPE + attention) + mf_varlen_attn_bwd",
+                   "step": "mf_pack + mf_varlen_attn_fwd (RoPE + attention) + "
+                           "mf_varlen_attn_bwd_after_fwd (one shared workspace)",
                    "l2": "no flush: Q, K, V, dO alone are %.2f GB, far above the 126 MB L2" % (
                        4 * elem * 2 / 1e9),
                    "parallelism": "replicas: one pack per GPU, no data-path collective"},

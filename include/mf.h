@@ -169,6 +169,28 @@ mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
                              void* ws, size_t ws_bytes, mf_stream stream);
 
 /*
+ * The backward of a training step whose forward ran on the SAME workspace.
+ * mf_varlen_attn_fwd / _fwd_3d leave the rotated fp16 operands Q' = R q and
+ * K' = R k in the workspace at the offsets the backward reads them from, so this
+ * call skips the backward's own rotation pre-pass (one read of q and k and one
+ * write of Q', K').  Arguments as mf_varlen_attn_bwd, plus pos_axes (2 for d_pos
+ * [T][2], 3 for editing packs' [T][3]).  Preconditions, which the call cannot
+ * check: ws (sized by mf_attn_workspace_bytes(..., bwd = 1), which also fits the
+ * forward) was last used by the forward of these q, k, d_pos, n, T, heads and
+ * head_dim on the same stream, and neither q nor k changed since.  The fp16 range
+ * check of Q' and K' is then the forward's: read it with mf_get_status after the
+ * forward.  Results equal mf_varlen_attn_bwd's (dQ up to its atomic summation
+ * order).  No counterpart on the pages: a workspace-sharing form of the backward.
+ */
+mf_status mf_varlen_attn_bwd_after_fwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                       const mf_bf16* o, const float* lse, const mf_bf16* d_o,
+                                       const int32_t* d_cu_seqlens, const int32_t* d_pos,
+                                       int32_t pos_axes, int32_t n, int32_t T, int32_t max_len,
+                                       int32_t heads, int32_t head_dim, float softmax_scale,
+                                       mf_bf16* dq, mf_bf16* dk, mf_bf16* dv, void* ws,
+                                       size_t ws_bytes, mf_stream stream);
+
+/*
  * Frame-aware 3D positions for editing packs.  The pages say that editing
  * extends the 2D rotary embedding with a frame dimension that tells source and
  * target visual tokens apart (hyper.ai summary "Method"; paperlayer.ai summary

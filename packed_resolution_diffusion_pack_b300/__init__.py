@@ -190,8 +190,12 @@ def varlen_attn_fwd(q, k, v, cu_seqlens, pos, max_len, softmax_scale: float = 0.
 
 
 def varlen_attn_bwd(q, k, v, o, lse, d_o, cu_seqlens, pos, max_len, softmax_scale: float = 0.0,
-                    dq=None, dk=None, dv=None, ws=None, stream=None):
-    """Gradients (dq, dk, dv) with respect to the un-rotated q, k and v."""
+                    dq=None, dk=None, dv=None, ws=None, stream=None, after_fwd: bool = False):
+    """Gradients (dq, dk, dv) with respect to the un-rotated q, k and v.
+
+    after_fwd=True: `ws` is the workspace the forward of these q, k, pos just used
+    (sized for the backward); the forward's rotated operands are reused and the
+    backward's own rotation pre-pass is skipped (mf_varlen_attn_bwd_after_fwd)."""
     torch = _torch()
     _check_thd("q", q)
     T, h, d = q.shape
@@ -201,6 +205,15 @@ def varlen_attn_bwd(q, k, v, o, lse, d_o, cu_seqlens, pos, max_len, softmax_scal
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    if after_fwd:
+        if ws is None:
+            raise ValueError("after_fwd needs the workspace the forward used")
+        check(load().mf_varlen_attn_bwd_after_fwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(cu_seqlens), _ptr(pos),
+            3 if _is_3d(pos) else 2, n, T, int(max_len), h, d, float(softmax_scale), _ptr(dq),
+            _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream_ptr(stream)),
+            "mf_varlen_attn_bwd_after_fwd")
+        return dq, dk, dv
     ws = workspace(T, n, h, d, True, q.device) if ws is None else ws
     fn = "mf_varlen_attn_bwd_3d" if _is_3d(pos) else "mf_varlen_attn_bwd"
     check(getattr(load(), fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),

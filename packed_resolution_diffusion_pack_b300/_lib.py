@@ -33,6 +33,9 @@ SIGNATURES = {
                                           _p, _p, _p, _sz, _p]),
     "mf_varlen_attn_bwd": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32,
                                           _i32, _f32, _p, _p, _p, _p, _sz, _p]),
+    "mf_varlen_attn_bwd_after_fwd": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _i32, _i32,
+                                                    _i32, _i32, _i32, _i32, _f32, _p, _p, _p, _p,
+                                                    _sz, _p]),
     "mf_varlen_attn_fwd_noalloc": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32,
                                                   _i32, _f32, _p, _p, _p]),
     "mf_pack3d_size": (ctypes.c_int, [_p, _i32, _p, _p]),

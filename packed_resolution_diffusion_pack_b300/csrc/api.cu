@@ -200,7 +200,8 @@ static mf_status attn_bwd_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16
                                const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t naxes,
                                int32_t n, int32_t T, int32_t max_len, int32_t heads,
                                int32_t head_dim, float softmax_scale, mf_bf16* dq, mf_bf16* dk,
-                               mf_bf16* dv, void* ws, size_t ws_bytes, mf_stream stream) {
+                               mf_bf16* dv, void* ws, size_t ws_bytes, mf_stream stream,
+                               bool reuse_rotated = false) {
   const void* ptrs[9] = {q, k, v, o, lse, d_o, dq, dk, dv};
   mf_status st = check_attn(ptrs, 9, d_cu_seqlens, n, T, max_len, heads, head_dim, ws, ws_bytes,
                             true);
@@ -221,9 +222,11 @@ static mf_status attn_bwd_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16
   // Q' = R q, K' = R k in fp16, as in the forward (same logits as the LSE came from)
   auto* q16 = reinterpret_cast<uint16_t*>(w + L.q16);
   auto* k16 = reinterpret_cast<uint16_t*>(w + L.k16);
-  e = launch_prep_f16(q, k, nullptr, q16, k16, nullptr, d_pos, naxes, T, heads, head_dim, status,
-                      s);
-  if (e != cudaSuccess) return MF_ERR_CUDA;
+  if (!reuse_rotated) {
+    e = launch_prep_f16(q, k, nullptr, q16, k16, nullptr, d_pos, naxes, T, heads, head_dim, status,
+                        s);
+    if (e != cudaSuccess) return MF_ERR_CUDA;
+  }
   AttnBwdArgs a;
   a.q = q16;
   a.k = k16;
@@ -274,6 +277,18 @@ mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
                              void* ws, size_t ws_bytes, mf_stream stream) {
   return attn_bwd_impl(q, k, v, o, lse, d_o, d_cu_seqlens, d_pos, 2, n, T, max_len, heads,
                        head_dim, softmax_scale, dq, dk, dv, ws, ws_bytes, stream);
+}
+
+mf_status mf_varlen_attn_bwd_after_fwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                       const mf_bf16* o, const float* lse, const mf_bf16* d_o,
+                                       const int32_t* d_cu_seqlens, const int32_t* d_pos,
+                                       int32_t pos_axes, int32_t n, int32_t T, int32_t max_len,
+                                       int32_t heads, int32_t head_dim, float softmax_scale,
+                                       mf_bf16* dq, mf_bf16* dk, mf_bf16* dv, void* ws,
+                                       size_t ws_bytes, mf_stream stream) {
+  if (pos_axes != 2 && pos_axes != 3) return MF_ERR_INVALID_ARG;
+  return attn_bwd_impl(q, k, v, o, lse, d_o, d_cu_seqlens, d_pos, pos_axes, n, T, max_len, heads,
+                       head_dim, softmax_scale, dq, dk, dv, ws, ws_bytes, stream, true);
 }
 
 mf_status mf_varlen_attn_fwd_3d(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,

@@ -267,3 +267,30 @@ def test_full_extreme_aspect(cuda_lib):
     wl = synth.extreme_aspect()
     # the 32x128 panorama (sample 0) and the last 64x64 filler
     _full_size("extreme_aspect", fwd_rows=32, bwd_pairs=[(len(wl.specs) - 1, 5)])
+
+
+@pytest.mark.parametrize("edit", [False, True])
+def test_bwd_after_fwd_reuses_rotated_operands(cuda_lib, edit):
+    """One workspace for forward and backward with the backward's rotation pre-pass
+    skipped gives the regular backward's results (dK, dV bit for bit; dQ up to its
+    atomic summation order)."""
+    mf = cuda_lib
+    if edit:
+        specs = [(7, 8, 16, 8, 16), (1, 16, 16, 12, 20), (3, 5, 7, 5, 7)]
+        cu, pos = mf.pack3d(specs)
+        T, max_len = mf.pack3d_size(specs)
+    else:
+        specs = RAGGED_SPECS
+        cu, pos = mf.pack(specs)
+        T, max_len = mf.pack_size(specs)
+    q, k, v, do = (dev(x) for x in random_inputs(T, 2, 128, 31))
+    n = len(specs)
+    o, lse = mf.varlen_attn_fwd(q, k, v, cu, pos, max_len, ws=mf.workspace(T, n, 2, 128, False))
+    ref = mf.varlen_attn_bwd(q, k, v, o, lse, do, cu, pos, max_len, ws=mf.workspace(T, n, 2, 128, True))
+    ws = mf.workspace(T, n, 2, 128, True)
+    o2, lse2 = mf.varlen_attn_fwd(q, k, v, cu, pos, max_len, ws=ws)
+    got = mf.varlen_attn_bwd(q, k, v, o2, lse2, do, cu, pos, max_len, ws=ws, after_fwd=True)
+    mf.get_status(ws)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    assert torch.equal(ref[1], got[1]) and torch.equal(ref[2], got[2])
+    _close_ulp(ref[0], got[0])
