@@ -68,9 +68,14 @@ def lib(so: str | None = None):
         L.oracle_rope3d.argtypes = [p, p, i64, i64, i64, f64, i32, p]
         L.oracle_adaln.argtypes = [p, p, i64, i64, p, p, f64, p]
         L.oracle_gated_residual.argtypes = [p, p, p, i64, i64, p, p]
+        L.oracle_e4m3_array.argtypes = [p, i64, p]
+        L.oracle_quant_e4m3.argtypes = [p, p, p, p, i64, i64, i64, i32, p, p, p, p, p, p]
+        L.oracle_attn_fwd_e4m3.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, f64, i32, p,
+                                           p]
         for f in (L.oracle_pack, L.oracle_rope2d, L.oracle_attn_fwd, L.oracle_attn_bwd,
                   L.oracle_attn_fwd_rows, L.oracle_cfg_euler, L.oracle_adaln,
-                  L.oracle_gated_residual, L.oracle_pack3d, L.oracle_rope3d):
+                  L.oracle_gated_residual, L.oracle_pack3d, L.oracle_rope3d,
+                  L.oracle_e4m3_array, L.oracle_quant_e4m3, L.oracle_attn_fwd_e4m3):
             f.restype = ctypes.c_int
         _libs[key] = L
     return _libs[key]
@@ -235,6 +240,55 @@ def gated_residual(x, h, cu, gate, so: str | None = None):
     lib(so).oracle_gated_residual(x.ctypes.data, h.ctypes.data, cu.ctypes.data, len(cu) - 1,
                                   x.shape[1], gate.ctypes.data, out.ctypes.data)
     return out
+
+
+def e4m3(x, so: str | None = None):
+    """Nearest OCP E4M3 value of each element (ties to even, saturating at +-448),
+    as float64."""
+    x = _f64(x)
+    y = np.empty_like(x)
+    lib(so).oracle_e4m3_array(x.ctypes.data, x.size, y.ctypes.data)
+    return y
+
+
+def quant_e4m3(q, k, v, pos, round: bool = True, base: float = ROPE_BASE,
+               so: str | None = None):
+    """The 8-bit variant's operands: (qh, sq, kh, sk, vh, sv) with qh, kh, vh
+    [T, h, d] (e4m3 values as float64), sq [T, h], sk and sv [h].  q and k are
+    rotated first (pos [T, 2]: 2D rotation, [T, 3]: frame-aware 3D, None: none)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, h, d = q.shape
+    if pos is None:
+        qr, kr = q, k
+    elif np.asarray(pos).shape[1] == 3:
+        qr, kr = rope3d(q, pos, base=base, so=so), rope3d(k, pos, base=base, so=so)
+    else:
+        qr, kr = rope2d(q, pos, base=base, so=so), rope2d(k, pos, base=base, so=so)
+    qh, kh, vh = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+    sq = np.empty((T, h))
+    sk, sv = np.empty(h), np.empty(h)
+    if lib(so).oracle_quant_e4m3(_f64(qr).ctypes.data, k.ctypes.data, _f64(kr).ctypes.data,
+                                 v.ctypes.data, T, h, d, 1 if round else 0, qh.ctypes.data,
+                                 sq.ctypes.data, kh.ctypes.data, sk.ctypes.data, vh.ctypes.data,
+                                 sv.ctypes.data) != 0:
+        raise ValueError("head_dim must be even")
+    return qh, sq, kh, sk, vh, sv
+
+
+def attn_fwd_e4m3(q, k, v, cu, pos, scale=None, round: bool = True, base: float = ROPE_BASE,
+                  so: str | None = None):
+    """O [T, h, d] and LSE [h, T] of the 8-bit variant of the forward (operands and
+    probabilities rounded to e4m3; round=False keeps every value exact)."""
+    qh, sq, kh, sk, vh, sv = quant_e4m3(q, k, v, pos, round=round, base=base, so=so)
+    T, h, d = qh.shape
+    cu = np.ascontiguousarray(cu, dtype=np.int64)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = np.zeros_like(qh)
+    lse = np.zeros((h, T))
+    lib(so).oracle_attn_fwd_e4m3(qh.ctypes.data, sq.ctypes.data, kh.ctypes.data, sk.ctypes.data,
+                                 vh.ctypes.data, sv.ctypes.data, cu.ctypes.data, len(cu) - 1, T,
+                                 h, d, scale, 1 if round else 0, o.ctypes.data, lse.ctypes.data)
+    return o, lse
 
 
 def sample_head_slice(x, cu, i: int, a: int):

@@ -428,3 +428,158 @@ int oracle_rope3d(const double* x, const int64_t* pos, int64_t T, int64_t heads,
       rope3_vec(x + (t * heads + a) * d, pos + 3 * t, d, base, sign, y + (t * heads + a) * d);
   return ORACLE_OK;
 }
+
+/* ------------------------------------------------- e4m3 forward variant */
+/*
+ * The 8-bit variant of the attention forward.  The pages give no low-precision
+ * recipe (it is an engineering variant of the same attention); every step below
+ * is this variant's own definition, written in the order the variant takes it.
+ *
+ * E4M3 is the OCP 8-bit floating-point format: a sign bit, 4 exponent bits with
+ * bias 7 and 3 mantissa bits; normals (1 + m/8) 2^(e-7) for e = 1..15, except that
+ * e = 15 with m = 7 is NaN, so the largest finite value is 448; subnormals
+ * (m/8) 2^-6; no infinities.  oracle_e4m3 rounds a double to the nearest such
+ * value, ties to the even mantissa, and saturates beyond +-448 (the
+ * "satfinite" conversion).
+ */
+double oracle_e4m3(double x) {
+  if (x != x) return x;
+  const double a = fabs(x);
+  if (a >= 448.0) return x < 0 ? -448.0 : 448.0;
+  if (a == 0.0) return x;
+  int ex;
+  frexp(a, &ex);             /* a = f 2^ex, f in [0.5, 1): binade [2^(ex-1), 2^ex) */
+  int e = ex - 1;
+  if (e < -6) e = -6;        /* subnormals share the quantum of the lowest binade */
+  const double quantum = ldexp(1.0, e - 3);
+  const double r = nearbyint(a / quantum) * quantum; /* default mode: ties to even */
+  const double out = r > 448.0 ? 448.0 : r;
+  return x < 0 ? -out : out;
+}
+
+/*
+ * Quantisation of the operands (their values as doubles; the codes are these
+ * values' e4m3 encodings).  Inputs: the rotated qr, kr, the un-rotated k and v,
+ * all [T][heads][d].  round = 0 replaces e4m3 rounding by the identity.
+ *  Q: per (token, head) row, sq = max_e |q'_e| / 448 (0 for an all-zero row),
+ *     qh = e4m3(q' / sq)  (0 where sq = 0).
+ *  K: per head, sk = max over the head's tokens and rotary pairs (2P, 2P+1) of
+ *     the pair norm sqrt(k_2P^2 + k_2P+1^2) of the UN-rotated k, / 448.  A rotation
+ *     keeps each pair's norm, so the norm bounds every rotated component at every
+ *     position: kh = e4m3(k' / sk).
+ *  V: per head, sv = max |v| / 448, vh = e4m3(v / sv).
+ * Outputs qh, kh, vh [T][heads][d]; sq [T][heads]; sk, sv [heads].
+ */
+int oracle_quant_e4m3(const double* qr, const double* k, const double* kr, const double* v,
+                      int64_t T, int64_t heads, int64_t d, int round, double* qh, double* sq,
+                      double* kh, double* sk, double* vh, double* sv) {
+  if (d % 2 != 0) return ORACLE_ERR;
+  for (int64_t a = 0; a < heads; ++a) {
+    double kmax = 0.0, vmax = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+      const double* kk = k + (t * heads + a) * d;
+      const double* vv = v + (t * heads + a) * d;
+      for (int64_t e = 0; e < d; e += 2) {
+        const double nrm = sqrt(kk[e] * kk[e] + kk[e + 1] * kk[e + 1]);
+        if (nrm > kmax) kmax = nrm;
+      }
+      for (int64_t e = 0; e < d; ++e)
+        if (fabs(vv[e]) > vmax) vmax = fabs(vv[e]);
+    }
+    sk[a] = kmax / 448.0;
+    sv[a] = vmax / 448.0;
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t a = 0; a < heads; ++a) {
+      const int64_t row = (t * heads + a) * d;
+      double qmax = 0.0;
+      for (int64_t e = 0; e < d; ++e)
+        if (fabs(qr[row + e]) > qmax) qmax = fabs(qr[row + e]);
+      sq[t * heads + a] = qmax / 448.0;
+      for (int64_t e = 0; e < d; ++e) {
+        const double xq = qmax > 0 ? qr[row + e] / (qmax / 448.0) : 0.0;
+        const double xk = sk[a] > 0 ? kr[row + e] / sk[a] : 0.0;
+        const double xv = sv[a] > 0 ? v[row + e] / sv[a] : 0.0;
+        qh[row + e] = round ? oracle_e4m3(xq) : xq;
+        kh[row + e] = round ? oracle_e4m3(xk) : xk;
+        vh[row + e] = round ? oracle_e4m3(xv) : xv;
+      }
+    }
+  return ORACLE_OK;
+}
+
+/*
+ * Attention of one sample from the quantised operands, one query row at a time,
+ * with the probabilities themselves rounded to e4m3 before they weight V.  The
+ * rounding of a probability depends on the reference it is taken against, so the
+ * row follows the variant's steps over keys in tiles of 128 from the sample's
+ * first key (base-2 logits, a running maximum and a fixed bias):
+ *   x_k   = log2(e) * scale * sq_j * sk * <qh_j, kh_k>          (all keys of the tile)
+ *   tile 0 sets m = max_k x_k;  a later tile replaces m by its own maximum M only
+ *         when M > m + 2, and then multiplies l and the accumulator by 2^(m - M);
+ *   p_k   = 2^(x_k - m + 6)       (at most 2^8 < 448: no saturation)
+ *   l    += p_k;   acc += e4m3(p_k) * vh_k
+ * and at the end O_j = sv * acc / l, LSE_j = ln(2) * (m - 6 + log2 l).
+ * With round = 0 nothing is rounded and O, LSE are the exact attention of the
+ * (unrounded) scaled operands.
+ */
+int oracle_attn_fwd_e4m3(const double* qh, const double* sq, const double* kh, const double* sk,
+                         const double* vh, const double* sv, const int64_t* cu, int64_t n,
+                         int64_t T, int64_t heads, int64_t d, double scale, int round, double* o,
+                         double* lse) {
+  const double log2e = 1.4426950408889634074;
+  const int64_t tile = 128;
+  int64_t npairs = n * heads;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t pr = 0; pr < npairs; ++pr) {
+    const int64_t i = pr / heads, a = pr % heads;
+    const int64_t s0 = cu[i], L = cu[i + 1] - cu[i];
+    if (L <= 0) continue;
+    double* x = (double*)malloc(sizeof(double) * (size_t)tile);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int64_t j = s0; j < s0 + L; ++j) {
+      const double* qj = qh + (j * heads + a) * d;
+      const double c = log2e * scale * sq[j * heads + a] * sk[a];
+      double m = 0.0, l = 0.0;
+      for (int64_t e = 0; e < d; ++e) acc[e] = 0.0;
+      for (int64_t t0 = 0; t0 < L; t0 += tile) {
+        const int64_t nk = L - t0 < tile ? L - t0 : tile;
+        double M = -INFINITY;
+        for (int64_t kk = 0; kk < nk; ++kk) {
+          const double* kv = kh + ((s0 + t0 + kk) * heads + a) * d;
+          double dot = 0.0;
+          for (int64_t e = 0; e < d; ++e) dot += qj[e] * kv[e];
+          x[kk] = c * dot;
+          if (x[kk] > M) M = x[kk];
+        }
+        if (t0 == 0) {
+          m = M;
+        } else if (M > m + 2.0) {
+          const double f = exp2(m - M);
+          l *= f;
+          for (int64_t e = 0; e < d; ++e) acc[e] *= f;
+          m = M;
+        }
+        for (int64_t kk = 0; kk < nk; ++kk) {
+          const double p = exp2(x[kk] - m + 6.0);
+          const double pr8 = round ? oracle_e4m3(p) : p;
+          const double* vk = vh + ((s0 + t0 + kk) * heads + a) * d;
+          l += p;
+          for (int64_t e = 0; e < d; ++e) acc[e] += pr8 * vk[e];
+        }
+      }
+      for (int64_t e = 0; e < d; ++e) o[(j * heads + a) * d + e] = sv[a] * acc[e] / l;
+      lse[a * T + j] = (m - 6.0 + log2(l)) * 0.69314718055994530942;
+    }
+    free(x);
+    free(acc);
+  }
+  return ORACLE_OK;
+}
+
+/* oracle_e4m3 applied to n values. */
+int oracle_e4m3_array(const double* x, int64_t n, double* y) {
+  for (int64_t i = 0; i < n; ++i) y[i] = oracle_e4m3(x[i]);
+  return ORACLE_OK;
+}

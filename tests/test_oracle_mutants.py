@@ -56,6 +56,21 @@ MUTANTS = [
      "out[off + 2 * j] = x * cos(theta) + y * sin(theta);"),
     ("gated_first_sample_gate", "out[t * Dm + e] = x[t * Dm + e] + gate[s * Dm + e] * h[t * Dm + e];",
      "out[t * Dm + e] = x[t * Dm + e] + gate[e] * h[t * Dm + e];"),
+    ("e4m3_truncates", "nearbyint(a / quantum) * quantum", "floor(a / quantum) * quantum"),
+    ("e4m3_no_subnormal_floor", "if (e < -6) e = -6;", "if (e < -9) e = -9;"),
+    ("e4m3_two_mantissa_bits", "ldexp(1.0, e - 3)", "ldexp(1.0, e - 2)"),
+    ("quant_k_scale_from_max_abs", "const double nrm = sqrt(kk[e] * kk[e] + kk[e + 1] * kk[e + 1]);",
+     "const double nrm = fabs(kk[e]) > fabs(kk[e + 1]) ? fabs(kk[e]) : fabs(kk[e + 1]);"),
+    ("quant_q_scale_per_head", "if (fabs(qr[row + e]) > qmax) qmax = fabs(qr[row + e]);",
+     "if (fabs(qr[e]) > qmax) qmax = fabs(qr[e]);"),
+    ("attn_e4m3_lse_without_bias", "lse[a * T + j] = (m - 6.0 + log2(l)) * 0.69314718055994530942;",
+     "lse[a * T + j] = (m + log2(l)) * 0.69314718055994530942;"),
+    ("attn_e4m3_l_not_rescaled", "          l *= f;\n", "\n"),
+    ("attn_e4m3_rescale_inverted", "const double f = exp2(m - M);", "const double f = exp2(M - m);"),
+    ("attn_e4m3_missing_v_scale", "o[(j * heads + a) * d + e] = sv[a] * acc[e] / l;",
+     "o[(j * heads + a) * d + e] = acc[e] / l;"),
+    ("attn_e4m3_missing_k_scale", "const double c = log2e * scale * sq[j * heads + a] * sk[a];",
+     "const double c = log2e * scale * sq[j * heads + a];"),
 ]
 
 
