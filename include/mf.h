@@ -231,6 +231,60 @@ mf_status mf_varlen_attn_bwd_3d(const mf_bf16* q, const mf_bf16* k, const mf_bf1
                                 void* ws, size_t ws_bytes, mf_stream stream);
 
 /*
+ * The 8-bit (E4M3) variant of the attention forward.  The pages give no
+ * low-precision recipe; this is an engineering variant of mf_varlen_attn_fwd (same
+ * operation, same arguments) that runs both GEMMs on 8-bit operands at twice the
+ * tensor-core rate of 16-bit ones.  Its steps, each value rounded to the nearest
+ * E4M3 value (OCP 8-bit floating point: 4 exponent bits with bias 7, 3 mantissa
+ * bits, largest finite 448; ties to even, saturating):
+ *   - every block below is divided by its scale s: the smallest power of two with
+ *     (the block's largest magnitude A) / s <= 448, so the division is exact;
+ *   - Q' = R q, one block per (token, head) row;
+ *   - K' = R k, one block per head, with A the largest pair norm |(k_2P, k_2P+1)|
+ *     of the un-rotated k over the head's tokens: the pair norm bounds every
+ *     rotated component at any position;
+ *   - V, one block per head;
+ *   - S = Q'K'^T in fp32 from the E4M3 codes, then, per query row and tile of
+ *     128 keys from the sample's first key, base-2 logits
+ *     x = log2(e) * scale * sq * sk * S.  The running maximum m is set by the
+ *     first tile and raised only when a tile's maximum exceeds it by more than 2
+ *     (then l and the accumulator are rescaled);
+ *   - P = 2^(x - m + 6) <= 256 rounded to E4M3 before it weights V; l sums the
+ *     unrounded P;
+ *   - O = sv * (sum_k P~_k V~_k) / l in bf16, LSE = ln 2 * (m - 6 + log2 l).
+ * Accuracy: expect O errors of a few per cent of |O| against the exact attention
+ * (3 mantissa bits on both operands and probabilities); LSE within the largest
+ * logit change that the operand rounding permits.
+ * d_pos: NULL (no rotation), [T][2] (pos_axes = 2) or [T][3] (pos_axes = 3, the
+ * frame-aware 3D rotation).  Workspace: mf_attn_workspace_bytes(T, n, heads,
+ * head_dim, 0), the forward's.  head_dim must be 128 (64 returns
+ * MF_ERR_UNSUPPORTED before any launch); pos_axes other than 2 or 3 with a
+ * non-NULL d_pos returns MF_ERR_INVALID_ARG.  Other arguments and errors as
+ * mf_varlen_attn_fwd.
+ */
+mf_status mf_varlen_attn_fwd_fp8(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                 const int32_t* d_cu_seqlens, const int32_t* d_pos,
+                                 int32_t pos_axes, int32_t n, int32_t T, int32_t max_len,
+                                 int32_t heads, int32_t head_dim, float softmax_scale, mf_bf16* o,
+                                 float* lse, void* ws, size_t ws_bytes, mf_stream stream);
+
+/*
+ * The operands of the 8-bit forward on their own (its first two passes), for
+ * callers that keep E4M3 copies: q8, k8, v8 DEVICE E4M3 [T][heads][128] bytes;
+ * qscale DEVICE fp32 [T][heads], the Q row scales (powers of two; 0 for an
+ * all-zero row); kv_max2 DEVICE fp32 [2][heads]: the squared largest pair norm of
+ * k and the squared largest |v| of each head (the K and V scales are the powers of
+ * two that mf_varlen_attn_fwd_fp8 describes, for A = sqrt(kv_max2)).
+ * The call zeroes kv_max2 itself.  q, k, v, q8, k8, v8 16-byte aligned, qscale,
+ * kv_max2 and d_pos 4-byte aligned.  head_dim must be 128 (else
+ * MF_ERR_UNSUPPORTED); d_pos as in mf_varlen_attn_fwd_fp8.
+ */
+mf_status mf_quant_e4m3(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                        const int32_t* d_pos, int32_t pos_axes, int32_t T, int32_t heads,
+                        int32_t head_dim, uint8_t* q8, uint8_t* k8, uint8_t* v8, float* qscale,
+                        float* kv_max2, mf_stream stream);
+
+/*
  * Varlen attention forward that allocates nothing and takes no workspace.
  * (The pages have no counterpart to this call: it is for callers of this library.)
  * Some callers cannot allocate device memory: a plugin inside a framework that
@@ -333,11 +387,12 @@ mf_status mf_get_status(void* ws, mf_stream stream);
  * milliseconds and the number of launches since the last reset.  Ids:
  *   MF_K_PACK 0, MF_K_ROPE 1, MF_K_SCHEDULE 2, MF_K_ATTN_FWD 3, MF_K_BWD_PRE 4,
  *   MF_K_ATTN_BWD 5, MF_K_DQ_POST 6, MF_K_CFG_EULER 7, MF_K_ADALN 8,
- *   MF_K_GATED_RESIDUAL 9.
+ *   MF_K_GATED_RESIDUAL 9, MF_K_F8_AMAX 10, MF_K_F8_QUANT 11, MF_K_ATTN_FWD_F8 12.
  * Process-wide state guarded by a mutex; not for use under stream capture.
  */
 enum { MF_K_PACK = 0, MF_K_ROPE, MF_K_SCHEDULE, MF_K_ATTN_FWD, MF_K_BWD_PRE, MF_K_ATTN_BWD,
-       MF_K_DQ_POST, MF_K_CFG_EULER, MF_K_ADALN, MF_K_GATED_RESIDUAL, MF_K_COUNT };
+       MF_K_DQ_POST, MF_K_CFG_EULER, MF_K_ADALN, MF_K_GATED_RESIDUAL, MF_K_F8_AMAX,
+       MF_K_F8_QUANT, MF_K_ATTN_FWD_F8, MF_K_COUNT };
 mf_status mf_timing_enable(int32_t on);
 mf_status mf_timing_reset(void);
 mf_status mf_timing_read(int32_t id, double* total_ms, int64_t* launches);

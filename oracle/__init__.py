@@ -280,6 +280,14 @@ def attn_fwd_e4m3(q, k, v, cu, pos, scale=None, round: bool = True, base: float 
     """O [T, h, d] and LSE [h, T] of the 8-bit variant of the forward (operands and
     probabilities rounded to e4m3; round=False keeps every value exact)."""
     qh, sq, kh, sk, vh, sv = quant_e4m3(q, k, v, pos, round=round, base=base, so=so)
+    return attn_fwd_e4m3_quantized(qh, sq, kh, sk, vh, sv, cu, scale=scale, round=round, so=so)
+
+
+def attn_fwd_e4m3_quantized(qh, sq, kh, sk, vh, sv, cu, scale=None, round: bool = True,
+                            so: str | None = None):
+    """The attention steps of the 8-bit variant on operands that quant_e4m3 made
+    (for example over a whole head, then applied to one sample's slice)."""
+    qh, sq, kh, sk, vh, sv = (_f64(a) for a in (qh, sq, kh, sk, vh, sv))
     T, h, d = qh.shape
     cu = np.ascontiguousarray(cu, dtype=np.int64)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)

@@ -458,16 +458,29 @@ double oracle_e4m3(double x) {
 }
 
 /*
+ * Scale of a block whose largest magnitude is A: the smallest power of two s with
+ * A / s <= 448 (0 when A = 0).  A power of two makes x / s exact, so the rounding
+ * to e4m3 is the only rounding of the operands.  With A = m 2^p, m in [1, 2):
+ * s = 2^(p - 8) when m <= 1.75 (A / s = 256 m <= 448), else 2^(p - 7).
+ */
+static double e4m3_scale(double A) {
+  if (!(A > 0.0)) return 0.0;
+  int ex;
+  const double f = frexp(A, &ex); /* A = f 2^ex, f in [0.5, 1): m = 2f, p = ex - 1 */
+  return ldexp(1.0, (ex - 1) - 8 + (2.0 * f > 1.75 ? 1 : 0));
+}
+
+/*
  * Quantisation of the operands (their values as doubles; the codes are these
  * values' e4m3 encodings).  Inputs: the rotated qr, kr, the un-rotated k and v,
  * all [T][heads][d].  round = 0 replaces e4m3 rounding by the identity.
- *  Q: per (token, head) row, sq = max_e |q'_e| / 448 (0 for an all-zero row),
- *     qh = e4m3(q' / sq)  (0 where sq = 0).
- *  K: per head, sk = max over the head's tokens and rotary pairs (2P, 2P+1) of
- *     the pair norm sqrt(k_2P^2 + k_2P+1^2) of the UN-rotated k, / 448.  A rotation
- *     keeps each pair's norm, so the norm bounds every rotated component at every
- *     position: kh = e4m3(k' / sk).
- *  V: per head, sv = max |v| / 448, vh = e4m3(v / sv).
+ *  Q: per (token, head) row, sq = e4m3_scale(max_e |q'_e|), qh = e4m3(q' / sq)
+ *     (0 where sq = 0).
+ *  K: per head, sk = e4m3_scale of the largest pair norm
+ *     sqrt(k_2P^2 + k_2P+1^2) of the UN-rotated k over the head's tokens and
+ *     rotary pairs (2P, 2P+1).  A rotation keeps each pair's norm, so the norm
+ *     bounds every rotated component at every position: kh = e4m3(k' / sk).
+ *  V: per head, sv = e4m3_scale(max |v|), vh = e4m3(v / sv).
  * Outputs qh, kh, vh [T][heads][d]; sq [T][heads]; sk, sv [heads].
  */
 int oracle_quant_e4m3(const double* qr, const double* k, const double* kr, const double* v,
@@ -486,8 +499,8 @@ int oracle_quant_e4m3(const double* qr, const double* k, const double* kr, const
       for (int64_t e = 0; e < d; ++e)
         if (fabs(vv[e]) > vmax) vmax = fabs(vv[e]);
     }
-    sk[a] = kmax / 448.0;
-    sv[a] = vmax / 448.0;
+    sk[a] = e4m3_scale(kmax);
+    sv[a] = e4m3_scale(vmax);
   }
 #pragma omp parallel for schedule(static)
   for (int64_t t = 0; t < T; ++t)
@@ -496,9 +509,10 @@ int oracle_quant_e4m3(const double* qr, const double* k, const double* kr, const
       double qmax = 0.0;
       for (int64_t e = 0; e < d; ++e)
         if (fabs(qr[row + e]) > qmax) qmax = fabs(qr[row + e]);
-      sq[t * heads + a] = qmax / 448.0;
+      const double s = e4m3_scale(qmax);
+      sq[t * heads + a] = s;
       for (int64_t e = 0; e < d; ++e) {
-        const double xq = qmax > 0 ? qr[row + e] / (qmax / 448.0) : 0.0;
+        const double xq = s > 0 ? qr[row + e] / s : 0.0;
         const double xk = sk[a] > 0 ? kr[row + e] / sk[a] : 0.0;
         const double xv = sv[a] > 0 ? v[row + e] / sv[a] : 0.0;
         qh[row + e] = round ? oracle_e4m3(xq) : xq;

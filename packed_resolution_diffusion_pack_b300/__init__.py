@@ -19,6 +19,7 @@ __all__ = [
     "MFError", "STATUS_NAMES", "load", "library_path", "pack_size", "pack", "rope2d_qk",
     "attn_workspace_bytes", "workspace", "varlen_attn_fwd", "varlen_attn_bwd", "get_status",
     "cfg_euler_step", "adaln_modulate", "gated_residual", "pack3d_size", "pack3d", "rope3d_qk",
+    "varlen_attn_fwd_fp8", "quant_e4m3",
 ]
 
 
@@ -221,6 +222,46 @@ def varlen_attn_bwd(q, k, v, o, lse, d_o, cu_seqlens, pos, max_len, softmax_scal
                               float(softmax_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
                               ws.numel(), _stream_ptr(stream)), fn)
     return dq, dk, dv
+
+
+def varlen_attn_fwd_fp8(q, k, v, cu_seqlens, pos, max_len, softmax_scale: float = 0.0, o=None,
+                        lse=None, ws=None, stream=None):
+    """The 8-bit (E4M3) variant of varlen_attn_fwd (head_dim 128): same arguments
+    and outputs, both GEMMs on E4M3 operands and probabilities (mf.h states its
+    scaling and rounding steps).  Returns (o [T, h, d] bf16, lse [h, T] fp32)."""
+    torch = _torch()
+    _check_thd("q", q)
+    T, h, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        _check_thd(name, t, T, h, d)
+    n = cu_seqlens.numel() - 1
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((h, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = workspace(T, n, h, d, False, q.device) if ws is None else ws
+    axes = 3 if _is_3d(pos) else 2
+    check(load().mf_varlen_attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(pos),
+                                        axes, n, T, int(max_len), h, d, float(softmax_scale),
+                                        _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+                                        _stream_ptr(stream)), "mf_varlen_attn_fwd_fp8")
+    return o, lse
+
+
+def quant_e4m3(q, k, v, pos, stream=None):
+    """The 8-bit forward's operands: (q8, k8, v8) uint8 [T, h, 128] (E4M3 codes),
+    qscale fp32 [T, h] and kv_max2 fp32 [2, h] (squared largest pair norm of k and
+    squared largest |v| per head)."""
+    torch = _torch()
+    _check_thd("q", q)
+    T, h, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        _check_thd(name, t, T, h, d)
+    q8, k8, v8 = (torch.empty((T, h, d), dtype=torch.uint8, device=q.device) for _ in range(3))
+    qscale = torch.empty((T, h), dtype=torch.float32, device=q.device)
+    kv_max2 = torch.empty((2, h), dtype=torch.float32, device=q.device)
+    check(load().mf_quant_e4m3(_ptr(q), _ptr(k), _ptr(v), _ptr(pos), 3 if _is_3d(pos) else 2, T,
+                               h, d, _ptr(q8), _ptr(k8), _ptr(v8), _ptr(qscale), _ptr(kv_max2),
+                               _stream_ptr(stream)), "mf_quant_e4m3")
+    return q8, k8, v8, qscale, kv_max2
 
 
 def varlen_attn_fwd_noalloc(q, k, v, cu_seqlens, pos, max_len, softmax_scale: float = 0.0,

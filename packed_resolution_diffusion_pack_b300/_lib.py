@@ -36,6 +36,10 @@ SIGNATURES = {
     "mf_varlen_attn_bwd_after_fwd": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _i32, _i32,
                                                     _i32, _i32, _i32, _i32, _f32, _p, _p, _p, _p,
                                                     _sz, _p]),
+    "mf_varlen_attn_fwd_fp8": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32,
+                                              _i32, _f32, _p, _p, _p, _sz, _p]),
+    "mf_quant_e4m3": (ctypes.c_int, [_p, _p, _p, _p, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p,
+                                     _p]),
     "mf_varlen_attn_fwd_noalloc": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32,
                                                   _i32, _f32, _p, _p, _p]),
     "mf_pack3d_size": (ctypes.c_int, [_p, _i32, _p, _p]),
@@ -56,7 +60,7 @@ SIGNATURES = {
 
 # kernel ids of the opt-in timing (mf.h MF_K_*)
 KERNELS = ["pack", "rope", "schedule", "attn_fwd", "bwd_pre", "attn_bwd", "dq_post", "cfg_euler",
-           "adaln", "gated_residual"]
+           "adaln", "gated_residual", "f8_amax", "f8_quant", "attn_fwd_f8"]
 
 
 class MFError(RuntimeError):

@@ -31,6 +31,19 @@ WsLayout ws_layout(int64_t T, int64_t n, int64_t heads, int64_t head_dim, bool b
   if (!bwd) {
     L.v16 = off;
     off = align_up(off + 2 * elems, 1024);
+    // the 8-bit forward's operands and scales reuse the 16-bit operand space
+    size_t o8 = L.q16;
+    L.q8 = o8;
+    o8 = align_up(o8 + elems, 1024);
+    L.k8 = o8;
+    o8 = align_up(o8 + elems, 1024);
+    L.v8 = o8;
+    o8 = align_up(o8 + elems, 1024);
+    L.qscale = o8;
+    o8 = align_up(o8 + 4 * static_cast<size_t>(heads) * T, 256);
+    L.amax2 = o8;
+    o8 = align_up(o8 + 8 * static_cast<size_t>(heads), 1024);
+    if (o8 > off) off = o8;
   } else {
     L.hmax = off;
     off = align_up(off + 8 * static_cast<size_t>(heads), 256);
@@ -195,6 +208,60 @@ static mf_status attn_fwd_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16
   return cuda_status(launch_attn_fwd(a, s));
 }
 
+// The 8-bit variant of the forward: E4M3 operands with per-row Q and per-head K,
+// V scales, E4M3 probabilities, fp32 accumulation; head_dim 128.
+static mf_status attn_fwd_e4m3_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                    const int32_t* d_cu_seqlens, const int32_t* d_pos,
+                                    int32_t naxes, int32_t n, int32_t T, int32_t max_len,
+                                    int32_t heads, int32_t head_dim, float softmax_scale,
+                                    mf_bf16* o, float* lse, void* ws, size_t ws_bytes,
+                                    mf_stream stream) {
+  const void* ptrs[5] = {q, k, v, o, lse};
+  mf_status st = check_attn(ptrs, 5, d_cu_seqlens, n, T, max_len, heads, head_dim, ws, ws_bytes,
+                            false);
+  if (st != MF_OK) return st;
+  if (head_dim != 128) return MF_ERR_UNSUPPORTED;
+  if (d_pos != nullptr && !aligned(d_pos, 4)) return MF_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(T, n, heads, head_dim, false);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  auto* status = reinterpret_cast<uint32_t*>(w + L.status);
+  auto* order = reinterpret_cast<int32_t*>(w + L.order);
+  auto* prefix = reinterpret_cast<int32_t*>(w + L.prefix);
+  auto* amax2 = reinterpret_cast<uint32_t*>(w + L.amax2);
+  // the schedule also zeroes the per-head maxima
+  cudaError_t e = launch_schedule(d_cu_seqlens, n, T, max_len, heads, 256, status, order, prefix,
+                                  reinterpret_cast<float*>(amax2), 2 * heads, s);
+  if (e != cudaSuccess) return MF_ERR_CUDA;
+  if (T == 0) return MF_OK;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(head_dim));
+  auto* q8 = w + L.q8;
+  auto* k8 = w + L.k8;
+  auto* v8 = w + L.v8;
+  auto* qscale = reinterpret_cast<float*>(w + L.qscale);
+  e = launch_prep_e4m3(q, k, v, q8, k8, v8, qscale, amax2, d_pos, naxes, T, heads, head_dim, s);
+  if (e != cudaSuccess) return MF_ERR_CUDA;
+  AttnFwdArgs a;
+  a.q = reinterpret_cast<const uint16_t*>(q8);
+  a.k = reinterpret_cast<const uint16_t*>(k8);
+  a.v = reinterpret_cast<const uint16_t*>(v8);
+  a.f8 = true;
+  a.qscale = qscale;
+  a.amax2 = amax2;
+  a.cu = d_cu_seqlens;
+  a.order = order;
+  a.prefix = prefix;
+  a.status = status;
+  a.o = o;
+  a.lse = lse;
+  a.n = n;
+  a.T = T;
+  a.heads = heads;
+  a.head_dim = head_dim;
+  a.scale = scale;
+  return cuda_status(launch_attn_fwd(a, s));
+}
+
 static mf_status attn_bwd_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
                                const mf_bf16* o, const float* lse, const mf_bf16* d_o,
                                const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t naxes,
@@ -289,6 +356,40 @@ mf_status mf_varlen_attn_bwd_after_fwd(const mf_bf16* q, const mf_bf16* k, const
   if (pos_axes != 2 && pos_axes != 3) return MF_ERR_INVALID_ARG;
   return attn_bwd_impl(q, k, v, o, lse, d_o, d_cu_seqlens, d_pos, pos_axes, n, T, max_len, heads,
                        head_dim, softmax_scale, dq, dk, dv, ws, ws_bytes, stream, true);
+}
+
+mf_status mf_varlen_attn_fwd_fp8(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                 const int32_t* d_cu_seqlens, const int32_t* d_pos,
+                                 int32_t pos_axes, int32_t n, int32_t T, int32_t max_len,
+                                 int32_t heads, int32_t head_dim, float softmax_scale, mf_bf16* o,
+                                 float* lse, void* ws, size_t ws_bytes, mf_stream stream) {
+  if (d_pos != nullptr && pos_axes != 2 && pos_axes != 3) return MF_ERR_INVALID_ARG;
+  return attn_fwd_e4m3_impl(q, k, v, d_cu_seqlens, d_pos, d_pos ? pos_axes : 2, n, T, max_len,
+                            heads, head_dim, softmax_scale, o, lse, ws, ws_bytes, stream);
+}
+
+mf_status mf_quant_e4m3(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                        const int32_t* d_pos, int32_t pos_axes, int32_t T, int32_t heads,
+                        int32_t head_dim, uint8_t* q8, uint8_t* k8, uint8_t* v8, float* qscale,
+                        float* kv_max2, mf_stream stream) {
+  if (T < 0 || heads < 1) return MF_ERR_INVALID_ARG;
+  if (head_dim != 128) return MF_ERR_UNSUPPORTED;
+  if (d_pos != nullptr && pos_axes != 2 && pos_axes != 3) return MF_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(heads) * T > INT32_MAX) return MF_ERR_OVERFLOW;
+  const void* ps[9] = {q, k, v, q8, k8, v8, qscale, kv_max2, d_pos};
+  for (int i = 0; i < 8; ++i)
+    if (ps[i] == nullptr) return MF_ERR_INVALID_ARG;
+  for (int i = 0; i < 6; ++i)
+    if (!aligned(ps[i], 16)) return MF_ERR_UNSUPPORTED;
+  if (!aligned(qscale, 4) || !aligned(kv_max2, 4) || (d_pos && !aligned(d_pos, 4)))
+    return MF_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(kv_max2, 0, 8 * static_cast<size_t>(heads), s) != cudaSuccess)
+    return MF_ERR_CUDA;
+  if (T == 0) return MF_OK;
+  return cuda_status(launch_prep_e4m3(q, k, v, q8, k8, v8, qscale,
+                                      reinterpret_cast<uint32_t*>(kv_max2), d_pos,
+                                      d_pos ? pos_axes : 2, T, heads, head_dim, s));
 }
 
 mf_status mf_varlen_attn_fwd_3d(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,

@@ -73,6 +73,22 @@ bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t T, int64_t heads,
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_thd_u8(CUtensorMap* map, const void* base, int64_t T, int64_t heads,
+                      int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+  if (encode == nullptr) return false;
+  const int64_t rows = T > 0 ? T : 1;
+  cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(heads * 128)};
+  cuuint32_t box[3] = {128, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_f32_thd(CUtensorMap* map, const void* base, int64_t T, int64_t heads,
                        int64_t head_dim, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
@@ -215,22 +231,39 @@ constexpr uint32_t kFwdRegsLow = 88, kFwdRegsHigh = 208;
 static_assert(128 * kFwdRegsLow + 256 * kFwdRegsHigh <= kFwdThreads * 168,
               "forward register split exceeds the launch total");
 
-template <int D>
+// F8: the 8-bit variant (E4M3 operands and probabilities, head_dim 128).
+template <int D, bool F8>
 struct FwdCfg {
   static constexpr int BM = 128;                  // query rows per Q tile
   static constexpr int BN = 128;                  // keys per K/V tile
-  static constexpr int CHUNK = 128 * 128;         // one 64-column chunk of a 128-row tile
-  static constexpr int TILE = BM * D * 2;         // bytes of one 128 x D bf16 tile
-  static constexpr int NSLOT = D == 128 ? 4 : 8;  // K/V ring slots
+  static constexpr int EB = F8 ? 1 : 2;           // bytes per operand element
+  static constexpr int KSTEP = F8 ? 32 : 16;      // K elements per MMA (32 bytes either way)
+  static constexpr int CHUNK = 128 * 128;         // one 128-byte-wide column chunk of a 128-row tile
+  static constexpr int TILE = BM * D * EB;        // bytes of one 128 x D operand tile
+  static constexpr int NCH = TILE / CHUNK;        // TMA boxes per tile
+  static constexpr int NSLOT = F8 ? 8 : (D == 128 ? 4 : 8);  // K/V ring slots
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = 2 * TILE;
-  static constexpr int OFF_BAR = OFF_KV + NSLOT * TILE;
+  // bf16 O staging of the epilogue: the tile's own Q buffer, except in the 8-bit
+  // variant whose Q tiles are half that size (a separate 2 x BM x D x 2 bytes)
+  static constexpr int OFF_STG = OFF_KV + NSLOT * TILE;
+  static constexpr int STG = F8 ? 2 * BM * D * 2 : 0;
+  static constexpr int OFF_BAR = OFF_STG + STG;
   static constexpr int OFF_MISC = OFF_BAR + 256;
   static constexpr int SMEM = OFF_MISC + 64;
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
-  // fp16 operands throughout: S = Q'K'^T and O += P V' (V' MN-major)
+  // S = Q'K'^T and O += P V' (V' MN-major); operand format code 0 is fp16 under
+  // kind::f16 and E4M3 under kind::f8f6f4
   static constexpr uint32_t IDESC_S = idesc_f32acc(128, 128, kF16, 0, 0);
   static constexpr uint32_t IDESC_PV = idesc_f32acc(128, D, kF16, 0, 1);
+  // Online softmax in base 2: the running maximum m is raised only when a tile's
+  // maximum exceeds it by more than TAU, and P = 2^(x - m + BIAS) <= 2^(TAU + BIAS).
+  // 16-bit P: TAU 8, BIAS 0 (P <= 256).  E4M3 P: TAU 2, BIAS 6, so P <= 256 < 448
+  // still, and the binades down to 2^-12 of the row maximum keep 3 mantissa bits.
+  static constexpr float TAU = F8 ? 2.f : 8.f;
+  static constexpr float BIAS = F8 ? 6.f : 0.f;
+  static_assert(!F8 || D == 128, "the 8-bit variant holds a 128-element row in one 128-byte chunk");
+  static_assert(SMEM <= 232448, "dynamic shared memory over the 227 KB limit");
 };
 
 struct FwdParams {
@@ -240,16 +273,18 @@ struct FwdParams {
   uint32_t* status;
   __nv_bfloat16* o;
   float* lse;
+  const float* qscale;    // 8-bit variant: [T][heads] Q row scales
+  const uint32_t* amax2;  // 8-bit variant: [2][heads] squared K pair-norm / V maxima
   int32_t n, T, heads;
   float scale_log2;
 };
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, F8>;
   // All shared memory is dynamic (no static __shared__), so its base is the
   // start of the CTA's window: 1024-byte aligned, as the 128B-swizzled tiles need.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -322,8 +357,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tma_prefetch_desc(&tm_v);
         mbar_arrive_expect_tx(bar_q, (has1 ? 2 : 1) * C::TILE);
         for (int t = 0; t < (has1 ? 2 : 1); ++t)
-          for (int ch = 0; ch < D / 64; ++ch)
-            tma_load_3d(sQ + t * C::TILE + ch * C::CHUNK, &tm_q, bar_q, ch * 64, w.head,
+          for (int ch = 0; ch < C::NCH; ++ch)
+            tma_load_3d(sQ + t * C::TILE + ch * C::CHUNK, &tm_q, bar_q, ch * (128 / C::EB), w.head,
                         w.start + q0 + t * C::BM);
         int32_t issued = 0;
         bool ok = true;
@@ -336,9 +371,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               break;
             }
             mbar_arrive_expect_tx(bar_full + 8 * slot, C::TILE);
-            for (int ch = 0; ch < D / 64; ++ch)
+            for (int ch = 0; ch < C::NCH; ++ch)
               tma_load_3d(sKV + slot * C::TILE + ch * C::CHUNK, kv ? &tm_v : &tm_k,
-                          bar_full + 8 * slot, ch * 64, w.head, w.start + j * C::BN);
+                          bar_full + 8 * slot, ch * (128 / C::EB), w.head, w.start + j * C::BN);
             ++issued;
           }
         }
@@ -367,23 +402,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint64_t dkv_k = sdesc_sw128(sKV, 16, 1024);          // K-major (K tiles)
         const uint64_t dkv_m = sdesc_sw128(sKV, C::CHUNK, 1024);    // MN-major (V tiles)
         constexpr uint64_t kTile = C::TILE >> 4;
+        // K step kk starts kk * 32 bytes into the 128-byte rows (next chunk every 4)
         auto kofs = [](int kk) -> uint64_t { return ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4; };
         auto issue_s = [&](int t, int32_t j) {
           const uint64_t a0 = dq0 + t * kTile;
           const uint64_t b0 = dkv_k + ((2 * j) % C::NSLOT) * kTile;
           const uint32_t d = tmem + (t ? C::S_COL1 : C::S_COL0);
   #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(d, a0 + kofs(kk), b0 + kofs(kk), C::IDESC_S, kk > 0);
+          for (int kk = 0; kk < D / C::KSTEP; ++kk) {
+            if constexpr (F8)
+              mma_ss_f8(d, a0 + kofs(kk), b0 + kofs(kk), C::IDESC_S, kk > 0);
+            else
+              mma_ss(d, a0 + kofs(kk), b0 + kofs(kk), C::IDESC_S, kk > 0);
+          }
           mma_commit(bar_s + 8 * t);
         };
         auto issue_pv = [&](int t, int32_t j) {
           const uint64_t b0 = dkv_m + ((2 * j + 1) % C::NSLOT) * kTile;
           const uint32_t d = tmem + (t ? C::O_COL1 : C::O_COL0);
           const uint32_t a = tmem + (t ? C::S_COL1 : C::S_COL0);
+          // P step kk: 32 bytes of each TMEM lane (8 columns); V rows kk * KSTEP on
   #pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_ts(d, a + kk * 8, b0 + ((kk * 2048) >> 4), C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < C::BN / C::KSTEP; ++kk) {
+            const uint64_t b = b0 + ((kk * C::KSTEP * 128) >> 4);
+            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+            if constexpr (F8)
+              mma_ts_f8(d, a + kk * 8, b, C::IDESC_PV, acc);
+            else
+              mma_ts(d, a + kk * 8, b, C::IDESC_PV, acc);
+          }
         };
         if (ok) ok = kv_wait(0);
         if (ok) {
@@ -433,7 +480,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint32_t tS = tmem + lane_off + (t ? C::S_COL1 : C::S_COL0);
       const uint32_t tO = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
       const int32_t qrow = q0 + t * C::BM + static_cast<int32_t>(row);
-      const float sl2 = p.scale_log2;
+      // logit scale in base 2; the 8-bit variant folds in the row's Q scale and the
+      // head's K scale (kept positive, so that masked -inf columns stay -inf)
+      float sl2 = p.scale_log2;
+      if constexpr (F8) {
+        const float sk = e4m3_scale(sqrtf(__uint_as_float(p.amax2[w.head]))).s;
+        const float sq =
+            qrow < w.len ? p.qscale[(static_cast<int64_t>(w.start) + qrow) * p.heads + w.head] : 0.f;
+        sl2 = fmaxf(sl2 * sq * sk, 1e-30f);
+      }
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int32_t j = 0; j < nkv; ++j) {
@@ -474,7 +529,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (j == 0) {
           m = m_new;
         } else {
-          const bool need = m_new > m + 8.f;
+          const bool need = m_new > m + C::TAU;
           if (__any_sync(0xffffffffu, need)) {
             const float f = need ? ex2_approx(m - m_new) : 1.f;
             if (need) {
@@ -493,9 +548,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tmem_wait_st();
           }
         }
-        // P = 2^(s scale log2e - m), two columns per packed FMA; two packed sums
-        const uint64_t sl2x2 = f32x2_pack(sl2, sl2), negm2 = f32x2_pack(-m, -m);
+        // P = 2^(s scale log2e - m + BIAS), two columns per packed FMA; two packed sums
+        const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
+        const uint64_t negm2 = f32x2_pack(C::BIAS - m, C::BIAS - m);
         uint64_t sum2[2] = {f32x2_pack(0.f, 0.f), f32x2_pack(0.f, 0.f)};
+        if constexpr (F8) {
+          // E4M3 P: four columns per 32-bit TMEM column, 32 columns in all
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const int c0 = hh * 64 + 4 * u;
+              const uint64_t xa = f32x2_fma(
+                  f32x2_pack(__uint_as_float(s[c0]), __uint_as_float(s[c0 + 1])), sl2x2, negm2);
+              const uint64_t xb = f32x2_fma(
+                  f32x2_pack(__uint_as_float(s[c0 + 2]), __uint_as_float(s[c0 + 3])), sl2x2, negm2);
+              float x0, x1, x2, x3;
+              f32x2_unpack(xa, x0, x1);
+              f32x2_unpack(xb, x2, x3);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+              sum2[0] = f32x2_add(sum2[0], f32x2_pack(p0, p1));
+              sum2[1] = f32x2_add(sum2[1], f32x2_pack(p2, p3));
+              pk[u] = pack_e4m3x4(p0, p1, p2, p3);
+            }
+            tmem_st16(tS + hh * 16, pk);
+          }
+        } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
@@ -511,6 +591,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             pk[u] = pack_f16x2(p0, p1);
           }
           tmem_st16(tS + c * 16, pk);
+        }
         }
         float sa, sb, sc, sd;
         f32x2_unpack(sum2[0], sa, sb);
@@ -530,8 +611,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // done) as [128 rows][D], 16-byte units XOR-swizzled by row, then written
         // out with coalesced row stores by the warpgroup
         constexpr int UNITS = D / 8;
-        uint8_t* so = smem_raw + C::OFF_Q + t * C::TILE;
-        const float inv = 1.f / l;
+        uint8_t* so = smem_raw + (F8 ? C::OFF_STG + t * C::BM * D * 2 : C::OFF_Q + t * C::TILE);
+        // the 8-bit variant's head V scale
+        const float sv = F8 ? e4m3_scale(sqrtf(__uint_as_float(p.amax2[p.heads + w.head]))).s : 1.f;
+        const float inv = sv / l;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t r[32];
@@ -550,7 +633,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         if (qrow < w.len)
           p.lse[static_cast<int64_t>(w.head) * p.T + w.start + qrow] =
-              (m + log2f(l)) * 0.69314718055994530942f;
+              (m - C::BIAS + log2f(l)) * 0.69314718055994530942f;
         if (t) named_bar_sync(2, 128); else named_bar_sync(1, 128);
         const int32_t r0 = q0 + t * C::BM;  // first query row of the tile (in sample)
         const int32_t nrows = min(C::BM, w.len - r0);
@@ -574,21 +657,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool F8>
 static cudaError_t launch_fwd_d(const AttnFwdArgs& a, cudaStream_t s) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, F8>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_thd(&tq, a.q, a.T, a.heads, D, 128, true) ||
-      !make_tmap_thd(&tk, a.k, a.T, a.heads, D, 128, true) ||
-      !make_tmap_thd(&tv, a.v, a.T, a.heads, D, 128, true))
+  if (F8) {
+    if (!make_tmap_thd_u8(&tq, a.q, a.T, a.heads, 128) ||
+        !make_tmap_thd_u8(&tk, a.k, a.T, a.heads, 128) ||
+        !make_tmap_thd_u8(&tv, a.v, a.T, a.heads, 128))
+      return cudaErrorInvalidValue;
+  } else if (!make_tmap_thd(&tq, a.q, a.T, a.heads, D, 128, true) ||
+             !make_tmap_thd(&tk, a.k, a.T, a.heads, D, 128, true) ||
+             !make_tmap_thd(&tv, a.v, a.T, a.heads, D, 128, true)) {
     return cudaErrorInvalidValue;
+  }
   FwdParams p;
   p.cu = a.cu;
   p.order = a.order;
@@ -596,6 +685,8 @@ static cudaError_t launch_fwd_d(const AttnFwdArgs& a, cudaStream_t s) {
   p.status = a.status;
   p.o = reinterpret_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
+  p.qscale = a.qscale;
+  p.amax2 = a.amax2;
   p.n = a.n;
   p.T = a.T;
   p.heads = a.heads;
@@ -603,14 +694,16 @@ static cudaError_t launch_fwd_d(const AttnFwdArgs& a, cudaStream_t s) {
   const int64_t blocks = (static_cast<int64_t>(a.T + 2 * C::BM - 1) / (2 * C::BM) + a.n) * a.heads;
   if (blocks <= 0) return cudaSuccess;
   {
-    KernelTimer kt(MF_K_ATTN_FWD, s);
-    attn_fwd_kernel<D><<<static_cast<unsigned>(blocks), kFwdThreads, C::SMEM, s>>>(tq, tk, tv, p);
+    KernelTimer kt(F8 ? MF_K_ATTN_FWD_F8 : MF_K_ATTN_FWD, s);
+    attn_fwd_kernel<D, F8>
+        <<<static_cast<unsigned>(blocks), kFwdThreads, C::SMEM, s>>>(tq, tk, tv, p);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_attn_fwd(const AttnFwdArgs& a, cudaStream_t s) {
-  return a.head_dim == 128 ? launch_fwd_d<128>(a, s) : launch_fwd_d<64>(a, s);
+  if (a.f8) return a.head_dim == 128 ? launch_fwd_d<128, true>(a, s) : cudaErrorInvalidValue;
+  return a.head_dim == 128 ? launch_fwd_d<128, false>(a, s) : launch_fwd_d<64, false>(a, s);
 }
 
 }  // namespace mf

@@ -73,11 +73,30 @@ __device__ __forceinline__ void rope_sincos_fast(float p, float w_hi, float w_lo
   *c = cc;
 }
 
+// Scale of an E4M3 block whose largest magnitude is A: the smallest power of two s
+// with A / s <= 448.  With A = m 2^p, m in [1, 2): s = 2^(p - 8) when m <= 1.75
+// (then A / s = 256 m <= 448), else 2^(p - 7).  Worked on the bits, so s and 1 / s
+// are exact and x / s = x * (1 / s) rounds nowhere; s is clamped to the normal
+// range (A below 2^-118 gets 2^-126).  A = 0 gives s = 1 / s = 0.
+struct E4m3Scale {
+  float s, inv;
+};
+__device__ __forceinline__ E4m3Scale e4m3_scale(float A) {
+  if (!(A > 0.f)) return {0.f, 0.f};
+  const uint32_t b = __float_as_uint(A);
+  int e = static_cast<int>(b >> 23) - 127 - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  e = e < -126 ? -126 : (e > 126 ? 126 : e);
+  return {__uint_as_float(static_cast<uint32_t>(127 + e) << 23),
+          __uint_as_float(static_cast<uint32_t>(127 - e) << 23)};
+}
+
 // --------------------------------------------------------- workspace layout
 // [0, 256)            device status word (uint32, flags kFlag*)
 // [256, +sched)       schedule: int32 order[n], int32 prefix[n+1]
 // then 1024-aligned:  q16, k16  fp16 [T][h][d]  (rotated Q', K')
 // fwd only:           v16 fp16 [T][h][d]
+// e4m3 fwd (inside the same total): q8, k8, v8 E4M3 [T][h][d] from q16's offset,
+//                     qscale fp32 [T][h], amax2 uint32 [2][h]
 // bwd only:           hmax fp32 [2][h] (per-head max ||dO_j||, max ||v_k||),
 //                     pad fp32 [128] (64 x -inf, 64 x 0: -LSE log2 e / D of rows
 //                     past a sample), nlse2 fp32 [h][T] (-LSE * log2 e), delta fp32 [h][T],
@@ -86,6 +105,7 @@ struct WsLayout {
   size_t status = 0;
   size_t order = 0, prefix = 0;
   size_t q16 = 0, k16 = 0, v16 = 0;
+  size_t q8 = 0, k8 = 0, v8 = 0, qscale = 0, amax2 = 0;
   size_t hmax = 0, pad = 0, nlse2 = 0, delta = 0, dq_acc = 0;
   size_t total = 0;
 };
@@ -110,6 +130,15 @@ cudaError_t launch_prep_f16(const uint16_t* q, const uint16_t* k, const uint16_t
                             uint16_t* q_out, uint16_t* k_out, uint16_t* v_out,
                             const int32_t* d_pos, int32_t naxes, int32_t T, int32_t heads,
                             int32_t head_dim, uint32_t* status, cudaStream_t s);
+// bf16 in, E4M3 out: the 8-bit forward's operands (head_dim 128 only).  Q' = R q
+// scaled per (token, head) row to a largest magnitude of 448 (the scale, largest
+// |q'| / 448, in qscale [T][heads]); K' = R k and V scaled per head from the maxima
+// that the first pass gathers in amax2 [2][heads] (squared largest pair norm of k,
+// squared largest |v|; zero on entry).
+cudaError_t launch_prep_e4m3(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                             uint8_t* q8, uint8_t* k8, uint8_t* v8, float* qscale,
+                             uint32_t* amax2, const int32_t* d_pos, int32_t naxes, int32_t T,
+                             int32_t heads, int32_t head_dim, cudaStream_t s);
 // Builds the longest-first work list (items of `blk` rows per sample and head)
 // and validates cu_seqlens; zeroes the status word first, and `nzero` floats at
 // `zero` (may be null).
@@ -118,9 +147,12 @@ cudaError_t launch_schedule(const int32_t* d_cu, int32_t n, int32_t T, int32_t m
                             int32_t* prefix, float* zero, int32_t nzero, cudaStream_t s);
 
 struct AttnFwdArgs {
-  const uint16_t* q;  // fp16 Q' (rotated)
-  const uint16_t* k;  // fp16 K' (rotated)
-  const uint16_t* v;  // fp16 V'
+  const uint16_t* q;  // fp16 Q' (rotated); E4M3 bytes when f8
+  const uint16_t* k;  // fp16 K' (rotated); E4M3 bytes when f8
+  const uint16_t* v;  // fp16 V'; E4M3 bytes when f8
+  bool f8 = false;    // the 8-bit variant (head_dim 128)
+  const float* qscale = nullptr;     // f8: [T][heads] Q row scales
+  const uint32_t* amax2 = nullptr;   // f8: [2][heads] squared K pair-norm and V maxima
   const int32_t* cu;
   const int32_t* order;
   const int32_t* prefix;
@@ -187,6 +219,9 @@ class KernelTimer {
 // Element type bf16, or fp16 when `f16` (same size and layout).
 bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t T, int64_t heads,
                    int64_t head_dim, int box_rows, bool f16 = false);
+// One-byte elements [T][heads][128] with a {128, 1, box_rows} box, 128-byte swizzle.
+bool make_tmap_thd_u8(CUtensorMap* map, const void* base, int64_t T, int64_t heads,
+                      int box_rows);
 // fp32 [T][heads][head_dim] map with a {head_dim, 1, box_rows} box, no swizzle
 // (the target of tiled reduce-adds).
 bool make_tmap_f32_thd(CUtensorMap* map, const void* base, int64_t T, int64_t heads,

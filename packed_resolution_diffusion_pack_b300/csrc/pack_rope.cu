@@ -9,6 +9,7 @@
 // column; pair (2j, 2j+1) of a half by p * 10000^(-2j/(d/2)).
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
@@ -266,6 +267,186 @@ __global__ void __launch_bounds__(256) rope_kernel(const uint4* __restrict__ q,
     dst[idx] = make_uint4(w[0], w[1], w[2], w[3]);
   }
   if (F16_OUT && !(vmax <= 65504.f)) atomicOr(status, kFlagFp16Range);
+}
+
+// ---------------------------------------------------- e4m3 operands
+// Operands of the 8-bit forward variant, in two passes over bf16 q, k, v.
+//
+// Pass 1 (f8_amax_kernel): per-head maxima for the K and V scales.
+//   amax2[h]         = max over the head's tokens and rotary pairs of
+//                      k_2P^2 + k_2P+1^2, the squared norm of the un-rotated pair.
+//                      A rotation keeps a pair's norm, so its root bounds every
+//                      rotated component at every position.
+//   amax2[heads + h] = max v^2.
+// The values are non-negative floats, whose bit patterns order like unsigned
+// integers, so atomicMax on the bits takes the maximum; amax2 is zero on entry.
+// Chunks of 8 elements are read 16 bytes at a time, a warp's 32 lanes covering two
+// rows; each half-warp reduces its row with shuffles, then one lane per row merges
+// it into the block's per-head maxima in shared memory, flushed to amax2 at the end.
+template <int D>
+__global__ void __launch_bounds__(256) f8_amax_kernel(const uint4* __restrict__ k,
+                                                      const uint4* __restrict__ v, int64_t rows,
+                                                      int32_t heads, bool smem_heads,
+                                                      uint32_t* __restrict__ amax2) {
+  extern __shared__ uint32_t s_max[];  // [2][heads] when smem_heads
+  constexpr int CPR = D / 8;           // 16-byte chunks per row
+  static_assert(CPR == 16, "a half-warp covers one row");
+  if (smem_heads)
+    for (int i = threadIdx.x; i < 2 * heads; i += blockDim.x) s_max[i] = 0u;
+  __syncthreads();
+  uint32_t* tgt = smem_heads ? s_max : amax2;
+  const int lane = threadIdx.x & 31;
+  const int64_t total = 2 * rows * CPR;  // K chunks, then V chunks
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t base = (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32;
+       base < total; base += warps * 32) {
+    const int64_t c = base + lane;
+    float mx = 0.f;
+    const bool valid = c < total;
+    const bool is_v = valid && c >= rows * CPR;
+    if (valid) {
+      const uint4 x = is_v ? v[c - rows * CPR] : k[c];
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float a = __uint_as_float(w[u] << 16);
+        const float b = __uint_as_float(w[u] & 0xFFFF0000u);
+        mx = is_v ? fmaxf(mx, fmaxf(a * a, b * b)) : fmaxf(mx, fmaf(a, a, b * b));
+      }
+    }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (valid && (lane & 15) == 0) {
+      const int64_t row = (is_v ? c - rows * CPR : c) / CPR;
+      const int h = static_cast<int>(row % heads);
+      atomicMax(tgt + (is_v ? heads : 0) + h, __float_as_uint(mx));
+    }
+  }
+  if (smem_heads) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < 2 * heads; i += blockDim.x)
+      if (s_max[i] != 0u) atomicMax(amax2 + i, s_max[i]);
+  }
+}
+
+// Pass 2 (f8_quant_kernel): one block per kRopeTok tokens, all heads; rows
+// (token, head) of Q, then K, then V; a half-warp owns a row, lane l of it the
+// elements [8l, 8l + 8) = rotary pairs [4l, 4l + 4).  Each block's scale s is the
+// power of two of e4m3_scale, so x / s is exact:
+//   Q: rotated; s from the row's largest |q'|, written to qscale[token][head];
+//   K: rotated; s from sqrt(amax2[h]), the head's largest pair norm;
+//   V: s from sqrt(amax2[heads + h]), the head's largest |v|;
+// each x / s rounded to E4M3 (nearest even, saturating) into [T][heads][D] bytes.
+template <int D>
+__global__ void __launch_bounds__(256) f8_quant_kernel(const uint4* __restrict__ q,
+                                                       const uint4* __restrict__ k,
+                                                       const uint4* __restrict__ v,
+                                                       uint2* __restrict__ q8,
+                                                       uint2* __restrict__ k8,
+                                                       uint2* __restrict__ v8,
+                                                       float* __restrict__ qscale,
+                                                       const uint32_t* __restrict__ amax2,
+                                                       const int32_t* __restrict__ pos, int32_t T,
+                                                       int32_t heads,
+                                                       const __grid_constant__ RopeFreqs f) {
+  constexpr int NP = D / 2;
+  constexpr int CPR = D / 8;
+  static_assert(CPR == 16, "a half-warp covers one row");
+  __shared__ float2 cs[kRopeTok][NP];
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRopeTok;
+  for (int i = threadIdx.x; i < kRopeTok * NP; i += blockDim.x) {
+    const int tt = i / NP, P = i % NP;
+    float c = 1.f, s = 0.f;
+    if (t0 + tt < T && pos != nullptr) {
+      const float pp = static_cast<float>(pos[(t0 + tt) * f.naxes + f.axis[P]]);
+      rope_sincos(pp, f.omega[P], f.omega_lo[P], 1.f, &s, &c);
+    }
+    cs[tt][P] = make_float2(c, s);
+  }
+  __syncthreads();
+  const int ntok = static_cast<int>(T - t0 < kRopeTok ? T - t0 : kRopeTok);
+  const int per = ntok * heads;  // rows of one operand in this block
+  const int nrows = 3 * per;
+  const int lane = threadIdx.x & 31, l16 = lane & 15;
+  const int nwarps = blockDim.x >> 5;
+  for (int base = (threadIdx.x >> 5) * 2; base < nrows; base += nwarps * 2) {
+    const int row = base + (lane >> 4);
+    const bool valid = row < nrows;
+    int which = 0, tt = 0, hh = 0;
+    float y[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) y[u] = 0.f;
+    int64_t idx = 0;
+    if (valid) {
+      which = row / per;
+      const int rem = row - which * per;
+      tt = rem / heads;
+      hh = rem - tt * heads;
+      idx = ((t0 + tt) * heads + hh) * CPR + l16;
+      const uint4 x = (which == 0 ? q : which == 1 ? k : v)[idx];
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float a = __uint_as_float(w[u] << 16);
+        const float b = __uint_as_float(w[u] & 0xFFFF0000u);
+        if (which < 2) {
+          const float2 r = cs[tt][l16 * 4 + u];
+          y[2 * u] = fmaf(a, r.x, -b * r.y);
+          y[2 * u + 1] = fmaf(a, r.y, b * r.x);
+        } else {
+          y[2 * u] = a;
+          y[2 * u + 1] = b;
+        }
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) amax = fmaxf(amax, fabsf(y[u]));
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (valid) {
+      float ref = amax;
+      if (which > 0) ref = sqrtf(__uint_as_float(amax2[(which - 1) * heads + hh]));
+      const E4m3Scale sc = e4m3_scale(ref);
+      const float inv = sc.inv;
+      if (which == 0 && l16 == 0) qscale[(t0 + tt) * heads + hh] = sc.s;
+      uint2* dst = which == 0 ? q8 : which == 1 ? k8 : v8;
+      dst[idx] = make_uint2(pack_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv),
+                            pack_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv));
+    }
+  }
+}
+
+cudaError_t launch_prep_e4m3(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                             uint8_t* q8, uint8_t* k8, uint8_t* v8, float* qscale,
+                             uint32_t* amax2, const int32_t* d_pos, int32_t naxes, int32_t T,
+                             int32_t heads, int32_t head_dim, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (head_dim != 128) return cudaErrorInvalidValue;
+  const int64_t rows = static_cast<int64_t>(T) * heads;
+  const int64_t chunks = 2 * rows * 16;
+  const int amax_blocks = static_cast<int>(std::min<int64_t>((chunks + 255) / 256, 148 * 8));
+  const bool smem_heads = heads <= 4096;
+  {
+    KernelTimer kt(MF_K_F8_AMAX, s);
+    f8_amax_kernel<128><<<amax_blocks, 256, smem_heads ? 8 * heads : 0, s>>>(
+        reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), rows, heads,
+        smem_heads, amax2);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const RopeFreqs f = make_rope_freqs(head_dim, naxes);
+  const int blocks = (T + kRopeTok - 1) / kRopeTok;
+  {
+    KernelTimer kt(MF_K_F8_QUANT, s);
+    f8_quant_kernel<128><<<blocks, 256, 0, s>>>(
+        reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k),
+        reinterpret_cast<const uint4*>(v), reinterpret_cast<uint2*>(q8),
+        reinterpret_cast<uint2*>(k8), reinterpret_cast<uint2*>(v8), qscale, amax2, d_pos, T,
+        heads, f);
+  }
+  return cudaGetLastError();
 }
 
 template <bool F16_OUT>

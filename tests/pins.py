@@ -551,11 +551,12 @@ def _e4m3_inputs(seed, specs, h, d, scales=None):
 
 
 def pin_quant_e4m3(so=None):
-    """Quantised operands: every value is an e4m3 value; the largest magnitude of a
-    Q row and of a head's V is exactly 448; every rotated K component stays within
-    448 at every position; dequantised values are within half an e4m3 quantum of
-    the exact rotated operands (2^-4 relative in the normal range, 2^-10 of the
-    scale below it)."""
+    """Quantised operands: every scale is a power of two, the smallest that brings
+    the block's largest magnitude to at most 448 (so that largest magnitude lands in
+    (224, 448]); every value is an e4m3 value; every rotated K component stays
+    within 448 at every position; dequantised values are within half an e4m3
+    quantum of the exact rotated operands (2^-4 relative in the normal range, 2^-10
+    of the scale below it)."""
     rng = _rng(41)
     specs = [(7, 9, 13), (3, 16, 4), (0, 5, 31)]
     scales = [rng.uniform(0.5, 2, 3) for _ in range(3)]
@@ -564,16 +565,16 @@ def pin_quant_e4m3(so=None):
     qr, kr = oracle.rope2d(q, pos), oracle.rope2d(k, pos)
     for a in (qh, kh, vh):
         assert np.array_equal(oracle.e4m3(a), a)
-    assert np.all(np.abs(qh).max(axis=2) == 448.0)
-    assert np.all(np.abs(vh).max(axis=(0, 2)) == 448.0)
+    for s_, amax in ((sq, np.abs(qr).max(axis=2)), (sv, np.abs(v).max(axis=(0, 2))),
+                     (sk, np.sqrt(k[..., 0::2] ** 2 + k[..., 1::2] ** 2).max(axis=(0, 2)))):
+        assert np.all(np.exp2(np.round(np.log2(s_))) == s_)
+        assert np.all((amax / s_ > 224.0) & (amax / s_ <= 448.0))
+    assert np.all(np.abs(qh).max(axis=2) >= 224.0) and np.all(np.abs(vh).max(axis=(0, 2)) >= 224.0)
     assert np.abs(kh).max() <= 448.0
     for hat, s, ref in ((qh, sq[:, :, None], qr), (kh, sk[None, :, None], kr),
                         (vh, sv[None, :, None], v)):
         err = np.abs(hat * s - ref)
         assert np.all(err <= 2.0 ** -4 * np.abs(ref) + 2.0 ** -10 * s + 1e-15)
-    # K's scale is tight: the largest pair norm is reached by a rotated component
-    # at some angle, so no smaller scale bounds all positions
-    assert np.all(sk * 448.0 <= np.sqrt(2.0) * np.abs(k).max(axis=(0, 2)) + 1e-12)
     assert np.all(sk * 448.0 >= np.abs(kr).max(axis=(0, 2)) - 1e-12)
 
 

@@ -141,3 +141,29 @@ def test_pack3d_size_host():
     assert lib.mf_varlen_attn_fwd_3d(p(1 << 20), p(1 << 21), p(1 << 22), p(1 << 23), None, 1, 8, 8,
                                      1, 64, 0.0, p(1 << 24), p(1 << 25), p(1 << 26), 1 << 20,
                                      None) == 1  # 3D positions are required
+
+
+def test_fp8_argument_errors_on_host():
+    """The 8-bit forward and its quantisation: head_dim 64, a bad pos_axes, null or
+    misaligned buffers are rejected before any launch."""
+    lib = mf.load()
+    p = ctypes.c_void_p
+    base = 1 << 20
+    q, k, v, o, lse = (p(base + i * 4096) for i in range(5))
+    cu, pos, ws = p(base + 40960), p(base + 45056), p(base + 65536)
+    big = 1 << 40
+    assert lib.mf_varlen_attn_fwd_fp8(q, k, v, cu, pos, 2, 1, 10, 10, 2, 64, 0.0, o, lse, ws, big,
+                                      None) == 2
+    assert lib.mf_varlen_attn_fwd_fp8(q, k, v, cu, pos, 4, 1, 10, 10, 2, 128, 0.0, o, lse, ws, big,
+                                      None) == 1
+    assert lib.mf_varlen_attn_fwd_fp8(q, None, v, cu, pos, 2, 1, 10, 10, 2, 128, 0.0, o, lse, ws,
+                                      big, None) == 1
+    assert lib.mf_varlen_attn_fwd_fp8(q, k, v, cu, pos, 2, 1, 10, 10, 2, 128, 0.0, o, lse, ws, 16,
+                                      None) == 1  # workspace too small
+    q8, k8, v8, qs, kv = (p(base + 8192 * (i + 1)) for i in range(5))
+    assert lib.mf_quant_e4m3(q, k, v, pos, 2, 10, 2, 64, q8, k8, v8, qs, kv, None) == 2
+    assert lib.mf_quant_e4m3(q, k, v, pos, 5, 10, 2, 128, q8, k8, v8, qs, kv, None) == 1
+    assert lib.mf_quant_e4m3(q, k, v, pos, 2, 10, 2, 128, None, k8, v8, qs, kv, None) == 1
+    assert lib.mf_quant_e4m3(q, k, v, pos, 2, 10, 2, 128, p(base + 8200), k8, v8, qs, kv,
+                             None) == 2
+    assert lib.mf_quant_e4m3(q, k, v, pos, 2, -1, 2, 128, q8, k8, v8, qs, kv, None) == 1

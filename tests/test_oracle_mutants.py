@@ -59,6 +59,9 @@ MUTANTS = [
     ("e4m3_truncates", "nearbyint(a / quantum) * quantum", "floor(a / quantum) * quantum"),
     ("e4m3_no_subnormal_floor", "if (e < -6) e = -6;", "if (e < -9) e = -9;"),
     ("e4m3_two_mantissa_bits", "ldexp(1.0, e - 3)", "ldexp(1.0, e - 2)"),
+    ("e4m3_scale_threshold", "(2.0 * f > 1.75 ? 1 : 0)", "(2.0 * f > 1.5 ? 1 : 0)"),
+    ("e4m3_scale_not_power_of_two", "  if (!(A > 0.0)) return 0.0;\n  int ex;",
+     "  if (!(A > 0.0)) return 0.0;\n  if (A > 0.0) return A / 448.0;\n  int ex;"),
     ("quant_k_scale_from_max_abs", "const double nrm = sqrt(kk[e] * kk[e] + kk[e + 1] * kk[e + 1]);",
      "const double nrm = fabs(kk[e]) > fabs(kk[e + 1]) ? fabs(kk[e]) : fabs(kk[e + 1]);"),
     ("quant_q_scale_per_head", "if (fabs(qr[row + e]) > qmax) qmax = fabs(qr[row + e]);",
