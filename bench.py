@@ -424,6 +424,9 @@ def gpu_arm(args):
     }
     if not args.no_extras:
         line["extras"] = neighbours(mf, wl, pk["hbm_gbs"])
+        if d == 128:
+            line["extras"]["fp8_forward"] = fp8_forward(mf, wl, qd, kd, vd, cu, pos, max_len, ws,
+                                                        peak_tc, pk["hbm_gbs"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, q, k, v, do, args.cpu_budget_s)
     if rank == 0:
@@ -479,6 +482,53 @@ def neighbours(mf, wl, hbm_gbs, reps=20):
         out[name] = {"ms": ms, "achieved_gbs": gbs, "frac_of_hbm": gbs / hbm_gbs, "shape": shape,
                      "bytes": nbytes}
     return out
+
+
+def fp8_forward(mf, wl, qd, kd, vd, cu, pos, max_len, ws, peak_bf16, hbm_gbs, reps=10):
+    """The 8-bit (E4M3) variant of the forward on the same pack, outside the timed
+    step: the whole call (schedule, the two quantisation passes, attention) timed
+    with CUDA events, and each kernel's device time.  The tensor-core peak for E4M3
+    operands is twice the measured bf16 one (the nominal dense ratio, 4.5 vs
+    2.25 PFLOP/s).  Algorithmic bytes: the maxima pass reads k and v (4 T h d); the
+    quantiser reads q, k, v (6 T h d) and writes the E4M3 copies (3 T h d) and
+    the Q row scales (4 T h)."""
+    import torch
+    T, h, d = wl.total, wl.heads, wl.head_dim
+    o = torch.empty_like(qd)
+    lse = torch.empty((h, T), dtype=torch.float32, device="cuda")
+    call = lambda: mf.varlen_attn_fwd_fp8(qd, kd, vd, cu, pos, max_len, o=o, lse=lse, ws=ws)  # noqa: E731
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    mf.timing_enable(True)
+    mf.timing_reset()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(reps):
+        call()
+    ev1.record()
+    torch.cuda.synchronize()
+    kern = mf.timing_read()
+    mf.timing_enable(False)
+    mf.get_status(ws)
+    ms = ev0.elapsed_time(ev1) / reps
+    flops = wl.flops_fwd()
+    peak8 = 2.0 * peak_bf16
+    elems = float(T * h * d)
+    per = lambda name: kern[name][0] / max(1, kern[name][1])  # noqa: E731
+    attn_ms = per("attn_fwd_f8")
+    amax_bytes, quant_bytes = 4.0 * elems, 9.0 * elems + 4.0 * T * h
+    return {
+        "ms_per_call": ms, "tflops_per_call": flops / (ms / 1e3) / 1e12,
+        "attn_ms": attn_ms, "attn_tflops": flops / (attn_ms / 1e3) / 1e12,
+        "attn_frac_of_e4m3_peak": flops / (attn_ms / 1e3) / 1e12 / peak8,
+        "e4m3_peak_tflops": peak8,
+        "amax_ms": per("f8_amax"),
+        "amax_frac_of_hbm": amax_bytes / (per("f8_amax") / 1e3) / 1e9 / hbm_gbs,
+        "quant_ms": per("f8_quant"),
+        "quant_frac_of_hbm": quant_bytes / (per("f8_quant") / 1e3) / 1e9 / hbm_gbs,
+        "call": "mf_varlen_attn_fwd_fp8 (E4M3 operands and probabilities, fp32 accumulation)",
+    }
 
 
 def _recorded_traffic(kernel):

@@ -555,11 +555,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if constexpr (F8) {
           // E4M3 P: four columns per 32-bit TMEM column, 32 columns in all
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t pk[16];
+          for (int hh = 0; hh < 4; ++hh) {
+            uint32_t pk[8];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const int c0 = hh * 64 + 4 * u;
+            for (int u = 0; u < 8; ++u) {
+              const int c0 = hh * 32 + 4 * u;
               const uint64_t xa = f32x2_fma(
                   f32x2_pack(__uint_as_float(s[c0]), __uint_as_float(s[c0 + 1])), sl2x2, negm2);
               const uint64_t xb = f32x2_fma(
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               sum2[1] = f32x2_add(sum2[1], f32x2_pack(p2, p3));
               pk[u] = pack_e4m3x4(p0, p1, p2, p3);
             }
-            tmem_st16(tS + hh * 16, pk);
+            tmem_st8(tS + hh * 8, pk);
           }
         } else {
 #pragma unroll

@@ -270,8 +270,14 @@ __global__ void __launch_bounds__(256) rope_kernel(const uint4* __restrict__ q,
 }
 
 // ---------------------------------------------------- e4m3 operands
-// Operands of the 8-bit forward variant, in two passes over bf16 q, k, v.
-//
+// Operands of the 8-bit forward variant, in two passes over bf16 q, k, v.  In both
+// passes a warp works on one token at a time: a half-warp covers one row (token,
+// head) of D = 128 with 16-byte chunks of 8 elements (lane l of the half: elements
+// [8l, 8l + 8) = rotary pairs [4l, 4l + 4)), and a warp keeps kF8Unroll pairs of
+// rows (consecutive heads) in flight, every load issued before any is used.
+constexpr int kF8Unroll = 4;
+constexpr int kF8Warps = 8;  // warps per block (256 threads)
+
 // Pass 1 (f8_amax_kernel): per-head maxima for the K and V scales.
 //   amax2[h]         = max over the head's tokens and rotary pairs of
 //                      k_2P^2 + k_2P+1^2, the squared norm of the un-rotated pair.
@@ -280,12 +286,12 @@ __global__ void __launch_bounds__(256) rope_kernel(const uint4* __restrict__ q,
 //   amax2[heads + h] = max v^2.
 // The values are non-negative floats, whose bit patterns order like unsigned
 // integers, so atomicMax on the bits takes the maximum; amax2 is zero on entry.
-// Chunks of 8 elements are read 16 bytes at a time, a warp's 32 lanes covering two
-// rows; each half-warp reduces its row with shuffles, then one lane per row merges
-// it into the block's per-head maxima in shared memory, flushed to amax2 at the end.
+// Each half-warp reduces its row with shuffles, then one lane per row merges it
+// into the block's per-head maxima in shared memory, flushed to amax2 at the end.
+// Warps stride over tokens (one wave of resident blocks).
 template <int D>
 __global__ void __launch_bounds__(256) f8_amax_kernel(const uint4* __restrict__ k,
-                                                      const uint4* __restrict__ v, int64_t rows,
+                                                      const uint4* __restrict__ v, int32_t T,
                                                       int32_t heads, bool smem_heads,
                                                       uint32_t* __restrict__ amax2) {
   extern __shared__ uint32_t s_max[];  // [2][heads] when smem_heads
@@ -295,31 +301,36 @@ __global__ void __launch_bounds__(256) f8_amax_kernel(const uint4* __restrict__ 
     for (int i = threadIdx.x; i < 2 * heads; i += blockDim.x) s_max[i] = 0u;
   __syncthreads();
   uint32_t* tgt = smem_heads ? s_max : amax2;
-  const int lane = threadIdx.x & 31;
-  const int64_t total = 2 * rows * CPR;  // K chunks, then V chunks
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t base = (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 32;
-       base < total; base += warps * 32) {
-    const int64_t c = base + lane;
-    float mx = 0.f;
-    const bool valid = c < total;
-    const bool is_v = valid && c >= rows * CPR;
-    if (valid) {
-      const uint4 x = is_v ? v[c - rows * CPR] : k[c];
-      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  const int lane = threadIdx.x & 31, hl = lane >> 4, l16 = lane & 15;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kF8Warps;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kF8Warps + (threadIdx.x >> 5); t < T;
+       t += nw) {
+    const uint4* kt = k + t * heads * CPR + l16;
+    const uint4* vt = v + t * heads * CPR + l16;
+    for (int hb = 0; hb < heads; hb += 2 * kF8Unroll) {
+      uint4 x[2 * kF8Unroll];  // K rows, then V rows of the same heads
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float a = __uint_as_float(w[u] << 16);
-        const float b = __uint_as_float(w[u] & 0xFFFF0000u);
-        mx = is_v ? fmaxf(mx, fmaxf(a * a, b * b)) : fmaxf(mx, fmaf(a, a, b * b));
+      for (int u = 0; u < 2 * kF8Unroll; ++u) {
+        const int h = hb + 2 * (u % kF8Unroll) + hl;
+        x[u] = h < heads ? (u < kF8Unroll ? kt : vt)[h * CPR] : make_uint4(0u, 0u, 0u, 0u);
       }
-    }
 #pragma unroll
-    for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (valid && (lane & 15) == 0) {
-      const int64_t row = (is_v ? c - rows * CPR : c) / CPR;
-      const int h = static_cast<int>(row % heads);
-      atomicMax(tgt + (is_v ? heads : 0) + h, __float_as_uint(mx));
+      for (int u = 0; u < 2 * kF8Unroll; ++u) {
+        const bool is_v = u >= kF8Unroll;
+        const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+        float mx = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = __uint_as_float(w[e] << 16);
+          const float b = __uint_as_float(w[e] & 0xFFFF0000u);
+          mx = is_v ? fmaxf(mx, fmaxf(a * a, b * b)) : fmaxf(mx, fmaf(a, a, b * b));
+        }
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1)
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const int h = hb + 2 * (u % kF8Unroll) + hl;
+        if (h < heads && l16 == 0) atomicMax(tgt + (is_v ? heads : 0) + h, __float_as_uint(mx));
+      }
     }
   }
   if (smem_heads) {
@@ -329,14 +340,14 @@ __global__ void __launch_bounds__(256) f8_amax_kernel(const uint4* __restrict__ 
   }
 }
 
-// Pass 2 (f8_quant_kernel): one block per kRopeTok tokens, all heads; rows
-// (token, head) of Q, then K, then V; a half-warp owns a row, lane l of it the
-// elements [8l, 8l + 8) = rotary pairs [4l, 4l + 4).  Each block's scale s is the
-// power of two of e4m3_scale, so x / s is exact:
+// Pass 2 (f8_quant_kernel): one warp per token, all heads of Q, then K, then V.
+// Each block's scale s is the power of two of e4m3_scale, so x / s is exact:
 //   Q: rotated; s from the row's largest |q'|, written to qscale[token][head];
 //   K: rotated; s from sqrt(amax2[h]), the head's largest pair norm;
 //   V: s from sqrt(amax2[heads + h]), the head's largest |v|;
 // each x / s rounded to E4M3 (nearest even, saturating) into [T][heads][D] bytes.
+// The warp's first loads are issued before it builds its token's (cos, sin)
+// table, and each later round while the previous one is converted.
 template <int D>
 __global__ void __launch_bounds__(256) f8_quant_kernel(const uint4* __restrict__ q,
                                                        const uint4* __restrict__ k,
@@ -351,70 +362,83 @@ __global__ void __launch_bounds__(256) f8_quant_kernel(const uint4* __restrict__
                                                        const __grid_constant__ RopeFreqs f) {
   constexpr int NP = D / 2;
   constexpr int CPR = D / 8;
-  static_assert(CPR == 16, "a half-warp covers one row");
-  __shared__ float2 cs[kRopeTok][NP];
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRopeTok;
-  for (int i = threadIdx.x; i < kRopeTok * NP; i += blockDim.x) {
-    const int tt = i / NP, P = i % NP;
+  static_assert(CPR == 16 && NP == 64, "a half-warp covers one row");
+  __shared__ float2 cs_all[kF8Warps][NP];
+  const int wid = threadIdx.x >> 5;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kF8Warps + wid;
+  if (t >= T) return;  // warp-uniform; no block-wide barrier follows
+  float2* cs = cs_all[wid];
+  const int lane = threadIdx.x & 31, hl = lane >> 4, l16 = lane & 15;
+  const int nh = (heads + 2 * kF8Unroll - 1) / (2 * kF8Unroll);  // rounds per operand
+  const int nit = 3 * nh;
+  const int64_t row0 = t * heads;
+  auto load_round = [&](int it, uint4 (&x)[kF8Unroll]) {
+    const int which = it / nh;
+    const int hb = (it - which * nh) * 2 * kF8Unroll;
+    const uint4* src = which == 0 ? q : which == 1 ? k : v;
+#pragma unroll
+    for (int u = 0; u < kF8Unroll; ++u) {
+      const int h = hb + 2 * u + hl;
+      x[u] = (it < nit && h < heads) ? src[(row0 + h) * CPR + l16] : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  uint4 x[kF8Unroll];
+  load_round(0, x);
+  for (int P = lane; P < NP; P += 32) {
     float c = 1.f, s = 0.f;
-    if (t0 + tt < T && pos != nullptr) {
-      const float pp = static_cast<float>(pos[(t0 + tt) * f.naxes + f.axis[P]]);
+    if (pos != nullptr) {
+      const float pp = static_cast<float>(pos[t * f.naxes + f.axis[P]]);
       rope_sincos(pp, f.omega[P], f.omega_lo[P], 1.f, &s, &c);
     }
-    cs[tt][P] = make_float2(c, s);
+    cs[P] = make_float2(c, s);
   }
-  __syncthreads();
-  const int ntok = static_cast<int>(T - t0 < kRopeTok ? T - t0 : kRopeTok);
-  const int per = ntok * heads;  // rows of one operand in this block
-  const int nrows = 3 * per;
-  const int lane = threadIdx.x & 31, l16 = lane & 15;
-  const int nwarps = blockDim.x >> 5;
-  for (int base = (threadIdx.x >> 5) * 2; base < nrows; base += nwarps * 2) {
-    const int row = base + (lane >> 4);
-    const bool valid = row < nrows;
-    int which = 0, tt = 0, hh = 0;
-    float y[8];
+  __syncwarp();
+  for (int it = 0; it < nit; ++it) {
+    uint4 xn[kF8Unroll];
+    load_round(it + 1, xn);
+    const int which = it / nh;
+    const int hb = (it - which * nh) * 2 * kF8Unroll;
+    uint2* dst = which == 0 ? q8 : which == 1 ? k8 : v8;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) y[u] = 0.f;
-    int64_t idx = 0;
-    if (valid) {
-      which = row / per;
-      const int rem = row - which * per;
-      tt = rem / heads;
-      hh = rem - tt * heads;
-      idx = ((t0 + tt) * heads + hh) * CPR + l16;
-      const uint4 x = (which == 0 ? q : which == 1 ? k : v)[idx];
-      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    for (int u = 0; u < kF8Unroll; ++u) {
+      const int h = hb + 2 * u + hl;
+      const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+      float y[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float a = __uint_as_float(w[u] << 16);
-        const float b = __uint_as_float(w[u] & 0xFFFF0000u);
+      for (int e = 0; e < 4; ++e) {
+        const float a = __uint_as_float(w[e] << 16);
+        const float b = __uint_as_float(w[e] & 0xFFFF0000u);
         if (which < 2) {
-          const float2 r = cs[tt][l16 * 4 + u];
-          y[2 * u] = fmaf(a, r.x, -b * r.y);
-          y[2 * u + 1] = fmaf(a, r.y, b * r.x);
+          const float2 r = cs[l16 * 4 + e];
+          y[2 * e] = fmaf(a, r.x, -b * r.y);
+          y[2 * e + 1] = fmaf(a, r.y, b * r.x);
         } else {
-          y[2 * u] = a;
-          y[2 * u + 1] = b;
+          y[2 * e] = a;
+          y[2 * e + 1] = b;
         }
       }
-    }
-    float amax = 0.f;
+      float ref;
+      if (which == 0) {  // warp-uniform branch: the row maximum of Q'
+        ref = 0.f;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) amax = fmaxf(amax, fabsf(y[u]));
+        for (int e = 0; e < 8; ++e) ref = fmaxf(ref, fabsf(y[e]));
 #pragma unroll
-    for (int off = 8; off > 0; off >>= 1)
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (valid) {
-      float ref = amax;
-      if (which > 0) ref = sqrtf(__uint_as_float(amax2[(which - 1) * heads + hh]));
-      const E4m3Scale sc = e4m3_scale(ref);
-      const float inv = sc.inv;
-      if (which == 0 && l16 == 0) qscale[(t0 + tt) * heads + hh] = sc.s;
-      uint2* dst = which == 0 ? q8 : which == 1 ? k8 : v8;
-      dst[idx] = make_uint2(pack_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv),
-                            pack_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv));
+        for (int off = 8; off > 0; off >>= 1)
+          ref = fmaxf(ref, __shfl_xor_sync(0xffffffffu, ref, off));
+      } else {
+        ref = h < heads ? sqrtf(__uint_as_float(amax2[(which - 1) * heads + h])) : 0.f;
+      }
+      if (h < heads) {
+        const E4m3Scale sc = e4m3_scale(ref);
+        if (which == 0 && l16 == 0) qscale[row0 + h] = sc.s;
+        const float inv = sc.inv;
+        dst[(row0 + h) * CPR + l16] =
+            make_uint2(pack_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv),
+                       pack_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv));
+      }
     }
+#pragma unroll
+    for (int u = 0; u < kF8Unroll; ++u) x[u] = xn[u];
   }
 }
 
@@ -424,20 +448,31 @@ cudaError_t launch_prep_e4m3(const uint16_t* q, const uint16_t* k, const uint16_
                              int32_t heads, int32_t head_dim, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (head_dim != 128) return cudaErrorInvalidValue;
-  const int64_t rows = static_cast<int64_t>(T) * heads;
-  const int64_t chunks = 2 * rows * 16;
-  const int amax_blocks = static_cast<int>(std::min<int64_t>((chunks + 255) / 256, 148 * 8));
   const bool smem_heads = heads <= 4096;
+  // one wave of resident blocks (each loops over the chunks)
+  static int per_sm = 0, sms = 0;
+  if (per_sm == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f8_amax_kernel<128>, 256,
+                                                      8 * 4096) != cudaSuccess || per_sm < 1) {
+      per_sm = 1;
+      sms = sms > 0 ? sms : 148;
+    }
+  }
+  const int amax_blocks = static_cast<int>(std::max<int64_t>(
+      1, std::min<int64_t>((T + kF8Warps - 1) / kF8Warps, static_cast<int64_t>(per_sm) * sms)));
   {
     KernelTimer kt(MF_K_F8_AMAX, s);
     f8_amax_kernel<128><<<amax_blocks, 256, smem_heads ? 8 * heads : 0, s>>>(
-        reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), rows, heads,
+        reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), T, heads,
         smem_heads, amax2);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const RopeFreqs f = make_rope_freqs(head_dim, naxes);
-  const int blocks = (T + kRopeTok - 1) / kRopeTok;
+  const int blocks = (T + kF8Warps - 1) / kF8Warps;
   {
     KernelTimer kt(MF_K_F8_QUANT, s);
     f8_quant_kernel<128><<<blocks, 256, 0, s>>>(
