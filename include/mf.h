@@ -247,11 +247,11 @@ mf_status mf_varlen_attn_bwd_3d(const mf_bf16* q, const mf_bf16* k, const mf_bf1
  *   - S = Q'K'^T in fp32 from the E4M3 codes, then, per query row and tile of
  *     128 keys from the sample's first key, base-2 logits
  *     x = log2(e) * scale * sq * sk * S.  The running maximum m is set by the
- *     first tile and raised only when a tile's maximum exceeds it by more than 2
- *     (then l and the accumulator are rescaled);
- *   - P = 2^(x - m + 6) <= 256 rounded to E4M3 before it weights V; l sums the
+ *     first tile and raised only when a tile's maximum exceeds it by more than 8
+ *     (then l and the accumulator are rescaled), as in the 16-bit forward;
+ *   - P = 2^(x - m) <= 256 rounded to E4M3 before it weights V; l sums the
  *     unrounded P;
- *   - O = sv * (sum_k P~_k V~_k) / l in bf16, LSE = ln 2 * (m - 6 + log2 l).
+ *   - O = sv * (sum_k P~_k V~_k) / l in bf16, LSE = ln 2 * (m + log2 l).
  * Accuracy: expect O errors of a few per cent of |O| against the exact attention
  * (3 mantissa bits on both operands and probabilities); LSE within the largest
  * logit change that the operand rounding permits.

@@ -528,13 +528,13 @@ int oracle_quant_e4m3(const double* qr, const double* k, const double* kr, const
  * with the probabilities themselves rounded to e4m3 before they weight V.  The
  * rounding of a probability depends on the reference it is taken against, so the
  * row follows the variant's steps over keys in tiles of 128 from the sample's
- * first key (base-2 logits, a running maximum and a fixed bias):
+ * first key (base-2 logits and a running maximum that lags by at most 8):
  *   x_k   = log2(e) * scale * sq_j * sk * <qh_j, kh_k>          (all keys of the tile)
  *   tile 0 sets m = max_k x_k;  a later tile replaces m by its own maximum M only
- *         when M > m + 2, and then multiplies l and the accumulator by 2^(m - M);
- *   p_k   = 2^(x_k - m + 6)       (at most 2^8 < 448: no saturation)
+ *         when M > m + 8, and then multiplies l and the accumulator by 2^(m - M);
+ *   p_k   = 2^(x_k - m)           (at most 2^8 < 448: no saturation)
  *   l    += p_k;   acc += e4m3(p_k) * vh_k
- * and at the end O_j = sv * acc / l, LSE_j = ln(2) * (m - 6 + log2 l).
+ * and at the end O_j = sv * acc / l, LSE_j = ln(2) * (m + log2 l).
  * With round = 0 nothing is rounded and O, LSE are the exact attention of the
  * (unrounded) scaled operands.
  */
@@ -569,14 +569,14 @@ int oracle_attn_fwd_e4m3(const double* qh, const double* sq, const double* kh, c
         }
         if (t0 == 0) {
           m = M;
-        } else if (M > m + 2.0) {
+        } else if (M > m + 8.0) {
           const double f = exp2(m - M);
           l *= f;
           for (int64_t e = 0; e < d; ++e) acc[e] *= f;
           m = M;
         }
         for (int64_t kk = 0; kk < nk; ++kk) {
-          const double p = exp2(x[kk] - m + 6.0);
+          const double p = exp2(x[kk] - m);
           const double pr8 = round ? oracle_e4m3(p) : p;
           const double* vk = vh + ((s0 + t0 + kk) * heads + a) * d;
           l += p;
@@ -584,7 +584,7 @@ int oracle_attn_fwd_e4m3(const double* qh, const double* sq, const double* kh, c
         }
       }
       for (int64_t e = 0; e < d; ++e) o[(j * heads + a) * d + e] = sv[a] * acc[e] / l;
-      lse[a * T + j] = (m - 6.0 + log2(l)) * 0.69314718055994530942;
+      lse[a * T + j] = (m + log2(l)) * 0.69314718055994530942;
     }
     free(x);
     free(acc);

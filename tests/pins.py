@@ -580,7 +580,7 @@ def pin_quant_e4m3(so=None):
 
 def pin_attn_e4m3_exact_limit(so=None):
     """With rounding switched off the variant's tiled steps (running maximum raised
-    only past a margin, bias, rescaling of l and the accumulator) are exact: O and
+    only past a margin, rescaling of l and the accumulator) are exact: O and
     LSE equal the plain attention of the same operands to 1e-12, on a tiny pack and
     on samples of several 128-key tiles whose logits rise along the keys, so that
     later tiles raise the maximum and rescale."""
@@ -610,7 +610,10 @@ def pin_attn_e4m3_error_bounds(so=None):
       permits (scale * sum_e |q'_e| bk_e + bq_e |k'_e| + bq_e bk_e, with b the
       half-quantum bound of each rounded element);
       |dO_je| <= the sum of three terms: probability rounding
-      (2^-4 e^(2 delta) sum_k P_k |v~_ke| + 2^-14 sum_k |v~_ke|, since l >= 16),
+      (2^-4 e^(2 delta) sum_k P_k |v~_ke| + 2^-10 sum_k |v~_ke| / l_lb, the second
+      for probabilities in E4M3's subnormal range, with l >= l_lb =
+      sum_k exp(z_k - max z - 2 delta) because the running maximum never exceeds
+      the largest rounded logit),
       V rounding (e^(2 delta) sum_k P_k (2^-4 |v_ke| + 2^-10 sv)) and the
       softmax's response to the logit change ((e^(2 delta) - 1) sum_k P_k |v_ke|),
       |v~| <= (1 + 2^-4) |v| + 2^-10 sv.
@@ -637,8 +640,9 @@ def pin_attn_e4m3_error_bounds(so=None):
             z = sc * Q @ K.T
             P = np.exp(z - l[a, s0:s1][:, None])
             g = np.exp(2 * delta)[:, None]
+            l_lb = np.exp(z - z.max(axis=1, keepdims=True) - 2 * delta[:, None]).sum(axis=1)
             vt = (1 + 2.0 ** -4) * np.abs(V) + 2.0 ** -10 * sv[a]
-            bound = (2.0 ** -4 * g * (P @ vt) + 2.0 ** -14 * vt.sum(axis=0)[None, :]
+            bound = (2.0 ** -4 * g * (P @ vt) + 2.0 ** -10 * vt.sum(axis=0)[None, :] / l_lb[:, None]
                      + g * (P @ (2.0 ** -4 * np.abs(V) + 2.0 ** -10 * sv[a]))
                      + (g - 1) * (P @ np.abs(V)))
             assert np.all(np.abs(o8[s0:s1, a] - o[s0:s1, a]) <= bound + 1e-12)

@@ -66,8 +66,8 @@ MUTANTS = [
      "const double nrm = fabs(kk[e]) > fabs(kk[e + 1]) ? fabs(kk[e]) : fabs(kk[e + 1]);"),
     ("quant_q_scale_per_head", "if (fabs(qr[row + e]) > qmax) qmax = fabs(qr[row + e]);",
      "if (fabs(qr[e]) > qmax) qmax = fabs(qr[e]);"),
-    ("attn_e4m3_lse_without_bias", "lse[a * T + j] = (m - 6.0 + log2(l)) * 0.69314718055994530942;",
-     "lse[a * T + j] = (m + log2(l)) * 0.69314718055994530942;"),
+    ("attn_e4m3_lse_natural_log_of_l", "lse[a * T + j] = (m + log2(l)) * 0.69314718055994530942;",
+     "lse[a * T + j] = (m + log(l)) * 0.69314718055994530942;"),
     ("attn_e4m3_l_not_rescaled", "          l *= f;\n", "\n"),
     ("attn_e4m3_rescale_inverted", "const double f = exp2(m - M);", "const double f = exp2(M - m);"),
     ("attn_e4m3_missing_v_scale", "o[(j * heads + a) * d + e] = sv[a] * acc[e] / l;",
