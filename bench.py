@@ -527,6 +527,11 @@ def fp8_forward(mf, wl, qd, kd, vd, cu, pos, max_len, ws, peak_bf16, hbm_gbs, re
         "amax_frac_of_hbm": amax_bytes / (per("f8_amax") / 1e3) / 1e9 / hbm_gbs,
         "quant_ms": per("f8_quant"),
         "quant_frac_of_hbm": quant_bytes / (per("f8_quant") / 1e3) / 1e9 / hbm_gbs,
+        "roofline": {"bound": "tensor", "kernel": "attn_fwd_f8",
+                     "achieved": flops / (attn_ms / 1e3) / 1e12, "peak": peak8, "unit": "TFLOP/s",
+                     "frac": flops / (attn_ms / 1e3) / 1e12 / peak8,
+                     "traffic": _recorded_traffic("attn_fwd_f8"),
+                     "peak_kind": "2 x the measured bf16 peak (nominal E4M3 / bf16 dense ratio)"},
         "call": "mf_varlen_attn_fwd_fp8 (E4M3 operands and probabilities, fp32 accumulation)",
     }
 
