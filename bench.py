@@ -228,6 +228,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def gpu_local_cpus(bus: str):
+    """CPUs of the NUMA node next to the GPU at PCI address `bus` (sysfs
+    local_cpulist), limited to those this process may use; empty if unknown."""
+    path = f"/sys/bus/pci/devices/{bus.lower()[4:]}/local_cpulist"
+    try:
+        text = open(path).read().strip()
+    except OSError:
+        return set()
+    cpus = set()
+    for part in text.split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus & os.sched_getaffinity(0)
+
+
 def gpu_arm(args):
     import torch
     import torch.distributed as dist
@@ -251,6 +269,15 @@ def gpu_arm(args):
     q, k, v, do = synth.make_inputs(wl, with_do=True)
     T, max_len = mf.pack3d_size(wl.specs) if wl.edit else mf.pack_size(wl.specs)
     n, h, d = len(wl.specs), wl.heads, wl.head_dim
+    props = torch.cuda.get_device_properties(local)
+    bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    # Pinned host buffers are placed on the NUMA node of the allocating CPU: allocate
+    # them from the CPUs next to this GPU (as a data loader pinned to that node would),
+    # then restore the affinity.
+    saved = os.sched_getaffinity(0)
+    local_cpus = gpu_local_cpus(bus)
+    if local_cpus:
+        os.sched_setaffinity(0, local_cpus)
     pin = lambda b: synth.bits_to_torch(b).pin_memory()  # noqa: E731
     hq, hk, hv, hdo = pin(q), pin(k), pin(v), pin(do)
     qd, kd, vd, dod = (x.cuda() for x in (hq, hk, hv, hdo))
@@ -275,8 +302,6 @@ def gpu_arm(args):
     mf.get_status(ws)
     barrier()
 
-    props = torch.cuda.get_device_properties(local)
-    bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     mf.timing_enable(True)
     mf.timing_reset()
@@ -316,6 +341,7 @@ def gpu_arm(args):
     ev_up = [torch.cuda.Event() for _ in range(NB)]
     ev_comp = [torch.cuda.Event() for _ in range(NB)]
     ev_down = [torch.cuda.Event() for _ in range(NB)]
+    os.sched_setaffinity(0, saved)
     for b in range(NB):  # recorded once, so the first waits are satisfied
         ev_comp[b].record(s_comp)
         ev_down[b].record(s_down)

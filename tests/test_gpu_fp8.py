@@ -150,15 +150,21 @@ def test_fwd_empty_pack(cuda_lib):
     assert o.numel() == 0 and lse.numel() == 0
 
 
-def test_fwd_mixed_50k_sampled_pairs(cuda_lib):
-    """The 50k mixed pack the benchmark times (T = 48,019, 24 heads x 128), in the
+@pytest.mark.parametrize("name", ["mixed_50k", "edit_50k"])
+def test_fwd_full_size_sampled_pairs(cuda_lib, name):
+    """The 50k packs at full size (the mixed pack the benchmark times, T = 48,019,
+    and the editing pack with 3D positions, T = 48,230; 24 heads x 128), in the
     benchmark's call: (sample, head) pairs checked against the oracle, whose
     per-head scales come from quantising the whole head."""
     mf = cuda_lib
-    wl = synth.mixed_50k(0)
+    wl = synth.workload(name, 0)
     q, k, v = synth.make_inputs(wl, with_do=False)[:3]
-    cu, pos = mf.pack(wl.specs)
-    cu_r, pos_r = oracle.pack(wl.specs)
+    if wl.edit:
+        cu, pos = mf.pack3d(wl.specs)
+        cu_r, pos_r = oracle.pack3d(wl.specs)
+    else:
+        cu, pos = mf.pack(wl.specs)
+        cu_r, pos_r = oracle.pack(wl.specs)
     T, max_len = wl.total, wl.max_len
     ws = mf.workspace(T, len(wl.specs), wl.heads, 128, True)
     o, lse = mf.varlen_attn_fwd_fp8(dev(q), dev(k), dev(v), cu, pos, max_len, ws=ws)
