@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the timing of the attention's memory-bound neighbours")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--copy-streams", type=int, default=1,
+                    help="streams per copy direction in the end-to-end leg (2 or 3 measured "
+                         "no faster: the host link, not a copy engine, is the limit)")
     return ap.parse_args()
 
 
@@ -324,38 +327,48 @@ def gpu_arm(args):
 
     # ---- end to end through the public API with pinned host buffers.  Every step
     # uploads its q, k, v, dO from pinned host memory and downloads o, lse, dq, dk,
-    # dv; three streams pipeline consecutive steps (upload of step i, compute of
-    # step i-1, download of step i-2; the two copy directions use separate copy
-    # engines), as a data loader feeds a training loop.  Two device buffer sets;
-    # events keep a set's inputs until its compute has read them and its outputs
-    # until their download has read them.
+    # dv; separate streams pipeline consecutive steps (upload of step i, compute of
+    # step i-1, download of step i-2), as a data loader feeds a training loop.
+    # Each direction's tensors are dealt to --copy-streams streams, so that several
+    # copy engines work on one direction at once.  Two device buffer sets; events
+    # keep a set's inputs until its compute has read them and its outputs until
+    # their download has read them.
     pinned = lambda: torch.empty(hq.shape, dtype=hq.dtype, pin_memory=True)  # noqa: E731
     NB = 2
-    s_up, s_comp, s_down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    NC = max(1, args.copy_streams)  # streams per copy direction (copy engines work in parallel)
+    ups = [torch.cuda.Stream() for _ in range(NC)]
+    downs = [torch.cuda.Stream() for _ in range(NC)]
+    s_comp = torch.cuda.Stream()
     dev_in = [[torch.empty_like(qd) for _ in range(4)] for _ in range(NB)]
     dev_out = [{"o": torch.empty_like(qd), "lse": torch.empty((h, T), dtype=torch.float32, device="cuda"),
                 "dq": torch.empty_like(qd), "dk": torch.empty_like(qd), "dv": torch.empty_like(qd)}
                for _ in range(NB)]
     host_out = [{"o": pinned(), "lse": torch.empty((h, T), dtype=torch.float32, pin_memory=True),
                  "dq": pinned(), "dk": pinned(), "dv": pinned()} for _ in range(NB)]
-    ev_up = [torch.cuda.Event() for _ in range(NB)]
+    ev_up = [[torch.cuda.Event() for _ in range(NC)] for _ in range(NB)]
     ev_comp = [torch.cuda.Event() for _ in range(NB)]
-    ev_down = [torch.cuda.Event() for _ in range(NB)]
+    ev_down = [[torch.cuda.Event() for _ in range(NC)] for _ in range(NB)]
     os.sched_setaffinity(0, saved)
     for b in range(NB):  # recorded once, so the first waits are satisfied
         ev_comp[b].record(s_comp)
-        ev_down[b].record(s_down)
+        for c in range(NC):
+            ev_down[b][c].record(downs[c])
     e2e_steps = max(3, min(args.steps, 20))
+    # tensors dealt to the copy streams in turn (largest first)
+    in_names = list(range(4))
+    out_names = ["o", "dq", "dk", "dv", "lse"]
 
     def e2e_step(i):
         b = i % NB
-        s_up.wait_event(ev_comp[b])
-        with torch.cuda.stream(s_up):
-            for dst, src in zip(dev_in[b], (hq, hk, hv, hdo)):
-                dst.copy_(src, non_blocking=True)
-        ev_up[b].record(s_up)
-        s_comp.wait_event(ev_up[b])
-        s_comp.wait_event(ev_down[b])
+        for c, st in enumerate(ups):
+            st.wait_event(ev_comp[b])
+            with torch.cuda.stream(st):
+                for j in in_names[c::NC]:
+                    dev_in[b][j].copy_((hq, hk, hv, hdo)[j], non_blocking=True)
+            ev_up[b][c].record(st)
+        for c in range(NC):
+            s_comp.wait_event(ev_up[b][c])
+            s_comp.wait_event(ev_down[b][c])
         qq, kk, vv, dd = dev_in[b]
         out = dev_out[b]
         packer(wl.specs, cu=cu, pos=pos, stream=s_comp)
@@ -364,20 +377,26 @@ def gpu_arm(args):
         mf.varlen_attn_bwd(qq, kk, vv, out["o"], out["lse"], dd, cu, pos, max_len, dq=out["dq"],
                            dk=out["dk"], dv=out["dv"], ws=ws, stream=s_comp, after_fwd=True)
         ev_comp[b].record(s_comp)
-        s_down.wait_event(ev_comp[b])
-        with torch.cuda.stream(s_down):
-            for name, t in out.items():
-                host_out[b][name].copy_(t, non_blocking=True)
-        ev_down[b].record(s_down)
+        for c, st in enumerate(downs):
+            st.wait_event(ev_comp[b])
+            with torch.cuda.stream(st):
+                for name in out_names[c::NC]:
+                    host_out[b][name].copy_(out[name], non_blocking=True)
+            ev_down[b][c].record(st)
 
     for i in range(NB):
         e2e_step(i)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_up)
+    e0.record(ups[0])
+    for st in ups[1:]:
+        st.wait_event(e0)
     for i in range(e2e_steps):
         e2e_step(i)
-    e1.record(s_down)
+    last = (e2e_steps - 1) % NB
+    for c in range(1, NC):
+        downs[0].wait_event(ev_down[last][c])
+    e1.record(downs[0])
     barrier()
     mf.get_status(ws, s_comp)
     ms_e2e, _ = reduce_over_ranks(e0.elapsed_time(e1) / e2e_steps, 0.0, world)
@@ -444,8 +463,9 @@ def gpu_arm(args):
         "gpu_launches": int(sum(x[1] for x in kern.values())),
         "e2e": {"value": flops_all / (ms_e2e / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "copy_streams_per_direction": NC,
                 "how": "public API, pinned host buffers, upload / compute / download of "
-                       "consecutive steps pipelined on three streams"},
+                       "consecutive steps pipelined on separate streams"},
         "clocks": clocks,
     }
     if not args.no_extras:
