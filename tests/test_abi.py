@@ -167,3 +167,16 @@ def test_fp8_argument_errors_on_host():
     assert lib.mf_quant_e4m3(q, k, v, pos, 2, 10, 2, 128, p(base + 8200), k8, v8, qs, kv,
                              None) == 2
     assert lib.mf_quant_e4m3(q, k, v, pos, 2, -1, 2, 128, q8, k8, v8, qs, kv, None) == 1
+
+
+def test_binding_argument_counts_match_header():
+    """Every declaration in mf.h has as many parameters as its ctypes binding
+    declares (a drifted binding would shift every argument after the change)."""
+    src = open(os.path.join(ROOT, "include", "mf.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    decls = dict(re.findall(r"\b(mf_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", src))
+    assert len(decls) >= 9
+    for name, params in decls.items():
+        params = params.strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert len(_lib.SIGNATURES[name][1]) == n, (name, n, len(_lib.SIGNATURES[name][1]))
