@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(256) f8_amax_kernel(const uint4* __restrict__ 
 //   V: s from sqrt(amax2[heads + h]), the head's largest |v|;
 // each x / s rounded to E4M3 (nearest even, saturating) into [T][heads][D] bytes.
 // The warp's first loads are issued before it builds its token's (cos, sin)
-// table, and each later round while the previous one is converted.
+// table, and each later batch while the previous batch is converted.
 template <int D>
 __global__ void __launch_bounds__(256) f8_quant_kernel(const uint4* __restrict__ q,
                                                        const uint4* __restrict__ k,
@@ -369,10 +369,10 @@ __global__ void __launch_bounds__(256) f8_quant_kernel(const uint4* __restrict__
   if (t >= T) return;  // warp-uniform; no block-wide barrier follows
   float2* cs = cs_all[wid];
   const int lane = threadIdx.x & 31, hl = lane >> 4, l16 = lane & 15;
-  const int nh = (heads + 2 * kF8Unroll - 1) / (2 * kF8Unroll);  // rounds per operand
+  const int nh = (heads + 2 * kF8Unroll - 1) / (2 * kF8Unroll);  // batches per operand
   const int nit = 3 * nh;
   const int64_t row0 = t * heads;
-  auto load_round = [&](int it, uint4 (&x)[kF8Unroll]) {
+  auto load_batch = [&](int it, uint4 (&x)[kF8Unroll]) {
     const int which = it / nh;
     const int hb = (it - which * nh) * 2 * kF8Unroll;
     const uint4* src = which == 0 ? q : which == 1 ? k : v;
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(256) f8_quant_kernel(const uint4* __restrict__
     }
   };
   uint4 x[kF8Unroll];
-  load_round(0, x);
+  load_batch(0, x);
   for (int P = lane; P < NP; P += 32) {
     float c = 1.f, s = 0.f;
     if (pos != nullptr) {
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(256) f8_quant_kernel(const uint4* __restrict__
   __syncwarp();
   for (int it = 0; it < nit; ++it) {
     uint4 xn[kF8Unroll];
-    load_round(it + 1, xn);
+    load_batch(it + 1, xn);
     const int which = it / nh;
     const int hb = (it - which * nh) * 2 * kF8Unroll;
     uint2* dst = which == 0 ? q8 : which == 1 ? k8 : v8;
