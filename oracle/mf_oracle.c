@@ -29,8 +29,11 @@
  *    the attention; the gradient is the exact derivative of the definitions above
  *    (softmax Jacobian and the transpose of the rotation, which is its inverse).
  *
- * Every loop follows the definition directly, one query row at a time, in double.
- * No blocking, no fusion, no online softmax.
+ * Every loop follows the definition directly, one row at a time, in double: the
+ * forward one query row at a time, the backward in two passes (one query row at a
+ * time for dQ, one key row at a time for dK and dV, each recomputing the row's
+ * probabilities from the LSE), OpenMP across rows.  No blocking, no fusion, no
+ * online softmax.
  */
 #include <math.h>
 #include <stdint.h>
@@ -130,6 +133,16 @@ static void attn_row(const double* qr, const double* kr, const double* v, int64_
   }
 }
 
+/* Index of the sample holding each token: samp[t] = i for cu[i] <= t < cu[i+1]
+ * (zero-length samples hold no token).  Returns a malloc'd int64[T] or NULL. */
+static int64_t* sample_of_tokens(const int64_t* cu, int64_t n, int64_t T) {
+  int64_t* samp = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T + 1));
+  if (!samp) return NULL;
+  for (int64_t i = 0; i < n; ++i)
+    for (int64_t t = cu[i]; t < cu[i + 1]; ++t) samp[t] = i;
+  return samp;
+}
+
 static int rotate_qk(const double* q, const double* k, const int64_t* pos, int64_t T,
                      int64_t heads, int64_t d, double base, double** qr, double** kr) {
   *qr = (double*)malloc(sizeof(double) * (size_t)(T * heads * d + 1));
@@ -156,18 +169,18 @@ int oracle_attn_fwd(const double* q, const double* k, const double* v, const int
                     double scale, double base, double* o, double* lse) {
   double *qr, *kr;
   if (rotate_qk(q, k, pos, T, heads, d, base, &qr, &kr) != ORACLE_OK) return ORACLE_ERR;
-  int64_t npairs = n * heads;
-#pragma omp parallel for schedule(dynamic, 1)
-  for (int64_t pr = 0; pr < npairs; ++pr) {
-    int64_t i = pr / heads, a = pr % heads;
+  int64_t* samp = sample_of_tokens(cu, n, T);
+  if (!samp) { free(qr); free(kr); return ORACLE_ERR; }
+  /* every (token, head) row on its own: row r is token r / heads, head r % heads */
+#pragma omp parallel for schedule(dynamic, 64)
+  for (int64_t r = 0; r < T * heads; ++r) {
+    int64_t tj = r / heads, a = r % heads, i = samp[tj];
     int64_t s0 = cu[i], L = cu[i + 1] - cu[i];
-    if (L <= 0) continue;
     double* srow = (double*)malloc(sizeof(double) * (size_t)L);
-    for (int64_t j = 0; j < L; ++j)
-      attn_row(qr, kr, v, s0, L, s0 + j, a, heads, d, scale, srow, o + ((s0 + j) * heads + a) * d,
-               lse + a * T + s0 + j);
+    attn_row(qr, kr, v, s0, L, tj, a, heads, d, scale, srow, o + r * d, lse + a * T + tj);
     free(srow);
   }
+  free(samp);
   free(qr);
   free(kr);
   return ORACLE_OK;
@@ -219,45 +232,70 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
   if (rotate_qk(q, k, pos, T, heads, d, base, &qr, &kr) != ORACLE_OK) return ORACLE_ERR;
   double* o = (double*)malloc(sizeof(double) * (N + 1));
   double* lse = (double*)malloc(sizeof(double) * (size_t)(heads * T + 1));
+  double* D = (double*)malloc(sizeof(double) * (size_t)(heads * T + 1));
   double* dqr = (double*)calloc(N + 1, sizeof(double));
   double* dkr = (double*)calloc(N + 1, sizeof(double));
-  if (!qr || !kr || !o || !lse || !dqr || !dkr) {
-    free(qr); free(kr); free(o); free(lse); free(dqr); free(dkr);
+  int64_t* samp = sample_of_tokens(cu, n, T);
+  if (!qr || !kr || !o || !lse || !D || !dqr || !dkr || !samp) {
+    free(qr); free(kr); free(o); free(lse); free(D); free(dqr); free(dkr); free(samp);
     return ORACLE_ERR;
   }
   oracle_attn_fwd(q, k, v, cu, n, pos, T, heads, d, scale, base, o, lse);
   memset(dv, 0, sizeof(double) * N);
-  int64_t npairs = n * heads;
-#pragma omp parallel for schedule(dynamic, 1)
-  for (int64_t pr = 0; pr < npairs; ++pr) {
-    int64_t i = pr / heads, a = pr % heads;
+  /* D_j = <dO_j, O_j> of every (token, head) row r (token r / heads, head r % heads) */
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < T * heads; ++r) {
+    double acc = 0.0;
+    for (int64_t e = 0; e < d; ++e) acc += d_o[r * d + e] * o[r * d + e];
+    D[(r % heads) * T + r / heads] = acc;
+  }
+  /* Pass 1, one query row j at a time: over the keys k of its sample,
+   * P_jk = exp(S_jk - LSE_j), dP_jk = <dO_j, v_k>, dS_jk = P_jk (dP_jk - D_j), and
+   * dQ'_j = scale sum_k dS_jk k'_k. */
+#pragma omp parallel for schedule(dynamic, 64)
+  for (int64_t r = 0; r < T * heads; ++r) {
+    int64_t tj = r / heads, a = r % heads, i = samp[tj];
     int64_t s0 = cu[i], L = cu[i + 1] - cu[i];
-    if (L <= 0) continue;
-    double* prow = (double*)malloc(sizeof(double) * (size_t)L);
-    for (int64_t j = 0; j < L; ++j) {
-      int64_t rj = ((s0 + j) * heads + a) * d;
-      double Dj = 0.0;
-      for (int64_t e = 0; e < d; ++e) Dj += d_o[rj + e] * o[rj + e];
-      double lj = lse[a * T + s0 + j];
-      for (int64_t kk = 0; kk < L; ++kk) {
-        int64_t rk = ((s0 + kk) * heads + a) * d;
-        double acc = 0.0;
-        for (int64_t e = 0; e < d; ++e) acc += qr[rj + e] * kr[rk + e];
-        prow[kk] = exp(scale * acc - lj);
+    const double* qj = qr + r * d;
+    const double* doj = d_o + r * d;
+    double* dqj = dqr + r * d;
+    const double lj = lse[a * T + tj], Dj = D[a * T + tj];
+    for (int64_t kk = 0; kk < L; ++kk) {
+      int64_t rk = ((s0 + kk) * heads + a) * d;
+      double acc = 0.0, dp = 0.0;
+      for (int64_t e = 0; e < d; ++e) {
+        acc += qj[e] * kr[rk + e];
+        dp += doj[e] * v[rk + e];
       }
-      for (int64_t kk = 0; kk < L; ++kk) {
-        int64_t rk = ((s0 + kk) * heads + a) * d;
-        double dp = 0.0;
-        for (int64_t e = 0; e < d; ++e) dp += d_o[rj + e] * v[rk + e];
-        double ds = prow[kk] * (dp - Dj);
-        for (int64_t e = 0; e < d; ++e) {
-          dv[rk + e] += prow[kk] * d_o[rj + e];
-          dqr[rj + e] += scale * ds * kr[rk + e];
-          dkr[rk + e] += scale * ds * qr[rj + e];
-        }
+      const double p = exp(scale * acc - lj);
+      const double ds = p * (dp - Dj);
+      for (int64_t e = 0; e < d; ++e) dqj[e] += scale * ds * kr[rk + e];
+    }
+  }
+  /* Pass 2, one key row k at a time: over the queries j of its sample, the same
+   * P_jk and dS_jk, and dV_k = sum_j P_jk dO_j, dK'_k = scale sum_j dS_jk q'_j. */
+#pragma omp parallel for schedule(dynamic, 64)
+  for (int64_t r = 0; r < T * heads; ++r) {
+    int64_t tk = r / heads, a = r % heads, i = samp[tk];
+    int64_t s0 = cu[i], L = cu[i + 1] - cu[i];
+    const double* kk_r = kr + r * d;
+    const double* vk = v + r * d;
+    double* dvk = dv + r * d;
+    double* dkk = dkr + r * d;
+    for (int64_t jj = 0; jj < L; ++jj) {
+      int64_t tq = s0 + jj, rq = (tq * heads + a) * d;
+      double acc = 0.0, dp = 0.0;
+      for (int64_t e = 0; e < d; ++e) {
+        acc += qr[rq + e] * kk_r[e];
+        dp += d_o[rq + e] * vk[e];
+      }
+      const double pk = exp(scale * acc - lse[a * T + tq]);
+      const double dsk = pk * (dp - D[a * T + tq]);
+      for (int64_t e = 0; e < d; ++e) {
+        dvk[e] += pk * d_o[rq + e];
+        dkk[e] += scale * dsk * qr[rq + e];
       }
     }
-    free(prow);
   }
   if (pos) {
     oracle_rope2d(dqr, pos, T, heads, d, base, -1, dq);
@@ -266,7 +304,7 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
     memcpy(dq, dqr, sizeof(double) * N);
     memcpy(dk, dkr, sizeof(double) * N);
   }
-  free(qr); free(kr); free(o); free(lse); free(dqr); free(dkr);
+  free(qr); free(kr); free(o); free(lse); free(D); free(dqr); free(dkr); free(samp);
   return ORACLE_OK;
 }
 

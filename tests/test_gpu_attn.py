@@ -257,16 +257,22 @@ def test_full_cfg_2048(cuda_lib):
 
 
 def test_full_mixed_50k(cuda_lib):
+    """The benchmarked pack: the backward of its longest sample (4,291 tokens, 34
+    key blocks whose dQ contributions are summed into each query row) and of its
+    shortest, against the oracle's full backward of those (sample, head) pairs."""
     wl = synth.mixed_50k()
     L = np.array(wl.lengths)
-    small = int(np.argmin(L))
-    _full_size("mixed_50k", bwd_pairs=[(small, 0), (small, wl.heads - 1)])
+    small, large = int(np.argmin(L)), int(np.argmax(L))
+    _full_size("mixed_50k", bwd_pairs=[(large, 0), (large, wl.heads - 1), (small, 0),
+                                       (small, wl.heads - 1)])
 
 
 def test_full_extreme_aspect(cuda_lib):
+    """The 128x128 sample (about 16.5k tokens, 130 key blocks) under the per-head
+    scales of this workload, and the last 64x64 filler."""
     wl = synth.extreme_aspect()
-    # the 32x128 panorama (sample 0) and the last 64x64 filler
-    _full_size("extreme_aspect", fwd_rows=32, bwd_pairs=[(len(wl.specs) - 1, 5)])
+    big = int(np.argmax(np.array(wl.lengths)))
+    _full_size("extreme_aspect", fwd_rows=32, bwd_pairs=[(big, 5), (len(wl.specs) - 1, 5)])
 
 
 @pytest.mark.parametrize("edit", [False, True])

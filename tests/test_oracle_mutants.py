@@ -25,17 +25,19 @@ MUTANTS = [
     ("attn_no_scale", "srow[kk] = scale * acc;", "srow[kk] = acc;"),
     ("attn_lse_without_max", "double lj = m + log(l);", "double lj = log(l);"),
     ("attn_unnormalised", "double p = exp(srow[kk] - lj);", "double p = exp(srow[kk] - m);"),
-    ("bwd_missing_D", "double ds = prow[kk] * (dp - Dj);", "double ds = prow[kk] * dp;"),
+    ("bwd_missing_D", "const double ds = p * (dp - Dj);", "const double ds = p * dp;"),
+    ("bwd_missing_D_key_pass", "const double dsk = pk * (dp - D[a * T + tq]);",
+     "const double dsk = pk * dp;"),
     ("bwd_dk_forward_rotation", "oracle_rope2d(dkr, pos, T, heads, d, base, -1, dk);",
      "oracle_rope2d(dkr, pos, T, heads, d, base, +1, dk);"),
     ("bwd_dq_forward_rotation", "oracle_rope2d(dqr, pos, T, heads, d, base, -1, dq);",
      "oracle_rope2d(dqr, pos, T, heads, d, base, +1, dq);"),
-    ("bwd_dv_transposed", "dv[rk + e] += prow[kk] * d_o[rj + e];",
-     "dv[rj + e] += prow[kk] * d_o[rk + e];"),
-    ("bwd_dk_missing_scale", "dkr[rk + e] += scale * ds * qr[rj + e];",
-     "dkr[rk + e] += ds * qr[rj + e];"),
-    ("bwd_dq_unrotated_keys", "dqr[rj + e] += scale * ds * kr[rk + e];",
-     "dqr[rj + e] += scale * ds * k[rk + e];"),
+    ("bwd_dv_own_row", "dvk[e] += pk * d_o[rq + e];", "dvk[e] += pk * d_o[r * d + e];"),
+    ("bwd_dk_missing_scale", "dkk[e] += scale * dsk * qr[rq + e];", "dkk[e] += dsk * qr[rq + e];"),
+    ("bwd_dq_unrotated_keys", "dqj[e] += scale * ds * kr[rk + e];",
+     "dqj[e] += scale * ds * k[rk + e];"),
+    ("bwd_key_pass_wrong_lse", "const double pk = exp(scale * acc - lse[a * T + tq]);",
+     "const double pk = exp(scale * acc - lse[a * T + tk]);"),
     ("cfg_branches_swapped", "const double vg = vu + g * (vc - vu);",
      "const double vg = vc + g * (vu - vc);"),
     ("cfg_no_text_offset", "const int64_t img_c = start + sc[0];",
