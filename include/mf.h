@@ -299,14 +299,19 @@ mf_status mf_quant_e4m3(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
  *    launch (use mf_varlen_attn_fwd with a caller workspace for them).
  *  - The first call on each device looks up the array's device address once
  *    (cudaGetSymbolAddress, with that device current); make that first call before
- *    any stream capture.  Later calls only reuse the cached address.
+ *    any stream capture.  Later calls only reuse the cached address.  The cache is
+ *    keyed on the unique id of the current context, so after cudaDeviceReset (which
+ *    loads the library's module again in a new context) the next call looks the
+ *    address up afresh; make that call, too, before any stream capture.
  *  - Every call shares the one array, which keeps the previous call's contents;
  *    the forward rewrites everything it reads from it (status word, work list,
  *    fp16 operand copies), so no clearing is needed between calls.  Calls that
  *    overlap on the GPU (concurrent streams, other threads) race on the array:
  *    serialise them.
- *  - mf_get_status cannot be used for this call (it has no workspace argument);
- *    device-side errors are not reported back.
+ *  - Device-side errors (a malformed cu_seqlens, a wait that ran out, a value
+ *    outside the fp16 range of the internal operands) are recorded in the array's
+ *    status word, as mf_varlen_attn_fwd records them in its workspace; read them
+ *    with mf_noalloc_get_status.
  * No device memory is allocated by this call or by the library on its behalf.
  */
 #define MF_NOALLOC_MAX_ELEMS 4194304LL   /* T * heads * head_dim */
@@ -317,6 +322,17 @@ mf_status mf_varlen_attn_fwd_noalloc(const mf_bf16* q, const mf_bf16* k, const m
                                      int32_t n, int32_t T, int32_t max_len, int32_t heads,
                                      int32_t head_dim, float softmax_scale, mf_bf16* o,
                                      float* lse, mf_stream stream);
+
+/*
+ * Synchronise `stream` and report the device-side status that the last
+ * mf_varlen_attn_fwd_noalloc call on the current device recorded in the
+ * library's scratch array: MF_ERR_BAD_SEQLENS, MF_ERR_TIMEOUT, MF_ERR_OVERFLOW
+ * (a value left the fp16 range of the internal operands), MF_ERR_CUDA if the
+ * stream itself failed; MF_OK otherwise.  Allocates nothing.  Like the forward it
+ * reports on, it shares the one array: a call that overlaps another no-alloc
+ * forward on the GPU reads a status word that that call is rewriting.
+ */
+mf_status mf_noalloc_get_status(mf_stream stream);
 
 /*
  * Packed classifier-free guidance followed by one rectified-flow Euler step.

@@ -19,7 +19,7 @@ __all__ = [
     "MFError", "STATUS_NAMES", "load", "library_path", "pack_size", "pack", "rope2d_qk",
     "attn_workspace_bytes", "workspace", "varlen_attn_fwd", "varlen_attn_bwd", "get_status",
     "cfg_euler_step", "adaln_modulate", "gated_residual", "pack3d_size", "pack3d", "rope3d_qk",
-    "varlen_attn_fwd_fp8", "quant_e4m3",
+    "varlen_attn_fwd_fp8", "quant_e4m3", "varlen_attn_fwd_noalloc", "noalloc_get_status",
 ]
 
 
@@ -269,8 +269,13 @@ def varlen_attn_fwd_noalloc(q, k, v, cu_seqlens, pos, max_len, softmax_scale: fl
     """The forward without a workspace, for callers that cannot allocate device
     memory (e.g. a plugin handed only its inputs and outputs): its scratch is a
     fixed array inside the library (limits MF_NOALLOC_* in mf.h).  Pass `o` and
-    `lse` to keep this call itself free of allocations."""
+    `lse` to keep this call itself free of allocations.  The call takes 2D
+    positions only: pos must be None or int32 [T, 2] (an editing pack's [T, 3]
+    table raises ValueError).  Device-side errors of the call are read back with
+    noalloc_get_status."""
     torch = _torch()
+    if _is_3d(pos):
+        raise ValueError("the allocation-free forward takes 2D positions (int32 [T, 2]) only")
     _check_thd("q", q)
     T, h, d = q.shape
     for name, t in (("k", k), ("v", v)):
@@ -350,6 +355,13 @@ def get_status(ws, stream=None) -> None:
     """Synchronise and raise MFError if the last call on this workspace recorded a
     device-side error (malformed cu_seqlens, a wait that ran out)."""
     check(load().mf_get_status(_ptr(ws), _stream_ptr(stream)), "device status")
+
+
+def noalloc_get_status(stream=None) -> None:
+    """Synchronise and raise MFError if the last varlen_attn_fwd_noalloc call on
+    the current device recorded a device-side error (its status word lives in the
+    library's fixed scratch array)."""
+    check(load().mf_noalloc_get_status(_stream_ptr(stream)), "device status (noalloc)")
 
 
 def timing_enable(on: bool = True) -> None:

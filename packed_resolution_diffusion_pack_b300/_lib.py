@@ -42,6 +42,7 @@ SIGNATURES = {
                                      _p]),
     "mf_varlen_attn_fwd_noalloc": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32,
                                                   _i32, _f32, _p, _p, _p]),
+    "mf_noalloc_get_status": (ctypes.c_int, [_p]),
     "mf_pack3d_size": (ctypes.c_int, [_p, _i32, _p, _p]),
     "mf_pack3d": (ctypes.c_int, [_p, _i32, _p, _p, _p]),
     "mf_rope3d_qk": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _p]),

@@ -5,6 +5,8 @@
 // (which can synchronise the device) are not allowed.  This entry point needs no
 // workspace from them: its scratch is one file-scope device array of fixed size,
 // which every GPU that loads this library holds until the process exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -35,24 +37,63 @@ static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};
+struct Cached {
+  void* addr = nullptr;
+  unsigned long long ctx_id = 0;  // unique id of the context the address belongs to
+};
+Cached g_cache[kMaxDevices];
+
+// Unique id of the calling thread's current context (driver entry points through
+// the runtime, so the library needs no -lcuda).  A device reset or a new primary
+// context gets a new id; ids are never reused within a process.
+cudaError_t current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  if (get_current == nullptr || get_id == nullptr) {
+    cudaDriverEntryPointQueryResult q1, q2;
+    void *f1 = nullptr, *f2 = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 4000, cudaEnableDefault, &q1) !=
+            cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) !=
+            cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+      return cudaErrorNotSupported;
+    get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f1);
+    get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f2);
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
 
 // Device address of g_scratch on the current device, looked up once per device
-// (with that device current) and cached.
+// and context (with that device current) and cached.  The cache is keyed on the
+// context's unique id: after cudaDeviceReset the module is loaded again in a new
+// context, and the address is looked up afresh on the next call.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned long long id = 0;
+  if (current_context_id(&id) != cudaSuccess) {
+    // no context current yet: cudaSetDevice initialises the device's primary one
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return e;
+    e = current_context_id(&id);
+    if (e != cudaSuccess) return e;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_addr[dev] == nullptr) {
+  Cached& c = g_cache[dev];
+  if (c.addr == nullptr || c.ctx_id != id) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess) return e;
     if (p == nullptr) return cudaErrorInvalidSymbol;
-    g_addr[dev] = p;
+    c.addr = p;
+    c.ctx_id = id;
   }
-  *out = g_addr[dev];
+  *out = c.addr;
   return cudaSuccess;
 }
 
@@ -76,4 +117,13 @@ extern "C" mf_status mf_varlen_attn_fwd_noalloc(const mf_bf16* q, const mf_bf16*
   if (mf::scratch_address(&ws) != cudaSuccess) return MF_ERR_CUDA;
   return mf_varlen_attn_fwd(q, k, v, d_cu_seqlens, d_pos, n, T, max_len, heads, head_dim,
                             softmax_scale, o, lse, ws, mf::kScratchBytes, stream);
+}
+
+// The status word of the last allocation-free forward on the current device: it
+// sits at offset 0 of the scratch array, where mf_get_status reads it for a
+// caller workspace.
+extern "C" mf_status mf_noalloc_get_status(mf_stream stream) {
+  void* ws = nullptr;
+  if (mf::scratch_address(&ws) != cudaSuccess) return MF_ERR_CUDA;
+  return mf_get_status(ws, stream);
 }

@@ -180,3 +180,17 @@ def test_binding_argument_counts_match_header():
         params = params.strip()
         n = 0 if params in ("", "void") else params.count(",") + 1
         assert len(_lib.SIGNATURES[name][1]) == n, (name, n, len(_lib.SIGNATURES[name][1]))
+
+
+def test_noalloc_binding_rejects_editing_positions():
+    """The allocation-free forward takes 2D positions only: an editing pack's
+    [T, 3] table, or a table of the wrong dtype, is refused on the host before
+    the C call (it would otherwise be read with a stride of 2)."""
+    import torch
+    T = 8
+    q = torch.zeros((T, 1, 64), dtype=torch.bfloat16)
+    cu = torch.tensor([0, T], dtype=torch.int32)
+    with pytest.raises(ValueError, match="2D positions"):
+        mf.varlen_attn_fwd_noalloc(q, q, q, cu, torch.zeros((T, 3), dtype=torch.int32), T)
+    with pytest.raises(ValueError, match="int32"):
+        mf.varlen_attn_fwd_noalloc(q, q, q, cu, torch.zeros((T, 2), dtype=torch.int64), T)

@@ -78,3 +78,23 @@ def test_noalloc_python_binding():
     torch.cuda.synchronize()
     assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
     assert np.isfinite(lse.cpu().numpy()).all()
+
+
+def test_noalloc_status_reports_device_errors():
+    """The status word in the scratch array reports what the last allocation-free
+    forward found on the device: a malformed cu_seqlens is MF_ERR_BAD_SEQLENS,
+    and the next well-formed call clears it."""
+    import packed_resolution_diffusion_pack_b300 as mf
+    T = 64
+    q = dev(synth.normal_bf16_bits(0, 2, (T, 1, 64)))
+    bad = torch.tensor([0, 40, 30], dtype=torch.int32, device="cuda")
+    mf.varlen_attn_fwd_noalloc(q, q, q, bad, None, 64)
+    with pytest.raises(mf.MFError) as ei:
+        mf.noalloc_get_status()
+    assert ei.value.status == 6  # MF_ERR_BAD_SEQLENS
+    good = torch.tensor([0, 40, 64], dtype=torch.int32, device="cuda")
+    o, lse = mf.varlen_attn_fwd_noalloc(q, q, q, good, None, 40)
+    mf.noalloc_get_status()
+    o_ref, lse_ref = mf.varlen_attn_fwd(q, q, q, good, None, 40)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
