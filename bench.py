@@ -34,6 +34,9 @@ import synth  # noqa: E402
 
 METRIC = "packed 2D-RoPE varlen attention TFLOP/s fwd/bwd at 50k tokens; % BF16 peak"
 UNIT = "TFLOP/s"
+# NVIDIA's dense bf16 tensor figure for one B300: the denominator the targets of
+# the problem statement (>= 55 % forward, >= 40 % backward) are stated against.
+NOMINAL_BF16_TFLOPS = 2250.0
 
 
 def parse():
@@ -440,7 +443,7 @@ def gpu_arm(args):
     ach = per_launch[dom]["achieved_tflops"]
     roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_tc,
                 "unit": "TFLOP/s", "frac": ach / peak_tc, "traffic": traffic,
-                "peak_kind": peak_name}
+                "peak_kind": peak_name, "frac_of_nominal": ach / NOMINAL_BF16_TFLOPS}
     fwd_ms = per_launch["attn_fwd"]["ms_per_launch"]
     bwd_ms = per_launch["attn_bwd"]["ms_per_launch"]
     line = {
@@ -458,6 +461,11 @@ def gpu_arm(args):
         "fwd_frac_of_peak": flops_fwd / (fwd_ms / 1e3) / 1e12 / peak_tc,
         "bwd_frac_of_peak": flops_bwd / (bwd_ms / 1e3) / 1e12 / peak_tc,
         "peak_tflops": peak_tc,
+        # the targets are stated against the nominal dense bf16 peak
+        "fwd_frac_of_nominal": flops_fwd / (fwd_ms / 1e3) / 1e12 / NOMINAL_BF16_TFLOPS,
+        "bwd_frac_of_nominal": flops_bwd / (bwd_ms / 1e3) / 1e12 / NOMINAL_BF16_TFLOPS,
+        "nominal_peak_tflops": NOMINAL_BF16_TFLOPS,
+        "targets_vs_nominal": {"fwd": 0.55, "bwd": 0.40},
         "roofline": roofline,
         "kernels": per_launch,
         "gpu_launches": int(sum(x[1] for x in kern.values())),
@@ -583,24 +591,24 @@ def fp8_forward(mf, wl, qd, kd, vd, cu, pos, max_len, ws, peak_bf16, hbm_gbs, re
 
 
 def _recorded_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary
-    (profiles/dram_mixed_50k.md, lines `traffic <kernel> <source> <sha16> <bytes>`),
-    if that summary was taken on the current kernel source (else None)."""
+    """DRAM bytes per launch of `kernel` from the committed capture records
+    (profiles/dram_traffic.json), if the record was taken on the current kernel
+    source (the SHA-256 prefix it stores still matches); else None."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "dram_mixed_50k.md")
     try:
-        lines = open(path).read().splitlines()
-    except OSError:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            records = json.load(f)["records"]
+    except (OSError, KeyError, ValueError):
         return None
-    for line in lines:
-        parts = line.split()
-        if len(parts) == 5 and parts[0] == "traffic" and parts[1] == kernel:
-            src = os.path.join(ROOT, "packed_resolution_diffusion_pack_b300", "csrc", parts[2])
-            try:
-                sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-            except OSError:
-                return None
-            return int(parts[4]) if sha == parts[3] else None
+    for rec in records:
+        if rec.get("kernel") != kernel:
+            continue
+        src = os.path.join(ROOT, "packed_resolution_diffusion_pack_b300", "csrc", rec["source"])
+        try:
+            sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        except OSError:
+            return None
+        return int(rec["dram_bytes_per_launch"]) if sha == rec["sha16"] else None
     return None
 
 

@@ -25,14 +25,21 @@ def test_gpu_local_cpus_parses_sysfs_lists(monkeypatch):
     assert bench.gpu_local_cpus("00000000:FF:00.0") == set()
 
 
-def test_recorded_traffic_lines_are_read():
-    """Every traffic line of the committed DRAM summary names a kernel source
-    file that exists, and an unknown kernel gives None."""
-    path = os.path.join(bench.ROOT, "profiles", "dram_mixed_50k.md")
-    lines = [ln.split() for ln in open(path).read().splitlines() if ln.startswith("traffic ")]
-    assert {ln[1] for ln in lines} >= {"attn_fwd", "attn_bwd", "attn_fwd_f8"}
-    for ln in lines:
-        assert os.path.exists(os.path.join(bench.ROOT, "packed_resolution_diffusion_pack_b300",
-                                           "csrc", ln[2]))
-        assert len(ln[3]) == 16 and int(ln[4]) > 0
+def test_recorded_traffic_records_are_read():
+    """Every record of the committed DRAM traffic file names a kernel source that
+    exists and a positive byte count; a record whose hash matches the source is
+    returned, a stale hash or an unknown kernel gives None."""
+    import hashlib
+    import json
+    path = os.path.join(bench.ROOT, "profiles", "dram_traffic.json")
+    records = json.load(open(path))["records"]
+    assert {r["kernel"] for r in records} >= {"attn_fwd", "attn_bwd"}
+    for r in records:
+        src = os.path.join(bench.ROOT, "packed_resolution_diffusion_pack_b300", "csrc", r["source"])
+        assert os.path.exists(src)
+        assert len(r["sha16"]) == 16 and int(r["dram_bytes_per_launch"]) > 0
+        assert os.path.exists(os.path.join(bench.ROOT, "profiles", r["summary"]))
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        got = bench._recorded_traffic(r["kernel"])
+        assert got == (int(r["dram_bytes_per_launch"]) if sha == r["sha16"] else None)
     assert bench._recorded_traffic("no_such_kernel") is None
