@@ -605,20 +605,13 @@ def pin_attn_e4m3_exact_limit(so=None):
 
 
 def pin_attn_e4m3_error_bounds(so=None):
-    """Against the exact attention of the un-rounded operands, with rounding on:
-      |dLSE_j| <= delta_j, the largest change of a logit that the operand rounding
-      permits (scale * sum_e |q'_e| bk_e + bq_e |k'_e| + bq_e bk_e, with b the
-      half-quantum bound of each rounded element);
-      |dO_je| <= the sum of three terms: probability rounding
-      (2^-4 e^(2 delta) sum_k P_k |v~_ke| + 2^-10 sum_k |v~_ke| / l_lb, the second
-      for probabilities in E4M3's subnormal range, with l >= l_lb =
-      sum_k exp(z_k - max z - 2 delta) because the running maximum never exceeds
-      the largest rounded logit),
-      V rounding (e^(2 delta) sum_k P_k (2^-4 |v_ke| + 2^-10 sv)) and the
-      softmax's response to the logit change ((e^(2 delta) - 1) sum_k P_k |v_ke|),
-      |v~| <= (1 + 2^-4) |v| + 2^-10 sv.
+    """Against the exact attention of the un-rounded operands, with rounding on,
+    the 8-bit oracle lies within the rigorous per-row bounds of e4m3_bound (LSE
+    within the largest logit change the operand rounding permits; O within the
+    sum of the probability-rounding, V-rounding and softmax-response terms).
     On this data (per-head scales up to 2 on q, k and v) the mean error is about 6 %
     of the mean |O|; the last check allows 10 %."""
+    from e4m3_bound import e4m3_attention_bounds
     rng = _rng(44)
     specs = [(9, 6, 11), (4, 20, 9), (1, 1, 1)]
     scales = [rng.uniform(0.5, 2, 2) for _ in range(3)]
@@ -632,18 +625,8 @@ def pin_attn_e4m3_error_bounds(so=None):
     for i in range(len(specs)):
         s0, s1 = int(cu[i]), int(cu[i + 1])
         for a in range(h):
-            Q, K, V = qr[s0:s1, a], kr[s0:s1, a], v[s0:s1, a]
-            bq = 2.0 ** -4 * np.abs(Q) + 2.0 ** -10 * sq[s0:s1, a][:, None]
-            bk = 2.0 ** -4 * np.abs(K) + 2.0 ** -10 * sk[a]
-            delta = sc * (np.abs(Q) @ bk.T + bq @ np.abs(K).T + bq @ bk.T).max(axis=1)
+            delta, bound = e4m3_attention_bounds(qr[s0:s1, a], kr[s0:s1, a], v[s0:s1, a],
+                                                 sq[s0:s1, a], sk[a], sv[a], sc, l[a, s0:s1])
             assert np.all(np.abs(l8[a, s0:s1] - l[a, s0:s1]) <= delta + 1e-9)
-            z = sc * Q @ K.T
-            P = np.exp(z - l[a, s0:s1][:, None])
-            g = np.exp(2 * delta)[:, None]
-            l_lb = np.exp(z - z.max(axis=1, keepdims=True) - 2 * delta[:, None]).sum(axis=1)
-            vt = (1 + 2.0 ** -4) * np.abs(V) + 2.0 ** -10 * sv[a]
-            bound = (2.0 ** -4 * g * (P @ vt) + 2.0 ** -10 * vt.sum(axis=0)[None, :] / l_lb[:, None]
-                     + g * (P @ (2.0 ** -4 * np.abs(V) + 2.0 ** -10 * sv[a]))
-                     + (g - 1) * (P @ np.abs(V)))
             assert np.all(np.abs(o8[s0:s1, a] - o[s0:s1, a]) <= bound + 1e-12)
     assert np.abs(o8 - o).mean() < 0.1 * np.abs(o).mean()
