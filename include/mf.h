@@ -395,6 +395,24 @@ mf_status mf_gated_residual(const mf_bf16* x, const mf_bf16* h, const int32_t* d
 mf_status mf_get_status(void* ws, mf_stream stream);
 
 /*
+ * Test hook for failure detection (no counterpart on the pages; not for
+ * production use).  Exactly mf_varlen_attn_fwd, except that in every CTA of the
+ * attention kernel the thread that issues the tensor-core work first waits on a
+ * barrier that nothing ever arrives on, for at most stall_us microseconds
+ * (1 .. 1,000,000; else MF_ERR_INVALID_ARG).  That wait runs out, and the kernel
+ * takes its time-out path: the CTA records MF_ERR_TIMEOUT in the workspace, lets
+ * its copies in flight land, frees its tensor memory and exits, so the context
+ * stays usable.  mf_get_status(ws) then returns MF_ERR_TIMEOUT; O and LSE are not
+ * written.  A later call on the same or another workspace runs normally.
+ */
+mf_status mf_test_varlen_attn_fwd_stalled(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                          const int32_t* d_cu_seqlens, const int32_t* d_pos,
+                                          int32_t n, int32_t T, int32_t max_len, int32_t heads,
+                                          int32_t head_dim, float softmax_scale, mf_bf16* o,
+                                          float* lse, void* ws, size_t ws_bytes,
+                                          int32_t stall_us, mf_stream stream);
+
+/*
  * Optional per-kernel timing (instrumentation; no counterpart on the pages).
  * When enabled, every kernel launch made by the calls above is bracketed by two
  * CUDA events recorded on the call's stream (a few microseconds of host work per

@@ -54,6 +54,9 @@ SIGNATURES = {
     "mf_adaln_modulate": (ctypes.c_int, [_p, _p, _i32, _i32, _i32, _p, _p, _f32, _p, _p]),
     "mf_gated_residual": (ctypes.c_int, [_p, _p, _p, _i32, _i32, _i32, _p, _p, _p]),
     "mf_get_status": (ctypes.c_int, [_p, _p]),
+    "mf_test_varlen_attn_fwd_stalled": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32,
+                                                       _i32, _i32, _f32, _p, _p, _p, _sz, _i32,
+                                                       _p]),
     "mf_timing_enable": (ctypes.c_int, [_i32]),
     "mf_timing_reset": (ctypes.c_int, []),
     "mf_timing_read": (ctypes.c_int, [_i32, _p, _p]),

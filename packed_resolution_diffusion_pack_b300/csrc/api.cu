@@ -167,7 +167,8 @@ static mf_status attn_fwd_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16
                                const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t naxes,
                                int32_t n, int32_t T, int32_t max_len, int32_t heads,
                                int32_t head_dim, float softmax_scale, mf_bf16* o, float* lse,
-                               void* ws, size_t ws_bytes, mf_stream stream) {
+                               void* ws, size_t ws_bytes, mf_stream stream,
+                               uint32_t stall_us = 0) {
   const void* ptrs[5] = {q, k, v, o, lse};
   mf_status st = check_attn(ptrs, 5, d_cu_seqlens, n, T, max_len, heads, head_dim, ws, ws_bytes,
                             false);
@@ -205,6 +206,7 @@ static mf_status attn_fwd_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16
   a.heads = heads;
   a.head_dim = head_dim;
   a.scale = scale;
+  a.stall_us = stall_us;
   return cuda_status(launch_attn_fwd(a, s));
 }
 
@@ -334,6 +336,18 @@ mf_status mf_varlen_attn_fwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
                              size_t ws_bytes, mf_stream stream) {
   return attn_fwd_impl(q, k, v, d_cu_seqlens, d_pos, 2, n, T, max_len, heads, head_dim,
                        softmax_scale, o, lse, ws, ws_bytes, stream);
+}
+
+mf_status mf_test_varlen_attn_fwd_stalled(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                          const int32_t* d_cu_seqlens, const int32_t* d_pos,
+                                          int32_t n, int32_t T, int32_t max_len, int32_t heads,
+                                          int32_t head_dim, float softmax_scale, mf_bf16* o,
+                                          float* lse, void* ws, size_t ws_bytes,
+                                          int32_t stall_us, mf_stream stream) {
+  if (stall_us < 1 || stall_us > 1000000) return MF_ERR_INVALID_ARG;
+  return attn_fwd_impl(q, k, v, d_cu_seqlens, d_pos, 2, n, T, max_len, heads, head_dim,
+                       softmax_scale, o, lse, ws, ws_bytes, stream,
+                       static_cast<uint32_t>(stall_us));
 }
 
 mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,

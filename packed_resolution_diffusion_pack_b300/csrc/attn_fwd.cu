@@ -275,6 +275,10 @@ struct FwdParams {
   const uint32_t* amax2;  // 8-bit variant: [2][heads] squared K pair-norm / V maxima
   int32_t n, T, heads;
   float scale_log2;
+  // test hook (0 = off): the MMA thread first waits, at most this many
+  // microseconds, on a barrier that nothing arrives on, so the CTA takes its
+  // time-out path (failure-detection tests; never set by the product calls)
+  uint32_t stall_us;
 };
 
 template <int D, bool F8>
@@ -307,6 +311,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t bar_p = bar_s + 16;                      // [2]
   const uint32_t bar_o = bar_p + 16;                      // [2]
   const uint32_t bar_drain = bar_o + 16;
+  const uint32_t bar_stall = bar_drain + 8;  // test hook: never arrived on
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -326,6 +331,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(bar_o, 1);
       mbar_init(bar_o + 8, 1);
       mbar_init(bar_drain, 1);
+      mbar_init(bar_stall, 1);
       fence_mbar_init();
     }
   }
@@ -387,7 +393,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     } else if (warp == 9) {
       // -------------------------------------------------------------- MMA issuer
       if (lane == 0) {
-        bool ok = mbar_wait(bar_q, 0, &s_abort);
+        bool ok = p.stall_us == 0 ||
+                  mbar_wait_for(bar_stall, 0, &s_abort, static_cast<uint64_t>(p.stall_us) * 1000u);
+        ok = ok && mbar_wait(bar_q, 0, &s_abort);
         tc_fence_after();
         auto kv_wait = [&](int32_t c) -> bool {
           const bool r = mbar_wait(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1, &s_abort);
@@ -688,6 +696,7 @@ static cudaError_t launch_fwd_d(const AttnFwdArgs& a, cudaStream_t s) {
   p.T = a.T;
   p.heads = a.heads;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.stall_us = a.stall_us;
   const int64_t blocks = (static_cast<int64_t>(a.T + 2 * C::BM - 1) / (2 * C::BM) + a.n) * a.heads;
   if (blocks <= 0) return cudaSuccess;
   {

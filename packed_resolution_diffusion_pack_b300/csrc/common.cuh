@@ -161,6 +161,7 @@ struct AttnFwdArgs {
   float* lse;
   int32_t n, T, heads, head_dim;
   float scale;
+  uint32_t stall_us = 0;  // test hook: see mf_test_varlen_attn_fwd_stalled
 };
 cudaError_t launch_attn_fwd(const AttnFwdArgs& a, cudaStream_t s);
 

@@ -103,10 +103,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (and
-// never blocks longer than kWaitLimitNs) if it does not, or if *abort becomes
-// non-zero meanwhile (another role of the CTA gave up).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          const volatile uint32_t* abort) {
+// never blocks longer than limit_ns, kWaitLimitNs for mbar_wait) if it does not,
+// or if *abort becomes non-zero meanwhile (another role of the CTA gave up).
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity,
+                                              const volatile uint32_t* abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
@@ -114,8 +114,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          const volatile uint32_t* abort) {
+  return mbar_wait_for(bar, parity, abort, kWaitLimitNs);
 }
 
 // Drain wait used while a CTA shuts down after giving up: waits for a phase
