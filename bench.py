@@ -421,12 +421,16 @@ def gpu_arm(args):
                  "load)" if full_clock else "sustained (cuBLAS, seconds-long loop)"))
     # algorithmic work per launch: FLOPs for the attention kernels, bytes for the
     # memory-bound ones (rope: the forward's pre-pass reads q, k, v bf16 and writes
-    # Q', K', V' fp16; the backward reuses them)
+    # Q', K', V' fp16; the backward reuses them).  The backward's five GEMMs of
+    # 4 sum(L^2) d h FLOP / 2 each: the dK/dV kernel ("attn_bwd") runs four of them
+    # (S^T, dP^T, dV, dK: 0.8 of the backward's FLOPs); the dQ kernel
+    # ("attn_bwd_q") runs the fifth (dQ: 0.2) and recomputes S and dP (0.4 more,
+    # executed but not credited).
     elems = float(T * h * d)
-    algo = {"attn_fwd": ("tensor", flops_fwd), "attn_bwd": ("tensor", flops_bwd),
+    algo = {"attn_fwd": ("tensor", flops_fwd), "attn_bwd": ("tensor", 0.8 * flops_bwd),
+            "attn_bwd_q": ("tensor", 0.2 * flops_bwd),
             "rope": ("hbm", 12.0 * elems + 8.0 * T),
-            "bwd_pre": ("hbm", 10.0 * elems + 4.0 * h * T),
-            "dq_post": ("hbm", 6.0 * elems + 8.0 * T)}
+            "bwd_pre": ("hbm", 6.0 * elems + 12.0 * h * T)}
     for name, (bound, amount) in algo.items():
         if name in per_launch:
             pl = per_launch[name]
@@ -434,18 +438,22 @@ def gpu_arm(args):
                 ach = amount / (pl["ms_per_launch"] / 1e3) / 1e12
                 pl.update(achieved_tflops=ach, frac=ach / peak_tc,
                           frac_of_sustained=ach / pk["bf16_sustained"],
-                          frac_of_burst=ach / pk["bf16_burst"])
+                          frac_of_burst=ach / pk["bf16_burst"],
+                          frac_of_nominal=ach / NOMINAL_BF16_TFLOPS)
+                if name == "attn_bwd_q":  # S, dP and dQ executed
+                    pl["executed_tflops"] = 3.0 * ach
             else:
                 ach = amount / (pl["ms_per_launch"] / 1e3) / 1e9
                 pl.update(achieved_gbs=ach, frac_of_hbm=ach / pk["hbm_gbs"])
-    dom = max(("attn_fwd", "attn_bwd"), key=lambda nm: kern[nm][0])
+    dom = max(("attn_fwd", "attn_bwd", "attn_bwd_q"), key=lambda nm: kern[nm][0])
     traffic = _recorded_traffic(dom)
     ach = per_launch[dom]["achieved_tflops"]
     roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_tc,
                 "unit": "TFLOP/s", "frac": ach / peak_tc, "traffic": traffic,
                 "peak_kind": peak_name, "frac_of_nominal": ach / NOMINAL_BF16_TFLOPS}
     fwd_ms = per_launch["attn_fwd"]["ms_per_launch"]
-    bwd_ms = per_launch["attn_bwd"]["ms_per_launch"]
+    # the backward's attention: the dK/dV kernel and the dQ kernel
+    bwd_ms = per_launch["attn_bwd"]["ms_per_launch"] + per_launch["attn_bwd_q"]["ms_per_launch"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,

@@ -155,7 +155,7 @@ mf_status mf_varlen_attn_fwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
  * from the forward.  Other arguments as in the forward.
  * dq, dk, dv: DEVICE bf16 [T][heads][head_dim] out.
  * ws / ws_bytes: workspace from mf_attn_workspace_bytes(T, n, heads, head_dim, 1)
- * (holds the rotated Q/K, D = rowsum(dO * O) and the fp32 dQ accumulator).
+ * (holds the rotated Q/K and D = rowsum(dO * O)).
  * Per sample and head: P = exp(S - LSE), dV = P^T dO, dP = dO V^T,
  * dS = P * (dP - D), dQ = R(-theta) scale dS K', dK = R(-theta) scale dS^T Q'.
  * Defined by: the training step of the rcap.io listing (loss.backward through the
@@ -179,8 +179,7 @@ mf_status mf_varlen_attn_bwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
  * forward) was last used by the forward of these q, k, d_pos, n, T, heads and
  * head_dim on the same stream, and neither q nor k changed since.  The fp16 range
  * check of Q' and K' is then the forward's: read it with mf_get_status after the
- * forward.  Results equal mf_varlen_attn_bwd's (dQ up to its atomic summation
- * order).  No counterpart on the pages: a workspace-sharing form of the backward.
+ * forward.  Results equal mf_varlen_attn_bwd's.  No counterpart on the pages: a workspace-sharing form of the backward.
  */
 mf_status mf_varlen_attn_bwd_after_fwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
                                        const mf_bf16* o, const float* lse, const mf_bf16* d_o,
@@ -411,6 +410,17 @@ mf_status mf_test_varlen_attn_fwd_stalled(const mf_bf16* q, const mf_bf16* k, co
                                           int32_t head_dim, float softmax_scale, mf_bf16* o,
                                           float* lse, void* ws, size_t ws_bytes,
                                           int32_t stall_us, mf_stream stream);
+/* The same hook in the backward's attention kernel: exactly mf_varlen_attn_bwd,
+ * except that its MMA-issuing thread first waits, at most stall_us microseconds,
+ * on a barrier that nothing arrives on.  mf_get_status(ws) then returns
+ * MF_ERR_TIMEOUT; dQ, dK and dV are not written.  A later call runs normally. */
+mf_status mf_test_varlen_attn_bwd_stalled(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                          const mf_bf16* o, const float* lse, const mf_bf16* d_o,
+                                          const int32_t* d_cu_seqlens, const int32_t* d_pos,
+                                          int32_t n, int32_t T, int32_t max_len, int32_t heads,
+                                          int32_t head_dim, float softmax_scale, mf_bf16* dq,
+                                          mf_bf16* dk, mf_bf16* dv, void* ws, size_t ws_bytes,
+                                          int32_t stall_us, mf_stream stream);
 
 /*
  * Optional per-kernel timing (instrumentation; no counterpart on the pages).
@@ -420,12 +430,12 @@ mf_status mf_test_varlen_attn_fwd_stalled(const mf_bf16* q, const mf_bf16* k, co
  * the recorded events and returns, for kernel `id`, the summed device time in
  * milliseconds and the number of launches since the last reset.  Ids:
  *   MF_K_PACK 0, MF_K_ROPE 1, MF_K_SCHEDULE 2, MF_K_ATTN_FWD 3, MF_K_BWD_PRE 4,
- *   MF_K_ATTN_BWD 5, MF_K_DQ_POST 6, MF_K_CFG_EULER 7, MF_K_ADALN 8,
+ *   MF_K_ATTN_BWD 5 (dK, dV), MF_K_ATTN_BWD_Q 6 (dQ), MF_K_CFG_EULER 7, MF_K_ADALN 8,
  *   MF_K_GATED_RESIDUAL 9, MF_K_F8_AMAX 10, MF_K_F8_QUANT 11, MF_K_ATTN_FWD_F8 12.
  * Process-wide state guarded by a mutex; not for use under stream capture.
  */
 enum { MF_K_PACK = 0, MF_K_ROPE, MF_K_SCHEDULE, MF_K_ATTN_FWD, MF_K_BWD_PRE, MF_K_ATTN_BWD,
-       MF_K_DQ_POST, MF_K_CFG_EULER, MF_K_ADALN, MF_K_GATED_RESIDUAL, MF_K_F8_AMAX,
+       MF_K_ATTN_BWD_Q, MF_K_CFG_EULER, MF_K_ADALN, MF_K_GATED_RESIDUAL, MF_K_F8_AMAX,
        MF_K_F8_QUANT, MF_K_ATTN_FWD_F8, MF_K_COUNT };
 mf_status mf_timing_enable(int32_t on);
 mf_status mf_timing_reset(void);

@@ -57,13 +57,16 @@ SIGNATURES = {
     "mf_test_varlen_attn_fwd_stalled": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32,
                                                        _i32, _i32, _f32, _p, _p, _p, _sz, _i32,
                                                        _p]),
+    "mf_test_varlen_attn_bwd_stalled": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _i32,
+                                                       _i32, _i32, _i32, _i32, _f32, _p, _p, _p,
+                                                       _p, _sz, _i32, _p]),
     "mf_timing_enable": (ctypes.c_int, [_i32]),
     "mf_timing_reset": (ctypes.c_int, []),
     "mf_timing_read": (ctypes.c_int, [_i32, _p, _p]),
 }
 
 # kernel ids of the opt-in timing (mf.h MF_K_*)
-KERNELS = ["pack", "rope", "schedule", "attn_fwd", "bwd_pre", "attn_bwd", "dq_post", "cfg_euler",
+KERNELS = ["pack", "rope", "schedule", "attn_fwd", "bwd_pre", "attn_bwd", "attn_bwd_q", "cfg_euler",
            "adaln", "gated_residual", "f8_amax", "f8_quant", "attn_fwd_f8"]
 
 

@@ -48,15 +48,20 @@ WsLayout ws_layout(int64_t T, int64_t n, int64_t heads, int64_t head_dim, bool b
     L.hmax = off;
     off = align_up(off + 8 * static_cast<size_t>(heads), 256);
     L.pad = off;
-    off = align_up(off + 4 * 128, 1024);
+    off = align_up(off + 4 * 256, 1024);
     L.nlse2 = off;
     off = align_up(off + 4 * static_cast<size_t>(heads) * T, 1024);
     L.delta = off;
     off = align_up(off + 4 * static_cast<size_t>(heads) * T, 1024);
-    L.dq_acc = off;
-    off = align_up(off + 4 * elems, 1024);
   }
   L.total = off;
+  // a backward workspace also serves the forward of the same call sizes (the
+  // training step shares one: mf_varlen_attn_bwd_after_fwd), so it is never
+  // smaller than the forward's
+  if (bwd) {
+    const size_t fwd_total = ws_layout(T, n, heads, head_dim, false).total;
+    if (fwd_total > L.total) L.total = fwd_total;
+  }
   return L;
 }
 
@@ -270,7 +275,7 @@ static mf_status attn_bwd_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16
                                int32_t n, int32_t T, int32_t max_len, int32_t heads,
                                int32_t head_dim, float softmax_scale, mf_bf16* dq, mf_bf16* dk,
                                mf_bf16* dv, void* ws, size_t ws_bytes, mf_stream stream,
-                               bool reuse_rotated = false) {
+                               bool reuse_rotated = false, uint32_t stall_us = 0) {
   const void* ptrs[9] = {q, k, v, o, lse, d_o, dq, dk, dv};
   mf_status st = check_attn(ptrs, 9, d_cu_seqlens, n, T, max_len, heads, head_dim, ws, ws_bytes,
                             true);
@@ -313,7 +318,6 @@ static mf_status attn_bwd_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16
   a.pad = reinterpret_cast<float*>(w + L.pad);
   a.nlse2 = reinterpret_cast<float*>(w + L.nlse2);
   a.delta = reinterpret_cast<float*>(w + L.delta);
-  a.dq_acc = reinterpret_cast<float*>(w + L.dq_acc);
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
@@ -322,6 +326,7 @@ static mf_status attn_bwd_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16
   a.heads = heads;
   a.head_dim = head_dim;
   a.scale = scale;
+  a.stall_us = stall_us;
   return cuda_status(launch_attn_bwd(a, s));
 }
 
@@ -347,6 +352,19 @@ mf_status mf_test_varlen_attn_fwd_stalled(const mf_bf16* q, const mf_bf16* k, co
   if (stall_us < 1 || stall_us > 1000000) return MF_ERR_INVALID_ARG;
   return attn_fwd_impl(q, k, v, d_cu_seqlens, d_pos, 2, n, T, max_len, heads, head_dim,
                        softmax_scale, o, lse, ws, ws_bytes, stream,
+                       static_cast<uint32_t>(stall_us));
+}
+
+mf_status mf_test_varlen_attn_bwd_stalled(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                          const mf_bf16* o, const float* lse, const mf_bf16* d_o,
+                                          const int32_t* d_cu_seqlens, const int32_t* d_pos,
+                                          int32_t n, int32_t T, int32_t max_len, int32_t heads,
+                                          int32_t head_dim, float softmax_scale, mf_bf16* dq,
+                                          mf_bf16* dk, mf_bf16* dv, void* ws, size_t ws_bytes,
+                                          int32_t stall_us, mf_stream stream) {
+  if (stall_us < 1 || stall_us > 1000000) return MF_ERR_INVALID_ARG;
+  return attn_bwd_impl(q, k, v, o, lse, d_o, d_cu_seqlens, d_pos, 2, n, T, max_len, heads,
+                       head_dim, softmax_scale, dq, dk, dv, ws, ws_bytes, stream, false,
                        static_cast<uint32_t>(stall_us));
 }
 

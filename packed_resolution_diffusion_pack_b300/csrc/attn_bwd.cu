@@ -8,22 +8,10 @@
 //   dQ = R(-theta) dQ',  dK = R(-theta) dK'   (R orthogonal, R^T = R(-theta)).
 //
 // Kernels:
-//   bwd_pre_kernel   D = rowsum(dO o O) in fp32 ([h][T]); zeroes the fp32 dQ
-//                    accumulator rows.
-//   attn_bwd_kernel  one CTA = one sample, one head, one 128-key tile (K_j, V_j
-//                    resident in smem); loops over the sample's 128-row Q tiles:
-//       warp 8     TMA: K, V once; (Q_i, dO_i) through a 2-stage ring.
-//       warp 9     MMA (one thread): S^T = K Q_i^T, dP^T = V dO_i^T (SS);
-//                  dV += P^T dO_i (P^T from TMEM, TS); dK += dS^T Q_i and
-//                  dQ_i = dS K (SS, dS^T staged in smem, read K- and MN-major).
-//       warps 0-3  thread = key row: P^T = exp2(S^T scale log2e - LSE log2e),
-//                  P^T -> TMEM (bf16), dS^T = P^T (dP^T - D) -> smem (bf16);
-//                  epilogue dV -> bf16, dK -> scale, R(-theta), bf16.
-//       warps 4-7  thread = query row: dQ_i from TMEM, scaled, added into the
-//                  fp32 accumulator with vector atomics.
-//   dq_post_kernel   dQ = R(-theta) dq_acc -> bf16.
-// TMEM: S^T [0,128) (P^T bf16 over its first 64 columns), dP^T [128,256) reused
-// for dQ_i, dV [256,256+D), dK [256+D,256+2D).
+//   bwd_pre_kernel      D = rowsum(dO o O) and -LSE log2 e in fp32 ([h][T]);
+//                       per-head maxima of ||dO|| and ||v||.
+//   attn_bwd_kv_kernel  dK, dV: one CTA per sample, head and 128-key tile.
+//   attn_bwd_q_kernel   dQ: one CTA per sample, head and 128-query tile.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -65,11 +53,11 @@ __device__ __forceinline__ bool find_item_b(const int32_t* __restrict__ cu,
 
 // ------------------------------------------------------------- preprocess
 // Rows are (token, head) pairs in THD order; 8 lanes per row, each covering D/8
-// elements.  Per row: D = <dO, O> -> delta[h][t]; -LSE * log2 e -> nlse2[h][t]; the
-// row of the fp32 dQ accumulator zeroed; ||dO|| and ||v|| folded into per-head
+// elements.  Per row: D = <dO, O> -> delta[h][t]; -LSE * log2 e -> nlse2[h][t];
+// ||dO|| and ||v|| folded into per-head
 // maxima (shared memory per block, then one atomicMax per head: non-negative
 // floats order like their bit patterns).  Block 0 also writes the pad rows
-// (64 x -inf as -LSE log2 e, 64 x 0 as D) that stand in for query rows past a
+// (128 x -inf as -LSE log2 e, 128 x 0 as D) that stand in for query rows past a
 // sample (they make P = 0 there).
 constexpr int kPreRowsPerBlock = 512;
 constexpr int kPreMaxHeads = 256;
@@ -91,14 +79,13 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
                                                       float* __restrict__ nlse2,
                                                       float* __restrict__ delta,
                                                       float* __restrict__ pad,
-                                                      float4* __restrict__ dq_acc,
                                                       float* __restrict__ hmax, int64_t rows,
                                                       int32_t T, int32_t heads) {
   constexpr int V = D / 64;  // uint4 (8 bf16) per lane
   __shared__ float s_max[2 * kPreMaxHeads];
   const bool smem_max = heads <= kPreMaxHeads;
   for (int i = threadIdx.x; i < 2 * kPreMaxHeads; i += blockDim.x) s_max[i] = 0.f;
-  if (blockIdx.x == 0 && threadIdx.x < 128) pad[threadIdx.x] = threadIdx.x < 64 ? -INFINITY : 0.f;
+  if (blockIdx.x == 0) pad[threadIdx.x] = threadIdx.x < 128 ? -INFINITY : 0.f;  // 256 threads
   __syncthreads();
   const int sub = threadIdx.x & 7;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kPreRowsPerBlock;
@@ -115,9 +102,6 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
         bf16x8_dot(b, b, ndo);
         bf16x8_dot(c, c, nv);
       }
-#pragma unroll
-      for (int u = 0; u < 2 * V; ++u)
-        dq_acc[row * (D / 4) + sub * 2 * V + u] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int m = 1; m < 8; m <<= 1) {
@@ -152,106 +136,73 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
   }
 }
 
-// --------------------------------------------------------- dQ post-process
-// dq[t][a][:] = R(-theta(pos_t)) dq_acc[t][a][:] (a plain cast without pos).  One
-// block handles kPostTok tokens: their (cos, sin) per rotary pair are formed once
-// in shared memory and shared by all heads; then 16-byte fp32 chunks (2 pairs) of
-// every head stream through it.
-constexpr int kPostTok = 4;
-
-template <int D>
-__global__ void __launch_bounds__(256) dq_post_kernel(const float4* __restrict__ acc,
-                                                      uint2* __restrict__ dq,
-                                                      const int32_t* __restrict__ pos, int32_t T,
-                                                      int32_t heads,
-                                                      const __grid_constant__ RopeFreqs f) {
-  constexpr int NP = D / 2;
-  __shared__ float2 cs[kPostTok][NP];
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kPostTok;
-  for (int i = threadIdx.x; i < kPostTok * NP; i += blockDim.x) {
-    const int tt = i / NP, P = i % NP;
-    float c = 1.f, sn = 0.f;
-    if (t0 + tt < T && pos != nullptr) {
-      const float pp = static_cast<float>(pos[(t0 + tt) * f.naxes + f.axis[P]]);
-      rope_sincos(pp, f.omega[P], f.omega_lo[P], -1.f, &sn, &c);
-    }
-    cs[tt][P] = make_float2(c, sn);
-  }
-  __syncthreads();
-  constexpr int CPR = D / 4;  // float4 chunks per head vector
-  const int per_tok = heads * CPR;
-  const int ntok = static_cast<int>(T - t0 < kPostTok ? T - t0 : kPostTok);
-  for (int i = threadIdx.x; i < ntok * per_tok; i += blockDim.x) {
-    const int tt = i / per_tok, ch = i % per_tok;
-    const int64_t idx = (t0 + tt) * per_tok + ch;
-    const float4 x = acc[idx];
-    const int P0 = (ch % CPR) * 2;
-    const float2 r0 = cs[tt][P0], r1 = cs[tt][P0 + 1];
-    dq[idx] = make_uint2(pack_bf16x2(fmaf(x.x, r0.x, -x.y * r0.y), fmaf(x.x, r0.y, x.y * r0.x)),
-                         pack_bf16x2(fmaf(x.z, r1.x, -x.w * r1.y), fmaf(x.z, r1.y, x.w * r1.x)));
-  }
-}
-
-// --------------------------------------------------------------- main kernel
-// One CTA = one sample, one head, one 128-key tile (K', V resident in smem); it
-// walks the sample's queries in 64-row tiles i.  Per tile (b = i % 2):
-//   S^T_i  = K' Q'_i^T        M=128 keys, N=64, K=d   SS fp16   -> TMEM ST[b]
-//   dP^T_i = V dO_i^T         M=128 keys, N=64, K=d   SS bf16   -> TMEM DPT
-//   P^T_i  = exp2(S^T scale log2e - LSE log2e) (bf16 -> ST[b] columns [0,32))
-//            (the preprocess stores -LSE log2e, so this is one packed FMA per pair)
-//   dS^T_i = P^T (dP^T - D) * ds_mul           (fp16 -> smem DS[b])
-//   dV    += P^T_i dO_i       M=128 keys, N=d, K=64   TS bf16
-//   dK    += dS^T_i Q'_i      M=128 keys, N=d, K=64   SS fp16
-//   dQ^T_i = K'^T dS^T_i      M=128 (d),  N=64, K=128 SS fp16   -> TMEM DQT
-// dQ is produced transposed (TMEM lane = head-dim index, column = query): the
-// warps that drain it write a [query][d] fp32 tile to shared memory with
-// conflict-free stores, and one thread adds the tile into the fp32 accumulator
-// with a TMA reduce-add (rows past the sample are zero, so they add nothing).
-// S^T is double-buffered; the (Q', dO) stage of tile i is released as soon as
-// dV_i and dK_i (its last readers) are issued, and dP^T_{i+1} and S^T_{i+2} are
-// issued ahead of the GEMMs that need the P/dS warpgroup, so that warpgroup's
-// exp/dS work overlaps the tensor core.
-//   warp 8     TMA: K', V once; (Q'_i, dO_i) through an NST-stage ring; the
-//              lanes copy the tile's -LSE * log2 e and D rows beside them with
-//              cp.async (pad rows past the sample), all on the stage barrier.
-//   warp 9     MMA issuer (one thread).
-//   warps 0-3  thread = key row: P^T, dS^T; epilogue dV, dK (scale, R(-theta)).
-//   warps 4-7  thread = head-dim row of dQ^T: smem tile + TMA reduce-add.
-// At d = 64 the dQ^T GEMM is padded to M = 128 with a zero smem chunk (its rows
-// 64-127 are ignored).
+// ------------------------------------------------------------ main kernels
+// The backward runs as two kernels that need no atomics: each output row is
+// written by exactly one CTA.
+//  attn_bwd_kv_kernel  one CTA = one sample, one head, one 128-key tile (K', V
+//    resident): over the sample's 128-row query tiles i it accumulates
+//      S^T_i  = K' Q'_i^T      M=128 keys, N=128, K=d    SS fp16  -> TMEM ST
+//      P^T_i  = exp2(S^T scale log2e - LSE log2e)  (bf16, back into ST)
+//      dP^T_i = V dO_i^T       M=128 keys, N=128, K=d    SS bf16  -> TMEM DPT
+//      dS^T_i = P^T (dP^T - D) * ds_mul            (fp16, back into DPT)
+//      dV    += P^T_i dO_i     M=128 keys, N=d,   K=128  TS bf16 (P^T from TMEM)
+//      dK    += dS^T_i Q'_i    M=128 keys, N=d,   K=128  TS fp16 (dS^T from TMEM)
+//    and writes dV and R(-theta) scale dK / ds_mul.
+//  attn_bwd_q_kernel   one CTA = one sample, one head, one 128-query tile (Q',
+//    dO resident): over the sample's 128-key tiles j it recomputes
+//      S_j  = Q' K'_j^T        M=128 queries, N=128, K=d  SS fp16  -> TMEM S[j % 2]
+//      dP_j = dO V_j^T         M=128 queries, N=128, K=d  SS bf16  -> TMEM DP
+//      dS_j = P (dP - D) * ds_mul, P = exp2(S scale log2e - LSE log2e)
+//                              (fp16, back into S[j % 2])
+//      dQ  += dS_j K'_j        M=128 queries, N=d, K=128  TS fp16 (dS from TMEM)
+//    and writes dQ = R(-theta) scale dQ' / ds_mul in bf16.
+// Splitting the work this way recomputes S and dP for dQ (7 GEMMs instead of
+// 5), but a single kernel would have to add every key tile's dQ contribution
+// into a global fp32 accumulator, and those additions (one fp32 add per key
+// tile, query and head-dim element, 15 GB at the 50k pack) are limited by the L2
+// reduction throughput (about 2.4 TB/s measured, with both bulk tensor
+// reduce-adds and per-element reductions): slower than the extra GEMMs.
+// Both kernels: warps 0-7 are two elementwise warpgroups, each covering 64 of the
+// 128 columns of a tile (thread = TMEM lane = the tile's row); warp 8 issues TMA;
+// warp 9 is the single MMA-issuing thread; warps 10-11 idle.  Every GEMM runs at
+// N = 128 or N = d.
 template <int D>
 struct BwdCfg {
-  static constexpr int BK = 128;                // keys per CTA
-  static constexpr int BQ = 64;                 // queries per tile
-  static constexpr int NST = 3;                 // (Q', dO) stages
-  static constexpr int KCHUNK = 128 * 128;      // 64-column chunk of a 128-row tile
-  static constexpr int QCHUNK = 64 * 128;       // 64-column chunk of a 64-row tile
-  static constexpr int KTILE = 128 * D * 2;     // K' or V tile
-  static constexpr int QTILE = 64 * D * 2;      // Q' or dO tile
-  static constexpr int DSTILE = 128 * 64 * 2;   // dS^T tile (one chunk)
-  static constexpr int DQTILE = BQ * D * 4;     // fp32 dQ staging tile [query][d]
-  static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = KTILE;
-  static constexpr int OFF_Z = 2 * KTILE;                         // zero chunk (d = 64)
-  static constexpr int OFF_Q = OFF_Z + (D == 64 ? KCHUNK : 0);    // [NST]
-  static constexpr int OFF_DO = OFF_Q + NST * QTILE;              // [NST]
-  static constexpr int OFF_DS = OFF_DO + NST * QTILE;             // [2]
-  static constexpr int OFF_DQ = OFF_DS + 2 * DSTILE;
-  static constexpr int OFF_VEC = OFF_DQ + DQTILE;                 // [NST] x (-LSE log2e, D) x 64
-  static constexpr int OFF_BAR = OFF_VEC + NST * 512;
-  static constexpr int OFF_MISC = OFF_BAR + 256;
-  static constexpr int SMEM = OFF_MISC + 64;
-  static constexpr uint32_t COL_ST0 = 0, COL_ST1 = 64, COL_DPT = 128, COL_DQT = 192;
-  static constexpr uint32_t COL_DV = 256, COL_DK = 256 + D;
+  static constexpr int BK = 128, BQ = 128;      // keys / queries per tile
+  static constexpr int CHUNK = 128 * 128;       // 64-column (128-byte) chunk of a 128-row tile
+  static constexpr int TILE = 128 * D * 2;      // any 128-row 16-bit operand tile
+  static constexpr int VEC = 2 * BQ * 4;        // per stage: -LSE log2 e, D of BQ queries
+  // kv kernel: K', V resident; (Q'_i, dO_i) through NST stages
+  static constexpr int NST = D == 128 ? 2 : 3;
+  static constexpr int KV_OFF_K = 0, KV_OFF_V = TILE, KV_OFF_Q = 2 * TILE;
+  static constexpr int KV_OFF_DO = KV_OFF_Q + NST * TILE;
+  static constexpr int KV_OFF_VEC = KV_OFF_DO + NST * TILE;
+  static constexpr int KV_OFF_BAR = KV_OFF_VEC + NST * VEC;
+  static constexpr int KV_OFF_MISC = KV_OFF_BAR + 256;
+  static constexpr int KV_SMEM = KV_OFF_MISC + 64;
+  // q kernel: Q', dO resident; K'_j, V_j through a ring of NSLOT tiles
+  static constexpr int NSLOT = D == 128 ? 5 : 10;
+  static constexpr int Q_OFF_Q = 0, Q_OFF_DO = TILE, Q_OFF_KV = 2 * TILE;
+  static constexpr int Q_OFF_BAR = Q_OFF_KV + NSLOT * TILE;
+  static constexpr int Q_OFF_MISC = Q_OFF_BAR + 256;
+  static constexpr int Q_SMEM = Q_OFF_MISC + 64;
+  // TMEM columns
+  static constexpr uint32_t KV_ST = 0, KV_DPT = 128, KV_DV = 256, KV_DK = 256 + D;
+  static constexpr uint32_t Q_S0 = 0, Q_DP = 256, Q_DQ = 384;
   // fp16 where Q', K' and the scaled dS meet; bf16 where the caller's V and dO do
   // (gradient-sized values keep bf16's range there).
-  static constexpr uint32_t IDESC_S = idesc_f32acc(128, 64, kF16, 0, 0);     // S^T
-  static constexpr uint32_t IDESC_DP = idesc_f32acc(128, 64, kBF16, 0, 0);   // dP^T
-  static constexpr uint32_t IDESC_DV = idesc_f32acc(128, D, kBF16, 0, 1);    // dV
-  static constexpr uint32_t IDESC_DK = idesc_f32acc(128, D, kF16, 0, 1);     // dK
-  static constexpr uint32_t IDESC_DQ = idesc_f32acc(128, 64, kF16, 1, 1);    // dQ^T
+  static constexpr uint32_t IDESC_S = idesc_f32acc(128, 128, kF16, 0, 0);   // S^T and S
+  static constexpr uint32_t IDESC_DP = idesc_f32acc(128, 128, kBF16, 0, 0); // dP^T and dP
+  static constexpr uint32_t IDESC_DV = idesc_f32acc(128, D, kBF16, 0, 1);   // dV (TS)
+  static constexpr uint32_t IDESC_DKQ = idesc_f32acc(128, D, kF16, 0, 1);   // dK, dQ (TS)
+  static_assert(KV_OFF_Q % 1024 == 0 && KV_OFF_DO % 1024 == 0 && Q_OFF_KV % 1024 == 0,
+                "swizzled tiles start on 1024-byte boundaries");
+  static_assert(KV_SMEM <= 232448 && Q_SMEM <= 232448, "shared memory over the per-CTA limit");
+  static_assert(8 + 16 * (NST > NSLOT ? NST : NSLOT) + 8 * 8 <= 256, "barrier area");
 };
-static_assert(BwdCfg<128>::SMEM <= 232448, "backward shared memory over the per-CTA limit");
+
+// 384 threads: 170 registers each at launch (65,536 / 384), no reallocation.
+constexpr int kBwdThreads = 384;
 
 struct BwdParams {
   const int32_t* cu;
@@ -262,6 +213,7 @@ struct BwdParams {
   const float* delta;
   const float* pad;
   uint32_t* status;
+  __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int32_t n, T, heads;
@@ -271,6 +223,9 @@ struct BwdParams {
   // |dS| <= |dP| + |D| <= 2 max||dO|| max||v||, which sets the power-of-two
   // scale under which dS is staged in fp16 (undone in the dK / dQ epilogues)
   const float* hmax;
+  // test hook (0 = off): the MMA thread first waits, at most this many
+  // microseconds, on a barrier that nothing arrives on (failure-detection tests)
+  uint32_t stall_us;
 };
 
 // 2^e with e = floor(log2(2^15 / bound)) clamped to [-64, 64]: scaled |dS| stays
@@ -283,20 +238,95 @@ __device__ __forceinline__ float ds_scale_for(float max_do, float max_v) {
   return exp2f(static_cast<float>(e));
 }
 
+// MMA-operand offsets in a 128B-swizzled tile, in the 16-byte units of a
+// descriptor's start-address field.  K-major operand: K-step kk of 16 elements
+// is 32 bytes into the 128-byte rows, the next 64-column chunk every 4 steps.
 template <int D>
-__global__ void __launch_bounds__(320, 1)
-    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
-                    const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+__device__ __forceinline__ uint64_t kofs(int kk) {
+  return ((kk >> 2) * BwdCfg<D>::CHUNK + (kk & 3) * 32) >> 4;
+}
+// MN-major operand: K-step kk of 16 rows of 128 bytes.
+__device__ __forceinline__ uint64_t mofs(int kk) { return (kk * 2048) >> 4; }
+
+// TMEM column of K-step kk (16 elements = 8 columns) of a 16-bit operand that the
+// two elementwise warpgroups packed into columns [0, 32) and [64, 96) of a
+// 128-column region (warpgroup h holds elements [64h, 64h + 64)).
+__device__ __forceinline__ uint32_t packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
+
+// 64 values v (two per 64-bit lane pair) of a row times dk_mul, rotated by R(-theta)
+// at the row's position coordinates (pv) when rotating, converted to bf16 and put
+// into a [128 rows][D] staging tile with 16-byte units XOR-swizzled by row.
+template <int D>
+__device__ __forceinline__ void stage_rotated_row(uint8_t* base, uint32_t row, int cc,
+                                                  const uint32_t (&r)[32], float mul,
+                                                  bool rotate, const float (&pv)[3],
+                                                  const RopeFreqs& f) {
+  constexpr int UNITS = D / 8;
+  float v[32];
+#pragma unroll
+  for (int u = 0; u < 32; ++u) v[u] = __uint_as_float(r[u]) * mul;
+  if (rotate) {
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int P = cc * 16 + u;  // pair index
+      float sn, cs;
+      const int ax = f.axis[P];
+      rope_sincos_fast(ax == 0 ? pv[0] : ax == 1 ? pv[1] : pv[2], f.omega[P], f.omega_lo[P], -1.f,
+                       &sn, &cs);
+      const float a = v[2 * u], b = v[2 * u + 1];
+      v[2 * u] = fmaf(a, cs, -b * sn);
+      v[2 * u + 1] = fmaf(a, sn, b * cs);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int unit = cc * 4 + u;
+    *reinterpret_cast<uint4*>(base + row * (D * 2) + ((unit ^ (row % UNITS)) << 4)) =
+        make_uint4(pack_bf16x2(v[8 * u], v[8 * u + 1]), pack_bf16x2(v[8 * u + 2], v[8 * u + 3]),
+                   pack_bf16x2(v[8 * u + 4], v[8 * u + 5]), pack_bf16x2(v[8 * u + 6], v[8 * u + 7]));
+  }
+}
+
+// Coalesced store of the first nrows rows of a staging tile (as staged above) to
+// global rows (row0 + r) of a [T][heads][D] bf16 tensor at head `head`, by 256
+// threads.
+template <int D>
+__device__ __forceinline__ void store_staged(const uint8_t* base, __nv_bfloat16* out, int64_t row0,
+                                             int32_t nrows, int32_t heads, int32_t head, int t256) {
+  constexpr int UNITS = D / 8;
+  const int u = t256 % UNITS;
+  for (int r = t256 / UNITS; r < nrows; r += 256 / UNITS) {
+    const int64_t g = ((row0 + r) * heads + head) * D + u * 8;
+    *reinterpret_cast<uint4*>(out + g) =
+        *reinterpret_cast<const uint4*>(base + r * (D * 2) + ((u ^ (r % UNITS)) << 4));
+  }
+}
+
+// Position coordinates (up to 3) of token t as floats; zeros without positions.
+__device__ __forceinline__ void token_pos(const BwdParams& p, int64_t t, bool ok, float (&pv)[3]) {
+  pv[0] = pv[1] = pv[2] = 0.f;
+  if (ok && p.pos != nullptr) {
+    const int32_t* pp = p.pos + t * p.f.naxes;
+    pv[0] = static_cast<float>(pp[0]);
+    pv[1] = static_cast<float>(pp[1]);
+    if (p.f.naxes == 3) pv[2] = static_cast<float>(pp[2]);
+  }
+}
+
+// ------------------------------------------------------------- dK, dV kernel
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
   using C = BwdCfg<D>;
   // All shared memory is dynamic (no static __shared__), so its base is the
   // start of the CTA's window: 1024-byte aligned, as the 128B-swizzled tiles need.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t sbase = smem_u32(smem_raw);
   uint8_t* gbase = smem_raw;
-  CtaMiscB& misc = *reinterpret_cast<CtaMiscB*>(smem_raw + C::OFF_MISC);
+  CtaMiscB& misc = *reinterpret_cast<CtaMiscB*>(smem_raw + C::KV_OFF_MISC);
   WorkItemB& s_w = misc.w;
   int& s_valid = misc.valid;
   uint32_t& s_tmem = misc.tmem;
@@ -305,22 +335,22 @@ __global__ void __launch_bounds__(320, 1)
     if (threadIdx.x == 0) atomicOr(p.status, kFlagSmemAlign);
     return;
   }
-  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sZ = sbase + C::OFF_Z;
-  const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO, sDS = sbase + C::OFF_DS;
-  const uint32_t sDQ = sbase + C::OFF_DQ, sVEC = sbase + C::OFF_VEC;
-  // per stage: -LSE log2 e at [st*128, +64), D at [st*128+64, +64)
-  const float* vec = reinterpret_cast<const float*>(gbase + C::OFF_VEC);
-  const uint32_t bars = sbase + C::OFF_BAR;
+  const uint32_t sK = sbase + C::KV_OFF_K, sV = sbase + C::KV_OFF_V;
+  const uint32_t sQ = sbase + C::KV_OFF_Q, sDO = sbase + C::KV_OFF_DO;
+  const uint32_t sVEC = sbase + C::KV_OFF_VEC;
+  // per stage: -LSE log2 e of the tile's queries at [st * 2BQ, +BQ), D at [+BQ, +2BQ)
+  const float* vec = reinterpret_cast<const float*>(gbase + C::KV_OFF_VEC);
+  const uint32_t bars = sbase + C::KV_OFF_BAR;
   const uint32_t bar_kv = bars;
   const uint32_t bar_full = bars + 8;                // [NST]
   const uint32_t bar_empty = bar_full + 8 * C::NST;  // [NST]
-  const uint32_t bar_st = bar_empty + 8 * C::NST;    // [2]
-  const uint32_t bar_dp = bar_st + 16;
-  const uint32_t bar_ds = bar_dp + 8;
-  const uint32_t bar_dq = bar_ds + 8;
-  const uint32_t bar_dq_empty = bar_dq + 8;
-  const uint32_t bar_done = bar_dq_empty + 8;
+  const uint32_t bar_st = bar_empty + 8 * C::NST;    // S^T_i in TMEM
+  const uint32_t bar_p = bar_st + 8;                 // P^T_i in TMEM (256 arrivals)
+  const uint32_t bar_dp = bar_p + 8;                 // dP^T_i in TMEM
+  const uint32_t bar_ds = bar_dp + 8;                // dS^T_i in TMEM (256 arrivals)
+  const uint32_t bar_done = bar_ds + 8;
   const uint32_t bar_drain = bar_done + 8;
+  const uint32_t bar_stall = bar_drain + 8;          // test hook: never arrived on
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -335,20 +365,14 @@ __global__ void __launch_bounds__(320, 1)
         mbar_init(bar_empty + 8 * i, 1);
       }
       mbar_init(bar_st, 1);
-      mbar_init(bar_st + 8, 1);
+      mbar_init(bar_p, 256);
       mbar_init(bar_dp, 1);
-      mbar_init(bar_ds, 128);
-      mbar_init(bar_dq, 1);
-      mbar_init(bar_dq_empty, 128);
+      mbar_init(bar_ds, 256);
       mbar_init(bar_done, 1);
       mbar_init(bar_drain, 1);
+      mbar_init(bar_stall, 1);
       fence_mbar_init();
     }
-  }
-  if (D == 64) {  // zero chunk padding the dQ^T GEMM to M = 128
-    uint4* z = reinterpret_cast<uint4*>(gbase + C::OFF_Z);
-    for (int i = threadIdx.x; i < C::KCHUNK / 16; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
   }
   __syncthreads();
   if (!s_valid) return;
@@ -365,16 +389,16 @@ __global__ void __launch_bounds__(320, 1)
   const int32_t nq = (w.len + C::BQ - 1) / C::BQ;  // query tiles
 
   if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
+    // -------------------------------------------------------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(bar_kv, 2 * C::KTILE);
+      mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
       for (int ch = 0; ch < D / 64; ++ch) {
-        tma_load_3d(sK + ch * C::KCHUNK, &tm_k, bar_kv, ch * 64, w.head, w.start + k0);
-        tma_load_3d(sV + ch * C::KCHUNK, &tm_v, bar_kv, ch * 64, w.head, w.start + k0);
+        tma_load_3d(sK + ch * C::CHUNK, &tm_k, bar_kv, ch * 64, w.head, w.start + k0);
+        tma_load_3d(sV + ch * C::CHUNK, &tm_v, bar_kv, ch * 64, w.head, w.start + k0);
       }
     }
     __syncwarp();
@@ -388,22 +412,24 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0) atomicOr(p.status, kFlagTimeout);
         break;
       }
+      const int32_t q0 = i * C::BQ;  // first query of the tile (in sample)
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar_full + 8 * st, 2 * C::QTILE);
+        mbar_arrive_expect_tx(bar_full + 8 * st, 2 * C::TILE);
         for (int ch = 0; ch < D / 64; ++ch) {
-          tma_load_3d(sQ + st * C::QTILE + ch * C::QCHUNK, &tm_q, bar_full + 8 * st, ch * 64,
-                      w.head, w.start + i * C::BQ);
-          tma_load_3d(sDO + st * C::QTILE + ch * C::QCHUNK, &tm_do, bar_full + 8 * st, ch * 64,
-                      w.head, w.start + i * C::BQ);
+          tma_load_3d(sQ + st * C::TILE + ch * C::CHUNK, &tm_q, bar_full + 8 * st, ch * 64,
+                      w.head, w.start + q0);
+          tma_load_3d(sDO + st * C::TILE + ch * C::CHUNK, &tm_do, bar_full + 8 * st, ch * 64,
+                      w.head, w.start + q0);
         }
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int q = static_cast<int>(lane) * 2 + u;
-        const int32_t qi = i * C::BQ + q;
+      for (int u = 0; u < C::BQ / 32; ++u) {
+        const int q = static_cast<int>(lane) * (C::BQ / 32) + u;
+        const int32_t qi = q0 + q;
         const bool q_ok = qi < w.len;
-        cp_async_4(sVEC + st * 512 + q * 4, q_ok ? p.nlse2 + gbase_row + qi : p.pad + q);
-        cp_async_4(sVEC + st * 512 + 256 + q * 4, q_ok ? p.delta + gbase_row + qi : p.pad + 64 + q);
+        cp_async_4(sVEC + st * C::VEC + q * 4, q_ok ? p.nlse2 + gbase_row + qi : p.pad + q);
+        cp_async_4(sVEC + st * C::VEC + C::BQ * 4 + q * 4,
+                   q_ok ? p.delta + gbase_row + qi : p.pad + C::BQ + q);
       }
       cp_async_arrive_noinc(bar_full + 8 * st);
       ++issued;
@@ -414,81 +440,61 @@ __global__ void __launch_bounds__(320, 1)
         mbar_wait_drain(bar_full + 8 * (c % C::NST), (c / C::NST) & 1);
     }
   } else if (warp == 9) {
-    // -------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
         const bool r = mbar_wait(bar, parity, &s_abort);
         tc_fence_after();
         return r;
       };
-      // Shared-memory descriptors: one base per operand buffer, then the start
-      // address field (16-byte units, bits 0-13) advanced by a small offset.
-      // K-major operand, K-step kk of 16 elements; `chunk` = bytes per 64-col chunk
-      auto kofs = [](int kk, uint32_t chunk) -> uint64_t {
-        return ((kk >> 2) * chunk + (kk & 3) * 32) >> 4;
-      };
-      // MN-major operand, K-step kk of 16 rows
-      auto mofs = [](int kk) -> uint64_t { return (kk * 2048) >> 4; };
-      const uint32_t lbo_a = D == 128 ? static_cast<uint32_t>(C::KCHUNK) : (sZ - sK);
+      // descriptors: one base per operand buffer, advanced by constant offsets
       const uint64_t dK_k = sdesc_sw128(sK, 16, 1024), dV_k = sdesc_sw128(sV, 16, 1024);
-      const uint64_t dK_m = sdesc_sw128(sK, lbo_a, 1024);
-      const uint64_t dQ_k0 = sdesc_sw128(sQ, 16, 1024), dQ_m0 = sdesc_sw128(sQ, C::QCHUNK, 1024);
-      const uint64_t dO_k0 = sdesc_sw128(sDO, 16, 1024), dO_m0 = sdesc_sw128(sDO, C::QCHUNK, 1024);
-      const uint64_t dS_k0 = sdesc_sw128(sDS, 16, 1024), dS_m0 = sdesc_sw128(sDS, C::DSTILE, 1024);
-      constexpr uint64_t kStage = C::QTILE >> 4, kDsBuf = C::DSTILE >> 4;
+      const uint64_t dQ_k0 = sdesc_sw128(sQ, 16, 1024), dQ_m0 = sdesc_sw128(sQ, C::CHUNK, 1024);
+      const uint64_t dO_k0 = sdesc_sw128(sDO, 16, 1024), dO_m0 = sdesc_sw128(sDO, C::CHUNK, 1024);
+      constexpr uint64_t kStage = C::TILE >> 4;
       auto full = [&](int32_t i) {
         return wait(bar_full + 8 * (i % C::NST), (i / C::NST) & 1);
       };
-      auto issue_st = [&](int32_t i) {  // S^T_i = K' Q'_i^T -> ST[i % 2]
+      auto issue_st = [&](int32_t i) {  // S^T_i = K' Q'_i^T -> ST
         const uint64_t q = dQ_k0 + (i % C::NST) * kStage;
-        const uint32_t d = tmem + ((i & 1) ? C::COL_ST1 : C::COL_ST0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(d, dK_k + kofs(kk, C::KCHUNK), q + kofs(kk, C::QCHUNK), C::IDESC_S, kk > 0);
-        mma_commit(bar_st + 8 * (i & 1));
+          mma_ss(tmem + C::KV_ST, dK_k + kofs<D>(kk), q + kofs<D>(kk), C::IDESC_S, kk > 0);
+        mma_commit(bar_st);
       };
       auto issue_dp = [&](int32_t i) {  // dP^T_i = V dO_i^T -> DPT
         const uint64_t o = dO_k0 + (i % C::NST) * kStage;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::COL_DPT, dV_k + kofs(kk, C::KCHUNK), o + kofs(kk, C::QCHUNK),
-                 C::IDESC_DP, kk > 0);
+          mma_ss(tmem + C::KV_DPT, dV_k + kofs<D>(kk), o + kofs<D>(kk), C::IDESC_DP, kk > 0);
         mma_commit(bar_dp);
       };
-      bool ok = wait(bar_kv, 0) && full(0);
+      bool ok = p.stall_us == 0 ||
+                mbar_wait_for(bar_stall, 0, &s_abort, static_cast<uint64_t>(p.stall_us) * 1000u);
+      ok = ok && wait(bar_kv, 0) && full(0);
       if (ok) {
         issue_st(0);
         issue_dp(0);
-        if (nq > 1) {
-          ok = full(1);
-          if (ok) issue_st(1);
-        }
       }
       for (int32_t i = 0; i < nq && ok; ++i) {
         const int32_t st = i % C::NST;
         const uint64_t q_m = dQ_m0 + st * kStage, o_m = dO_m0 + st * kStage;
-        const uint64_t ds_k = dS_k0 + (i & 1) * kDsBuf, ds_m = dS_m0 + (i & 1) * kDsBuf;
-        const uint32_t stb = tmem + ((i & 1) ? C::COL_ST1 : C::COL_ST0);
-        if (!(ok = wait(bar_ds, i & 1))) break;  // P^T_i in TMEM, dS^T_i in smem
+        if (!(ok = wait(bar_p, i & 1))) break;  // P^T_i in ST (both halves)
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)  // dV += P^T_i dO_i
-          mma_ts(tmem + C::COL_DV, stb + kk * 8, o_m + mofs(kk), C::IDESC_DV,
+          mma_ts(tmem + C::KV_DV, tmem + C::KV_ST + packed_col(kk), o_m + mofs(kk), C::IDESC_DV,
                  (i > 0 || kk > 0) ? 1u : 0u);
+        if (i + 1 < nq) {  // ST is free once dV_i (issued above) has read P^T_i
+          if (!(ok = full(i + 1))) break;
+          issue_st(i + 1);
+        }
+        if (!(ok = wait(bar_ds, i & 1))) break;  // dS^T_i in DPT (both halves)
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T_i Q'_i
-          mma_ss(tmem + C::COL_DK, ds_k + kofs(kk, C::DSTILE), q_m + mofs(kk), C::IDESC_DK,
-                 (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::KV_DK, tmem + C::KV_DPT + packed_col(kk), q_m + mofs(kk),
+                 C::IDESC_DKQ, (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(bar_empty + 8 * st);  // Q'_i, dO_i no longer read
-        if (i + 1 < nq) issue_dp(i + 1);  // DPT was read before bar_ds(i); stage i+1 landed
-        if (i > 0 && !(ok = wait(bar_dq_empty, (i - 1) & 1))) break;
-#pragma unroll
-        for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ^T_i = K'^T dS^T_i
-          mma_ss(tmem + C::COL_DQT, dK_m + mofs(kk), ds_m + mofs(kk), C::IDESC_DQ, kk > 0);
-        mma_commit(bar_dq);
-        if (i + 2 < nq) {  // ST[i % 2] is free once dV_i (issued above) has read P^T_i
-          if (!(ok = full(i + 2))) break;
-          issue_st(i + 2);
-        }
+        if (i + 1 < nq) issue_dp(i + 1);  // DPT is free once dK_i has read dS^T_i
       }
       if (ok) {
         mma_commit(bar_done);
@@ -499,11 +505,13 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(bar_drain);
       mbar_wait_drain(bar_drain, 0);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------ P / dS warpgroup (keys)
-    const uint32_t row = threadIdx.x;  // key row in the tile = TMEM lane
+  } else if (warp < 8) {
+    // ------------------------------------------ P / dS warpgroups (key rows), x 2
+    const int h = warp >> 2;                 // query half: columns [64h, 64h + 64)
+    const uint32_t row = threadIdx.x & 127;  // key row in the tile = TMEM lane
     const uint32_t lane_off = ((warp & 3) * 32) << 16;
-    const uint32_t tDPT = tmem + lane_off + C::COL_DPT;
+    const uint32_t tST = tmem + lane_off + C::KV_ST + 64 * h;
+    const uint32_t tDPT = tmem + lane_off + C::KV_DPT + 64 * h;
     const bool key_ok = k0 + static_cast<int32_t>(row) < w.len;
     const float sl2 = p.scale_log2;
     // dS is staged in fp16 as ds_mul * dS (a power of two; see ds_scale_for)
@@ -512,17 +520,15 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     for (int32_t i = 0; i < nq; ++i) {
       const int32_t st = i % C::NST;
-      const uint32_t tST = tmem + lane_off + ((i & 1) ? C::COL_ST1 : C::COL_ST0);
-      uint8_t* gds = gbase + C::OFF_DS + (i & 1) * C::DSTILE;
       ok = __all_sync(0xffffffffu, mbar_wait(bar_full + 8 * st, (i / C::NST) & 1, &s_abort) &&
-                                       mbar_wait(bar_st + 8 * (i & 1), (i >> 1) & 1, &s_abort));
+                                       mbar_wait(bar_st, i & 1, &s_abort));
       if (!ok) break;
       tc_fence_after();
-      const float4* vl4 = reinterpret_cast<const float4*>(vec + st * 128);  // -LSE log2 e
-      const float4* vd4 = vl4 + 16;                                           // D
-      // P^T: 64 queries, two per packed FMA; bf16 into ST columns [0, 32) (S^T
-      // values already read).  Key rows past the sample get P = 0 (their S^T
-      // holds another sample's keys).
+      const float4* vl4 = reinterpret_cast<const float4*>(vec + st * 2 * C::BQ + 64 * h);
+      const float4* vd4 = reinterpret_cast<const float4*>(vec + st * 2 * C::BQ + C::BQ + 64 * h);
+      // P^T: 64 queries, two per packed FMA; bf16 into ST columns [64h, 64h + 32)
+      // (this half's S^T values already read).  Key rows past the sample get
+      // P = 0 (their S^T holds another sample's keys).
       uint64_t pr2[32];
       {
         uint32_t r[64];
@@ -542,13 +548,13 @@ __global__ void __launch_bounds__(320, 1)
         for (int c4 = 0; c4 < 16; ++c4) {
           const float4 l = vl4[c4];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint64_t x = f32x2_fma(f32x2_pack(__uint_as_float(r[4 * c4 + 2 * h]),
-                                                    __uint_as_float(r[4 * c4 + 2 * h + 1])),
-                                         sl2x2, h ? f32x2_pack(l.z, l.w) : f32x2_pack(l.x, l.y));
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint64_t x = f32x2_fma(f32x2_pack(__uint_as_float(r[4 * c4 + 2 * hh]),
+                                                    __uint_as_float(r[4 * c4 + 2 * hh + 1])),
+                                         sl2x2, hh ? f32x2_pack(l.z, l.w) : f32x2_pack(l.x, l.y));
             float x0, x1;
             f32x2_unpack(x, x0, x1);
-            pr2[2 * c4 + h] = key_ok ? f32x2_pack(ex2_approx(x0), ex2_approx(x1)) : 0ull;
+            pr2[2 * c4 + hh] = key_ok ? f32x2_pack(ex2_approx(x0), ex2_approx(x1)) : 0ull;
           }
         }
         uint32_t pk[32];
@@ -560,12 +566,15 @@ __global__ void __launch_bounds__(320, 1)
         }
         tmem_st32(tST, pk);
       }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_p);
       ok = __all_sync(0xffffffffu, mbar_wait(bar_dp, i & 1, &s_abort));
       if (!ok) break;
       tc_fence_after();
-      // dS^T = P^T (dP^T - D) ds_mul, two queries per packed op; row -> smem
-      // DS[i % 2], 128B-swizzled K-major [key][query]: 16-byte unit u (queries
-      // 8u..8u+7) stored at u ^ (row % 8)
+      // dS^T = P^T (dP^T - D) ds_mul, two queries per packed op; fp16 into DPT
+      // columns [64h, 64h + 32) (each 32-column load is complete before the
+      // columns it overlaps are rewritten)
       const uint64_t dsm2 = f32x2_pack(ds_mul, ds_mul);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -577,157 +586,337 @@ __global__ void __launch_bounds__(320, 1)
         for (int u4 = 0; u4 < 8; ++u4) {
           const float4 dd = vd4[c * 8 + u4];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint64_t t2 = f32x2_sub(f32x2_pack(__uint_as_float(rd[u4 * 4 + 2 * h]),
-                                                     __uint_as_float(rd[u4 * 4 + 2 * h + 1])),
-                                          h ? f32x2_pack(dd.z, dd.w) : f32x2_pack(dd.x, dd.y));
-            const uint64_t ds2 = f32x2_mul(f32x2_mul(pr2[c * 16 + u4 * 2 + h], dsm2), t2);
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint64_t t2 = f32x2_sub(f32x2_pack(__uint_as_float(rd[u4 * 4 + 2 * hh]),
+                                                     __uint_as_float(rd[u4 * 4 + 2 * hh + 1])),
+                                          hh ? f32x2_pack(dd.z, dd.w) : f32x2_pack(dd.x, dd.y));
+            const uint64_t ds2 = f32x2_mul(f32x2_mul(pr2[c * 16 + u4 * 2 + hh], dsm2), t2);
             float ds0, ds1;
             f32x2_unpack(ds2, ds0, ds1);
             dsmax = fmax3(dsmax, fabsf(ds0), fabsf(ds1));
-            pd[u4 * 2 + h] = pack_f16x2(ds0, ds1);
+            pd[u4 * 2 + hh] = pack_f16x2(ds0, ds1);
           }
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int unit = c * 4 + u;
-          uint4* dst = reinterpret_cast<uint4*>(gds + row * 128 + ((unit ^ (row & 7)) << 4));
-          *dst = make_uint4(pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
-        }
+        tmem_st16(tDPT + c * 16, pd);
       }
       tmem_wait_st();
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar_ds);
     }
     if (!(dsmax <= 65504.f)) atomicOr(p.status, kFlagFp16Range);
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, &s_abort));
-    // the four warps agree (a warp whose wait ran out skips the epilogue, and so
+    // the eight warps agree (a warp whose wait ran out skips the epilogue, and so
     // must every other: the epilogue has a barrier among them)
-    const bool all_ok = !named_bar_or(2, 128, !ok);
+    const bool all_ok = !named_bar_or(1, 256, !ok);
     if (all_ok) {
       tc_fence_after();
-      // dV and dK rows (bf16) are staged in the (now idle) Q' / dO stage buffers
-      // as [128 keys][D] with 16-byte units XOR-swizzled by row, then written
-      // out by all four warps with coalesced row stores.
-      constexpr int UNITS = D / 8;  // 16-byte units per row
-      uint8_t* sdv = gbase + C::OFF_Q;
-      uint8_t* sdk = gbase + C::OFF_DO;
-      auto put = [&](uint8_t* base, int unit, uint4 val) {
-        *reinterpret_cast<uint4*>(base + row * (D * 2) + ((unit ^ (row % UNITS)) << 4)) = val;
-      };
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + C::COL_DV + cc * 32, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          put(sdv, cc * 4 + u,
-              make_uint4(pack_bf16x2(__uint_as_float(r[8 * u]), __uint_as_float(r[8 * u + 1])),
-                         pack_bf16x2(__uint_as_float(r[8 * u + 2]), __uint_as_float(r[8 * u + 3])),
-                         pack_bf16x2(__uint_as_float(r[8 * u + 4]), __uint_as_float(r[8 * u + 5])),
-                         pack_bf16x2(__uint_as_float(r[8 * u + 6]), __uint_as_float(r[8 * u + 7]))));
-      }
+      // dV and dK rows (bf16) are staged in the (now idle) first Q' / dO stage
+      // buffers, then written with coalesced row stores.  Warpgroup h converts
+      // columns [h D/2, (h + 1) D/2) of both.
+      uint8_t* sdv = gbase + C::KV_OFF_Q;
+      uint8_t* sdk = gbase + C::KV_OFF_DO;
+      float pv[3];
+      token_pos(p, static_cast<int64_t>(w.start) + k0 + row, key_ok, pv);
       const float dk_mul = p.scale / ds_mul;  // exact: ds_mul is a power of two
-      // the key row's position coordinates (2 or 3 of them)
-      float pv0 = 0.f, pv1 = 0.f, pv2 = 0.f;
-      if (key_ok && p.pos != nullptr) {
-        const int32_t* pp = p.pos + static_cast<int64_t>(w.start + k0 + row) * p.f.naxes;
-        pv0 = static_cast<float>(pp[0]);
-        pv1 = static_cast<float>(pp[1]);
-        if (p.f.naxes == 3) pv2 = static_cast<float>(pp[2]);
-      }
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int c2 = 0; c2 < D / 64; ++c2) {
+        const int cc = h * (D / 64) + c2;  // 32-column chunk
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + C::COL_DK + cc * 32, r);
+        tmem_ld32(tmem + lane_off + C::KV_DV + cc * 32, r);
         tmem_wait_ld();
-        float v[32];
-#pragma unroll
-        for (int u = 0; u < 32; ++u) v[u] = __uint_as_float(r[u]) * dk_mul;
-        if (p.pos != nullptr) {
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const int P = cc * 16 + u;  // pair index
-            float sn, cs;
-            const int ax = p.f.axis[P];
-            rope_sincos_fast(ax == 0 ? pv0 : ax == 1 ? pv1 : pv2, p.f.omega[P],
-                             p.f.omega_lo[P], -1.f, &sn, &cs);
-            const float a = v[2 * u], b = v[2 * u + 1];
-            v[2 * u] = fmaf(a, cs, -b * sn);
-            v[2 * u + 1] = fmaf(a, sn, b * cs);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          put(sdk, cc * 4 + u,
-              make_uint4(pack_bf16x2(v[8 * u], v[8 * u + 1]), pack_bf16x2(v[8 * u + 2], v[8 * u + 3]),
-                         pack_bf16x2(v[8 * u + 4], v[8 * u + 5]),
-                         pack_bf16x2(v[8 * u + 6], v[8 * u + 7])));
+        stage_rotated_row<D>(sdv, row, cc, r, 1.f, false, pv, p.f);
+        tmem_ld32(tmem + lane_off + C::KV_DK + cc * 32, r);
+        tmem_wait_ld();
+        stage_rotated_row<D>(sdk, row, cc, r, dk_mul, p.pos != nullptr, pv, p.f);
       }
-      named_bar_sync(2, 128);
+      named_bar_sync(1, 256);
       const int32_t nrows = min(C::BK, w.len - k0);
-      const int u = static_cast<int>(row) % UNITS;
-      for (int r = static_cast<int>(row) / UNITS; r < nrows; r += 128 / UNITS) {
-        const int64_t g = ((static_cast<int64_t>(w.start) + k0 + r) * p.heads + w.head) * D + u * 8;
-        const int off = r * (D * 2) + ((u ^ (r % UNITS)) << 4);
-        *reinterpret_cast<uint4*>(p.dv + g) = *reinterpret_cast<const uint4*>(sdv + off);
-        *reinterpret_cast<uint4*>(p.dk + g) = *reinterpret_cast<const uint4*>(sdk + off);
-      }
+      const int64_t row0 = static_cast<int64_t>(w.start) + k0;
+      store_staged<D>(sdv, p.dv, row0, nrows, p.heads, w.head, static_cast<int>(threadIdx.x));
+      store_staged<D>(sdk, p.dk, row0, nrows, p.heads, w.head, static_cast<int>(threadIdx.x));
     } else {
       s_abort = 1;
       atomicOr(p.status, kFlagTimeout);
     }
-  } else {
-    // ------------------------------------------ dQ^T warpgroup (head-dim rows)
-    // Per tile: dQ^T from TMEM (thread e = head-dim index), scaled, written as
-    // a [query][d] fp32 tile (rows past the sample = 0) to the staging buffer;
-    // one thread adds the tile into the accumulator with a TMA reduce-add.  The
-    // four warps agree on every step with a barrier-reduction, so a wait that
-    // ran out in one of them stops all of them at the same point.
-    const uint32_t e = threadIdx.x & 127;  // head-dim index = TMEM lane of dQ^T
-    const uint32_t lane_off = ((warp & 3) * 32) << 16;
-    const bool e_ok = e < static_cast<uint32_t>(D);
-    const bool leader = threadIdx.x == 128;
-    // softmax scale over the power-of-two dS staging scale (exact division)
-    const float dq_mul = p.scale / ds_scale_for(p.hmax[w.head], p.hmax[p.heads + w.head]);
-    float* stage = reinterpret_cast<float*>(gbase + C::OFF_DQ);
-    if (leader) tma_prefetch_desc(&tm_dq);
-    for (int32_t i = 0; i < nq; ++i) {
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, &s_abort));
-      uint32_t r0[32], r1[32];
-      if (ok) {
-        tc_fence_after();
-        tmem_ld32(tmem + lane_off + C::COL_DQT, r0);
-        tmem_ld32(tmem + lane_off + C::COL_DQT + 32, r1);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar_dq_empty);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------- dQ kernel
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = smem_u32(smem_raw);
+  uint8_t* gbase = smem_raw;
+  CtaMiscB& misc = *reinterpret_cast<CtaMiscB*>(smem_raw + C::Q_OFF_MISC);
+  WorkItemB& s_w = misc.w;
+  int& s_valid = misc.valid;
+  uint32_t& s_tmem = misc.tmem;
+  volatile uint32_t& s_abort = misc.abort;
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kFlagSmemAlign);
+    return;
+  }
+  const uint32_t sQ = sbase + C::Q_OFF_Q, sDO = sbase + C::Q_OFF_DO;
+  const uint32_t sKV = sbase + C::Q_OFF_KV;
+  const uint32_t bars = sbase + C::Q_OFF_BAR;
+  const uint32_t bar_q = bars;
+  const uint32_t bar_full = bars + 8;                  // [NSLOT]
+  const uint32_t bar_empty = bar_full + 8 * C::NSLOT;  // [NSLOT]
+  const uint32_t bar_s = bar_empty + 8 * C::NSLOT;     // [2] S_j in TMEM S[j % 2]
+  const uint32_t bar_dp = bar_s + 16;                  // dP_j in TMEM
+  const uint32_t bar_ds = bar_dp + 8;                  // dS_j in TMEM (256 arrivals)
+  const uint32_t bar_o = bar_ds + 8;                   // dQ complete
+  const uint32_t bar_drain = bar_o + 8;
+  const uint32_t bar_stall = bar_drain + 8;            // test hook: never arrived on
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    s_valid = ((*p.status & kFlagBadSeqlens) == 0) &&
+              find_item_b(p.cu, p.order, p.prefix, p.n, C::BQ, blockIdx.x, s_w);
+    if (s_valid) {
+      mbar_init(bar_q, 1);
+      for (int i = 0; i < C::NSLOT; ++i) {
+        mbar_init(bar_full + 8 * i, 1);
+        mbar_init(bar_empty + 8 * i, 1);
       }
-      if (leader) bulk_wait_read_all();  // the previous tile's reduce has read the buffer
-      if (named_bar_or(1, 128, !ok)) {
-        s_abort = 1;
-        if (lane == 0) atomicOr(p.status, kFlagTimeout);
-        break;
-      }
-      const int32_t nvalid = min(C::BQ, w.len - i * C::BQ);
-      if (e_ok) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          stage[c * D + e] = c < nvalid ? __uint_as_float(r0[c]) * dq_mul : 0.f;
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          stage[(32 + c) * D + e] = 32 + c < nvalid ? __uint_as_float(r1[c]) * dq_mul : 0.f;
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (leader) {
-        tma_reduce_add_3d(&tm_dq, sDQ, 0, w.head, w.start + i * C::BQ);
-        bulk_commit_group();
-      }
+      mbar_init(bar_s, 1);
+      mbar_init(bar_s + 8, 1);
+      mbar_init(bar_dp, 1);
+      mbar_init(bar_ds, 256);
+      mbar_init(bar_o, 1);
+      mbar_init(bar_drain, 1);
+      mbar_init(bar_stall, 1);
+      fence_mbar_init();
     }
-    if (leader) bulk_wait_all();
+  }
+  __syncthreads();
+  if (!s_valid) return;
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&s_tmem), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const WorkItemB w = s_w;
+  const int32_t q0 = w.blk * C::BQ;                // first query (in sample)
+  const int32_t nk = (w.len + C::BK - 1) / C::BK;  // key tiles
+
+  if (warp == 8) {
+    // -------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(bar_q, 2 * C::TILE);
+      for (int ch = 0; ch < D / 64; ++ch) {
+        tma_load_3d(sQ + ch * C::CHUNK, &tm_q, bar_q, ch * 64, w.head, w.start + q0);
+        tma_load_3d(sDO + ch * C::CHUNK, &tm_do, bar_q, ch * 64, w.head, w.start + q0);
+      }
+      // K'_j, V_j alternate through the ring: copy c = 2j + (0: K', 1: V)
+      int32_t issued = 0;
+      bool ok = true;
+      for (int32_t c = 0; c < 2 * nk && ok; ++c) {
+        const int32_t slot = c % C::NSLOT, use = c / C::NSLOT;
+        if (use > 0 && !mbar_wait(bar_empty + 8 * slot, (use - 1) & 1, &s_abort)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar_full + 8 * slot, C::TILE);
+        for (int ch = 0; ch < D / 64; ++ch)
+          tma_load_3d(sKV + slot * C::TILE + ch * C::CHUNK, (c & 1) ? &tm_v : &tm_k,
+                      bar_full + 8 * slot, ch * 64, w.head, w.start + (c >> 1) * C::BK);
+        ++issued;
+      }
+      if (!ok) {
+        s_abort = 1;
+        atomicOr(p.status, kFlagTimeout);
+      }
+      mbar_wait_drain(bar_q, 0);
+      for (int32_t c = (issued > C::NSLOT ? issued - C::NSLOT : 0); c < issued; ++c)
+        mbar_wait_drain(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1);
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        const bool r = mbar_wait(bar, parity, &s_abort);
+        tc_fence_after();
+        return r;
+      };
+      auto kv_wait = [&](int32_t c) {
+        return wait(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1);
+      };
+      const uint64_t dQ_k = sdesc_sw128(sQ, 16, 1024), dO_k = sdesc_sw128(sDO, 16, 1024);
+      const uint64_t kv_k = sdesc_sw128(sKV, 16, 1024);        // K' / V as K-major B
+      const uint64_t kv_m = sdesc_sw128(sKV, C::CHUNK, 1024);  // K' as MN-major B
+      constexpr uint64_t kTile = C::TILE >> 4;
+      auto issue_s = [&](int32_t j) {  // S_j = Q' K'_j^T -> S[j % 2]
+        const uint64_t b = kv_k + ((2 * j) % C::NSLOT) * kTile;
+        const uint32_t d = tmem + C::Q_S0 + (j & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(d, dQ_k + kofs<D>(kk), b + kofs<D>(kk), C::IDESC_S, kk > 0);
+        mma_commit(bar_s + 8 * (j & 1));
+      };
+      auto issue_dp = [&](int32_t j) {  // dP_j = dO V_j^T -> DP
+        const uint64_t b = kv_k + ((2 * j + 1) % C::NSLOT) * kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::Q_DP, dO_k + kofs<D>(kk), b + kofs<D>(kk), C::IDESC_DP, kk > 0);
+        mma_commit(bar_dp);
+      };
+      bool ok = p.stall_us == 0 ||
+                mbar_wait_for(bar_stall, 0, &s_abort, static_cast<uint64_t>(p.stall_us) * 1000u);
+      ok = ok && wait(bar_q, 0) && kv_wait(0);
+      if (ok) issue_s(0);
+      if (ok && nk > 1 && (ok = kv_wait(2))) issue_s(1);
+      if (ok && (ok = kv_wait(1))) issue_dp(0);
+      for (int32_t j = 0; j < nk && ok; ++j) {
+        if (!(ok = wait(bar_ds, j & 1))) break;  // dS_j in S[j % 2]; DP read
+        const uint64_t kb = kv_m + ((2 * j) % C::NSLOT) * kTile;
+        const uint32_t sa = tmem + C::Q_S0 + (j & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS_j K'_j
+          mma_ts(tmem + C::Q_DQ, sa + packed_col(kk), kb + mofs(kk), C::IDESC_DKQ,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar_empty + 8 * ((2 * j) % C::NSLOT));      // K'_j
+        mma_commit(bar_empty + 8 * ((2 * j + 1) % C::NSLOT));  // V_j
+        if (j + 1 < nk) {  // DP is free once the dS warps have read dP_j
+          if (!(ok = kv_wait(2 * j + 3))) break;
+          issue_dp(j + 1);
+        }
+        if (j + 2 < nk) {  // S[j % 2] is free once dQ_j (issued above) has read dS_j
+          if (!(ok = kv_wait(2 * j + 4))) break;
+          issue_s(j + 2);
+        }
+      }
+      if (ok) {
+        mma_commit(bar_o);
+      } else {
+        s_abort = 1;
+        atomicOr(p.status, kFlagTimeout);
+      }
+      mma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0);
+    }
+  } else if (warp < 8) {
+    // -------------------------------------- P / dS warpgroups (query rows), x 2
+    const int h = warp >> 2;                 // key half: columns [64h, 64h + 64)
+    const uint32_t row = threadIdx.x & 127;  // query row in the tile = TMEM lane
+    const uint32_t lane_off = ((warp & 3) * 32) << 16;
+    const int32_t qrow = q0 + static_cast<int32_t>(row);
+    const bool row_ok = qrow < w.len;
+    const int64_t g = static_cast<int64_t>(w.head) * p.T + w.start + qrow;
+    // rows past the sample: -inf makes P = 0 there
+    const float nl2 = row_ok ? p.nlse2[g] : -INFINITY;
+    const float drow = row_ok ? p.delta[g] : 0.f;
+    const float sl2 = p.scale_log2;
+    const float ds_mul = ds_scale_for(p.hmax[w.head], p.hmax[p.heads + w.head]);
+    const uint64_t sl2x2 = f32x2_pack(sl2, sl2), nl2x2 = f32x2_pack(nl2, nl2);
+    const uint64_t dsm2 = f32x2_pack(ds_mul, ds_mul), d2 = f32x2_pack(drow, drow);
+    const uint32_t tDP = tmem + lane_off + C::Q_DP + 64 * h;
+    float dsmax = 0.f;
+    bool ok = true;
+    for (int32_t j = 0; j < nk; ++j) {
+      const uint32_t tS = tmem + lane_off + C::Q_S0 + (j & 1) * 128 + 64 * h;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s + 8 * (j & 1), (j >> 1) & 1, &s_abort));
+      if (!ok) break;
+      tc_fence_after();
+      // P = exp2(S scale log2e - LSE log2e) over this half's 64 keys; keys past
+      // the sample end get P = 0
+      const int32_t nvalid = w.len - j * C::BK - 64 * h;
+      uint64_t pr2[32];
+      {
+        uint32_t r[64];
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tS, r0);
+          tmem_ld32(tS + 32, r1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            r[c] = r0[c];
+            r[32 + c] = r1[c];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const uint64_t x = f32x2_fma(
+              f32x2_pack(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), sl2x2, nl2x2);
+          float x0, x1;
+          f32x2_unpack(x, x0, x1);
+          pr2[u] = f32x2_pack(2 * u < nvalid ? ex2_approx(x0) : 0.f,
+                              2 * u + 1 < nvalid ? ex2_approx(x1) : 0.f);
+        }
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dp, j & 1, &s_abort));
+      if (!ok) break;
+      tc_fence_after();
+      // dS = P (dP - D) ds_mul, fp16 into S[j % 2] columns [64h, 64h + 32)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t rd[32];
+        tmem_ld32(tDP + c * 32, rd);
+        tmem_wait_ld();
+        uint32_t pd[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const uint64_t t2 = f32x2_sub(
+              f32x2_pack(__uint_as_float(rd[2 * u]), __uint_as_float(rd[2 * u + 1])), d2);
+          const uint64_t ds2 = f32x2_mul(f32x2_mul(pr2[c * 16 + u], dsm2), t2);
+          float ds0, ds1;
+          f32x2_unpack(ds2, ds0, ds1);
+          dsmax = fmax3(dsmax, fabsf(ds0), fabsf(ds1));
+          pd[u] = pack_f16x2(ds0, ds1);
+        }
+        tmem_st16(tS + c * 16, pd);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_ds);
+    }
+    if (!(dsmax <= 65504.f)) atomicOr(p.status, kFlagFp16Range);
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_o, 0, &s_abort));
+    const bool all_ok = !named_bar_or(1, 256, !ok);
+    if (all_ok) {
+      tc_fence_after();
+      // dQ rows: scale / ds_mul, R(-theta) at the query's position, bf16, staged
+      // in the (now idle) Q' buffer, then coalesced row stores.  Warpgroup h
+      // converts columns [h D/2, (h + 1) D/2).
+      uint8_t* sdq = gbase + C::Q_OFF_Q;
+      float pv[3];
+      token_pos(p, static_cast<int64_t>(w.start) + qrow, row_ok, pv);
+      const float dq_mul = p.scale / ds_mul;  // exact: ds_mul is a power of two
+#pragma unroll
+      for (int c2 = 0; c2 < D / 64; ++c2) {
+        const int cc = h * (D / 64) + c2;
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + C::Q_DQ + cc * 32, r);
+        tmem_wait_ld();
+        stage_rotated_row<D>(sdq, row, cc, r, dq_mul, p.pos != nullptr, pv, p.f);
+      }
+      named_bar_sync(1, 256);
+      store_staged<D>(sdq, p.dq, static_cast<int64_t>(w.start) + q0, min(C::BQ, w.len - q0),
+                      p.heads, w.head, static_cast<int>(threadIdx.x));
+    } else {
+      s_abort = 1;
+      atomicOr(p.status, kFlagTimeout);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -742,29 +931,30 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
   using C = BwdCfg<D>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kv_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::KV_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_bwd_q_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::Q_SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   const int64_t rows = static_cast<int64_t>(a.T) * a.heads;
-  const RopeFreqs f = make_rope_freqs(D, a.naxes);
   if (rows > 0) {
     const int64_t blocks = (rows + kPreRowsPerBlock - 1) / kPreRowsPerBlock;
     KernelTimer kt(MF_K_BWD_PRE, s);
     bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         reinterpret_cast<const uint4*>(a.o), reinterpret_cast<const uint4*>(a.d_o),
-        reinterpret_cast<const uint4*>(a.v), a.lse, a.nlse2, a.delta, a.pad,
-        reinterpret_cast<float4*>(a.dq_acc), a.hmax, rows, a.T, a.heads);
+        reinterpret_cast<const uint4*>(a.v), a.lse, a.nlse2, a.delta, a.pad, a.hmax, rows, a.T,
+        a.heads);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  CUtensorMap tq, tk, tv, tdo, tdq;
-  if (!make_tmap_thd(&tq, a.q, a.T, a.heads, D, C::BQ, true) ||
-      !make_tmap_thd(&tk, a.k, a.T, a.heads, D, C::BK, true) ||
-      !make_tmap_thd(&tv, a.v, a.T, a.heads, D, C::BK) ||
-      !make_tmap_thd(&tdo, a.d_o, a.T, a.heads, D, C::BQ) ||
-      !make_tmap_f32_thd(&tdq, a.dq_acc, a.T, a.heads, D, C::BQ))
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_thd(&tq, a.q, a.T, a.heads, D, 128, true) ||
+      !make_tmap_thd(&tk, a.k, a.T, a.heads, D, 128, true) ||
+      !make_tmap_thd(&tv, a.v, a.T, a.heads, D, 128) ||
+      !make_tmap_thd(&tdo, a.d_o, a.T, a.heads, D, 128))
     return cudaErrorInvalidValue;
   BwdParams p;
   p.cu = a.cu;
@@ -775,6 +965,7 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
   p.delta = a.delta;
   p.pad = a.pad;
   p.status = a.status;
+  p.dq = reinterpret_cast<__nv_bfloat16*>(a.dq);
   p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
   p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
   p.n = a.n;
@@ -782,22 +973,24 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
   p.heads = a.heads;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.f = f;
+  p.f = make_rope_freqs(D, a.naxes);
   p.hmax = a.hmax;
-  const int64_t blocks = (static_cast<int64_t>(a.T + C::BK - 1) / C::BK + a.n) * a.heads;
+  p.stall_us = a.stall_us;
+  // both kernels: one CTA per (sample, head, 128-row tile), longest samples first
+  const int64_t blocks = (static_cast<int64_t>(a.T + 127) / 128 + a.n) * a.heads;
   if (blocks > 0) {
     {
       KernelTimer kt(MF_K_ATTN_BWD, s);
-      attn_bwd_kernel<D><<<static_cast<unsigned>(blocks), 320, C::SMEM, s>>>(tq, tk, tv, tdo, tdq, p);
+      attn_bwd_kv_kernel<D><<<static_cast<unsigned>(blocks), kBwdThreads, C::KV_SMEM, s>>>(
+          tq, tk, tv, tdo, p);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-  }
-  if (rows > 0) {
-    KernelTimer kt(MF_K_DQ_POST, s);
-    dq_post_kernel<D><<<static_cast<unsigned>((a.T + kPostTok - 1) / kPostTok), 256, 0, s>>>(
-        reinterpret_cast<const float4*>(a.dq_acc), reinterpret_cast<uint2*>(a.dq),
-        a.pos, a.T, a.heads, f);
+    {
+      KernelTimer kt(MF_K_ATTN_BWD_Q, s);
+      attn_bwd_q_kernel<D><<<static_cast<unsigned>(blocks), kBwdThreads, C::Q_SMEM, s>>>(
+          tq, tk, tv, tdo, p);
+    }
     return cudaGetLastError();
   }
   return cudaSuccess;

@@ -98,15 +98,14 @@ __device__ __forceinline__ E4m3Scale e4m3_scale(float A) {
 // e4m3 fwd (inside the same total): q8, k8, v8 E4M3 [T][h][d] from q16's offset,
 //                     qscale fp32 [T][h], amax2 uint32 [2][h]
 // bwd only:           hmax fp32 [2][h] (per-head max ||dO_j||, max ||v_k||),
-//                     pad fp32 [128] (64 x -inf, 64 x 0: -LSE log2 e / D of rows
-//                     past a sample), nlse2 fp32 [h][T] (-LSE * log2 e), delta fp32 [h][T],
-//                     dq_acc fp32 [T][h][d]
+//                     pad fp32 [256] (128 x -inf, 128 x 0: -LSE log2 e / D of rows
+//                     past a sample), nlse2 fp32 [h][T] (-LSE * log2 e), delta fp32 [h][T]
 struct WsLayout {
   size_t status = 0;
   size_t order = 0, prefix = 0;
   size_t q16 = 0, k16 = 0, v16 = 0;
   size_t q8 = 0, k8 = 0, v8 = 0, qscale = 0, amax2 = 0;
-  size_t hmax = 0, pad = 0, nlse2 = 0, delta = 0, dq_acc = 0;
+  size_t hmax = 0, pad = 0, nlse2 = 0, delta = 0;
   size_t total = 0;
 };
 WsLayout ws_layout(int64_t T, int64_t n, int64_t heads, int64_t head_dim, bool bwd);
@@ -179,15 +178,15 @@ struct AttnBwdArgs {
   const int32_t* prefix;
   uint32_t* status;
   float* hmax;    // [2][h]: max ||dO_j||, max ||v_k|| per head (zeroed by the schedule)
-  float* pad;     // [128]: 64 x -inf then 64 x 0 (written by the preprocess)
+  float* pad;     // [256]: 128 x -inf then 128 x 0 (written by the preprocess)
   float* nlse2;   // [h][T]: -LSE * log2 e (written by the preprocess)
   float* delta;   // [h][T]
-  float* dq_acc;  // [T][h][d]
   uint16_t* dq;
   uint16_t* dk;
   uint16_t* dv;
   int32_t n, T, heads, head_dim;
   float scale;
+  uint32_t stall_us = 0;  // test hook: see mf_test_varlen_attn_bwd_stalled
 };
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, cudaStream_t s);
 

@@ -176,6 +176,11 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Global fp32 reduction (add at L2, no value returned).
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
 // 4-byte asynchronous global -> shared copy (no alignment beyond 4 bytes).
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared::cta.global [%0], [%1], 4;" ::"r"(dst),

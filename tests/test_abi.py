@@ -78,7 +78,8 @@ def test_attn_argument_errors_on_host():
     assert _fwd(lib, **{**a, "q": 0}) == 1
     assert _fwd(lib, **a, T=2 ** 30, h=64) == 3  # heads * T overflows int32
     assert lib.mf_attn_workspace_bytes(10, 1, 1, 96, 0) == 0
-    assert lib.mf_attn_workspace_bytes(10, 1, 2, 128, 1) > lib.mf_attn_workspace_bytes(10, 1, 2, 128, 0)
+    # a backward workspace also serves the forward (the training step shares one)
+    assert lib.mf_attn_workspace_bytes(10, 1, 2, 128, 1) >= lib.mf_attn_workspace_bytes(10, 1, 2, 128, 0)
 
 
 def test_rope_argument_errors_on_host():

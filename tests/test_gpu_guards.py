@@ -185,3 +185,39 @@ def test_wait_that_runs_out_is_reported_and_the_next_call_is_right(cuda_lib, d):
         mf.get_status(w)
         check_o(f64(o2), o_ref)
         check_lse(lse2.cpu().numpy(), lse_ref)
+
+
+def test_backward_wait_that_runs_out_is_reported_and_the_next_call_is_right(cuda_lib):
+    """The same for the backward's attention kernel: MF_ERR_TIMEOUT, dK and dV
+    untouched, then a normal backward on the same workspace matches the oracle."""
+    mf = cuda_lib
+    lib = mf.load()
+    h, d = 2, 128
+    cu, pos = mf.pack(SPECS)
+    T, max_len = mf.pack_size(SPECS)
+    n = len(SPECS)
+    q, k, v, do = (dev(x) for x in random_inputs(T, h, d, 84))
+    o, lse = mf.varlen_attn_fwd(q, k, v, cu, pos, max_len)
+    dq = torch.empty_like(q)
+    bk, dk = _guarded((T, h, d), torch.bfloat16)
+    bv, dv = _guarded((T, h, d), torch.bfloat16)
+    ws = mf.workspace(T, n, h, d, True)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = lib.mf_test_varlen_attn_bwd_stalled(p(q), p(k), p(v), p(o), p(lse), p(do), p(cu), p(pos),
+                                             n, T, max_len, h, d, 0.0, p(dq), p(dk), p(dv), p(ws),
+                                             ws.numel(), 20000, stream)
+    assert rc == 0, mf.STATUS_NAMES.get(rc, rc)
+    with pytest.raises(mf.MFError) as ei:
+        mf.get_status(ws)
+    assert ei.value.status == 5  # MF_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    assert bool((bk.view(torch.int16) == PAT16).all()) and bool((bv.view(torch.int16) == PAT16).all())
+    dq2, dk2, dv2 = mf.varlen_attn_bwd(q, k, v, o, lse, do, cu, pos, max_len, ws=ws)
+    mf.get_status(ws)
+    f = synth.bf16_bits_to_f64
+    cu_r, pos_r = oracle.pack(SPECS)
+    qb, kb, vb, dob = (synth.torch_to_bits(x.cpu()) for x in (q, k, v, do))
+    for name, g, r in zip(("dq", "dk", "dv"), (dq2, dk2, dv2),
+                          oracle.attn_bwd(f(qb), f(kb), f(vb), f(dob), cu_r, pos_r)):
+        check_grad(f64(g), r, name)
