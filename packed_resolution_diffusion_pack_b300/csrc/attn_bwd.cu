@@ -198,7 +198,7 @@ struct BwdCfg {
   static_assert(KV_OFF_Q % 1024 == 0 && KV_OFF_DO % 1024 == 0 && Q_OFF_KV % 1024 == 0,
                 "swizzled tiles start on 1024-byte boundaries");
   static_assert(KV_SMEM <= 232448 && Q_SMEM <= 232448, "shared memory over the per-CTA limit");
-  static_assert(8 + 16 * (NST > NSLOT ? NST : NSLOT) + 8 * 8 <= 256, "barrier area");
+  static_assert(8 * (2 + 2 * (NST > NSLOT ? NST : NSLOT) + 9) <= 256, "barrier area");
 };
 
 // 384 threads: 170 registers each at launch (65,536 / 384), no reallocation.
@@ -253,15 +253,13 @@ __device__ __forceinline__ uint64_t mofs(int kk) { return (kk * 2048) >> 4; }
 // 128-column region (warpgroup h holds elements [64h, 64h + 64)).
 __device__ __forceinline__ uint32_t packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
-// 64 values v (two per 64-bit lane pair) of a row times dk_mul, rotated by R(-theta)
-// at the row's position coordinates (pv) when rotating, converted to bf16 and put
-// into a [128 rows][D] staging tile with 16-byte units XOR-swizzled by row.
-template <int D>
-__device__ __forceinline__ void stage_rotated_row(uint8_t* base, uint32_t row, int cc,
-                                                  const uint32_t (&r)[32], float mul,
-                                                  bool rotate, const float (&pv)[3],
-                                                  const RopeFreqs& f) {
-  constexpr int UNITS = D / 8;
+// 32 consecutive values (columns [32 cc, 32 cc + 32)) of one output row: times
+// mul, rotated by R(-theta) at the row's position coordinates pv when rotating,
+// converted to bf16 and stored at dst (the row's first element) as four 16-byte
+// stores.
+__device__ __forceinline__ void store_row_chunk(__nv_bfloat16* dst, int cc,
+                                                const uint32_t (&r)[32], float mul, bool rotate,
+                                                const float (&pv)[3], const RopeFreqs& f) {
   float v[32];
 #pragma unroll
   for (int u = 0; u < 32; ++u) v[u] = __uint_as_float(r[u]) * mul;
@@ -278,28 +276,12 @@ __device__ __forceinline__ void stage_rotated_row(uint8_t* base, uint32_t row, i
       v[2 * u + 1] = fmaf(a, sn, b * cs);
     }
   }
+  uint4* out = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int unit = cc * 4 + u;
-    *reinterpret_cast<uint4*>(base + row * (D * 2) + ((unit ^ (row % UNITS)) << 4)) =
-        make_uint4(pack_bf16x2(v[8 * u], v[8 * u + 1]), pack_bf16x2(v[8 * u + 2], v[8 * u + 3]),
-                   pack_bf16x2(v[8 * u + 4], v[8 * u + 5]), pack_bf16x2(v[8 * u + 6], v[8 * u + 7]));
-  }
-}
-
-// Coalesced store of the first nrows rows of a staging tile (as staged above) to
-// global rows (row0 + r) of a [T][heads][D] bf16 tensor at head `head`, by 256
-// threads.
-template <int D>
-__device__ __forceinline__ void store_staged(const uint8_t* base, __nv_bfloat16* out, int64_t row0,
-                                             int32_t nrows, int32_t heads, int32_t head, int t256) {
-  constexpr int UNITS = D / 8;
-  const int u = t256 % UNITS;
-  for (int r = t256 / UNITS; r < nrows; r += 256 / UNITS) {
-    const int64_t g = ((row0 + r) * heads + head) * D + u * 8;
-    *reinterpret_cast<uint4*>(out + g) =
-        *reinterpret_cast<const uint4*>(base + r * (D * 2) + ((u ^ (r % UNITS)) << 4));
-  }
+  for (int u = 0; u < 4; ++u)
+    out[u] = make_uint4(pack_bf16x2(v[8 * u], v[8 * u + 1]), pack_bf16x2(v[8 * u + 2], v[8 * u + 3]),
+                        pack_bf16x2(v[8 * u + 4], v[8 * u + 5]),
+                        pack_bf16x2(v[8 * u + 6], v[8 * u + 7]));
 }
 
 // Position coordinates (up to 3) of token t as floats; zeros without positions.
@@ -313,7 +295,20 @@ __device__ __forceinline__ void token_pos(const BwdParams& p, int64_t t, bool ok
   }
 }
 
+// The CTA's k-th work item (static striding over the longest-first list).
+__device__ __forceinline__ bool cta_item(const BwdParams& p, int32_t k, WorkItemB& w) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(k) * gridDim.x;
+  if (idx > INT32_MAX) return false;
+  return find_item_b(p.cu, p.order, p.prefix, p.n, 128, static_cast<int32_t>(idx), w);
+}
+
 // ------------------------------------------------------------- dK, dV kernel
+// Persistent: one CTA per SM walks its share of the (sample, head, key tile)
+// items.  Per item: K', V loaded once (as soon as the previous item's last S^T
+// and dP^T have read theirs), (Q'_i, dO_i) through the stage ring that runs on
+// across items, the dV / dK accumulators freed for the next item as soon as the
+// elementwise warps have loaded them; the epilogue's conversion and stores then
+// overlap the next item's first GEMMs.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -327,55 +322,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sbase = smem_u32(smem_raw);
   uint8_t* gbase = smem_raw;
   CtaMiscB& misc = *reinterpret_cast<CtaMiscB*>(smem_raw + C::KV_OFF_MISC);
-  WorkItemB& s_w = misc.w;
-  int& s_valid = misc.valid;
   uint32_t& s_tmem = misc.tmem;
   volatile uint32_t& s_abort = misc.abort;
   if (sbase & 1023u) {
     if (threadIdx.x == 0) atomicOr(p.status, kFlagSmemAlign);
     return;
   }
+  if ((*p.status & kFlagBadSeqlens) != 0) return;  // the schedule listed no work
   const uint32_t sK = sbase + C::KV_OFF_K, sV = sbase + C::KV_OFF_V;
   const uint32_t sQ = sbase + C::KV_OFF_Q, sDO = sbase + C::KV_OFF_DO;
   const uint32_t sVEC = sbase + C::KV_OFF_VEC;
   // per stage: -LSE log2 e of the tile's queries at [st * 2BQ, +BQ), D at [+BQ, +2BQ)
   const float* vec = reinterpret_cast<const float*>(gbase + C::KV_OFF_VEC);
   const uint32_t bars = sbase + C::KV_OFF_BAR;
-  const uint32_t bar_kv = bars;
-  const uint32_t bar_full = bars + 8;                // [NST]
+  const uint32_t bar_kv = bars;                      // K', V of an item loaded
+  const uint32_t bar_kv_free = bars + 8;             // ... and no longer read
+  const uint32_t bar_full = bars + 16;               // [NST]
   const uint32_t bar_empty = bar_full + 8 * C::NST;  // [NST]
-  const uint32_t bar_st = bar_empty + 8 * C::NST;    // S^T_i in TMEM
-  const uint32_t bar_p = bar_st + 8;                 // P^T_i in TMEM (256 arrivals)
-  const uint32_t bar_dp = bar_p + 8;                 // dP^T_i in TMEM
-  const uint32_t bar_ds = bar_dp + 8;                // dS^T_i in TMEM (256 arrivals)
-  const uint32_t bar_done = bar_ds + 8;
-  const uint32_t bar_drain = bar_done + 8;
+  const uint32_t bar_st = bar_empty + 8 * C::NST;    // S^T in TMEM
+  const uint32_t bar_p = bar_st + 8;                 // P^T in TMEM (256 arrivals)
+  const uint32_t bar_dp = bar_p + 8;                 // dP^T in TMEM
+  const uint32_t bar_ds = bar_dp + 8;                // dS^T in TMEM (256 arrivals)
+  const uint32_t bar_done = bar_ds + 8;              // an item's dV, dK complete
+  const uint32_t bar_acc_free = bar_done + 8;        // ... and loaded (256 arrivals)
+  const uint32_t bar_drain = bar_acc_free + 8;
   const uint32_t bar_stall = bar_drain + 8;          // test hook: never arrived on
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     s_abort = 0;
-    s_valid = ((*p.status & kFlagBadSeqlens) == 0) &&
-              find_item_b(p.cu, p.order, p.prefix, p.n, C::BK, blockIdx.x, s_w);
-    if (s_valid) {
-      mbar_init(bar_kv, 1);
-      for (int i = 0; i < C::NST; ++i) {
-        // 32 cp.async arrivals (LSE / D rows) + the TMA issuer's expect-tx arrival
-        mbar_init(bar_full + 8 * i, 33);
-        mbar_init(bar_empty + 8 * i, 1);
-      }
-      mbar_init(bar_st, 1);
-      mbar_init(bar_p, 256);
-      mbar_init(bar_dp, 1);
-      mbar_init(bar_ds, 256);
-      mbar_init(bar_done, 1);
-      mbar_init(bar_drain, 1);
-      mbar_init(bar_stall, 1);
-      fence_mbar_init();
+    mbar_init(bar_kv, 1);
+    mbar_init(bar_kv_free, 1);
+    for (int i = 0; i < C::NST; ++i) {
+      // 32 cp.async arrivals (LSE / D rows) + the TMA issuer's expect-tx arrival
+      mbar_init(bar_full + 8 * i, 33);
+      mbar_init(bar_empty + 8 * i, 1);
     }
+    mbar_init(bar_st, 1);
+    mbar_init(bar_p, 256);
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_ds, 256);
+    mbar_init(bar_done, 1);
+    mbar_init(bar_acc_free, 256);
+    mbar_init(bar_drain, 1);
+    mbar_init(bar_stall, 1);
+    fence_mbar_init();
   }
   __syncthreads();
-  if (!s_valid) return;
   if (warp == 9) {
     tmem_alloc(smem_u32(&s_tmem), 512);
     tmem_relinquish();
@@ -384,9 +377,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const WorkItemB w = s_w;
-  const int32_t k0 = w.blk * C::BK;                // first key (in sample)
-  const int32_t nq = (w.len + C::BQ - 1) / C::BQ;  // query tiles
 
   if (warp == 8) {
     // -------------------------------------------------------------- TMA producer
@@ -395,48 +385,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
-      for (int ch = 0; ch < D / 64; ++ch) {
-        tma_load_3d(sK + ch * C::CHUNK, &tm_k, bar_kv, ch * 64, w.head, w.start + k0);
-        tma_load_3d(sV + ch * C::CHUNK, &tm_v, bar_kv, ch * 64, w.head, w.start + k0);
-      }
     }
     __syncwarp();
-    const int64_t gbase_row = static_cast<int64_t>(w.head) * p.T + w.start;
-    int32_t issued = 0;
-    for (int32_t i = 0; i < nq; ++i) {
-      const int32_t st = i % C::NST, use = i / C::NST;
-      if (use > 0 &&
-          !__all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * st, (use - 1) & 1, &s_abort))) {
-        s_abort = 1;
-        if (lane == 0) atomicOr(p.status, kFlagTimeout);
+    bool ok = true;
+    int32_t gt = 0, items = 0;  // tiles issued (all items), items started
+    WorkItemB w;
+    for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
+      const int32_t k0 = w.blk * C::BK, nq = (w.len + C::BQ - 1) / C::BQ;
+      if (k > 0 &&
+          !__all_sync(0xffffffffu, mbar_wait_bk(bar_kv_free, (k - 1) & 1, &s_abort))) {
+        ok = false;
         break;
       }
-      const int32_t q0 = i * C::BQ;  // first query of the tile (in sample)
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar_full + 8 * st, 2 * C::TILE);
+        mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
         for (int ch = 0; ch < D / 64; ++ch) {
-          tma_load_3d(sQ + st * C::TILE + ch * C::CHUNK, &tm_q, bar_full + 8 * st, ch * 64,
-                      w.head, w.start + q0);
-          tma_load_3d(sDO + st * C::TILE + ch * C::CHUNK, &tm_do, bar_full + 8 * st, ch * 64,
-                      w.head, w.start + q0);
+          tma_load_3d(sK + ch * C::CHUNK, &tm_k, bar_kv, ch * 64, w.head, w.start + k0);
+          tma_load_3d(sV + ch * C::CHUNK, &tm_v, bar_kv, ch * 64, w.head, w.start + k0);
         }
       }
+      ++items;
+      const int64_t gbase_row = static_cast<int64_t>(w.head) * p.T + w.start;
+      for (int32_t i = 0; i < nq; ++i, ++gt) {
+        const int32_t st = gt % C::NST, use = gt / C::NST;
+        if (use > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait_bk(bar_empty + 8 * st, (use - 1) & 1, &s_abort))) {
+          ok = false;
+          break;
+        }
+        const int32_t q0 = i * C::BQ;  // first query of the tile (in sample)
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_full + 8 * st, 2 * C::TILE);
+          for (int ch = 0; ch < D / 64; ++ch) {
+            tma_load_3d(sQ + st * C::TILE + ch * C::CHUNK, &tm_q, bar_full + 8 * st, ch * 64,
+                        w.head, w.start + q0);
+            tma_load_3d(sDO + st * C::TILE + ch * C::CHUNK, &tm_do, bar_full + 8 * st, ch * 64,
+                        w.head, w.start + q0);
+          }
+        }
 #pragma unroll
-      for (int u = 0; u < C::BQ / 32; ++u) {
-        const int q = static_cast<int>(lane) * (C::BQ / 32) + u;
-        const int32_t qi = q0 + q;
-        const bool q_ok = qi < w.len;
-        cp_async_4(sVEC + st * C::VEC + q * 4, q_ok ? p.nlse2 + gbase_row + qi : p.pad + q);
-        cp_async_4(sVEC + st * C::VEC + C::BQ * 4 + q * 4,
-                   q_ok ? p.delta + gbase_row + qi : p.pad + C::BQ + q);
+        for (int u = 0; u < C::BQ / 32; ++u) {
+          const int q = static_cast<int>(lane) * (C::BQ / 32) + u;
+          const int32_t qi = q0 + q;
+          const bool q_ok = qi < w.len;
+          cp_async_4(sVEC + st * C::VEC + q * 4, q_ok ? p.nlse2 + gbase_row + qi : p.pad + q);
+          cp_async_4(sVEC + st * C::VEC + C::BQ * 4 + q * 4,
+                     q_ok ? p.delta + gbase_row + qi : p.pad + C::BQ + q);
+        }
+        cp_async_arrive_noinc(bar_full + 8 * st);
       }
-      cp_async_arrive_noinc(bar_full + 8 * st);
-      ++issued;
     }
+    if (!ok) {
+      s_abort = 1;
+      if (lane == 0) atomicOr(p.status, kFlagTimeout);
+    }
+    // let every issued copy land before the CTA can exit
     if (lane == 0) {
-      mbar_wait_drain(bar_kv, 0);
-      for (int32_t c = (issued > C::NST ? issued - C::NST : 0); c < issued; ++c)
+      if (items > 0) mbar_wait_drain(bar_kv, (items - 1) & 1);
+      for (int32_t c = (gt > C::NST ? gt - C::NST : 0); c < gt; ++c)
         mbar_wait_drain(bar_full + 8 * (c % C::NST), (c / C::NST) & 1);
     }
   } else if (warp == 9) {
@@ -452,18 +458,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t dQ_k0 = sdesc_sw128(sQ, 16, 1024), dQ_m0 = sdesc_sw128(sQ, C::CHUNK, 1024);
       const uint64_t dO_k0 = sdesc_sw128(sDO, 16, 1024), dO_m0 = sdesc_sw128(sDO, C::CHUNK, 1024);
       constexpr uint64_t kStage = C::TILE >> 4;
-      auto full = [&](int32_t i) {
-        return wait(bar_full + 8 * (i % C::NST), (i / C::NST) & 1);
+      auto full = [&](int32_t g) {
+        return wait(bar_full + 8 * (g % C::NST), (g / C::NST) & 1);
       };
-      auto issue_st = [&](int32_t i) {  // S^T_i = K' Q'_i^T -> ST
-        const uint64_t q = dQ_k0 + (i % C::NST) * kStage;
+      auto issue_st = [&](int32_t g) {  // S^T = K' Q'_g^T -> ST
+        const uint64_t q = dQ_k0 + (g % C::NST) * kStage;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(tmem + C::KV_ST, dK_k + kofs<D>(kk), q + kofs<D>(kk), C::IDESC_S, kk > 0);
         mma_commit(bar_st);
       };
-      auto issue_dp = [&](int32_t i) {  // dP^T_i = V dO_i^T -> DPT
-        const uint64_t o = dO_k0 + (i % C::NST) * kStage;
+      auto issue_dp = [&](int32_t g) {  // dP^T = V dO_g^T -> DPT
+        const uint64_t o = dO_k0 + (g % C::NST) * kStage;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(tmem + C::KV_DPT, dV_k + kofs<D>(kk), o + kofs<D>(kk), C::IDESC_DP, kk > 0);
@@ -471,34 +477,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       bool ok = p.stall_us == 0 ||
                 mbar_wait_for(bar_stall, 0, &s_abort, static_cast<uint64_t>(p.stall_us) * 1000u);
-      ok = ok && wait(bar_kv, 0) && full(0);
-      if (ok) {
-        issue_st(0);
-        issue_dp(0);
-      }
-      for (int32_t i = 0; i < nq && ok; ++i) {
-        const int32_t st = i % C::NST;
-        const uint64_t q_m = dQ_m0 + st * kStage, o_m = dO_m0 + st * kStage;
-        if (!(ok = wait(bar_p, i & 1))) break;  // P^T_i in ST (both halves)
+      int32_t gt = 0;  // tiles of earlier items
+      WorkItemB w;
+      for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
+        const int32_t nq = (w.len + C::BQ - 1) / C::BQ;
+        if (!(ok = wait(bar_kv, k & 1) && full(gt))) break;
+        issue_st(gt);
+        issue_dp(gt);
+        for (int32_t i = 0; i < nq; ++i) {
+          const int32_t g = gt + i, st = g % C::NST;
+          const uint64_t q_m = dQ_m0 + st * kStage, o_m = dO_m0 + st * kStage;
+          if (!(ok = wait(bar_p, g & 1))) break;  // P^T in ST (both halves)
+          // the previous item's accumulators must have been loaded
+          if (i == 0 && k > 0 && !(ok = wait(bar_acc_free, (k - 1) & 1))) break;
 #pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)  // dV += P^T_i dO_i
-          mma_ts(tmem + C::KV_DV, tmem + C::KV_ST + packed_col(kk), o_m + mofs(kk), C::IDESC_DV,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        if (i + 1 < nq) {  // ST is free once dV_i (issued above) has read P^T_i
-          if (!(ok = full(i + 1))) break;
-          issue_st(i + 1);
+          for (int kk = 0; kk < C::BQ / 16; ++kk)  // dV += P^T dO
+            mma_ts(tmem + C::KV_DV, tmem + C::KV_ST + packed_col(kk), o_m + mofs(kk),
+                   C::IDESC_DV, (i > 0 || kk > 0) ? 1u : 0u);
+          if (i + 1 < nq) {  // ST is free once dV (issued above) has read P^T
+            if (!(ok = full(g + 1))) break;
+            issue_st(g + 1);
+          } else {
+            mma_commit(bar_kv_free);  // the item's last S^T and dP^T are issued
+          }
+          if (!(ok = wait(bar_ds, g & 1))) break;  // dS^T in DPT (both halves)
+#pragma unroll
+          for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T Q'
+            mma_ts(tmem + C::KV_DK, tmem + C::KV_DPT + packed_col(kk), q_m + mofs(kk),
+                   C::IDESC_DKQ, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar_empty + 8 * st);  // Q'_g, dO_g no longer read
+          if (i + 1 < nq) issue_dp(g + 1);  // DPT is free once dK has read dS^T
         }
-        if (!(ok = wait(bar_ds, i & 1))) break;  // dS^T_i in DPT (both halves)
-#pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk)  // dK += dS^T_i Q'_i
-          mma_ts(tmem + C::KV_DK, tmem + C::KV_DPT + packed_col(kk), q_m + mofs(kk),
-                 C::IDESC_DKQ, (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar_empty + 8 * st);  // Q'_i, dO_i no longer read
-        if (i + 1 < nq) issue_dp(i + 1);  // DPT is free once dK_i has read dS^T_i
-      }
-      if (ok) {
+        if (!ok) break;
         mma_commit(bar_done);
-      } else {
+        gt += nq;
+      }
+      if (!ok) {
         s_abort = 1;
         atomicOr(p.status, kFlagTimeout);
       }
@@ -512,129 +526,133 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = ((warp & 3) * 32) << 16;
     const uint32_t tST = tmem + lane_off + C::KV_ST + 64 * h;
     const uint32_t tDPT = tmem + lane_off + C::KV_DPT + 64 * h;
-    const bool key_ok = k0 + static_cast<int32_t>(row) < w.len;
     const float sl2 = p.scale_log2;
-    // dS is staged in fp16 as ds_mul * dS (a power of two; see ds_scale_for)
-    const float ds_mul = ds_scale_for(p.hmax[w.head], p.hmax[p.heads + w.head]);
     float dsmax = 0.f;  // scaled |dS|: flag values outside the fp16 range
     bool ok = true;
-    for (int32_t i = 0; i < nq; ++i) {
-      const int32_t st = i % C::NST;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_full + 8 * st, (i / C::NST) & 1, &s_abort) &&
-                                       mbar_wait(bar_st, i & 1, &s_abort));
-      if (!ok) break;
-      tc_fence_after();
-      const float4* vl4 = reinterpret_cast<const float4*>(vec + st * 2 * C::BQ + 64 * h);
-      const float4* vd4 = reinterpret_cast<const float4*>(vec + st * 2 * C::BQ + C::BQ + 64 * h);
-      // P^T: 64 queries, two per packed FMA; bf16 into ST columns [64h, 64h + 32)
-      // (this half's S^T values already read).  Key rows past the sample get
-      // P = 0 (their S^T holds another sample's keys).
-      uint64_t pr2[32];
-      {
-        uint32_t r[64];
-        {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(tST, r0);
-          tmem_ld32(tST + 32, r1);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            r[c] = r0[c];
-            r[32 + c] = r1[c];
-          }
-        }
-        const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
-#pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const float4 l = vl4[c4];
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint64_t x = f32x2_fma(f32x2_pack(__uint_as_float(r[4 * c4 + 2 * hh]),
-                                                    __uint_as_float(r[4 * c4 + 2 * hh + 1])),
-                                         sl2x2, hh ? f32x2_pack(l.z, l.w) : f32x2_pack(l.x, l.y));
-            float x0, x1;
-            f32x2_unpack(x, x0, x1);
-            pr2[2 * c4 + hh] = key_ok ? f32x2_pack(ex2_approx(x0), ex2_approx(x1)) : 0ull;
-          }
-        }
-        uint32_t pk[32];
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          float a, b;
-          f32x2_unpack(pr2[u], a, b);
-          pk[u] = pack_bf16x2(a, b);
-        }
-        tmem_st32(tST, pk);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_p);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_dp, i & 1, &s_abort));
-      if (!ok) break;
-      tc_fence_after();
-      // dS^T = P^T (dP^T - D) ds_mul, two queries per packed op; fp16 into DPT
-      // columns [64h, 64h + 32) (each 32-column load is complete before the
-      // columns it overlaps are rewritten)
+    int32_t gt = 0;
+    WorkItemB w;
+    for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
+      const int32_t k0 = w.blk * C::BK, nq = (w.len + C::BQ - 1) / C::BQ;
+      const bool key_ok = k0 + static_cast<int32_t>(row) < w.len;
+      // dS is staged in fp16 as ds_mul * dS (a power of two; see ds_scale_for)
+      const float ds_mul = ds_scale_for(p.hmax[w.head], p.hmax[p.heads + w.head]);
       const uint64_t dsm2 = f32x2_pack(ds_mul, ds_mul);
+      for (int32_t i = 0; i < nq; ++i) {
+        const int32_t g = gt + i, st = g % C::NST;
+        ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_full + 8 * st, (g / C::NST) & 1, &s_abort) &&
+                                         mbar_wait_bk(bar_st, g & 1, &s_abort));
+        if (!ok) break;
+        tc_fence_after();
+        const float4* vl4 = reinterpret_cast<const float4*>(vec + st * 2 * C::BQ + 64 * h);
+        const float4* vd4 = reinterpret_cast<const float4*>(vec + st * 2 * C::BQ + C::BQ + 64 * h);
+        // P^T: 64 queries, two per packed FMA; bf16 into ST columns [64h, 64h + 32)
+        // (this half's S^T values already read).  Key rows past the sample get
+        // P = 0 (their S^T holds another sample's keys).
+        uint64_t pr2[32];
+        {
+          uint32_t r[64];
+          {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tST, r0);
+            tmem_ld32(tST + 32, r1);
+            tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t rd[32];
-        tmem_ld32(tDPT + c * 32, rd);
-        tmem_wait_ld();
-        uint32_t pd[16];
-#pragma unroll
-        for (int u4 = 0; u4 < 8; ++u4) {
-          const float4 dd = vd4[c * 8 + u4];
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint64_t t2 = f32x2_sub(f32x2_pack(__uint_as_float(rd[u4 * 4 + 2 * hh]),
-                                                     __uint_as_float(rd[u4 * 4 + 2 * hh + 1])),
-                                          hh ? f32x2_pack(dd.z, dd.w) : f32x2_pack(dd.x, dd.y));
-            const uint64_t ds2 = f32x2_mul(f32x2_mul(pr2[c * 16 + u4 * 2 + hh], dsm2), t2);
-            float ds0, ds1;
-            f32x2_unpack(ds2, ds0, ds1);
-            dsmax = fmax3(dsmax, fabsf(ds0), fabsf(ds1));
-            pd[u4 * 2 + hh] = pack_f16x2(ds0, ds1);
+            for (int c = 0; c < 32; ++c) {
+              r[c] = r0[c];
+              r[32 + c] = r1[c];
+            }
           }
+          const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 l = vl4[c4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint64_t x = f32x2_fma(f32x2_pack(__uint_as_float(r[4 * c4 + 2 * hh]),
+                                                      __uint_as_float(r[4 * c4 + 2 * hh + 1])),
+                                           sl2x2, hh ? f32x2_pack(l.z, l.w) : f32x2_pack(l.x, l.y));
+              float x0, x1;
+              f32x2_unpack(x, x0, x1);
+              pr2[2 * c4 + hh] = key_ok ? f32x2_pack(ex2_approx(x0), ex2_approx(x1)) : 0ull;
+            }
+          }
+          uint32_t pk[32];
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            float a, b;
+            f32x2_unpack(pr2[u], a, b);
+            pk[u] = pack_bf16x2(a, b);
+          }
+          tmem_st32(tST, pk);
         }
-        tmem_st16(tDPT + c * 16, pd);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_p);
+        ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_dp, g & 1, &s_abort));
+        if (!ok) break;
+        tc_fence_after();
+        // dS^T = P^T (dP^T - D) ds_mul, two queries per packed op; fp16 into DPT
+        // columns [64h, 64h + 32) (each 32-column load is complete before the
+        // columns it overlaps are rewritten)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t rd[32];
+          tmem_ld32(tDPT + c * 32, rd);
+          tmem_wait_ld();
+          uint32_t pd[16];
+#pragma unroll
+          for (int u4 = 0; u4 < 8; ++u4) {
+            const float4 dd = vd4[c * 8 + u4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint64_t t2 = f32x2_sub(f32x2_pack(__uint_as_float(rd[u4 * 4 + 2 * hh]),
+                                                       __uint_as_float(rd[u4 * 4 + 2 * hh + 1])),
+                                            hh ? f32x2_pack(dd.z, dd.w) : f32x2_pack(dd.x, dd.y));
+              const uint64_t ds2 = f32x2_mul(f32x2_mul(pr2[c * 16 + u4 * 2 + hh], dsm2), t2);
+              float ds0, ds1;
+              f32x2_unpack(ds2, ds0, ds1);
+              dsmax = fmax3(dsmax, fabsf(ds0), fabsf(ds1));
+              pd[u4 * 2 + hh] = pack_f16x2(ds0, ds1);
+            }
+          }
+          tmem_st16(tDPT + c * 16, pd);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_ds);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_ds);
-    }
-    if (!(dsmax <= 65504.f)) atomicOr(p.status, kFlagFp16Range);
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, &s_abort));
-    // the eight warps agree (a warp whose wait ran out skips the epilogue, and so
-    // must every other: the epilogue has a barrier among them)
-    const bool all_ok = !named_bar_or(1, 256, !ok);
-    if (all_ok) {
+      if (!ok) break;
+      // epilogue: this warpgroup's columns [h D/2, (h + 1) D/2) of dV and dK into
+      // registers, the accumulators released, then dV and R(-theta) scale dK /
+      // ds_mul stored straight to the key row
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_done, k & 1, &s_abort)))) break;
       tc_fence_after();
-      // dV and dK rows (bf16) are staged in the (now idle) first Q' / dO stage
-      // buffers, then written with coalesced row stores.  Warpgroup h converts
-      // columns [h D/2, (h + 1) D/2) of both.
-      uint8_t* sdv = gbase + C::KV_OFF_Q;
-      uint8_t* sdk = gbase + C::KV_OFF_DO;
-      float pv[3];
-      token_pos(p, static_cast<int64_t>(w.start) + k0 + row, key_ok, pv);
-      const float dk_mul = p.scale / ds_mul;  // exact: ds_mul is a power of two
+      uint32_t rv[D / 64][32], rk[D / 64][32];
 #pragma unroll
       for (int c2 = 0; c2 < D / 64; ++c2) {
         const int cc = h * (D / 64) + c2;  // 32-column chunk
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + C::KV_DV + cc * 32, r);
-        tmem_wait_ld();
-        stage_rotated_row<D>(sdv, row, cc, r, 1.f, false, pv, p.f);
-        tmem_ld32(tmem + lane_off + C::KV_DK + cc * 32, r);
-        tmem_wait_ld();
-        stage_rotated_row<D>(sdk, row, cc, r, dk_mul, p.pos != nullptr, pv, p.f);
+        tmem_ld32(tmem + lane_off + C::KV_DV + cc * 32, rv[c2]);
+        tmem_ld32(tmem + lane_off + C::KV_DK + cc * 32, rk[c2]);
       }
-      named_bar_sync(1, 256);
-      const int32_t nrows = min(C::BK, w.len - k0);
-      const int64_t row0 = static_cast<int64_t>(w.start) + k0;
-      store_staged<D>(sdv, p.dv, row0, nrows, p.heads, w.head, static_cast<int>(threadIdx.x));
-      store_staged<D>(sdk, p.dk, row0, nrows, p.heads, w.head, static_cast<int>(threadIdx.x));
-    } else {
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar_acc_free);
+      if (key_ok) {
+        float pv[3];
+        token_pos(p, static_cast<int64_t>(w.start) + k0 + row, true, pv);
+        const int64_t off = ((static_cast<int64_t>(w.start) + k0 + row) * p.heads + w.head) * D;
+        const float dk_mul = p.scale / ds_mul;  // exact: ds_mul is a power of two
+#pragma unroll
+        for (int c2 = 0; c2 < D / 64; ++c2) {
+          const int cc = h * (D / 64) + c2;
+          store_row_chunk(p.dv + off, cc, rv[c2], 1.f, false, pv, p.f);
+          store_row_chunk(p.dk + off, cc, rk[c2], dk_mul, p.pos != nullptr, pv, p.f);
+        }
+      }
+      gt += nq;
+    }
+    if (!(dsmax <= 65504.f)) atomicOr(p.status, kFlagFp16Range);
+    if (!ok) {
       s_abort = 1;
       atomicOr(p.status, kFlagTimeout);
     }
@@ -648,6 +666,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ----------------------------------------------------------------- dQ kernel
+// Persistent like the dK / dV kernel: per (sample, head, query tile) item, Q' and
+// dO are loaded once (as soon as the previous item's last S and dP have read
+// theirs), K'_j and V_j run through a ring that carries on across items, and the
+// dQ accumulator is freed for the next item as soon as the elementwise warps
+// have loaded it.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -657,52 +680,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t sbase = smem_u32(smem_raw);
-  uint8_t* gbase = smem_raw;
   CtaMiscB& misc = *reinterpret_cast<CtaMiscB*>(smem_raw + C::Q_OFF_MISC);
-  WorkItemB& s_w = misc.w;
-  int& s_valid = misc.valid;
   uint32_t& s_tmem = misc.tmem;
   volatile uint32_t& s_abort = misc.abort;
   if (sbase & 1023u) {
     if (threadIdx.x == 0) atomicOr(p.status, kFlagSmemAlign);
     return;
   }
+  if ((*p.status & kFlagBadSeqlens) != 0) return;  // the schedule listed no work
   const uint32_t sQ = sbase + C::Q_OFF_Q, sDO = sbase + C::Q_OFF_DO;
   const uint32_t sKV = sbase + C::Q_OFF_KV;
   const uint32_t bars = sbase + C::Q_OFF_BAR;
-  const uint32_t bar_q = bars;
-  const uint32_t bar_full = bars + 8;                  // [NSLOT]
+  const uint32_t bar_q = bars;                         // Q', dO of an item loaded
+  const uint32_t bar_q_free = bars + 8;                // ... and no longer read
+  const uint32_t bar_full = bars + 16;                 // [NSLOT]
   const uint32_t bar_empty = bar_full + 8 * C::NSLOT;  // [NSLOT]
-  const uint32_t bar_s = bar_empty + 8 * C::NSLOT;     // [2] S_j in TMEM S[j % 2]
-  const uint32_t bar_dp = bar_s + 16;                  // dP_j in TMEM
-  const uint32_t bar_ds = bar_dp + 8;                  // dS_j in TMEM (256 arrivals)
-  const uint32_t bar_o = bar_ds + 8;                   // dQ complete
-  const uint32_t bar_drain = bar_o + 8;
+  const uint32_t bar_s = bar_empty + 8 * C::NSLOT;     // [2] S in TMEM S[g % 2]
+  const uint32_t bar_dp = bar_s + 16;                  // dP in TMEM
+  const uint32_t bar_ds = bar_dp + 8;                  // dS in TMEM (256 arrivals)
+  const uint32_t bar_o = bar_ds + 8;                   // an item's dQ complete
+  const uint32_t bar_acc_free = bar_o + 8;             // ... and loaded (256 arrivals)
+  const uint32_t bar_drain = bar_acc_free + 8;
   const uint32_t bar_stall = bar_drain + 8;            // test hook: never arrived on
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     s_abort = 0;
-    s_valid = ((*p.status & kFlagBadSeqlens) == 0) &&
-              find_item_b(p.cu, p.order, p.prefix, p.n, C::BQ, blockIdx.x, s_w);
-    if (s_valid) {
-      mbar_init(bar_q, 1);
-      for (int i = 0; i < C::NSLOT; ++i) {
-        mbar_init(bar_full + 8 * i, 1);
-        mbar_init(bar_empty + 8 * i, 1);
-      }
-      mbar_init(bar_s, 1);
-      mbar_init(bar_s + 8, 1);
-      mbar_init(bar_dp, 1);
-      mbar_init(bar_ds, 256);
-      mbar_init(bar_o, 1);
-      mbar_init(bar_drain, 1);
-      mbar_init(bar_stall, 1);
-      fence_mbar_init();
+    mbar_init(bar_q, 1);
+    mbar_init(bar_q_free, 1);
+    for (int i = 0; i < C::NSLOT; ++i) {
+      mbar_init(bar_full + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, 1);
     }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_s + 8, 1);
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_ds, 256);
+    mbar_init(bar_o, 1);
+    mbar_init(bar_acc_free, 256);
+    mbar_init(bar_drain, 1);
+    mbar_init(bar_stall, 1);
+    fence_mbar_init();
   }
   __syncthreads();
-  if (!s_valid) return;
   if (warp == 9) {
     tmem_alloc(smem_u32(&s_tmem), 512);
     tmem_relinquish();
@@ -711,9 +731,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const WorkItemB w = s_w;
-  const int32_t q0 = w.blk * C::BQ;                // first query (in sample)
-  const int32_t nk = (w.len + C::BK - 1) / C::BK;  // key tiles
 
   if (warp == 8) {
     // -------------------------------------------------------------- TMA producer
@@ -722,32 +739,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(bar_q, 2 * C::TILE);
-      for (int ch = 0; ch < D / 64; ++ch) {
-        tma_load_3d(sQ + ch * C::CHUNK, &tm_q, bar_q, ch * 64, w.head, w.start + q0);
-        tma_load_3d(sDO + ch * C::CHUNK, &tm_do, bar_q, ch * 64, w.head, w.start + q0);
-      }
-      // K'_j, V_j alternate through the ring: copy c = 2j + (0: K', 1: V)
-      int32_t issued = 0;
       bool ok = true;
-      for (int32_t c = 0; c < 2 * nk && ok; ++c) {
-        const int32_t slot = c % C::NSLOT, use = c / C::NSLOT;
-        if (use > 0 && !mbar_wait(bar_empty + 8 * slot, (use - 1) & 1, &s_abort)) {
+      int32_t gc = 0, items = 0;  // K'/V copies issued (all items), items started
+      WorkItemB w;
+      for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
+        const int32_t q0 = w.blk * C::BQ, nk = (w.len + C::BK - 1) / C::BK;
+        if (k > 0 && !mbar_wait_bk(bar_q_free, (k - 1) & 1, &s_abort)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar_full + 8 * slot, C::TILE);
-        for (int ch = 0; ch < D / 64; ++ch)
-          tma_load_3d(sKV + slot * C::TILE + ch * C::CHUNK, (c & 1) ? &tm_v : &tm_k,
-                      bar_full + 8 * slot, ch * 64, w.head, w.start + (c >> 1) * C::BK);
-        ++issued;
+        mbar_arrive_expect_tx(bar_q, 2 * C::TILE);
+        for (int ch = 0; ch < D / 64; ++ch) {
+          tma_load_3d(sQ + ch * C::CHUNK, &tm_q, bar_q, ch * 64, w.head, w.start + q0);
+          tma_load_3d(sDO + ch * C::CHUNK, &tm_do, bar_q, ch * 64, w.head, w.start + q0);
+        }
+        ++items;
+        // K'_j, V_j alternate through the ring: copy 2j (K'_j), 2j + 1 (V_j)
+        for (int32_t c = 0; c < 2 * nk; ++c, ++gc) {
+          const int32_t slot = gc % C::NSLOT, use = gc / C::NSLOT;
+          if (use > 0 && !mbar_wait_bk(bar_empty + 8 * slot, (use - 1) & 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar_full + 8 * slot, C::TILE);
+          for (int ch = 0; ch < D / 64; ++ch)
+            tma_load_3d(sKV + slot * C::TILE + ch * C::CHUNK, (c & 1) ? &tm_v : &tm_k,
+                        bar_full + 8 * slot, ch * 64, w.head, w.start + (c >> 1) * C::BK);
+        }
       }
       if (!ok) {
         s_abort = 1;
         atomicOr(p.status, kFlagTimeout);
       }
-      mbar_wait_drain(bar_q, 0);
-      for (int32_t c = (issued > C::NSLOT ? issued - C::NSLOT : 0); c < issued; ++c)
+      if (items > 0) mbar_wait_drain(bar_q, (items - 1) & 1);
+      for (int32_t c = (gc > C::NSLOT ? gc - C::NSLOT : 0); c < gc; ++c)
         mbar_wait_drain(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1);
     }
   } else if (warp == 9) {
@@ -765,16 +790,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t kv_k = sdesc_sw128(sKV, 16, 1024);        // K' / V as K-major B
       const uint64_t kv_m = sdesc_sw128(sKV, C::CHUNK, 1024);  // K' as MN-major B
       constexpr uint64_t kTile = C::TILE >> 4;
-      auto issue_s = [&](int32_t j) {  // S_j = Q' K'_j^T -> S[j % 2]
-        const uint64_t b = kv_k + ((2 * j) % C::NSLOT) * kTile;
-        const uint32_t d = tmem + C::Q_S0 + (j & 1) * 128;
+      // S of global step g (its K' is copy c) -> S[g % 2]; dP (V is copy c) -> DP
+      auto issue_s = [&](int32_t g, int32_t c) {
+        const uint64_t b = kv_k + (c % C::NSLOT) * kTile;
+        const uint32_t d = tmem + C::Q_S0 + (g & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(d, dQ_k + kofs<D>(kk), b + kofs<D>(kk), C::IDESC_S, kk > 0);
-        mma_commit(bar_s + 8 * (j & 1));
+        mma_commit(bar_s + 8 * (g & 1));
       };
-      auto issue_dp = [&](int32_t j) {  // dP_j = dO V_j^T -> DP
-        const uint64_t b = kv_k + ((2 * j + 1) % C::NSLOT) * kTile;
+      auto issue_dp = [&](int32_t c) {
+        const uint64_t b = kv_k + (c % C::NSLOT) * kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(tmem + C::Q_DP, dO_k + kofs<D>(kk), b + kofs<D>(kk), C::IDESC_DP, kk > 0);
@@ -782,32 +808,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       bool ok = p.stall_us == 0 ||
                 mbar_wait_for(bar_stall, 0, &s_abort, static_cast<uint64_t>(p.stall_us) * 1000u);
-      ok = ok && wait(bar_q, 0) && kv_wait(0);
-      if (ok) issue_s(0);
-      if (ok && nk > 1 && (ok = kv_wait(2))) issue_s(1);
-      if (ok && (ok = kv_wait(1))) issue_dp(0);
-      for (int32_t j = 0; j < nk && ok; ++j) {
-        if (!(ok = wait(bar_ds, j & 1))) break;  // dS_j in S[j % 2]; DP read
-        const uint64_t kb = kv_m + ((2 * j) % C::NSLOT) * kTile;
-        const uint32_t sa = tmem + C::Q_S0 + (j & 1) * 128;
+      int32_t gs = 0, gc = 0;  // steps and K'/V copies of earlier items
+      WorkItemB w;
+      for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
+        const int32_t nk = (w.len + C::BK - 1) / C::BK;
+        if (!(ok = wait(bar_q, k & 1) && kv_wait(gc))) break;
+        issue_s(gs, gc);
+        if (nk > 1) {
+          if (!(ok = kv_wait(gc + 2))) break;
+          issue_s(gs + 1, gc + 2);
+        }
+        if (!(ok = kv_wait(gc + 1))) break;
+        issue_dp(gc + 1);
+        for (int32_t j = 0; j < nk; ++j) {
+          const int32_t g = gs + j, c = gc + 2 * j;
+          if (j == nk - 1) mma_commit(bar_q_free);  // the item's last S and dP are issued
+          if (!(ok = wait(bar_ds, g & 1))) break;   // dS in S[g % 2]; DP read
+          // the previous item's accumulator must have been loaded
+          if (j == 0 && k > 0 && !(ok = wait(bar_acc_free, (k - 1) & 1))) break;
+          const uint64_t kb = kv_m + (c % C::NSLOT) * kTile;
+          const uint32_t sa = tmem + C::Q_S0 + (g & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS_j K'_j
-          mma_ts(tmem + C::Q_DQ, sa + packed_col(kk), kb + mofs(kk), C::IDESC_DKQ,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar_empty + 8 * ((2 * j) % C::NSLOT));      // K'_j
-        mma_commit(bar_empty + 8 * ((2 * j + 1) % C::NSLOT));  // V_j
-        if (j + 1 < nk) {  // DP is free once the dS warps have read dP_j
-          if (!(ok = kv_wait(2 * j + 3))) break;
-          issue_dp(j + 1);
+          for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K'_j
+            mma_ts(tmem + C::Q_DQ, sa + packed_col(kk), kb + mofs(kk), C::IDESC_DKQ,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar_empty + 8 * (c % C::NSLOT));        // K'_j
+          mma_commit(bar_empty + 8 * ((c + 1) % C::NSLOT));  // V_j
+          if (j + 1 < nk) {  // DP is free once the dS warps have read dP
+            if (!(ok = kv_wait(c + 3))) break;
+            issue_dp(c + 3);
+          }
+          if (j + 2 < nk) {  // S[g % 2] is free once dQ (issued above) has read dS
+            if (!(ok = kv_wait(c + 4))) break;
+            issue_s(g + 2, c + 4);
+          }
         }
-        if (j + 2 < nk) {  // S[j % 2] is free once dQ_j (issued above) has read dS_j
-          if (!(ok = kv_wait(2 * j + 4))) break;
-          issue_s(j + 2);
-        }
-      }
-      if (ok) {
+        if (!ok) break;
         mma_commit(bar_o);
-      } else {
+        gs += nk;
+        gc += 2 * nk;
+      }
+      if (!ok) {
         s_abort = 1;
         atomicOr(p.status, kFlagTimeout);
       }
@@ -819,101 +860,110 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int h = warp >> 2;                 // key half: columns [64h, 64h + 64)
     const uint32_t row = threadIdx.x & 127;  // query row in the tile = TMEM lane
     const uint32_t lane_off = ((warp & 3) * 32) << 16;
-    const int32_t qrow = q0 + static_cast<int32_t>(row);
-    const bool row_ok = qrow < w.len;
-    const int64_t g = static_cast<int64_t>(w.head) * p.T + w.start + qrow;
-    // rows past the sample: -inf makes P = 0 there
-    const float nl2 = row_ok ? p.nlse2[g] : -INFINITY;
-    const float drow = row_ok ? p.delta[g] : 0.f;
-    const float sl2 = p.scale_log2;
-    const float ds_mul = ds_scale_for(p.hmax[w.head], p.hmax[p.heads + w.head]);
-    const uint64_t sl2x2 = f32x2_pack(sl2, sl2), nl2x2 = f32x2_pack(nl2, nl2);
-    const uint64_t dsm2 = f32x2_pack(ds_mul, ds_mul), d2 = f32x2_pack(drow, drow);
     const uint32_t tDP = tmem + lane_off + C::Q_DP + 64 * h;
+    const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
     float dsmax = 0.f;
     bool ok = true;
-    for (int32_t j = 0; j < nk; ++j) {
-      const uint32_t tS = tmem + lane_off + C::Q_S0 + (j & 1) * 128 + 64 * h;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s + 8 * (j & 1), (j >> 1) & 1, &s_abort));
-      if (!ok) break;
-      tc_fence_after();
-      // P = exp2(S scale log2e - LSE log2e) over this half's 64 keys; keys past
-      // the sample end get P = 0
-      const int32_t nvalid = w.len - j * C::BK - 64 * h;
-      uint64_t pr2[32];
-      {
-        uint32_t r[64];
+    int32_t gs = 0;
+    WorkItemB w;
+    for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
+      const int32_t q0 = w.blk * C::BQ, nk = (w.len + C::BK - 1) / C::BK;
+      const int32_t qrow = q0 + static_cast<int32_t>(row);
+      const bool row_ok = qrow < w.len;
+      const int64_t gidx = static_cast<int64_t>(w.head) * p.T + w.start + qrow;
+      // rows past the sample: -inf makes P = 0 there
+      const float nl2 = row_ok ? p.nlse2[gidx] : -INFINITY;
+      const float drow = row_ok ? p.delta[gidx] : 0.f;
+      const float ds_mul = ds_scale_for(p.hmax[w.head], p.hmax[p.heads + w.head]);
+      const uint64_t nl2x2 = f32x2_pack(nl2, nl2);
+      const uint64_t dsm2 = f32x2_pack(ds_mul, ds_mul), d2 = f32x2_pack(drow, drow);
+      for (int32_t j = 0; j < nk; ++j) {
+        const int32_t g = gs + j;
+        const uint32_t tS = tmem + lane_off + C::Q_S0 + (g & 1) * 128 + 64 * h;
+        ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_s + 8 * (g & 1), (g >> 1) & 1, &s_abort));
+        if (!ok) break;
+        tc_fence_after();
+        // P = exp2(S scale log2e - LSE log2e) over this half's 64 keys; keys past
+        // the sample end get P = 0
+        const int32_t nvalid = w.len - j * C::BK - 64 * h;
+        uint64_t pr2[32];
         {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(tS, r0);
-          tmem_ld32(tS + 32, r1);
-          tmem_wait_ld();
+          uint32_t r[64];
+          {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tS, r0);
+            tmem_ld32(tS + 32, r1);
+            tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            r[c] = r0[c];
-            r[32 + c] = r1[c];
+            for (int c = 0; c < 32; ++c) {
+              r[c] = r0[c];
+              r[32 + c] = r1[c];
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const uint64_t x = f32x2_fma(
+                f32x2_pack(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), sl2x2, nl2x2);
+            float x0, x1;
+            f32x2_unpack(x, x0, x1);
+            pr2[u] = f32x2_pack(2 * u < nvalid ? ex2_approx(x0) : 0.f,
+                                2 * u + 1 < nvalid ? ex2_approx(x1) : 0.f);
           }
         }
+        ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_dp, g & 1, &s_abort));
+        if (!ok) break;
+        tc_fence_after();
+        // dS = P (dP - D) ds_mul, fp16 into S[g % 2] columns [64h, 64h + 32)
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const uint64_t x = f32x2_fma(
-              f32x2_pack(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), sl2x2, nl2x2);
-          float x0, x1;
-          f32x2_unpack(x, x0, x1);
-          pr2[u] = f32x2_pack(2 * u < nvalid ? ex2_approx(x0) : 0.f,
-                              2 * u + 1 < nvalid ? ex2_approx(x1) : 0.f);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t rd[32];
+          tmem_ld32(tDP + c * 32, rd);
+          tmem_wait_ld();
+          uint32_t pd[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const uint64_t t2 = f32x2_sub(
+                f32x2_pack(__uint_as_float(rd[2 * u]), __uint_as_float(rd[2 * u + 1])), d2);
+            const uint64_t ds2 = f32x2_mul(f32x2_mul(pr2[c * 16 + u], dsm2), t2);
+            float ds0, ds1;
+            f32x2_unpack(ds2, ds0, ds1);
+            dsmax = fmax3(dsmax, fabsf(ds0), fabsf(ds1));
+            pd[u] = pack_f16x2(ds0, ds1);
+          }
+          tmem_st16(tS + c * 16, pd);
         }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_ds);
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_dp, j & 1, &s_abort));
       if (!ok) break;
+      // epilogue: this warpgroup's columns [h D/2, (h + 1) D/2) of dQ into
+      // registers, the accumulator released, then R(-theta) scale dQ' / ds_mul
+      // stored straight to the query row
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_o, k & 1, &s_abort)))) break;
       tc_fence_after();
-      // dS = P (dP - D) ds_mul, fp16 into S[j % 2] columns [64h, 64h + 32)
+      uint32_t rq[D / 64][32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t rd[32];
-        tmem_ld32(tDP + c * 32, rd);
-        tmem_wait_ld();
-        uint32_t pd[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const uint64_t t2 = f32x2_sub(
-              f32x2_pack(__uint_as_float(rd[2 * u]), __uint_as_float(rd[2 * u + 1])), d2);
-          const uint64_t ds2 = f32x2_mul(f32x2_mul(pr2[c * 16 + u], dsm2), t2);
-          float ds0, ds1;
-          f32x2_unpack(ds2, ds0, ds1);
-          dsmax = fmax3(dsmax, fabsf(ds0), fabsf(ds1));
-          pd[u] = pack_f16x2(ds0, ds1);
-        }
-        tmem_st16(tS + c * 16, pd);
-      }
-      tmem_wait_st();
+      for (int c2 = 0; c2 < D / 64; ++c2)
+        tmem_ld32(tmem + lane_off + C::Q_DQ + (h * (D / 64) + c2) * 32, rq[c2]);
+      tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(bar_ds);
+      mbar_arrive(bar_acc_free);
+      if (row_ok) {
+        float pv[3];
+        token_pos(p, static_cast<int64_t>(w.start) + qrow, true, pv);
+        const int64_t off = ((static_cast<int64_t>(w.start) + qrow) * p.heads + w.head) * D;
+        const float dq_mul = p.scale / ds_mul;  // exact: ds_mul is a power of two
+#pragma unroll
+        for (int c2 = 0; c2 < D / 64; ++c2)
+          store_row_chunk(p.dq + off, h * (D / 64) + c2, rq[c2], dq_mul, p.pos != nullptr, pv,
+                          p.f);
+      }
+      gs += nk;
     }
     if (!(dsmax <= 65504.f)) atomicOr(p.status, kFlagFp16Range);
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_o, 0, &s_abort));
-    const bool all_ok = !named_bar_or(1, 256, !ok);
-    if (all_ok) {
-      tc_fence_after();
-      // dQ rows: scale / ds_mul, R(-theta) at the query's position, bf16, staged
-      // in the (now idle) Q' buffer, then coalesced row stores.  Warpgroup h
-      // converts columns [h D/2, (h + 1) D/2).
-      uint8_t* sdq = gbase + C::Q_OFF_Q;
-      float pv[3];
-      token_pos(p, static_cast<int64_t>(w.start) + qrow, row_ok, pv);
-      const float dq_mul = p.scale / ds_mul;  // exact: ds_mul is a power of two
-#pragma unroll
-      for (int c2 = 0; c2 < D / 64; ++c2) {
-        const int cc = h * (D / 64) + c2;
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + C::Q_DQ + cc * 32, r);
-        tmem_wait_ld();
-        stage_rotated_row<D>(sdq, row, cc, r, dq_mul, p.pos != nullptr, pv, p.f);
-      }
-      named_bar_sync(1, 256);
-      store_staged<D>(sdq, p.dq, static_cast<int64_t>(w.start) + q0, min(C::BQ, w.len - q0),
-                      p.heads, w.head, static_cast<int>(threadIdx.x));
-    } else {
+    if (!ok) {
       s_abort = 1;
       atomicOr(p.status, kFlagTimeout);
     }
@@ -924,6 +974,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// Multiprocessor count of the current device (cached per device).
+static int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
 template <int D>
@@ -976,20 +1040,20 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
   p.f = make_rope_freqs(D, a.naxes);
   p.hmax = a.hmax;
   p.stall_us = a.stall_us;
-  // both kernels: one CTA per (sample, head, 128-row tile), longest samples first
-  const int64_t blocks = (static_cast<int64_t>(a.T + 127) / 128 + a.n) * a.heads;
-  if (blocks > 0) {
+  // both kernels: one item per (sample, head, 128-row tile), longest samples
+  // first; one persistent CTA per SM (at most one per item)
+  const int64_t items = (static_cast<int64_t>(a.T + 127) / 128 + a.n) * a.heads;
+  if (items > 0) {
+    const unsigned grid = static_cast<unsigned>(items < sm_count() ? items : sm_count());
     {
       KernelTimer kt(MF_K_ATTN_BWD, s);
-      attn_bwd_kv_kernel<D><<<static_cast<unsigned>(blocks), kBwdThreads, C::KV_SMEM, s>>>(
-          tq, tk, tv, tdo, p);
+      attn_bwd_kv_kernel<D><<<grid, kBwdThreads, C::KV_SMEM, s>>>(tq, tk, tv, tdo, p);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     {
       KernelTimer kt(MF_K_ATTN_BWD_Q, s);
-      attn_bwd_q_kernel<D><<<static_cast<unsigned>(blocks), kBwdThreads, C::Q_SMEM, s>>>(
-          tq, tk, tv, tdo, p);
+      attn_bwd_q_kernel<D><<<grid, kBwdThreads, C::Q_SMEM, s>>>(tq, tk, tv, tdo, p);
     }
     return cudaGetLastError();
   }

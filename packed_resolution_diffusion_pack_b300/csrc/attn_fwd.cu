@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int kv = 0; kv < 2; ++kv) {
             const int32_t c = 2 * j + kv;
             const int32_t slot = c % C::NSLOT, use = c / C::NSLOT;
-            if (use > 0 && !mbar_wait(bar_empty + 8 * slot, (use - 1) & 1, &s_abort)) {
+            if (use > 0 && !mbar_wait_bk(bar_empty + 8 * slot, (use - 1) & 1, &s_abort)) {
               ok = false;
               break;
             }
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int32_t j = 0; j < nkv; ++j) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_s + 8 * t, j & 1, &s_abort));
+        ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_s + 8 * t, j & 1, &s_abort));
         if (!ok) break;
         tc_fence_after();
         uint32_t s[128];
@@ -607,7 +607,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_before();
         mbar_arrive(bar_p + 8 * t);
       }
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_o + 8 * t, 0, &s_abort));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_o + 8 * t, 0, &s_abort));
       // the warpgroup's four warps agree before the epilogue's barrier
       const bool all_ok = !(t ? named_bar_or(2, 128, !ok) : named_bar_or(1, 128, !ok));
       if (all_ok) {

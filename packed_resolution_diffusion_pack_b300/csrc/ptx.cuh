@@ -105,21 +105,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete.  Returns false (and
 // never blocks longer than limit_ns, kWaitLimitNs for mbar_wait) if it does not,
 // or if *abort becomes non-zero meanwhile (another role of the CTA gave up).
+__device__ __forceinline__ void nanosleep_ns(uint32_t ns) {
+  asm volatile("nanosleep.u32 %0;" ::"r"(ns));
+}
+// backoff_ns > 0: sleep that long between polls.  Warps that poll an mbarrier
+// back to back slow the CTA's tensor-core pipe (measured on B300: a chain of
+// 128x128x16 MMAs went from 74 to 104 cycles each with eight polling warps, and
+// stayed at 74 with the same warps sleeping 32 ns between polls), so every
+// waiter except the single MMA-issuing thread backs off.
 __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity,
-                                              const volatile uint32_t* abort, uint64_t limit_ns) {
+                                              const volatile uint32_t* abort, uint64_t limit_ns,
+                                              uint32_t backoff_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 32; ++i) {
+      if (backoff_ns) nanosleep_ns(backoff_ns);
       if (mbar_try_wait(bar, parity)) return true;
+    }
     if (*abort) return false;
     if (globaltimer() - t0 > limit_ns) return false;
   }
 }
+// The MMA-issuing thread's wait: polls (its wake-up latency is on the critical path).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           const volatile uint32_t* abort) {
   return mbar_wait_for(bar, parity, abort, kWaitLimitNs);
+}
+// Every other role's wait: polls with a 32 ns back-off.
+constexpr uint32_t kWaitBackoffNs = 32;
+__device__ __forceinline__ bool mbar_wait_bk(uint32_t bar, uint32_t parity,
+                                             const volatile uint32_t* abort) {
+  return mbar_wait_for(bar, parity, abort, kWaitLimitNs, kWaitBackoffNs);
 }
 
 // Drain wait used while a CTA shuts down after giving up: waits for a phase
