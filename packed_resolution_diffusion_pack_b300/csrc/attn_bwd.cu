@@ -180,25 +180,27 @@ struct BwdCfg {
   static constexpr int KV_OFF_BAR = KV_OFF_VEC + NST * VEC;
   static constexpr int KV_OFF_MISC = KV_OFF_BAR + 256;
   static constexpr int KV_SMEM = KV_OFF_MISC + 64;
-  // q kernel: Q', dO resident; K'_j, V_j through a ring of NSLOT tiles
-  static constexpr int NSLOT = D == 128 ? 5 : 10;
-  static constexpr int Q_OFF_Q = 0, Q_OFF_DO = TILE, Q_OFF_KV = 2 * TILE;
-  static constexpr int Q_OFF_BAR = Q_OFF_KV + NSLOT * TILE;
+  // q kernel: Q', dO resident; K'_j through a ring of KSLOT tiles, V_j of VSLOT
+  static constexpr int KSLOT = 3, VSLOT = 2;
+  static constexpr int Q_OFF_Q = 0, Q_OFF_DO = TILE, Q_OFF_K = 2 * TILE;
+  static constexpr int Q_OFF_V = Q_OFF_K + KSLOT * TILE;
+  static constexpr int Q_OFF_BAR = Q_OFF_V + VSLOT * TILE;
   static constexpr int Q_OFF_MISC = Q_OFF_BAR + 256;
   static constexpr int Q_SMEM = Q_OFF_MISC + 64;
   // TMEM columns
   static constexpr uint32_t KV_ST = 0, KV_DPT = 128, KV_DV = 256, KV_DK = 256 + D;
-  static constexpr uint32_t Q_S0 = 0, Q_DP = 256, Q_DQ = 384;
+  static constexpr uint32_t Q_S = 0, Q_DP = 128, Q_DQ = 384;  // DP: two buffers
   // fp16 where Q', K' and the scaled dS meet; bf16 where the caller's V and dO do
   // (gradient-sized values keep bf16's range there).
   static constexpr uint32_t IDESC_S = idesc_f32acc(128, 128, kF16, 0, 0);   // S^T and S
   static constexpr uint32_t IDESC_DP = idesc_f32acc(128, 128, kBF16, 0, 0); // dP^T and dP
   static constexpr uint32_t IDESC_DV = idesc_f32acc(128, D, kBF16, 0, 1);   // dV (TS)
   static constexpr uint32_t IDESC_DKQ = idesc_f32acc(128, D, kF16, 0, 1);   // dK, dQ (TS)
-  static_assert(KV_OFF_Q % 1024 == 0 && KV_OFF_DO % 1024 == 0 && Q_OFF_KV % 1024 == 0,
+  static_assert(KV_OFF_Q % 1024 == 0 && KV_OFF_DO % 1024 == 0 && Q_OFF_K % 1024 == 0,
                 "swizzled tiles start on 1024-byte boundaries");
   static_assert(KV_SMEM <= 232448 && Q_SMEM <= 232448, "shared memory over the per-CTA limit");
-  static_assert(8 * (2 + 2 * (NST > NSLOT ? NST : NSLOT) + 9) <= 256, "barrier area");
+  static_assert(8 * (2 + 2 * NST + 9) <= 256 && 8 * (2 + 2 * (KSLOT + VSLOT) + 12) <= 256,
+                "barrier areas");
 };
 
 // 384 threads: 170 registers each at launch (65,536 / 384), no reallocation.
@@ -668,9 +670,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ----------------------------------------------------------------- dQ kernel
 // Persistent like the dK / dV kernel: per (sample, head, query tile) item, Q' and
 // dO are loaded once (as soon as the previous item's last S and dP have read
-// theirs), K'_j and V_j run through a ring that carries on across items, and the
-// dQ accumulator is freed for the next item as soon as the elementwise warps
-// have loaded it.
+// theirs) and the dQ accumulator is freed for the next item as soon as the
+// elementwise warps have loaded it.  Per global step g (key tile j of an item):
+//   S_g  -> TMEM S (one buffer: the elementwise warps copy it to registers and
+//           release it at once, so S_{g+1} follows as soon as they have)
+//   dP_g -> TMEM DP[g % 2], issued two steps ahead
+//   dS_g = P (dP - D) ds_mul, written over dP_g in DP[g % 2]
+//   dQ  += dS_g K'_g (TS, dS from TMEM)
+// MMA order per step: S_{g+1}, dQ_g, dP_{g+2}: the dS of step g+1 is computed
+// while the tensor core runs step g's GEMMs.  K'_j goes through a 3-slot ring
+// (read by S_j and dQ_j), V_j through a 2-slot ring (read by dP_j only).
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -689,33 +698,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   if ((*p.status & kFlagBadSeqlens) != 0) return;  // the schedule listed no work
   const uint32_t sQ = sbase + C::Q_OFF_Q, sDO = sbase + C::Q_OFF_DO;
-  const uint32_t sKV = sbase + C::Q_OFF_KV;
+  const uint32_t sK = sbase + C::Q_OFF_K, sV = sbase + C::Q_OFF_V;
   const uint32_t bars = sbase + C::Q_OFF_BAR;
-  const uint32_t bar_q = bars;                         // Q', dO of an item loaded
-  const uint32_t bar_q_free = bars + 8;                // ... and no longer read
-  const uint32_t bar_full = bars + 16;                 // [NSLOT]
-  const uint32_t bar_empty = bar_full + 8 * C::NSLOT;  // [NSLOT]
-  const uint32_t bar_s = bar_empty + 8 * C::NSLOT;     // [2] S in TMEM S[g % 2]
-  const uint32_t bar_dp = bar_s + 16;                  // dP in TMEM
-  const uint32_t bar_ds = bar_dp + 8;                  // dS in TMEM (256 arrivals)
-  const uint32_t bar_o = bar_ds + 8;                   // an item's dQ complete
-  const uint32_t bar_acc_free = bar_o + 8;             // ... and loaded (256 arrivals)
+  const uint32_t bar_q = bars;                          // Q', dO of an item loaded
+  const uint32_t bar_q_free = bars + 8;                 // ... and no longer read
+  const uint32_t bar_kfull = bars + 16;                 // [KSLOT]
+  const uint32_t bar_kempty = bar_kfull + 8 * C::KSLOT;  // [KSLOT]
+  const uint32_t bar_vfull = bar_kempty + 8 * C::KSLOT;  // [VSLOT]
+  const uint32_t bar_vempty = bar_vfull + 8 * C::VSLOT;  // [VSLOT]
+  const uint32_t bar_s = bar_vempty + 8 * C::VSLOT;      // S in TMEM
+  const uint32_t bar_s_free = bar_s + 8;                 // ... copied out (256 arrivals)
+  const uint32_t bar_dp = bar_s_free + 8;                // [2] dP in DP[g % 2]
+  const uint32_t bar_ds = bar_dp + 16;                   // [2] dS in DP[g % 2] (256 arrivals)
+  const uint32_t bar_o = bar_ds + 16;                    // an item's dQ complete
+  const uint32_t bar_acc_free = bar_o + 8;               // ... and loaded (256 arrivals)
   const uint32_t bar_drain = bar_acc_free + 8;
-  const uint32_t bar_stall = bar_drain + 8;            // test hook: never arrived on
+  const uint32_t bar_stall = bar_drain + 8;              // test hook: never arrived on
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     s_abort = 0;
     mbar_init(bar_q, 1);
     mbar_init(bar_q_free, 1);
-    for (int i = 0; i < C::NSLOT; ++i) {
-      mbar_init(bar_full + 8 * i, 1);
-      mbar_init(bar_empty + 8 * i, 1);
+    for (int i = 0; i < C::KSLOT; ++i) {
+      mbar_init(bar_kfull + 8 * i, 1);
+      mbar_init(bar_kempty + 8 * i, 1);
+    }
+    for (int i = 0; i < C::VSLOT; ++i) {
+      mbar_init(bar_vfull + 8 * i, 1);
+      mbar_init(bar_vempty + 8 * i, 1);
     }
     mbar_init(bar_s, 1);
-    mbar_init(bar_s + 8, 1);
+    mbar_init(bar_s_free, 256);
     mbar_init(bar_dp, 1);
+    mbar_init(bar_dp + 8, 1);
     mbar_init(bar_ds, 256);
+    mbar_init(bar_ds + 8, 256);
     mbar_init(bar_o, 1);
     mbar_init(bar_acc_free, 256);
     mbar_init(bar_drain, 1);
@@ -740,7 +758,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
       bool ok = true;
-      int32_t gc = 0, items = 0;  // K'/V copies issued (all items), items started
+      int32_t gs = 0, items = 0;  // steps (K', V copies) of earlier items, items started
       WorkItemB w;
       for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
         const int32_t q0 = w.blk * C::BQ, nk = (w.len + C::BK - 1) / C::BK;
@@ -754,26 +772,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(sDO + ch * C::CHUNK, &tm_do, bar_q, ch * 64, w.head, w.start + q0);
         }
         ++items;
-        // K'_j, V_j alternate through the ring: copy 2j (K'_j), 2j + 1 (V_j)
-        for (int32_t c = 0; c < 2 * nk; ++c, ++gc) {
-          const int32_t slot = gc % C::NSLOT, use = gc / C::NSLOT;
-          if (use > 0 && !mbar_wait_bk(bar_empty + 8 * slot, (use - 1) & 1, &s_abort)) {
+        for (int32_t j = 0; j < nk; ++j) {
+          const int32_t g = gs + j;
+          const int32_t ks = g % C::KSLOT, ku = g / C::KSLOT;
+          if (ku > 0 && !mbar_wait_bk(bar_kempty + 8 * ks, (ku - 1) & 1, &s_abort)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar_full + 8 * slot, C::TILE);
+          mbar_arrive_expect_tx(bar_kfull + 8 * ks, C::TILE);
           for (int ch = 0; ch < D / 64; ++ch)
-            tma_load_3d(sKV + slot * C::TILE + ch * C::CHUNK, (c & 1) ? &tm_v : &tm_k,
-                        bar_full + 8 * slot, ch * 64, w.head, w.start + (c >> 1) * C::BK);
+            tma_load_3d(sK + ks * C::TILE + ch * C::CHUNK, &tm_k, bar_kfull + 8 * ks, ch * 64,
+                        w.head, w.start + j * C::BK);
+          const int32_t vs = g % C::VSLOT, vu = g / C::VSLOT;
+          if (vu > 0 && !mbar_wait_bk(bar_vempty + 8 * vs, (vu - 1) & 1, &s_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar_vfull + 8 * vs, C::TILE);
+          for (int ch = 0; ch < D / 64; ++ch)
+            tma_load_3d(sV + vs * C::TILE + ch * C::CHUNK, &tm_v, bar_vfull + 8 * vs, ch * 64,
+                        w.head, w.start + j * C::BK);
         }
+        gs += nk;
       }
       if (!ok) {
         s_abort = 1;
         atomicOr(p.status, kFlagTimeout);
       }
+      // every issued copy lands before the CTA exits: at most one per slot is in
+      // flight (a slot is reloaded only after its previous copy was consumed)
       if (items > 0) mbar_wait_drain(bar_q, (items - 1) & 1);
-      for (int32_t c = (gc > C::NSLOT ? gc - C::NSLOT : 0); c < gc; ++c)
-        mbar_wait_drain(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1);
+      for (int32_t g = (gs > C::KSLOT ? gs - C::KSLOT : 0); g < gs; ++g)
+        mbar_wait_drain(bar_kfull + 8 * (g % C::KSLOT), (g / C::KSLOT) & 1);
+      for (int32_t g = (gs > C::VSLOT ? gs - C::VSLOT : 0); g < gs; ++g)
+        mbar_wait_drain(bar_vfull + 8 * (g % C::VSLOT), (g / C::VSLOT) & 1);
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
@@ -783,70 +815,64 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         return r;
       };
-      auto kv_wait = [&](int32_t c) {
-        return wait(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1);
-      };
       const uint64_t dQ_k = sdesc_sw128(sQ, 16, 1024), dO_k = sdesc_sw128(sDO, 16, 1024);
-      const uint64_t kv_k = sdesc_sw128(sKV, 16, 1024);        // K' / V as K-major B
-      const uint64_t kv_m = sdesc_sw128(sKV, C::CHUNK, 1024);  // K' as MN-major B
+      const uint64_t k_k = sdesc_sw128(sK, 16, 1024);        // K' as K-major B (S)
+      const uint64_t k_m = sdesc_sw128(sK, C::CHUNK, 1024);  // K' as MN-major B (dQ)
+      const uint64_t v_k = sdesc_sw128(sV, 16, 1024);        // V as K-major B (dP)
       constexpr uint64_t kTile = C::TILE >> 4;
-      // S of global step g (its K' is copy c) -> S[g % 2]; dP (V is copy c) -> DP
-      auto issue_s = [&](int32_t g, int32_t c) {
-        const uint64_t b = kv_k + (c % C::NSLOT) * kTile;
-        const uint32_t d = tmem + C::Q_S0 + (g & 1) * 128;
+      auto issue_s = [&](int32_t g) {  // S_g = Q' K'_g^T -> S
+        if (!wait(bar_kfull + 8 * (g % C::KSLOT), (g / C::KSLOT) & 1)) return false;
+        const uint64_t b = k_k + (g % C::KSLOT) * kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(d, dQ_k + kofs<D>(kk), b + kofs<D>(kk), C::IDESC_S, kk > 0);
-        mma_commit(bar_s + 8 * (g & 1));
+          mma_ss(tmem + C::Q_S, dQ_k + kofs<D>(kk), b + kofs<D>(kk), C::IDESC_S, kk > 0);
+        mma_commit(bar_s);
+        return true;
       };
-      auto issue_dp = [&](int32_t c) {
-        const uint64_t b = kv_k + (c % C::NSLOT) * kTile;
+      auto issue_dp = [&](int32_t g) {  // dP_g = dO V_g^T -> DP[g % 2]; V_g then released
+        if (!wait(bar_vfull + 8 * (g % C::VSLOT), (g / C::VSLOT) & 1)) return false;
+        const uint64_t b = v_k + (g % C::VSLOT) * kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::Q_DP, dO_k + kofs<D>(kk), b + kofs<D>(kk), C::IDESC_DP, kk > 0);
-        mma_commit(bar_dp);
+          mma_ss(tmem + C::Q_DP + (g & 1) * 128, dO_k + kofs<D>(kk), b + kofs<D>(kk),
+                 C::IDESC_DP, kk > 0);
+        mma_commit(bar_dp + 8 * (g & 1));
+        mma_commit(bar_vempty + 8 * (g % C::VSLOT));
+        return true;
       };
       bool ok = p.stall_us == 0 ||
                 mbar_wait_for(bar_stall, 0, &s_abort, static_cast<uint64_t>(p.stall_us) * 1000u);
-      int32_t gs = 0, gc = 0;  // steps and K'/V copies of earlier items
+      int32_t gs = 0;  // steps of earlier items
       WorkItemB w;
       for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
         const int32_t nk = (w.len + C::BK - 1) / C::BK;
-        if (!(ok = wait(bar_q, k & 1) && kv_wait(gc))) break;
-        issue_s(gs, gc);
-        if (nk > 1) {
-          if (!(ok = kv_wait(gc + 2))) break;
-          issue_s(gs + 1, gc + 2);
-        }
-        if (!(ok = kv_wait(gc + 1))) break;
-        issue_dp(gc + 1);
+        if (!(ok = wait(bar_q, k & 1))) break;
+        // S is free once the elementwise warps have copied out the previous step's
+        if (gs > 0 && !(ok = wait(bar_s_free, (gs - 1) & 1))) break;
+        if (!(ok = issue_s(gs) && issue_dp(gs))) break;
+        if (nk > 1 && !(ok = issue_dp(gs + 1))) break;
         for (int32_t j = 0; j < nk; ++j) {
-          const int32_t g = gs + j, c = gc + 2 * j;
+          const int32_t g = gs + j;
           if (j == nk - 1) mma_commit(bar_q_free);  // the item's last S and dP are issued
-          if (!(ok = wait(bar_ds, g & 1))) break;   // dS in S[g % 2]; DP read
+          if (j + 1 < nk) {  // S_{g+1} once S_g is copied out
+            if (!(ok = wait(bar_s_free, g & 1) && issue_s(g + 1))) break;
+          }
+          if (!(ok = wait(bar_ds + 8 * (g & 1), (g >> 1) & 1))) break;  // dS_g in DP[g % 2]
           // the previous item's accumulator must have been loaded
           if (j == 0 && k > 0 && !(ok = wait(bar_acc_free, (k - 1) & 1))) break;
-          const uint64_t kb = kv_m + (c % C::NSLOT) * kTile;
-          const uint32_t sa = tmem + C::Q_S0 + (g & 1) * 128;
+          const uint64_t kb = k_m + (g % C::KSLOT) * kTile;
+          const uint32_t da = tmem + C::Q_DP + (g & 1) * 128;
 #pragma unroll
-          for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K'_j
-            mma_ts(tmem + C::Q_DQ, sa + packed_col(kk), kb + mofs(kk), C::IDESC_DKQ,
+          for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K'_g
+            mma_ts(tmem + C::Q_DQ, da + packed_col(kk), kb + mofs(kk), C::IDESC_DKQ,
                    (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar_empty + 8 * (c % C::NSLOT));        // K'_j
-          mma_commit(bar_empty + 8 * ((c + 1) % C::NSLOT));  // V_j
-          if (j + 1 < nk) {  // DP is free once the dS warps have read dP
-            if (!(ok = kv_wait(c + 3))) break;
-            issue_dp(c + 3);
-          }
-          if (j + 2 < nk) {  // S[g % 2] is free once dQ (issued above) has read dS
-            if (!(ok = kv_wait(c + 4))) break;
-            issue_s(g + 2, c + 4);
-          }
+          mma_commit(bar_kempty + 8 * (g % C::KSLOT));  // K'_g read by S_g and dQ
+          // DP[g % 2] is free once dQ (issued above) has read dS_g
+          if (j + 2 < nk && !(ok = issue_dp(g + 2))) break;
         }
         if (!ok) break;
         mma_commit(bar_o);
         gs += nk;
-        gc += 2 * nk;
       }
       if (!ok) {
         s_abort = 1;
@@ -860,7 +886,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int h = warp >> 2;                 // key half: columns [64h, 64h + 64)
     const uint32_t row = threadIdx.x & 127;  // query row in the tile = TMEM lane
     const uint32_t lane_off = ((warp & 3) * 32) << 16;
-    const uint32_t tDP = tmem + lane_off + C::Q_DP + 64 * h;
+    const uint32_t tS = tmem + lane_off + C::Q_S + 64 * h;
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
     float dsmax = 0.f;
@@ -880,41 +906,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t dsm2 = f32x2_pack(ds_mul, ds_mul), d2 = f32x2_pack(drow, drow);
       for (int32_t j = 0; j < nk; ++j) {
         const int32_t g = gs + j;
-        const uint32_t tS = tmem + lane_off + C::Q_S0 + (g & 1) * 128 + 64 * h;
-        ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_s + 8 * (g & 1), (g >> 1) & 1, &s_abort));
+        const uint32_t tDP = tmem + lane_off + C::Q_DP + (g & 1) * 128 + 64 * h;
+        ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_s, g & 1, &s_abort));
         if (!ok) break;
         tc_fence_after();
+        // S to registers, released at once
+        uint32_t r[64];
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tS, r0);
+          tmem_ld32(tS + 32, r1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            r[c] = r0[c];
+            r[32 + c] = r1[c];
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar_s_free);
         // P = exp2(S scale log2e - LSE log2e) over this half's 64 keys; keys past
         // the sample end get P = 0
         const int32_t nvalid = w.len - j * C::BK - 64 * h;
         uint64_t pr2[32];
-        {
-          uint32_t r[64];
-          {
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tS, r0);
-            tmem_ld32(tS + 32, r1);
-            tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              r[c] = r0[c];
-              r[32 + c] = r1[c];
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const uint64_t x = f32x2_fma(
-                f32x2_pack(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), sl2x2, nl2x2);
-            float x0, x1;
-            f32x2_unpack(x, x0, x1);
-            pr2[u] = f32x2_pack(2 * u < nvalid ? ex2_approx(x0) : 0.f,
-                                2 * u + 1 < nvalid ? ex2_approx(x1) : 0.f);
-          }
+        for (int u = 0; u < 32; ++u) {
+          const uint64_t x = f32x2_fma(
+              f32x2_pack(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), sl2x2, nl2x2);
+          float x0, x1;
+          f32x2_unpack(x, x0, x1);
+          pr2[u] = f32x2_pack(2 * u < nvalid ? ex2_approx(x0) : 0.f,
+                              2 * u + 1 < nvalid ? ex2_approx(x1) : 0.f);
         }
-        ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_dp, g & 1, &s_abort));
+        ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_dp + 8 * (g & 1), (g >> 1) & 1, &s_abort));
         if (!ok) break;
         tc_fence_after();
-        // dS = P (dP - D) ds_mul, fp16 into S[g % 2] columns [64h, 64h + 32)
+        // dS = P (dP - D) ds_mul, fp16 over dP in DP[g % 2] columns [64h, 64h + 32)
+        // (each 32-column load is complete before the columns it overlaps are
+        // rewritten)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t rd[32];
@@ -931,11 +960,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             dsmax = fmax3(dsmax, fabsf(ds0), fabsf(ds1));
             pd[u] = pack_f16x2(ds0, ds1);
           }
-          tmem_st16(tS + c * 16, pd);
+          tmem_st16(tDP + c * 16, pd);
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar_ds);
+        mbar_arrive(bar_ds + 8 * (g & 1));
       }
       if (!ok) break;
       // epilogue: this warpgroup's columns [h D/2, (h + 1) D/2) of dQ into
