@@ -445,6 +445,7 @@ def gpu_arm(args):
             else:
                 ach = amount / (pl["ms_per_launch"] / 1e3) / 1e9
                 pl.update(achieved_gbs=ach, frac_of_hbm=ach / pk["hbm_gbs"])
+            pl.update(algorithmic=amount, traffic=_recorded_traffic(name))
     dom = max(("attn_fwd", "attn_bwd", "attn_bwd_q"), key=lambda nm: kern[nm][0])
     traffic = _recorded_traffic(dom)
     ach = per_launch[dom]["achieved_tflops"]
@@ -528,6 +529,8 @@ def neighbours(mf, wl, hbm_gbs, reps=20):
         "cfg_euler_step": (lambda: mf.cfg_euler_step(v, specs, 4.0, 0.05, z), 12.0 * N * C,
                            f"32 pairs of 2048^2 (16384 image tokens each), C={C}"),
     }
+    traffic_name = {"adaln_modulate": "adaln", "gated_residual": "gated_residual",
+                    "cfg_euler_step": "cfg_euler"}
     out = {}
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for name, (fn, nbytes, shape) in cases.items():
@@ -542,7 +545,7 @@ def neighbours(mf, wl, hbm_gbs, reps=20):
         ms = ev0.elapsed_time(ev1) / reps
         gbs = nbytes / (ms / 1e3) / 1e9
         out[name] = {"ms": ms, "achieved_gbs": gbs, "frac_of_hbm": gbs / hbm_gbs, "shape": shape,
-                     "bytes": nbytes}
+                     "bytes": nbytes, "traffic": _recorded_traffic(traffic_name[name])}
     return out
 
 
@@ -589,6 +592,7 @@ def fp8_forward(mf, wl, qd, kd, vd, cu, pos, max_len, ws, peak_bf16, hbm_gbs, re
         "amax_frac_of_hbm": amax_bytes / (per("f8_amax") / 1e3) / 1e9 / hbm_gbs,
         "quant_ms": per("f8_quant"),
         "quant_frac_of_hbm": quant_bytes / (per("f8_quant") / 1e3) / 1e9 / hbm_gbs,
+        "amax_traffic": _recorded_traffic("f8_amax"), "quant_traffic": _recorded_traffic("f8_quant"),
         "roofline": {"bound": "tensor", "kernel": "attn_fwd_f8",
                      "achieved": flops / (attn_ms / 1e3) / 1e12, "peak": peak8, "unit": "TFLOP/s",
                      "frac": flops / (attn_ms / 1e3) / 1e12 / peak8,
