@@ -487,6 +487,8 @@ def gpu_arm(args):
     }
     if not args.no_extras:
         line["extras"] = neighbours(mf, wl, pk["hbm_gbs"])
+        line["extras"]["forward_only"] = forward_only(mf, wl, qd, kd, vd, cu, pos, max_len, ws,
+                                                      peak_tc)
         if d == 128:
             line["extras"]["fp8_forward"] = fp8_forward(mf, wl, qd, kd, vd, cu, pos, max_len, ws,
                                                         peak_tc, pk["hbm_gbs"])
@@ -546,6 +548,52 @@ def neighbours(mf, wl, hbm_gbs, reps=20):
         gbs = nbytes / (ms / 1e3) / 1e9
         out[name] = {"ms": ms, "achieved_gbs": gbs, "frac_of_hbm": gbs / hbm_gbs, "shape": shape,
                      "bytes": nbytes, "traffic": _recorded_traffic(traffic_name[name])}
+    return out
+
+
+def forward_only(mf, wl, qd, kd, vd, cu, pos, max_len, ws, peak_bf16, reps=10):
+    """The forward alone (a sampling step's attention), outside the timed step, in
+    its two forms on the same pack: the two-pass call (mf_varlen_attn_fwd: the fp16
+    rotation pre-pass, then attention on the rotated operands) and the
+    rotate-on-load call (mf_varlen_attn_fwd_fused_rope: a (cos, sin) table, then
+    attention that rotates the bf16 Q and K tiles in shared memory).  Both give the
+    same O and LSE bit for bit.  Each call timed with CUDA events over `reps` calls,
+    and each kernel's device time."""
+    import torch
+    T, h = wl.total, wl.heads
+    o = torch.empty_like(qd)
+    lse = torch.empty((h, T), dtype=torch.float32, device="cuda")
+    flops = wl.flops_fwd()
+    forms = {
+        "two_pass": (lambda: mf.varlen_attn_fwd(qd, kd, vd, cu, pos, max_len, o=o, lse=lse, ws=ws),
+                     ("schedule", "rope", "attn_fwd")),
+        "fused_rope": (lambda: mf.varlen_attn_fwd_fused_rope(qd, kd, vd, cu, pos, max_len, o=o,
+                                                             lse=lse, ws=ws),
+                       ("schedule", "rope_table", "attn_fwd_rot")),
+    }
+    out = {}
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for name, (call, kernels) in forms.items():
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        mf.timing_enable(True)
+        mf.timing_reset()
+        ev0.record()
+        for _ in range(reps):
+            call()
+        ev1.record()
+        torch.cuda.synchronize()
+        kern = mf.timing_read()
+        mf.timing_enable(False)
+        mf.get_status(ws)
+        ms = ev0.elapsed_time(ev1) / reps
+        per = {k: kern[k][0] / max(1, kern[k][1]) for k in kernels}
+        attn_ms = per[kernels[-1]]
+        out[name] = {"ms_per_call": ms, "tflops_per_call": flops / (ms / 1e3) / 1e12,
+                     "kernel_ms": per, "attn_tflops": flops / (attn_ms / 1e3) / 1e12,
+                     "attn_frac": flops / (attn_ms / 1e3) / 1e12 / peak_bf16}
+    out["fused_over_two_pass"] = out["two_pass"]["ms_per_call"] / out["fused_rope"]["ms_per_call"]
     return out
 
 

@@ -149,6 +149,31 @@ mf_status mf_varlen_attn_fwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
                              size_t ws_bytes, mf_stream stream);
 
 /*
+ * The same forward with the 2D RoPE applied on the tile load (no rotation
+ * pre-pass): the attention kernel's TMA warp stages the caller's bf16 Q, K and V
+ * tiles in shared memory, two further warps rotate the Q and K tiles there (and
+ * convert V to the kernel's fp16 operand type) in place, and the tensor core reads
+ * the result.  The angles come from a small (cos, sin) table of v * omega_P for
+ * v in [0, min(max_len, T)), built by one launch per call from the same
+ * evaluation the pre-pass uses, so O and LSE are bit-identical to
+ * mf_varlen_attn_fwd's for the same inputs.  Arguments, shapes, workspace
+ * (mf_attn_workspace_bytes(..., 0)) and errors as mf_varlen_attn_fwd, plus: a
+ * position outside [0, min(max_len, T)) is an error recorded in the workspace
+ * (mf_get_status: MF_ERR_INVALID_ARG; such a coordinate is read as 0).  Positions
+ * from mf_pack always lie in that range (r < H and c < W, each at most L_i).
+ * It leaves no rotated operands in the workspace: a training step's backward
+ * after it is mf_varlen_attn_bwd, not mf_varlen_attn_bwd_after_fwd.
+ * Defined by: paperlayer.ai 3.3 "Training Infrastructure" (rotary embeddings
+ * inside the fused Transformer chain) and 3.2.1 (the attention); rcap.io post
+ * (per_sample_2d_rope applied within the packed step).
+ */
+mf_status mf_varlen_attn_fwd_fused_rope(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                        const int32_t* d_cu_seqlens, const int32_t* d_pos,
+                                        int32_t n, int32_t T, int32_t max_len, int32_t heads,
+                                        int32_t head_dim, float softmax_scale, mf_bf16* o,
+                                        float* lse, void* ws, size_t ws_bytes, mf_stream stream);
+
+/*
  * Varlen attention backward (gradients with respect to the UN-rotated q and k,
  * i.e. the rotation's transpose R(-theta) is folded in).
  * q, k, v, o, d_o: DEVICE bf16 [T][heads][head_dim]; lse: DEVICE fp32 [heads][T]
@@ -431,12 +456,14 @@ mf_status mf_test_varlen_attn_bwd_stalled(const mf_bf16* q, const mf_bf16* k, co
  * milliseconds and the number of launches since the last reset.  Ids:
  *   MF_K_PACK 0, MF_K_ROPE 1, MF_K_SCHEDULE 2, MF_K_ATTN_FWD 3, MF_K_BWD_PRE 4,
  *   MF_K_ATTN_BWD 5 (dK, dV), MF_K_ATTN_BWD_Q 6 (dQ), MF_K_CFG_EULER 7, MF_K_ADALN 8,
- *   MF_K_GATED_RESIDUAL 9, MF_K_F8_AMAX 10, MF_K_F8_QUANT 11, MF_K_ATTN_FWD_F8 12.
+ *   MF_K_GATED_RESIDUAL 9, MF_K_F8_AMAX 10, MF_K_F8_QUANT 11, MF_K_ATTN_FWD_F8 12,
+ *   MF_K_ROPE_TABLE 13, MF_K_ATTN_FWD_ROT 14 (the rotate-on-load forward's table and
+ *   attention kernels).
  * Process-wide state guarded by a mutex; not for use under stream capture.
  */
 enum { MF_K_PACK = 0, MF_K_ROPE, MF_K_SCHEDULE, MF_K_ATTN_FWD, MF_K_BWD_PRE, MF_K_ATTN_BWD,
        MF_K_ATTN_BWD_Q, MF_K_CFG_EULER, MF_K_ADALN, MF_K_GATED_RESIDUAL, MF_K_F8_AMAX,
-       MF_K_F8_QUANT, MF_K_ATTN_FWD_F8, MF_K_COUNT };
+       MF_K_F8_QUANT, MF_K_ATTN_FWD_F8, MF_K_ROPE_TABLE, MF_K_ATTN_FWD_ROT, MF_K_COUNT };
 mf_status mf_timing_enable(int32_t on);
 mf_status mf_timing_reset(void);
 mf_status mf_timing_read(int32_t id, double* total_ms, int64_t* launches);

@@ -20,6 +20,7 @@ __all__ = [
     "attn_workspace_bytes", "workspace", "varlen_attn_fwd", "varlen_attn_bwd", "get_status",
     "cfg_euler_step", "adaln_modulate", "gated_residual", "pack3d_size", "pack3d", "rope3d_qk",
     "varlen_attn_fwd_fp8", "quant_e4m3", "varlen_attn_fwd_noalloc", "noalloc_get_status",
+    "varlen_attn_fwd_fused_rope",
 ]
 
 
@@ -187,6 +188,30 @@ def varlen_attn_fwd(q, k, v, cu_seqlens, pos, max_len, softmax_scale: float = 0.
     check(getattr(load(), fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(pos), n, T,
                               int(max_len), h, d, float(softmax_scale), _ptr(o), _ptr(lse),
                               _ptr(ws), ws.numel(), _stream_ptr(stream)), fn)
+    return o, lse
+
+
+def varlen_attn_fwd_fused_rope(q, k, v, cu_seqlens, pos, max_len, softmax_scale: float = 0.0,
+                               o=None, lse=None, ws=None, stream=None):
+    """varlen_attn_fwd with the 2D RoPE applied on the attention kernel's tile load
+    (no rotation pre-pass; pos [T, 2] int32 or None).  Same outputs, bit for bit.
+    The workspace keeps no rotated operands: a backward after it is varlen_attn_bwd
+    with after_fwd=False.  Returns (o [T, h, d] bf16, lse [h, T] fp32)."""
+    torch = _torch()
+    if _is_3d(pos):
+        raise ValueError("varlen_attn_fwd_fused_rope takes 2D positions [T, 2]")
+    _check_thd("q", q)
+    T, h, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        _check_thd(name, t, T, h, d)
+    n = cu_seqlens.numel() - 1
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((h, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = workspace(T, n, h, d, False, q.device) if ws is None else ws
+    check(load().mf_varlen_attn_fwd_fused_rope(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(pos), n, T, int(max_len), h, d,
+        float(softmax_scale), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream_ptr(stream)),
+        "mf_varlen_attn_fwd_fused_rope")
     return o, lse
 
 

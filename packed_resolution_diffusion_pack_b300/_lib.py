@@ -31,6 +31,8 @@ SIGNATURES = {
     "mf_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "mf_varlen_attn_fwd": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32,
                                           _p, _p, _p, _sz, _p]),
+    "mf_varlen_attn_fwd_fused_rope": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32,
+                                                     _i32, _f32, _p, _p, _p, _sz, _p]),
     "mf_varlen_attn_bwd": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32,
                                           _i32, _f32, _p, _p, _p, _p, _sz, _p]),
     "mf_varlen_attn_bwd_after_fwd": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _i32, _i32,
@@ -67,7 +69,8 @@ SIGNATURES = {
 
 # kernel ids of the opt-in timing (mf.h MF_K_*)
 KERNELS = ["pack", "rope", "schedule", "attn_fwd", "bwd_pre", "attn_bwd", "attn_bwd_q", "cfg_euler",
-           "adaln", "gated_residual", "f8_amax", "f8_quant", "attn_fwd_f8"]
+           "adaln", "gated_residual", "f8_amax", "f8_quant", "attn_fwd_f8", "rope_table",
+           "attn_fwd_rot"]
 
 
 class MFError(RuntimeError):

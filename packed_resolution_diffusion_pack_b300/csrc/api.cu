@@ -215,6 +215,59 @@ static mf_status attn_fwd_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16
   return cuda_status(launch_attn_fwd(a, s));
 }
 
+// The forward with the rotation applied on the tile load: schedule, the (cos, sin)
+// table, and the attention kernel on the caller's bf16 q, k, v.
+static mf_status attn_fwd_rot_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                   const int32_t* d_cu_seqlens, const int32_t* d_pos, int32_t n,
+                                   int32_t T, int32_t max_len, int32_t heads, int32_t head_dim,
+                                   float softmax_scale, mf_bf16* o, float* lse, void* ws,
+                                   size_t ws_bytes, mf_stream stream) {
+  const void* ptrs[5] = {q, k, v, o, lse};
+  mf_status st = check_attn(ptrs, 5, d_cu_seqlens, n, T, max_len, heads, head_dim, ws, ws_bytes,
+                            false);
+  if (st != MF_OK) return st;
+  if (d_pos != nullptr && !aligned(d_pos, 8)) return MF_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(T, n, heads, head_dim, false);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  auto* status = reinterpret_cast<uint32_t*>(w + L.status);
+  auto* order = reinterpret_cast<int32_t*>(w + L.order);
+  auto* prefix = reinterpret_cast<int32_t*>(w + L.prefix);
+  cudaError_t e =
+      launch_schedule(d_cu_seqlens, n, T, max_len, heads, 256, status, order, prefix, nullptr, 0, s);
+  if (e != cudaSuccess) return MF_ERR_CUDA;
+  if (T == 0) return MF_OK;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(head_dim));
+  // table rows: every coordinate of a valid pack is below max(H, W) <= L_i <= max_len
+  // (and below T); 4 T head_dim bytes at most, inside the operand region
+  const int32_t rows = max_len < T ? (max_len > 0 ? max_len : 1) : T;
+  auto* rtab = reinterpret_cast<float*>(w + L.q16);
+  if (d_pos != nullptr) {
+    e = launch_rope_table(head_dim, rows, rtab, s);
+    if (e != cudaSuccess) return MF_ERR_CUDA;
+  }
+  AttnFwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.rot = true;
+  a.pos = d_pos;
+  a.rtab = rtab;
+  a.rtab_rows = rows;
+  a.cu = d_cu_seqlens;
+  a.order = order;
+  a.prefix = prefix;
+  a.status = status;
+  a.o = o;
+  a.lse = lse;
+  a.n = n;
+  a.T = T;
+  a.heads = heads;
+  a.head_dim = head_dim;
+  a.scale = scale;
+  return cuda_status(launch_attn_fwd(a, s));
+}
+
 // The 8-bit variant of the forward: E4M3 operands with per-row Q and per-head K,
 // V scales, E4M3 probabilities, fp32 accumulation; head_dim 128.
 static mf_status attn_fwd_e4m3_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
@@ -341,6 +394,15 @@ mf_status mf_varlen_attn_fwd(const mf_bf16* q, const mf_bf16* k, const mf_bf16* 
                              size_t ws_bytes, mf_stream stream) {
   return attn_fwd_impl(q, k, v, d_cu_seqlens, d_pos, 2, n, T, max_len, heads, head_dim,
                        softmax_scale, o, lse, ws, ws_bytes, stream);
+}
+
+mf_status mf_varlen_attn_fwd_fused_rope(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
+                                        const int32_t* d_cu_seqlens, const int32_t* d_pos,
+                                        int32_t n, int32_t T, int32_t max_len, int32_t heads,
+                                        int32_t head_dim, float softmax_scale, mf_bf16* o,
+                                        float* lse, void* ws, size_t ws_bytes, mf_stream stream) {
+  return attn_fwd_rot_impl(q, k, v, d_cu_seqlens, d_pos, n, T, max_len, heads, head_dim,
+                           softmax_scale, o, lse, ws, ws_bytes, stream);
 }
 
 mf_status mf_test_varlen_attn_fwd_stalled(const mf_bf16* q, const mf_bf16* k, const mf_bf16* v,
@@ -561,6 +623,7 @@ mf_status mf_get_status(void* ws, mf_stream stream) {
   if (flags & kFlagTimeout) return MF_ERR_TIMEOUT;
   if (flags & kFlagFp16Range) return MF_ERR_OVERFLOW;
   if (flags & kFlagSmemAlign) return MF_ERR_CUDA;
+  if (flags & kFlagPosRange) return MF_ERR_INVALID_ARG;
   return MF_OK;
 }
 

@@ -15,7 +15,11 @@
 //               fp16 (11 significant bits), accumulation fp32.  The two Q tiles
 //               ping-pong so the tensor core works on one while the other's
 //               softmax runs.
-//   warps 10-11 idle (they complete the third warpgroup).
+//   warps 10-11 idle (they complete the third warpgroup), except in the
+//               rotate-on-load form (ROT): there they apply the 2D rotation to
+//               the bf16 Q and K tiles in shared memory as soon as TMA has
+//               landed them, and convert the V tiles to fp16, in place (see
+//               rot_tile below), before the MMA issuer may read them.
 //   warps 0-7   two softmax warpgroups, one per Q tile; thread = query row =
 //               TMEM lane.  Online softmax in base 2: row max by a tree of
 //               three-input maxima, packed two-lane FMAs and adds around the
@@ -231,8 +235,9 @@ constexpr uint32_t kFwdRegsLow = 88, kFwdRegsHigh = 208;
 static_assert(128 * kFwdRegsLow + 256 * kFwdRegsHigh <= kFwdThreads * 168,
               "forward register split exceeds the launch total");
 
-// F8: the 8-bit variant (E4M3 operands and probabilities, head_dim 128).
-template <int D, bool F8>
+// F8: the 8-bit variant (E4M3 operands and probabilities, head_dim 128); ROT: the
+// rotate-on-load form (a larger barrier region and the staged positions).
+template <int D, bool F8, bool ROT = false>
 struct FwdCfg {
   static constexpr int BM = 128;                  // query rows per Q tile
   static constexpr int BN = 128;                  // keys per K/V tile
@@ -249,8 +254,11 @@ struct FwdCfg {
   static constexpr int OFF_STG = OFF_KV + NSLOT * TILE;
   static constexpr int STG = F8 ? 2 * BM * D * 2 : 0;
   static constexpr int OFF_BAR = OFF_STG + STG;
-  static constexpr int OFF_MISC = OFF_BAR + 256;
-  static constexpr int SMEM = OFF_MISC + 64;
+  static constexpr int OFF_MISC = OFF_BAR + (ROT ? 512 : 256);
+  // rotate-on-load form: token positions staged per transform warp, int2 [2][192]
+  // (its rows of Q tile 0, Q tile 1 and the current K tile)
+  static constexpr int OFF_POS = OFF_MISC + 64;
+  static constexpr int SMEM = OFF_POS + (ROT ? 2 * 192 * 8 : 0);
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
   // S = Q'K'^T and O += P V' (V' MN-major); operand format code 0 is fp16 under
   // kind::f16 and E4M3 under kind::f8f6f4
@@ -279,14 +287,152 @@ struct FwdParams {
   // microseconds, on a barrier that nothing arrives on, so the CTA takes its
   // time-out path (failure-detection tests; never set by the product calls)
   uint32_t stall_us;
+  // rotate-on-load form only: (r, c) per token (null: no rotation), and the
+  // (cos, sin) table of angle v * omega_P for v in [0, rtab_rows), [v][D/2]
+  const int32_t* pos;
+  const float4* rtab;
+  int32_t rtab_rows;
 };
 
-template <int D, bool F8>
+// ------------------------------------------------------ rotation on load
+// One bf16 tile of 128 token rows x D in shared memory, as TMA lands it (64-column
+// chunks of 128 rows x 128 bytes, the 16-byte units of row r XOR-swizzled by
+// r % 8), rewritten in place as the fp16 operand the 16-bit forward's pre-pass
+// would have produced for those rows: with ROTATE, pair P = (2P, 2P + 1) of the
+// row of token t turned by the angle pos[t][axis_P] * omega_P,
+//   y0 = x0 cos - x1 sin,  y1 = x0 sin + x1 cos   (fp32: a product, then one FMA),
+// the first D/4 pairs by the row coordinate r and the rest by the column c
+// (paperlayer.ai summary 3.2.1, per-sample 2D rotary positions); without, the
+// bf16 values converted.  Same fp32 operations and roundings as the pre-pass, so
+// the operands, and hence O and LSE, are bit-identical to the two-pass forward's.
+// Rows past the pack (zero-filled by TMA) are left unrotated.  vmax collects the
+// largest |y| (fp16 range check); a position outside [0, rtab_rows) sets `bad`
+// and is read as 0.
+//
+// The 64 threads of warps 10-11 share a tile.  Thread tid owns the 16-byte unit
+// column tid % 8 of rows tid / 8 + 8 i (i < 16) in every chunk: 8 consecutive
+// lanes cover one 128-byte row chunk (conflict-free), and since r % 8 is the same
+// for all of a thread's rows, so is its logical unit, hence its 4 pairs.  A warp's
+// rows are those with (r / 4) % 2 = its index; their positions come staged in
+// shared memory (spos[m] for row (m % 4) + 8 (m / 4) + 4 warp, see pos_row), and
+// rows are taken RB at a time with every load of the batch issued before any
+// use (the loop is bound by load latency otherwise).
+__device__ __forceinline__ int pos_row(int m, int wi) { return (m & 3) + 8 * (m >> 2) + 4 * wi; }
+
+template <int D>
+__device__ __forceinline__ void rot_tile_qk(uint8_t* tile, int64_t row0, int32_t T, bool has_pos,
+                                            const int2* spos, const float4* __restrict__ rtab,
+                                            int32_t rtab_rows, uint32_t tid, float& vmax,
+                                            uint32_t& bad) {
+  constexpr int NP = D / 2, NCH = D / 64;
+  constexpr int RB = 2;  // rows per batch (register limit of the 88-register warps)
+  const int up = tid & 7, rr = tid >> 3, ul = up ^ rr;
+  uint8_t* base = tile + rr * 128 + up * 16;
+#pragma unroll 1
+  for (int ib = 0; ib < 16; ib += RB) {
+    int2 pv[RB];
+    bool rot[RB];
+#pragma unroll
+    for (int u = 0; u < RB; ++u) {
+      const int64_t t = row0 + rr + 8 * (ib + u);
+      rot[u] = has_pos && t < T;
+      pv[u] = spos[(rr & 3) + 4 * (ib + u)];
+    }
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) {
+      const int P0 = ch * 32 + ul * 4;  // first of the unit's 4 pairs
+      const bool col = P0 >= NP / 2;    // pairs of the column coordinate
+      uint4 x[RB];
+      float4 ta[RB], tb[RB];
+#pragma unroll
+      for (int u = 0; u < RB; ++u)
+        x[u] = *reinterpret_cast<const uint4*>(base + ch * (128 * 128) + (ib + u) * 1024);
+#pragma unroll
+      for (int u = 0; u < RB; ++u) {
+        int32_t v = col ? pv[u].y : pv[u].x;
+        if (v < 0 || v >= rtab_rows) {
+          bad |= rot[u] ? 1u : 0u;
+          v = 0;
+        }
+        const float4* e = rtab + ((static_cast<int64_t>(v) * NP + P0) >> 1);
+        if (rot[u]) {
+          ta[u] = __ldg(e);
+          tb[u] = __ldg(e + 1);
+        } else {
+          ta[u] = make_float4(1.f, 0.f, 1.f, 0.f);
+          tb[u] = ta[u];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < RB; ++u) {
+        const uint32_t wv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+        const float cs[4] = {ta[u].x, ta[u].z, tb[u].x, tb[u].z};
+        const float sn[4] = {ta[u].y, ta[u].w, tb[u].y, tb[u].w};
+        uint32_t yv[4];
+#pragma unroll
+        for (int k2 = 0; k2 < 4; k2 += 2) {
+          // two pairs per packed op: (a0, b0) the even elements, (a1, b1) the odd
+          const uint64_t x0 = f32x2_pack(__uint_as_float(wv[k2] << 16),
+                                         __uint_as_float(wv[k2 + 1] << 16));
+          const uint64_t x1 = f32x2_pack(__uint_as_float(wv[k2] & 0xFFFF0000u),
+                                         __uint_as_float(wv[k2 + 1] & 0xFFFF0000u));
+          const uint64_t nx1 = f32x2_pack(__uint_as_float((wv[k2] & 0xFFFF0000u) ^ 0x80000000u),
+                                          __uint_as_float((wv[k2 + 1] & 0xFFFF0000u) ^ 0x80000000u));
+          const uint64_t c2 = f32x2_pack(cs[k2], cs[k2 + 1]), s2 = f32x2_pack(sn[k2], sn[k2 + 1]);
+          const uint64_t y0 = f32x2_fma(x0, c2, f32x2_mul(nx1, s2));  // x0 c + (-x1) s
+          const uint64_t y1 = f32x2_fma(x0, s2, f32x2_mul(x1, c2));   // x0 s + x1 c
+          float y00, y01, y10, y11;
+          f32x2_unpack(y0, y00, y01);
+          f32x2_unpack(y1, y10, y11);
+          vmax = fmax3(vmax, fabsf(y00), fabsf(y10));
+          vmax = fmax3(vmax, fabsf(y01), fabsf(y11));
+          yv[k2] = pack_f16x2(y00, y10);
+          yv[k2 + 1] = pack_f16x2(y01, y11);
+        }
+        *reinterpret_cast<uint4*>(base + ch * (128 * 128) + (ib + u) * 1024) =
+            make_uint4(yv[0], yv[1], yv[2], yv[3]);
+      }
+    }
+  }
+}
+
+// The V tile: bf16 to fp16 in place (the pre-pass's V' = v), eight units per
+// batch; same unit ownership as rot_tile_qk.
+template <int D>
+__device__ __forceinline__ void cvt_tile_v(uint8_t* tile, uint32_t tid, float& vmax) {
+  constexpr int NCH = D / 64;
+  uint8_t* base = tile + (tid >> 3) * 128 + (tid & 7) * 16;
+#pragma unroll 1
+  for (int b = 0; b < 16 * NCH; b += 8) {
+    uint4 x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = b + u;  // chunk i / 16, row tid / 8 + 8 (i % 16)
+      x[u] = *reinterpret_cast<const uint4*>(base + (i >> 4) * (128 * 128) + (i & 15) * 1024);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = b + u;
+      const uint32_t wv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+      uint32_t yv[4];
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2) {
+        const float a0 = __uint_as_float(wv[k2] << 16), a1 = __uint_as_float(wv[k2] & 0xFFFF0000u);
+        vmax = fmax3(vmax, fabsf(a0), fabsf(a1));
+        yv[k2] = pack_f16x2(a0, a1);
+      }
+      *reinterpret_cast<uint4*>(base + (i >> 4) * (128 * 128) + (i & 15) * 1024) =
+          make_uint4(yv[0], yv[1], yv[2], yv[3]);
+    }
+  }
+}
+
+template <int D, bool F8, bool ROT>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = FwdCfg<D, F8>;
+  using C = FwdCfg<D, F8, ROT>;
   // All shared memory is dynamic (no static __shared__), so its base is the
   // start of the CTA's window: 1024-byte aligned, as the 128B-swizzled tiles need.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -312,6 +458,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t bar_o = bar_p + 16;                      // [2]
   const uint32_t bar_drain = bar_o + 16;
   const uint32_t bar_stall = bar_drain + 8;  // test hook: never arrived on
+  // rotate-on-load form: Q tile t / ring slot rewritten in place and fenced
+  const uint32_t bar_qr = bar_stall + 8;     // [2]
+  const uint32_t bar_rdy = bar_qr + 16;      // [NSLOT]
+  static_assert(!ROT || !F8, "the rotate-on-load form is a 16-bit forward");
+  static_assert(8 * (ROT ? 10 + 3 * C::NSLOT : 8 + 2 * C::NSLOT) <= C::OFF_MISC - C::OFF_BAR,
+                "barrier region too small");
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -332,6 +484,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(bar_o + 8, 1);
       mbar_init(bar_drain, 1);
       mbar_init(bar_stall, 1);
+      if (ROT) {
+        mbar_init(bar_qr, 64);
+        mbar_init(bar_qr + 8, 64);
+        for (int i = 0; i < C::NSLOT; ++i) mbar_init(bar_rdy + 8 * i, 64);
+      }
       fence_mbar_init();
     }
   }
@@ -395,10 +552,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (lane == 0) {
         bool ok = p.stall_us == 0 ||
                   mbar_wait_for(bar_stall, 0, &s_abort, static_cast<uint64_t>(p.stall_us) * 1000u);
-        ok = ok && mbar_wait(bar_q, 0, &s_abort);
+        ok = ok && mbar_wait(ROT ? bar_qr : bar_q, 0, &s_abort);
         tc_fence_after();
         auto kv_wait = [&](int32_t c) -> bool {
-          const bool r = mbar_wait(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1, &s_abort);
+          const bool r = mbar_wait((ROT ? bar_rdy : bar_full) + 8 * (c % C::NSLOT),
+                                   (c / C::NSLOT) & 1, &s_abort);
           tc_fence_after();
           return r;
         };
@@ -441,6 +599,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (ok) ok = kv_wait(0);
         if (ok) {
           issue_s(0, 0);
+          if (ROT && has1) {
+            ok = mbar_wait(bar_qr + 8, 0, &s_abort);
+            tc_fence_after();
+          }
+        }
+        if (ok) {
           if (has1) issue_s(1, 0);
           mma_commit(bar_empty + 8 * (0 % C::NSLOT));
         }
@@ -475,6 +639,75 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mma_commit(bar_drain);
         mbar_wait_drain(bar_drain, 0);
       }
+    } else if (ROT) {
+      // ------------------------------------------- rotation on load (warps 10-11)
+      // Tiles in the order the MMA issuer consumes them: Q_0, K_0, Q_1, V_0, K_1,
+      // V_1, ...; each one rewritten in place, fenced for the tensor core's
+      // (async-proxy) reads and released on its own barrier.
+      const uint32_t tid = threadIdx.x - 320;
+      float vmax = 0.f;
+      uint32_t bad = 0;
+      const int64_t qrow0 = static_cast<int64_t>(w.start) + q0;
+      const int2* pos2 = reinterpret_cast<const int2*>(p.pos);
+      const bool has_pos = pos2 != nullptr;
+      const int wi = static_cast<int>(warp) - 10;
+      int2* sp = reinterpret_cast<int2*>(smem_raw + C::OFF_POS) + 192 * wi;  // Q0, Q1, K
+      // this lane's two rows (m = lane, lane + 32) of the warp's share of a tile
+      auto pos_ld = [&](int64_t row0, int m) -> int2 {
+        const int64_t t = row0 + pos_row(m, wi);
+        return has_pos && t < p.T ? pos2[t] : make_int2(0, 0);
+      };
+      auto release = [&](uint32_t bar) {
+        fence_proxy_async_smem();
+        mbar_arrive(bar);
+      };
+      sp[lane] = pos_ld(qrow0, lane);
+      sp[lane + 32] = pos_ld(qrow0, lane + 32);
+      sp[64 + lane] = pos_ld(qrow0 + C::BM, lane);
+      sp[96 + lane] = pos_ld(qrow0 + C::BM, lane + 32);
+      int2 ka = pos_ld(w.start, lane), kb = pos_ld(w.start, lane + 32);  // next K tile's
+      __syncwarp();
+      bool ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_q, 0, &s_abort));
+      if (ok) {
+        rot_tile_qk<D>(smem_raw + C::OFF_Q, qrow0, p.T, has_pos, sp, p.rtab, p.rtab_rows, tid,
+                       vmax, bad);
+        release(bar_qr);
+      }
+      for (int32_t c = 0; ok && c < 2 * nkv; ++c) {
+        const int32_t slot = c % C::NSLOT;
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_bk(bar_full + 8 * slot, (c / C::NSLOT) & 1, &s_abort));
+        if (!ok) break;
+        uint8_t* tile = smem_raw + C::OFF_KV + slot * C::TILE;
+        const int64_t krow0 = static_cast<int64_t>(w.start) + (c >> 1) * C::BN;
+        if (c & 1) {
+          cvt_tile_v<D>(tile, tid, vmax);
+        } else {
+          // stage this K tile's positions, then prefetch the next tile's
+          __syncwarp();
+          sp[128 + lane] = ka;
+          sp[160 + lane] = kb;
+          __syncwarp();
+          if ((c >> 1) + 1 < nkv) {
+            ka = pos_ld(krow0 + C::BN, lane);
+            kb = pos_ld(krow0 + C::BN, lane + 32);
+          }
+          rot_tile_qk<D>(tile, krow0, p.T, has_pos, sp + 128, p.rtab, p.rtab_rows, tid, vmax,
+                         bad);
+        }
+        release(bar_rdy + 8 * slot);
+        if (c == 0 && has1) {
+          rot_tile_qk<D>(smem_raw + C::OFF_Q + C::TILE, qrow0 + C::BM, p.T, has_pos, sp + 64,
+                         p.rtab, p.rtab_rows, tid, vmax, bad);
+          release(bar_qr + 8);
+        }
+      }
+      if (!ok) {
+        s_abort = 1;
+        atomicOr(p.status, kFlagTimeout);
+      }
+      if (!(vmax <= 65504.f)) atomicOr(p.status, kFlagFp16Range);
+      if (bad) atomicOr(p.status, kFlagPosRange);
     }
   } else {
     warpgroup_reg_alloc<kFwdRegsHigh>();
@@ -662,12 +895,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool F8>
+template <int D, bool F8, bool ROT>
 static cudaError_t launch_fwd_d(const AttnFwdArgs& a, cudaStream_t s) {
-  using C = FwdCfg<D, F8>;
+  using C = FwdCfg<D, F8, ROT>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, F8>,
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, F8, ROT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
@@ -678,10 +911,10 @@ static cudaError_t launch_fwd_d(const AttnFwdArgs& a, cudaStream_t s) {
         !make_tmap_thd_u8(&tk, a.k, a.T, a.heads, 128) ||
         !make_tmap_thd_u8(&tv, a.v, a.T, a.heads, 128))
       return cudaErrorInvalidValue;
-  } else if (!make_tmap_thd(&tq, a.q, a.T, a.heads, D, 128, true) ||
-             !make_tmap_thd(&tk, a.k, a.T, a.heads, D, 128, true) ||
-             !make_tmap_thd(&tv, a.v, a.T, a.heads, D, 128, true)) {
-    return cudaErrorInvalidValue;
+  } else if (!make_tmap_thd(&tq, a.q, a.T, a.heads, D, 128, !ROT) ||
+             !make_tmap_thd(&tk, a.k, a.T, a.heads, D, 128, !ROT) ||
+             !make_tmap_thd(&tv, a.v, a.T, a.heads, D, 128, !ROT)) {
+    return cudaErrorInvalidValue;  // the rotate-on-load form maps the caller's bf16
   }
   FwdParams p;
   p.cu = a.cu;
@@ -697,19 +930,54 @@ static cudaError_t launch_fwd_d(const AttnFwdArgs& a, cudaStream_t s) {
   p.heads = a.heads;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.stall_us = a.stall_us;
+  p.pos = a.pos;
+  p.rtab = reinterpret_cast<const float4*>(a.rtab);
+  p.rtab_rows = a.rtab_rows;
   const int64_t blocks = (static_cast<int64_t>(a.T + 2 * C::BM - 1) / (2 * C::BM) + a.n) * a.heads;
   if (blocks <= 0) return cudaSuccess;
   {
-    KernelTimer kt(F8 ? MF_K_ATTN_FWD_F8 : MF_K_ATTN_FWD, s);
-    attn_fwd_kernel<D, F8>
+    KernelTimer kt(F8 ? MF_K_ATTN_FWD_F8 : ROT ? MF_K_ATTN_FWD_ROT : MF_K_ATTN_FWD, s);
+    attn_fwd_kernel<D, F8, ROT>
         <<<static_cast<unsigned>(blocks), kFwdThreads, C::SMEM, s>>>(tq, tk, tv, p);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_attn_fwd(const AttnFwdArgs& a, cudaStream_t s) {
-  if (a.f8) return a.head_dim == 128 ? launch_fwd_d<128, true>(a, s) : cudaErrorInvalidValue;
-  return a.head_dim == 128 ? launch_fwd_d<128, false>(a, s) : launch_fwd_d<64, false>(a, s);
+  if (a.f8) return a.head_dim == 128 ? launch_fwd_d<128, true, false>(a, s) : cudaErrorInvalidValue;
+  if (a.rot)
+    return a.head_dim == 128 ? launch_fwd_d<128, false, true>(a, s)
+                             : launch_fwd_d<64, false, true>(a, s);
+  return a.head_dim == 128 ? launch_fwd_d<128, false, false>(a, s)
+                           : launch_fwd_d<64, false, false>(a, s);
+}
+
+// (cos, sin) of v * omega_P for v in [0, rows), P in [0, head_dim / 2): the table
+// the rotate-on-load forward reads, computed with the pre-pass's own angle
+// evaluation (rope_sincos of float(v)), so both forms turn a pair identically.
+template <int D>
+__global__ void __launch_bounds__(256) rope_table_kernel(const __grid_constant__ RopeFreqs f,
+                                                         int32_t rows, float2* __restrict__ tab) {
+  constexpr int NP = D / 2;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<int64_t>(rows) * NP) return;
+  const int P = static_cast<int>(i % NP);
+  float sn, cs;
+  rope_sincos(static_cast<float>(i / NP), f.omega[P], f.omega_lo[P], 1.0f, &sn, &cs);
+  tab[i] = make_float2(cs, sn);
+}
+
+cudaError_t launch_rope_table(int32_t head_dim, int32_t rows, float* tab, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const RopeFreqs f = make_rope_freqs(head_dim, 2);
+  const int64_t n = static_cast<int64_t>(rows) * (head_dim / 2);
+  const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
+  KernelTimer kt(MF_K_ROPE_TABLE, s);
+  if (head_dim == 128)
+    rope_table_kernel<128><<<blocks, 256, 0, s>>>(f, rows, reinterpret_cast<float2*>(tab));
+  else
+    rope_table_kernel<64><<<blocks, 256, 0, s>>>(f, rows, reinterpret_cast<float2*>(tab));
+  return cudaGetLastError();
 }
 
 }  // namespace mf

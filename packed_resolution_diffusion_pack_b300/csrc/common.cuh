@@ -95,6 +95,8 @@ __device__ __forceinline__ E4m3Scale e4m3_scale(float A) {
 // [256, +sched)       schedule: int32 order[n], int32 prefix[n+1]
 // then 1024-aligned:  q16, k16  fp16 [T][h][d]  (rotated Q', K')
 // fwd only:           v16 fp16 [T][h][d]
+// rotate-on-load fwd:  rtab fp32 [R][d/2][2] from q16's offset, R <= T rows
+//                      (4 T d bytes, inside the 6 T h d of q16, k16, v16)
 // e4m3 fwd (inside the same total): q8, k8, v8 E4M3 [T][h][d] from q16's offset,
 //                     qscale fp32 [T][h], amax2 uint32 [2][h]
 // bwd only:           hmax fp32 [2][h] (per-head max ||dO_j||, max ||v_k||),
@@ -161,8 +163,18 @@ struct AttnFwdArgs {
   int32_t n, T, heads, head_dim;
   float scale;
   uint32_t stall_us = 0;  // test hook: see mf_test_varlen_attn_fwd_stalled
+  // rotate-on-load form: q, k, v are the caller's bf16 tensors; the kernel rotates
+  // Q and K (2D positions `pos`, may be null) and converts V in shared memory,
+  // reading (cos, sin) from rtab [rtab_rows][head_dim / 2]
+  bool rot = false;
+  const int32_t* pos = nullptr;
+  const float* rtab = nullptr;
+  int32_t rtab_rows = 0;
 };
 cudaError_t launch_attn_fwd(const AttnFwdArgs& a, cudaStream_t s);
+// The rotate-on-load forward's table: (cos, sin) of v * omega_P (2D frequencies)
+// for v in [0, rows), as [rows][head_dim / 2] float pairs.
+cudaError_t launch_rope_table(int32_t head_dim, int32_t rows, float* tab, cudaStream_t s);
 
 struct AttnBwdArgs {
   const uint16_t* q;    // fp16 Q' (rotated)

@@ -13,6 +13,7 @@ constexpr uint32_t kFlagTimeout = 1u;      // a bounded wait ran out
 constexpr uint32_t kFlagBadSeqlens = 2u;   // cu_seqlens not monotone / not ending at T / over max_len
 constexpr uint32_t kFlagSmemAlign = 4u;    // dynamic shared memory not 1024-byte aligned
 constexpr uint32_t kFlagFp16Range = 8u;    // a rotated Q/K value or a dS value left fp16 range
+constexpr uint32_t kFlagPosRange = 16u;    // rotate-on-load forward: a position outside its table
 
 // Upper bound for any single wait inside a kernel (ns).  Far above any legitimate
 // wait (microseconds), short enough to return control well before a watchdog.

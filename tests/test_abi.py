@@ -195,3 +195,27 @@ def test_noalloc_binding_rejects_editing_positions():
         mf.varlen_attn_fwd_noalloc(q, q, q, cu, torch.zeros((T, 3), dtype=torch.int32), T)
     with pytest.raises(ValueError, match="int32"):
         mf.varlen_attn_fwd_noalloc(q, q, q, cu, torch.zeros((T, 2), dtype=torch.int64), T)
+
+
+def test_fused_rope_forward_argument_errors_on_host():
+    """The rotate-on-load forward: unsupported head_dim, misaligned or null buffers
+    and a short workspace are rejected before any launch; 3D positions are refused
+    by the binding."""
+    import torch
+    lib = mf.load()
+    p = ctypes.c_void_p
+    base = 1 << 20
+    q, k, v, o, lse, cu, ws = (p(base + 4096 * i) for i in range(7))
+    pos = p(base + 65536)
+    fn = lib.mf_varlen_attn_fwd_fused_rope
+    big = lib.mf_attn_workspace_bytes(8, 1, 1, 64, 0)
+    assert fn(q, k, v, cu, pos, 1, 8, 8, 1, 96, 0.0, o, lse, ws, big, None) == 2
+    assert fn(q, k, v, cu, p(base + 65540), 1, 8, 8, 1, 64, 0.0, o, lse, ws, big, None) == 2
+    assert fn(q, None, v, cu, pos, 1, 8, 8, 1, 64, 0.0, o, lse, ws, big, None) == 1
+    assert fn(q, k, v, cu, pos, 1, 8, 8, 1, 64, 0.0, o, lse, ws, 16, None) == 1
+    assert fn(q, k, v, None, pos, 1, 8, 8, 1, 64, 0.0, o, lse, ws, big, None) == 1
+    T = 8
+    x = torch.zeros((T, 1, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="2D positions"):
+        mf.varlen_attn_fwd_fused_rope(x, x, x, torch.tensor([0, T], dtype=torch.int32),
+                                      torch.zeros((T, 3), dtype=torch.int32), T)
