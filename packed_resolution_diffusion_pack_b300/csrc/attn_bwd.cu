@@ -150,10 +150,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
 //    and writes dV and R(-theta) scale dK / ds_mul.
 //  attn_bwd_q_kernel   one CTA = one sample, one head, one 128-query tile (Q',
 //    dO resident): over the sample's 128-key tiles j it recomputes
-//      S_j  = Q' K'_j^T        M=128 queries, N=128, K=d  SS fp16  -> TMEM S[j % 2]
-//      dP_j = dO V_j^T         M=128 queries, N=128, K=d  SS bf16  -> TMEM DP
+//      S_j  = Q' K'_j^T        M=128 queries, N=128, K=d  SS fp16  -> TMEM S
+//      dP_j = dO V_j^T         M=128 queries, N=128, K=d  SS bf16  -> TMEM DP[j % 2]
 //      dS_j = P (dP - D) * ds_mul, P = exp2(S scale log2e - LSE log2e)
-//                              (fp16, back into S[j % 2])
+//                              (fp16, back into DP[j % 2])
 //      dQ  += dS_j K'_j        M=128 queries, N=d, K=128  TS fp16 (dS from TMEM)
 //    and writes dQ = R(-theta) scale dQ' / ds_mul in bf16.
 // Splitting the work this way recomputes S and dP for dQ (7 GEMMs instead of
@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
 #pragma unroll
         for (int u = 0; u < C::BQ / 32; ++u) {
-          const int q = static_cast<int>(lane) * (C::BQ / 32) + u;
+          const int q = u * 32 + static_cast<int>(lane);  // consecutive lanes, consecutive words
           const int32_t qi = q0 + q;
           const bool q_ok = qi < w.len;
           cp_async_4(sVEC + st * C::VEC + q * 4, q_ok ? p.nlse2 + gbase_row + qi : p.pad + q);

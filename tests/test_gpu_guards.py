@@ -4,8 +4,8 @@
   inside the attention kernel run out after a short limit.  The kernel must record
   MF_ERR_TIMEOUT, let its copies land, free its tensor memory and exit; the
   context must stay usable, and the next call must be correct.
-- Guard bands: every output (O, LSE, dQ, dK, dV, the 8-bit and allocation-free
-  forwards' outputs, the neighbours' outputs) and the caller's workspace are
+- Guard bands: every output (O, LSE, dQ, dK, dV, the 8-bit, rotate-on-load and
+  allocation-free forwards' outputs, the neighbours' outputs) and the caller's workspace are
   views into larger buffers whose head and tail hold a known bit pattern.  After
   the calls on ragged packs (last tiles cut short, zero-length and one-token
   samples, a short sample at the very end of the pack) the patterns must be
@@ -118,6 +118,26 @@ def test_fp8_and_noalloc_forwards_keep_their_guard_bands(cuda_lib):
     mf.noalloc_get_status()
     _intact(bo2, "allocation-free O")
     _intact(bl2, "allocation-free LSE")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fused_rope_forward_keeps_its_guard_bands(cuda_lib, d):
+    """The rotate-on-load forward writes O, LSE and its (cos, sin) table in the
+    workspace, and nothing around them; its outputs equal the two-pass forward's."""
+    mf = cuda_lib
+    h = 2
+    cu, pos = mf.pack(SPECS)
+    T, max_len = mf.pack_size(SPECS)
+    q, k, v, _ = (dev(x) if x is not None else None for x in random_inputs(T, h, d, 83, False))
+    bo, o = _guarded((T, h, d), torch.bfloat16)
+    bl, lse = _guarded((h, T), torch.float32)
+    bw, ws = _guarded_ws(T, len(SPECS), h, d, False)
+    mf.varlen_attn_fwd_fused_rope(q, k, v, cu, pos, max_len, o=o, lse=lse, ws=ws)
+    mf.get_status(ws)
+    for b, w in ((bo, "fused O"), (bl, "fused LSE"), (bw, "fused workspace")):
+        _intact(b, w)
+    o_ref, lse_ref = mf.varlen_attn_fwd(q, k, v, cu, pos, max_len)
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
 
 
 def test_neighbours_keep_their_guard_bands(cuda_lib):
