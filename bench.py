@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the timing of the attention's memory-bound neighbours")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--bwd-form", default="stored_ds", choices=["stored_ds", "recompute"],
+                    help="the backward's form: dS stored by the dK/dV kernel and read back by "
+                         "a streaming dQ GEMM (a larger workspace), or dQ recomputing S and dP")
     ap.add_argument("--copy-streams", type=int, default=1,
                     help="streams per copy direction in the end-to-end leg (2 or 3 measured "
                          "no faster: the host link, not a copy engine, is the limit)")
@@ -291,8 +294,11 @@ def gpu_arm(args):
     lse = torch.empty((h, T), dtype=torch.float32, device="cuda")
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
     # one workspace for forward and backward: the backward reuses the forward's
-    # rotated fp16 operands (mf_varlen_attn_bwd_after_fwd)
-    ws = mf.workspace(T, n, h, d, True)
+    # rotated fp16 operands (mf_varlen_attn_bwd_after_fwd); sized for the stored-dS
+    # form of the backward unless --bwd-form recompute (or the form is unavailable)
+    ds_ok = args.bwd_form == "stored_ds" and mf.attn_workspace_bytes_ds(T, n, h, d, max_len) > 0
+    ws = mf.workspace(T, n, h, d, True, store_ds_max_len=max_len if ds_ok else None)
+    bwd_form = "stored_ds" if ds_ok else "recompute"
     cu = torch.empty(n + 1, dtype=torch.int32, device="cuda")
     pos = torch.empty((T, 3 if wl.edit else 2), dtype=torch.int32, device="cuda")
     packer = mf.pack3d if wl.edit else mf.pack
@@ -429,6 +435,10 @@ def gpu_arm(args):
     elems = float(T * h * d)
     algo = {"attn_fwd": ("tensor", flops_fwd), "attn_bwd": ("tensor", 0.8 * flops_bwd),
             "attn_bwd_q": ("tensor", 0.2 * flops_bwd),
+            # stored-dS form: reads the padded dS^T blocks (a_i = L_i rounded up to
+            # 128) and K' once, writes dQ
+            "attn_bwd_dq": ("hbm", 2.0 * h * sum((128 * -(-L // 128)) ** 2 for L in wl.lengths)
+                            + 4.0 * elems),
             "rope": ("hbm", 12.0 * elems + 8.0 * T),
             "bwd_pre": ("hbm", 6.0 * elems + 12.0 * h * T)}
     for name, (bound, amount) in algo.items():
@@ -447,6 +457,7 @@ def gpu_arm(args):
                 pl.update(achieved_gbs=ach, frac_of_hbm=ach / pk["hbm_gbs"])
             pl.update(algorithmic=amount, traffic=_recorded_traffic(name))
     dom = max(("attn_fwd", "attn_bwd", "attn_bwd_q"), key=lambda nm: kern[nm][0])
+    q_kernel = "attn_bwd_dq" if bwd_form == "stored_ds" else "attn_bwd_q"
     traffic = _recorded_traffic(dom)
     ach = per_launch[dom]["achieved_tflops"]
     roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_tc,
@@ -454,7 +465,7 @@ def gpu_arm(args):
                 "peak_kind": peak_name, "frac_of_nominal": ach / NOMINAL_BF16_TFLOPS}
     fwd_ms = per_launch["attn_fwd"]["ms_per_launch"]
     # the backward's attention: the dK/dV kernel and the dQ kernel
-    bwd_ms = per_launch["attn_bwd"]["ms_per_launch"] + per_launch["attn_bwd_q"]["ms_per_launch"]
+    bwd_ms = per_launch["attn_bwd"]["ms_per_launch"] + per_launch[q_kernel]["ms_per_launch"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
@@ -462,6 +473,7 @@ def gpu_arm(args):
         "config": {"workload": workload_desc(wl), "global_tokens": T * world,
                    "step": "mf_pack + mf_varlen_attn_fwd (RoPE + attention) + "
                            "mf_varlen_attn_bwd_after_fwd (one shared workspace)",
+                   "bwd_form": bwd_form, "workspace_gb": round(ws.numel() / 1e9, 2),
                    "l2": "no flush: Q, K, V, dO alone are %.2f GB, far above the 126 MB L2" % (
                        4 * elem * 2 / 1e9),
                    "parallelism": "replicas: one pack per GPU, no data-path collective"},
@@ -489,6 +501,8 @@ def gpu_arm(args):
         line["extras"] = neighbours(mf, wl, pk["hbm_gbs"])
         line["extras"]["forward_only"] = forward_only(mf, wl, qd, kd, vd, cu, pos, max_len, ws,
                                                       peak_tc)
+        line["extras"]["backward_forms"] = backward_forms(mf, wl, qd, kd, vd, dod, cu, pos, max_len,
+                                                          o, lse, peak_tc)
         if d == 128:
             line["extras"]["fp8_forward"] = fp8_forward(mf, wl, qd, kd, vd, cu, pos, max_len, ws,
                                                         peak_tc, pk["hbm_gbs"])
@@ -594,6 +608,51 @@ def forward_only(mf, wl, qd, kd, vd, cu, pos, max_len, ws, peak_bf16, reps=10):
                      "kernel_ms": per, "attn_tflops": flops / (attn_ms / 1e3) / 1e12,
                      "attn_frac": flops / (attn_ms / 1e3) / 1e12 / peak_bf16}
     out["fused_over_two_pass"] = out["two_pass"]["ms_per_call"] / out["fused_rope"]["ms_per_call"]
+    return out
+
+
+def backward_forms(mf, wl, qd, kd, vd, dod, cu, pos, max_len, o, lse, peak_bf16, reps=5):
+    """The backward in its two forms on the same pack, outside the timed step, each
+    on a workspace of its own after a forward on it: recompute (the dQ kernel
+    recomputes S and dP; mf_attn_workspace_bytes) and stored dS (the dK / dV kernel
+    stores dS^T, a streaming kernel forms dQ from it; mf_attn_workspace_bytes_ds).
+    Per form: CUDA-event time per backward call and each attention kernel's time."""
+    import torch
+    T, n, h, d = wl.total, len(wl.specs), wl.heads, wl.head_dim
+    flops = wl.flops_bwd()
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    out = {}
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for form, ds_len, kq in (("recompute", None, "attn_bwd_q"),
+                             ("stored_ds", max_len, "attn_bwd_dq")):
+        if ds_len is not None and mf.attn_workspace_bytes_ds(T, n, h, d, ds_len) == 0:
+            continue
+        ws = mf.workspace(T, n, h, d, True, store_ds_max_len=ds_len)
+        mf.varlen_attn_fwd(qd, kd, vd, cu, pos, max_len, o=o, lse=lse, ws=ws)
+        call = lambda: mf.varlen_attn_bwd(qd, kd, vd, o, lse, dod, cu, pos, max_len, dq=dq,  # noqa: E731
+                                          dk=dk, dv=dv, ws=ws, after_fwd=True)
+        for _ in range(2):
+            call()
+        torch.cuda.synchronize()
+        mf.timing_enable(True)
+        mf.timing_reset()
+        ev0.record()
+        for _ in range(reps):
+            call()
+        ev1.record()
+        torch.cuda.synchronize()
+        kern = mf.timing_read()
+        mf.timing_enable(False)
+        mf.get_status(ws)
+        ms = ev0.elapsed_time(ev1) / reps
+        kv_ms = kern["attn_bwd"][0] / max(1, kern["attn_bwd"][1])
+        q_ms = kern[kq][0] / max(1, kern[kq][1])
+        out[form] = {"ms_per_call": ms, "workspace_gb": ws.numel() / 1e9, "dkdv_ms": kv_ms,
+                     "dq_ms": q_ms, "attn_ms": kv_ms + q_ms,
+                     "attn_tflops": flops / ((kv_ms + q_ms) / 1e3) / 1e12,
+                     "attn_frac": flops / ((kv_ms + q_ms) / 1e3) / 1e12 / peak_bf16}
+        del ws
+        torch.cuda.empty_cache()
     return out
 
 

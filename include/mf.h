@@ -127,6 +127,23 @@ mf_status mf_rope2d_qk(const mf_bf16* q, const mf_bf16* k, mf_bf16* q_out, mf_bf
 size_t mf_attn_workspace_bytes(int32_t T, int32_t n, int32_t heads, int32_t head_dim, int32_t bwd);
 
 /*
+ * Workspace bytes for the backward calls that selects their stored-dS form: the
+ * dK / dV kernel also writes each (sample, head)'s scaled fp16 dS^T (its rows
+ * padded to 128) into the workspace, and dQ = scale R(-theta) dS K' is then one
+ * streaming GEMM over it instead of a kernel that recomputes S and dP.  Faster,
+ * at the cost of memory: about 2 heads (T + 128 n) max_len bytes on top of
+ * mf_attn_workspace_bytes(..., 1) (10.5 GB for 48k tokens, 24 heads, max_len
+ * 4,291).  Any of the backward calls given a workspace of at least this size,
+ * for the same T, n, heads and max_len, uses that form; results agree with the
+ * other form within the backward's tolerance (not bit for bit: the two forms
+ * round dS from differently ordered GEMMs).  Returns 0 on invalid sizes, or when
+ * heads (T + 128 n) reaches 2^31 (the form is then unavailable).
+ * No counterpart on the pages: a memory-for-time form of the backward.
+ */
+size_t mf_attn_workspace_bytes_ds(int32_t T, int32_t n, int32_t heads, int32_t head_dim,
+                                  int32_t max_len);
+
+/*
  * Varlen attention forward with per-sample 2D RoPE.
  * q, k, v: DEVICE bf16 [T][heads][head_dim], un-rotated.
  * d_cu_seqlens: DEVICE int32[n+1]; d_pos: DEVICE int32[T][2], or NULL for no
@@ -458,12 +475,13 @@ mf_status mf_test_varlen_attn_bwd_stalled(const mf_bf16* q, const mf_bf16* k, co
  *   MF_K_ATTN_BWD 5 (dK, dV), MF_K_ATTN_BWD_Q 6 (dQ), MF_K_CFG_EULER 7, MF_K_ADALN 8,
  *   MF_K_GATED_RESIDUAL 9, MF_K_F8_AMAX 10, MF_K_F8_QUANT 11, MF_K_ATTN_FWD_F8 12,
  *   MF_K_ROPE_TABLE 13, MF_K_ATTN_FWD_ROT 14 (the rotate-on-load forward's table and
- *   attention kernels).
+ *   attention kernels), MF_K_ATTN_BWD_DQ 15 (dQ from the stored dS).
  * Process-wide state guarded by a mutex; not for use under stream capture.
  */
 enum { MF_K_PACK = 0, MF_K_ROPE, MF_K_SCHEDULE, MF_K_ATTN_FWD, MF_K_BWD_PRE, MF_K_ATTN_BWD,
        MF_K_ATTN_BWD_Q, MF_K_CFG_EULER, MF_K_ADALN, MF_K_GATED_RESIDUAL, MF_K_F8_AMAX,
-       MF_K_F8_QUANT, MF_K_ATTN_FWD_F8, MF_K_ROPE_TABLE, MF_K_ATTN_FWD_ROT, MF_K_COUNT };
+       MF_K_F8_QUANT, MF_K_ATTN_FWD_F8, MF_K_ROPE_TABLE, MF_K_ATTN_FWD_ROT, MF_K_ATTN_BWD_DQ,
+       MF_K_COUNT };
 mf_status mf_timing_enable(int32_t on);
 mf_status mf_timing_reset(void);
 mf_status mf_timing_read(int32_t id, double* total_ms, int64_t* launches);

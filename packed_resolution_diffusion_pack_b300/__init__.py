@@ -20,7 +20,7 @@ __all__ = [
     "attn_workspace_bytes", "workspace", "varlen_attn_fwd", "varlen_attn_bwd", "get_status",
     "cfg_euler_step", "adaln_modulate", "gated_residual", "pack3d_size", "pack3d", "rope3d_qk",
     "varlen_attn_fwd_fp8", "quant_e4m3", "varlen_attn_fwd_noalloc", "noalloc_get_status",
-    "varlen_attn_fwd_fused_rope",
+    "varlen_attn_fwd_fused_rope", "attn_workspace_bytes_ds",
 ]
 
 
@@ -152,10 +152,20 @@ def attn_workspace_bytes(T, n, heads, head_dim, bwd: bool) -> int:
     return int(load().mf_attn_workspace_bytes(T, n, heads, head_dim, 1 if bwd else 0))
 
 
-def workspace(T, n, heads, head_dim, bwd: bool, device=None):
-    """A device workspace of the size the library asks for (uint8 tensor)."""
+def attn_workspace_bytes_ds(T, n, heads, head_dim, max_len) -> int:
+    """Workspace bytes that select the backward's stored-dS form (0: unavailable)."""
+    return int(load().mf_attn_workspace_bytes_ds(T, n, heads, head_dim, int(max_len)))
+
+
+def workspace(T, n, heads, head_dim, bwd: bool, device=None, store_ds_max_len=None):
+    """A device workspace of the size the library asks for (uint8 tensor).  With
+    store_ds_max_len (the call's max_len), a backward workspace large enough for
+    the stored-dS form (mf_attn_workspace_bytes_ds)."""
     torch = _torch()
-    nbytes = attn_workspace_bytes(T, n, heads, head_dim, bwd)
+    if store_ds_max_len is not None:
+        nbytes = attn_workspace_bytes_ds(T, n, heads, head_dim, store_ds_max_len)
+    else:
+        nbytes = attn_workspace_bytes(T, n, heads, head_dim, bwd)
     if nbytes == 0:
         raise ValueError("invalid attention sizes")
     return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")

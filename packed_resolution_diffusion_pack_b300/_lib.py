@@ -29,6 +29,7 @@ SIGNATURES = {
     "mf_pack": (ctypes.c_int, [_p, _i32, _p, _p, _p]),
     "mf_rope2d_qk": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _p]),
     "mf_attn_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "mf_attn_workspace_bytes_ds": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "mf_varlen_attn_fwd": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _f32,
                                           _p, _p, _p, _sz, _p]),
     "mf_varlen_attn_fwd_fused_rope": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i32, _i32, _i32,
@@ -70,7 +71,7 @@ SIGNATURES = {
 # kernel ids of the opt-in timing (mf.h MF_K_*)
 KERNELS = ["pack", "rope", "schedule", "attn_fwd", "bwd_pre", "attn_bwd", "attn_bwd_q", "cfg_euler",
            "adaln", "gated_residual", "f8_amax", "f8_quant", "attn_fwd_f8", "rope_table",
-           "attn_fwd_rot"]
+           "attn_fwd_rot", "attn_bwd_dq"]
 
 
 class MFError(RuntimeError):

@@ -65,6 +65,15 @@ WsLayout ws_layout(int64_t T, int64_t n, int64_t heads, int64_t head_dim, bool b
   return L;
 }
 
+size_t ds_layout_bytes(int64_t T, int64_t n, int64_t heads, int64_t max_len, int64_t* cols) {
+  const int64_t A = (max_len > 0 ? (max_len + 127) / 128 : 1) * 128;
+  const int64_t rows = heads * (T + 128 * n);
+  // TMA row coordinates are int32: the last tile's rows must stay below 2^31
+  if (T < 0 || n < 0 || heads < 1 || rows > INT32_MAX - 256 || A > INT32_MAX) return 0;
+  if (cols) *cols = A;
+  return static_cast<size_t>(rows) * static_cast<size_t>(A) * 2;
+}
+
 static bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }
@@ -160,6 +169,14 @@ size_t mf_attn_workspace_bytes(int32_t T, int32_t n, int32_t heads, int32_t head
                                int32_t bwd) {
   if (T < 0 || n < 0 || heads < 1 || (head_dim != 64 && head_dim != 128)) return 0;
   return ws_layout(T, n, heads, head_dim, bwd != 0).total;
+}
+
+size_t mf_attn_workspace_bytes_ds(int32_t T, int32_t n, int32_t heads, int32_t head_dim,
+                                  int32_t max_len) {
+  if (T < 0 || n < 0 || heads < 1 || max_len < 0 || (head_dim != 64 && head_dim != 128)) return 0;
+  const size_t dsb = ds_layout_bytes(T, n, heads, max_len, nullptr);
+  if (dsb == 0) return 0;
+  return align_up(ws_layout(T, n, heads, head_dim, true).total, 1024) + dsb;
 }
 
 }  // extern "C"
@@ -355,6 +372,14 @@ static mf_status attn_bwd_impl(const mf_bf16* q, const mf_bf16* k, const mf_bf16
     if (e != cudaSuccess) return MF_ERR_CUDA;
   }
   AttnBwdArgs a;
+  // a workspace sized by mf_attn_workspace_bytes_ds selects the stored-dS form
+  int64_t ds_cols = 0;
+  const size_t dsb = ds_layout_bytes(T, n, heads, max_len, &ds_cols);
+  const size_t ds_off = align_up(L.total, 1024);
+  if (dsb > 0 && ws_bytes >= ds_off + dsb) {
+    a.ds = reinterpret_cast<uint16_t*>(w + ds_off);
+    a.ds_cols = ds_cols;
+  }
   a.q = q16;
   a.k = k16;
   a.v = v;

@@ -187,6 +187,13 @@ struct BwdCfg {
   static constexpr int Q_OFF_BAR = Q_OFF_V + VSLOT * TILE;
   static constexpr int Q_OFF_MISC = Q_OFF_BAR + 256;
   static constexpr int Q_SMEM = Q_OFF_MISC + 64;
+  // dQ-from-stored-dS kernel: (dS^T tile, K' tile) per stage, DQ_NS stages
+  static constexpr int DS_TILE = 128 * 128 * 2;
+  static constexpr int DQ_STAGE = DS_TILE + TILE;
+  static constexpr int DQ_NS = D == 128 ? 3 : 4;
+  static constexpr int DQ_OFF_BAR = DQ_NS * DQ_STAGE;
+  static constexpr int DQ_OFF_MISC = DQ_OFF_BAR + 256;
+  static constexpr int DQ_SMEM = DQ_OFF_MISC + 64;
   // TMEM columns
   static constexpr uint32_t KV_ST = 0, KV_DPT = 128, KV_DV = 256, KV_DK = 256 + D;
   static constexpr uint32_t Q_S = 0, Q_DP = 128, Q_DQ = 384;  // DP: two buffers
@@ -196,9 +203,13 @@ struct BwdCfg {
   static constexpr uint32_t IDESC_DP = idesc_f32acc(128, 128, kBF16, 0, 0); // dP^T and dP
   static constexpr uint32_t IDESC_DV = idesc_f32acc(128, D, kBF16, 0, 1);   // dV (TS)
   static constexpr uint32_t IDESC_DKQ = idesc_f32acc(128, D, kF16, 0, 1);   // dK, dQ (TS)
+  // dQ = dS K' with both operands MN-major in shared memory (dS^T rows are keys)
+  static constexpr uint32_t IDESC_DQS = idesc_f32acc(128, D, kF16, 1, 1);
   static_assert(KV_OFF_Q % 1024 == 0 && KV_OFF_DO % 1024 == 0 && Q_OFF_K % 1024 == 0,
                 "swizzled tiles start on 1024-byte boundaries");
-  static_assert(KV_SMEM <= 232448 && Q_SMEM <= 232448, "shared memory over the per-CTA limit");
+  static_assert(KV_SMEM <= 232448 && Q_SMEM <= 232448 && DQ_SMEM <= 232448,
+                "shared memory over the per-CTA limit");
+  static_assert(DQ_STAGE % 1024 == 0 && DS_TILE % 1024 == 0, "dS / K' tiles on 1024-byte boundaries");
   static_assert(8 * (2 + 2 * NST + 9) <= 256 && 8 * (2 + 2 * (KSLOT + VSLOT) + 12) <= 256,
                 "barrier areas");
 };
@@ -228,7 +239,20 @@ struct BwdParams {
   // test hook (0 = off): the MMA thread first waits, at most this many
   // microseconds, on a barrier that nothing arrives on (failure-detection tests)
   uint32_t stall_us;
+  // stored-dS form: scaled fp16 dS^T of ds_rows key rows and ds_cols queries in
+  // 8-query units, unit g of row r at (g ds_rows + r) (null: dQ recomputes)
+  uint16_t* ds;
+  int64_t ds_rows, ds_cols;
 };
+
+// First row of (sample, head)'s dS^T block in the stored-dS array: samples at
+// heads (cu[i] + 128 i), heads a_i rows apart, a_i = L_i rounded up to 128.  The
+// blocks never overlap: heads a_i <= heads (L_i + 127) < the next sample's offset.
+__device__ __forceinline__ int64_t ds_block_row(int32_t heads, int32_t start, int32_t sample,
+                                                int32_t head, int32_t padded_len) {
+  return static_cast<int64_t>(heads) * (static_cast<int64_t>(start) + 128LL * sample) +
+         static_cast<int64_t>(head) * padded_len;
+}
 
 // 2^e with e = floor(log2(2^15 / bound)) clamped to [-64, 64]: scaled |dS| stays
 // below 2^15 (fp16 max 65504) and small gradients keep fp16's precision.
@@ -539,6 +563,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // dS is staged in fp16 as ds_mul * dS (a power of two; see ds_scale_for)
       const float ds_mul = ds_scale_for(p.hmax[w.head], p.hmax[p.heads + w.head]);
       const uint64_t dsm2 = f32x2_pack(ds_mul, ds_mul);
+      // stored-dS form: this thread's key row; its 8-query unit g sits at
+      // ds_row + g ds_rows 8 (consecutive rows adjacent)
+      uint16_t* ds_row = nullptr;
+      if (p.ds != nullptr)
+        ds_row = p.ds + (ds_block_row(p.heads, w.start, w.sample, w.head, nq * C::BQ) + k0 + row) * 8;
       for (int32_t i = 0; i < nq; ++i) {
         const int32_t g = gt + i, st = g % C::NST;
         ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_full + 8 * st, (g / C::NST) & 1, &s_abort) &&
@@ -596,6 +625,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // dS^T = P^T (dP^T - D) ds_mul, two queries per packed op; fp16 into DPT
         // columns [64h, 64h + 32) (each 32-column load is complete before the
         // columns it overlaps are rewritten)
+        uint32_t xs[2][16];  // stored-dS form: this row's dS^T values, both chunks
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t rd[32];
@@ -618,10 +648,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
           }
           tmem_st16(tDPT + c * 16, pd);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) xs[c][e] = pd[e];
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar_ds);
+        if (ds_row != nullptr) {
+          // After the release (the tensor core runs dK meanwhile): queries
+          // [i BQ + 64h + 32c + 8u, +8) of the key row, as unit
+          // g = 16 i + 8h + 4c + u.  The 32 lanes of a warp hold consecutive key
+          // rows, so each store writes 512 contiguous bytes.
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(ds_row + (i * 16 + 8 * h + 4 * c + u) * p.ds_rows * 8) =
+                  make_uint4(xs[c][4 * u], xs[c][4 * u + 1], xs[c][4 * u + 2], xs[c][4 * u + 3]);
+        }
       }
       if (!ok) break;
       // epilogue: this warpgroup's columns [h D/2, (h + 1) D/2) of dV and dK into
@@ -1005,6 +1049,200 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// ------------------------------------------------------- dQ from stored dS
+// The stored-dS form's second kernel: dQ' = dS K' with the dK / dV kernel's scaled
+// fp16 dS^T read back from memory instead of recomputing S and dP.  Persistent,
+// one item per (sample, head, 128-query tile) as in attn_bwd_q_kernel.  Per key
+// tile j the TMA warp copies the dS^T block [keys of j][queries of the item] --
+// 16 runs of 128 rows x 16 bytes, one per 8-query unit, which land as the
+// unswizzled MN-major core-matrix layout (8 keys x 8 queries per 128 bytes) --
+// and K'_j into one of DQ_NS stages; the MMA thread issues dQ += dS K'_j (both
+// operands MN-major: dS^T rows are keys, K' rows are keys) into one of two TMEM
+// accumulators, so that one item's epilogue overlaps the next item's GEMMs; the
+// two elementwise warpgroups store R(-theta) scale dQ' / ds_mul in bf16.  Rows
+// and columns of dS^T past the sample end hold zeros (P = 0 there), so the
+// next sample's keys in a last tile add nothing.
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = smem_u32(smem_raw);
+  CtaMiscB& misc = *reinterpret_cast<CtaMiscB*>(smem_raw + C::DQ_OFF_MISC);
+  uint32_t& s_tmem = misc.tmem;
+  volatile uint32_t& s_abort = misc.abort;
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kFlagSmemAlign);
+    return;
+  }
+  if ((*p.status & kFlagBadSeqlens) != 0) return;  // the schedule listed no work
+  const uint32_t bars = sbase + C::DQ_OFF_BAR;
+  const uint32_t bar_full = bars;                        // [DQ_NS]
+  const uint32_t bar_empty = bar_full + 8 * C::DQ_NS;    // [DQ_NS]
+  const uint32_t bar_acc = bar_empty + 8 * C::DQ_NS;     // [2] an item's dQ complete
+  const uint32_t bar_acc_free = bar_acc + 16;            // [2] ... loaded (256 arrivals)
+  const uint32_t bar_drain = bar_acc_free + 16;
+  const uint32_t bar_stall = bar_drain + 8;              // test hook: never arrived on
+  static_assert(8 * (2 * C::DQ_NS + 6) <= 256, "barrier area");
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < C::DQ_NS; ++i) {
+      mbar_init(bar_full + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, 1);
+    }
+    mbar_init(bar_acc, 1);
+    mbar_init(bar_acc + 8, 1);
+    mbar_init(bar_acc_free, 256);
+    mbar_init(bar_acc_free + 8, 256);
+    mbar_init(bar_drain, 1);
+    mbar_init(bar_stall, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 9) {
+    tmem_alloc(smem_u32(&s_tmem), 2 * D < 32 ? 32 : 2 * D);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 8) {
+    // -------------------------------------------------------------- TMA producer
+    // lane 0 paces the ring; lanes 0-15 each copy one 8-query unit of a dS^T block
+    {
+      if (lane == 0) tma_prefetch_desc(&tm_k);
+      bool ok = true;
+      int32_t gs = 0, issued = 0;  // steps of earlier items; stage fills issued
+      WorkItemB w;
+      for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
+        const int32_t q0 = w.blk * C::BQ, nk = (w.len + C::BK - 1) / C::BK;
+        const int64_t row0 = ds_block_row(p.heads, w.start, w.sample, w.head, nk * C::BK);
+        for (int32_t j = 0; j < nk; ++j) {
+          const int32_t g = gs + j, st = g % C::DQ_NS, use = g / C::DQ_NS;
+          if (use > 0 &&
+              !__all_sync(0xffffffffu,
+                          mbar_wait_bk(bar_empty + 8 * st, (use - 1) & 1, &s_abort))) {
+            ok = false;
+            break;
+          }
+          const uint32_t sds = sbase + st * C::DQ_STAGE, sk = sds + C::DS_TILE;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar_full + 8 * st, C::DQ_STAGE);
+            for (int ch = 0; ch < D / 64; ++ch)
+              tma_load_3d(sk + ch * C::CHUNK, &tm_k, bar_full + 8 * st, ch * 64, w.head,
+                          w.start + j * C::BK);
+          }
+          __syncwarp();  // the byte count is posted before any copy can complete
+          if (lane < 16) {  // unit q0 / 8 + lane: keys row0 + 128 j .. + 127, 2 KB
+            const uint16_t* src =
+                p.ds + ((static_cast<int64_t>(q0 / 8 + static_cast<int>(lane))) * p.ds_rows +
+                        row0 + static_cast<int64_t>(j) * C::BK) * 8;
+            bulk_load(sds + lane * 2048, src, 2048, bar_full + 8 * st);
+          }
+          issued = g + 1;
+        }
+        gs += nk;
+      }
+      if (!ok && lane == 0) {
+        s_abort = 1;
+        atomicOr(p.status, kFlagTimeout);
+      }
+      // every issued copy lands before the CTA exits (at most one per stage)
+      if (lane == 0)
+        for (int32_t g = (issued > C::DQ_NS ? issued - C::DQ_NS : 0); g < issued; ++g)
+          mbar_wait_drain(bar_full + 8 * (g % C::DQ_NS), (g / C::DQ_NS) & 1);
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        const bool r = mbar_wait(bar, parity, &s_abort);
+        tc_fence_after();
+        return r;
+      };
+      // dS: unswizzled MN-major, 8-key groups 128 bytes apart (leading offset),
+      // 8-query core-matrix columns 2 KB apart (stride offset); a K-step of 16
+      // keys advances 256 bytes
+      const uint64_t a_m = sdesc_noswz(sbase, 128, 2048);
+      const uint64_t b_m = sdesc_sw128(sbase + C::DS_TILE, C::CHUNK, 1024);  // K' (MN-major)
+      constexpr uint64_t kStage = C::DQ_STAGE >> 4;
+      bool ok = p.stall_us == 0 ||
+                mbar_wait_for(bar_stall, 0, &s_abort, static_cast<uint64_t>(p.stall_us) * 1000u);
+      int32_t gs = 0;
+      WorkItemB w;
+      for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
+        const int32_t nk = (w.len + C::BK - 1) / C::BK, buf = k & 1;
+        // the accumulator's previous item (k - 2) must have been loaded
+        if (k >= 2 && !(ok = wait(bar_acc_free + 8 * buf, ((k >> 1) - 1) & 1))) break;
+        for (int32_t j = 0; j < nk; ++j) {
+          const int32_t g = gs + j, st = g % C::DQ_NS;
+          if (!(ok = wait(bar_full + 8 * st, (g / C::DQ_NS) & 1))) break;
+#pragma unroll
+          for (int kk = 0; kk < C::BK / 16; ++kk)  // dQ += dS K'_j, keys kk*16 .. +16
+            mma_ss(tmem + buf * D, a_m + st * kStage + ((kk * 256) >> 4),
+                   b_m + st * kStage + mofs(kk), C::IDESC_DQS, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar_empty + 8 * st);
+        }
+        if (!ok) break;
+        mma_commit(bar_acc + 8 * buf);
+        gs += nk;
+      }
+      if (!ok) {
+        s_abort = 1;
+        atomicOr(p.status, kFlagTimeout);
+      }
+      mma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------ epilogue warpgroups (query rows)
+    const int h = warp >> 2;                 // columns [h D/2, (h + 1) D/2) of dQ
+    const uint32_t row = threadIdx.x & 127;  // query row in the tile = TMEM lane
+    const uint32_t lane_off = ((warp & 3) * 32) << 16;
+    bool ok = true;
+    WorkItemB w;
+    for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
+      const int32_t buf = k & 1;
+      const int32_t qrow = w.blk * C::BQ + static_cast<int32_t>(row);
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_acc + 8 * buf, (k >> 1) & 1, &s_abort))))
+        break;
+      tc_fence_after();
+      uint32_t rq[D / 64][32];
+#pragma unroll
+      for (int c2 = 0; c2 < D / 64; ++c2)
+        tmem_ld32(tmem + lane_off + buf * D + (h * (D / 64) + c2) * 32, rq[c2]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar_acc_free + 8 * buf);
+      if (qrow < w.len) {
+        const float ds_mul = ds_scale_for(p.hmax[w.head], p.hmax[p.heads + w.head]);
+        float pv[3];
+        token_pos(p, static_cast<int64_t>(w.start) + qrow, true, pv);
+        const int64_t off = ((static_cast<int64_t>(w.start) + qrow) * p.heads + w.head) * D;
+        const float dq_mul = p.scale / ds_mul;  // exact: ds_mul is a power of two
+#pragma unroll
+        for (int c2 = 0; c2 < D / 64; ++c2)
+          store_row_chunk(p.dq + off, h * (D / 64) + c2, rq[c2], dq_mul, p.pos != nullptr, pv,
+                          p.f);
+      }
+    }
+    if (!ok) {
+      s_abort = 1;
+      atomicOr(p.status, kFlagTimeout);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * D < 32 ? 32 : 2 * D);
+  }
+}
+
 // Multiprocessor count of the current device (cached per device).
 static int sm_count() {
   static int cached[64] = {};
@@ -1029,6 +1267,9 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_bwd_q_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::Q_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::DQ_SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -1069,6 +1310,9 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
   p.f = make_rope_freqs(D, a.naxes);
   p.hmax = a.hmax;
   p.stall_us = a.stall_us;
+  p.ds = a.ds;
+  p.ds_cols = a.ds_cols;
+  p.ds_rows = static_cast<int64_t>(a.heads) * (static_cast<int64_t>(a.T) + 128LL * a.n);
   // both kernels: one item per (sample, head, 128-row tile), longest samples
   // first; one persistent CTA per SM (at most one per item)
   const int64_t items = (static_cast<int64_t>(a.T + 127) / 128 + a.n) * a.heads;
@@ -1080,7 +1324,10 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    {
+    if (a.ds != nullptr) {
+      KernelTimer kt(MF_K_ATTN_BWD_DQ, s);
+      attn_bwd_dq_kernel<D><<<grid, kBwdThreads, C::DQ_SMEM, s>>>(tk, p);
+    } else {
       KernelTimer kt(MF_K_ATTN_BWD_Q, s);
       attn_bwd_q_kernel<D><<<grid, kBwdThreads, C::Q_SMEM, s>>>(tq, tk, tv, tdo, p);
     }

@@ -199,7 +199,19 @@ struct AttnBwdArgs {
   int32_t n, T, heads, head_dim;
   float scale;
   uint32_t stall_us = 0;  // test hook: see mf_test_varlen_attn_bwd_stalled
+  // stored-dS form (null: the dQ kernel recomputes S and dP): the dK / dV kernel
+  // writes every (sample, head)'s scaled fp16 dS^T and a streaming kernel forms
+  // dQ = dS K' from it (layout: ds_layout_bytes)
+  uint16_t* ds = nullptr;
+  int64_t ds_cols = 0;
 };
+// Bytes of the stored-dS region for these sizes.  Rows (keys): (sample i, head a)
+// owns rows [r, r + a_i) from r = heads (cu[i] + 128 i) + a a_i, a_i = L_i rounded
+// up to 128, of R = heads (T + 128 n) rows.  Columns (queries) in groups of 8:
+// element (row, q) at ((q / 8) R + row) 8 + q % 8, for q below cols = max_len
+// rounded up to 128 -- so the 8-query units of consecutive rows are adjacent.
+// 0 if R does not fit int32.
+size_t ds_layout_bytes(int64_t T, int64_t n, int64_t heads, int64_t max_len, int64_t* cols);
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, cudaStream_t s);
 
 // Neighbours of the attention (neighbors.cu).  specs: host [2 * pairs][3].

@@ -358,6 +358,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The same descriptor for an unswizzled (interleaved) operand of 8 x 16-byte core
+// matrices.  For an MN-major operand in this layout the leading byte offset is the
+// stride between core matrices along K (per 8 rows) and the stride byte offset the
+// stride between them along MN -- the reverse of the swizzled MN-major layouts.
+// Start address 16-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_noswz(uint32_t saddr, uint32_t lbo_bytes,
+                                                uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // version; layout type 0 = no swizzle
+  return d;
+}
+
 // Instruction descriptor, kind::f16, FP32 D, dense.  A and B share one type
 // (`fmt`: 0 = F16, 1 = BF16).  a_mn / b_mn: operand stored MN-major (1) instead of
 // K-major (0).
