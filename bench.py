@@ -501,11 +501,11 @@ def gpu_arm(args):
         line["extras"] = neighbours(mf, wl, pk["hbm_gbs"])
         line["extras"]["forward_only"] = forward_only(mf, wl, qd, kd, vd, cu, pos, max_len, ws,
                                                       peak_tc)
-        line["extras"]["backward_forms"] = backward_forms(mf, wl, qd, kd, vd, dod, cu, pos, max_len,
-                                                          o, lse, peak_tc)
         if d == 128:
             line["extras"]["fp8_forward"] = fp8_forward(mf, wl, qd, kd, vd, cu, pos, max_len, ws,
                                                         peak_tc, pk["hbm_gbs"])
+        line["extras"]["backward_forms"] = backward_forms(mf, wl, qd, kd, vd, dod, cu, pos, max_len,
+                                                          o, lse, peak_tc)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, q, k, v, do, args.cpu_budget_s)
     if rank == 0:
