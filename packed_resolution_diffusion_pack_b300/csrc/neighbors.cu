@@ -147,6 +147,17 @@ __device__ __forceinline__ CuView cache_cu(const int32_t* __restrict__ cu, int32
   return CuView{cu, fits ? smem : nullptr, n};
 }
 
+// The two bf16 values of a 32-bit word as a packed fp32 pair (low half first).
+__device__ __forceinline__ uint64_t bf16x2_pair(uint32_t w) {
+  return f32x2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+// Sum over the warp's lanes.
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+  return v;
+}
+
 // Running mean / sum of squared deviations (count n) merged with another
 // partial (Chan, Golub and LeVeque's pairwise update; stable in fp32).
 __device__ __forceinline__ void merge_stats(float& n, float& mean, float& m2, float nb,
@@ -225,9 +236,12 @@ __global__ void __launch_bounds__(32 * kRowWarps) adaln_kernel(
 // the rows in turn (statistics from shared memory, then the modulated row written
 // straight to global memory).  Loads never wait on a row's reduction.  Measured
 // on the 50k pack at Dm = 3072: 0.69 of the copy bandwidth for adaln_kernel (a
-// warp per row serialises load, reduce and store), 0.62 / 0.75 / 0.77 for this
-// ring with 8 / 16 / 24 consumer warps.  Rows of at most kRingRowBytes; wider
-// rows take adaln_kernel.
+// warp per row serialises load, reduce and store); 0.62 / 0.75 / 0.77 for this
+// ring with 8 / 16 / 24 consumer warps merging per-chunk statistics pairwise, when
+// the consumers were issue bound (70 % issue active, a division per merge); 0.85
+// with the two-pass statistics and packed arithmetic below.  More slots than
+// consumers (32, 36) changed nothing.  Rows of at most kRingRowBytes; wider rows
+// take adaln_kernel.
 constexpr int kRingWarps = 24;                     // consumer warps (800 threads a block)
 constexpr int kRingSlots = 24;                     // rows in flight per block (at most)
 constexpr int kRingBytes = 196608;                 // ring size
@@ -288,42 +302,55 @@ __global__ void __launch_bounds__(32 * (kRingWarps + 1), 1) adaln_ring_kernel(
         s_end = __ldg(cu + s + 1);
       }
       const uint4* row = reinterpret_cast<const uint4*>(ring + slot * rowbytes);
-      float cnt = 0.f, mean = 0.f, m2 = 0.f;
+      // Two passes over the row in shared memory: the exact mean (fp32 sum), then the
+      // sum of squared deviations about it, both with packed two-lane arithmetic; the
+      // classic two-pass variance, as accurate as the pairwise merges it replaces at
+      // a fraction of their instructions (this loop is issue bound).
+      uint64_t s2a = 0, s2b = 0;  // two packed accumulators (0 bits = +0.0f pairs)
       for (int ch = lane; ch < D8; ch += 32) {
-        float f[8];
-        bf16x8_to_f32(row[ch], f);
-        const float cm = (((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]))) * 0.125f;
-        float a = 0.f, b = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          a = fmaf(f[e] - cm, f[e] - cm, a);
-          b = fmaf(f[e + 1] - cm, f[e + 1] - cm, b);
-        }
-        merge_stats(cnt, mean, m2, 8.f, cm, a + b);
+        const uint4 u = row[ch];
+        s2a = f32x2_add(s2a, bf16x2_pair(u.x));
+        s2b = f32x2_add(s2b, bf16x2_pair(u.y));
+        s2a = f32x2_add(s2a, bf16x2_pair(u.z));
+        s2b = f32x2_add(s2b, bf16x2_pair(u.w));
       }
-#pragma unroll
-      for (int m = 16; m > 0; m >>= 1) {
-        const float nb = __shfl_xor_sync(0xffffffffu, cnt, m);
-        const float mb = __shfl_xor_sync(0xffffffffu, mean, m);
-        const float qb = __shfl_xor_sync(0xffffffffu, m2, m);
-        if (cnt == 0.f) {
-          cnt = nb;
-          mean = mb;
-          m2 = qb;
-        } else {
-          merge_stats(cnt, mean, m2, nb, mb, qb);
-        }
+      float sa, sb, sc_, sd;
+      f32x2_unpack(s2a, sa, sb);
+      f32x2_unpack(s2b, sc_, sd);
+      const float mean = warp_sum((sa + sb) + (sc_ + sd)) * inv_dm;
+      const uint64_t nmean2 = f32x2_pack(-mean, -mean);
+      uint64_t q2a = 0, q2b = 0;
+      for (int ch = lane; ch < D8; ch += 32) {
+        const uint4 u = row[ch];
+        const uint64_t d0 = f32x2_add(bf16x2_pair(u.x), nmean2), d1 = f32x2_add(bf16x2_pair(u.y), nmean2);
+        const uint64_t d2 = f32x2_add(bf16x2_pair(u.z), nmean2), d3 = f32x2_add(bf16x2_pair(u.w), nmean2);
+        q2a = f32x2_fma(d0, d0, q2a);
+        q2b = f32x2_fma(d1, d1, q2b);
+        q2a = f32x2_fma(d2, d2, q2a);
+        q2b = f32x2_fma(d3, d3, q2b);
       }
+      f32x2_unpack(q2a, sa, sb);
+      f32x2_unpack(q2b, sc_, sd);
+      const float m2 = warp_sum((sa + sb) + (sc_ + sd));
       const float rstd = rsqrtf(m2 * inv_dm + eps);
       const int64_t base = static_cast<int64_t>(t) * D8, mbase = static_cast<int64_t>(s) * D8;
+      // y = ((x - mean) rstd)(1 + scale) + shift: (x - mean) rstd as x rstd - mean rstd
+      const uint64_t rstd2 = f32x2_pack(rstd, rstd), nmr2 = f32x2_pack(-mean * rstd, -mean * rstd);
+      const uint64_t one2 = f32x2_pack(1.f, 1.f);
       for (int ch = lane; ch < D8; ch += 32) {
-        float f[8], sh[8], sc[8];
-        bf16x8_to_f32(row[ch], f);
-        bf16x8_to_f32(__ldg(shift + mbase + ch), sh);
-        bf16x8_to_f32(__ldg(scale + mbase + ch), sc);
+        const uint4 u = row[ch], sh = __ldg(shift + mbase + ch), sc = __ldg(scale + mbase + ch);
+        const uint32_t xw[4] = {u.x, u.y, u.z, u.w}, hw[4] = {sh.x, sh.y, sh.z, sh.w};
+        const uint32_t cw[4] = {sc.x, sc.y, sc.z, sc.w};
+        uint32_t ow[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = fmaf((f[e] - mean) * rstd, 1.f + sc[e], sh[e]);
-        y[base + ch] = f32_to_bf16x8(f);
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t a2 = f32x2_fma(bf16x2_pair(xw[k]), rstd2, nmr2);
+          const uint64_t y2 = f32x2_fma(a2, f32x2_add(bf16x2_pair(cw[k]), one2), bf16x2_pair(hw[k]));
+          float y0, y1;
+          f32x2_unpack(y2, y0, y1);
+          ow[k] = pack_bf16x2(y0, y1);
+        }
+        y[base + ch] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
       }
       __syncwarp();  // every lane's reads of the slot are done
       if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
