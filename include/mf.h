@@ -197,7 +197,9 @@ mf_status mf_varlen_attn_fwd_fused_rope(const mf_bf16* q, const mf_bf16* k, cons
  * from the forward.  Other arguments as in the forward.
  * dq, dk, dv: DEVICE bf16 [T][heads][head_dim] out.
  * ws / ws_bytes: workspace from mf_attn_workspace_bytes(T, n, heads, head_dim, 1)
- * (holds the rotated Q/K and D = rowsum(dO * O)).
+ * (holds the rotated Q/K and D = rowsum(dO * O)); a workspace of at least
+ * mf_attn_workspace_bytes_ds(T, n, heads, head_dim, max_len) selects the faster
+ * stored-dS form of the computation (same results).
  * Per sample and head: P = exp(S - LSE), dV = P^T dO, dP = dO V^T,
  * dS = P * (dP - D), dQ = R(-theta) scale dS K', dK = R(-theta) scale dS^T Q'.
  * Defined by: the training step of the rcap.io listing (loss.backward through the
