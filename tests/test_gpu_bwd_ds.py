@@ -156,3 +156,84 @@ def test_full_extreme_aspect_big_sample(cuda_lib):
     def pairs(wl):
         return [(int(np.argmax(np.array(wl.lengths))), 5)]
     _full_pairs("extreme_aspect", pairs)
+
+
+def test_zero_length_and_one_token_samples(cuda_lib):
+    """Zero-length samples between others, one-token samples and a 3-token sample
+    at the end of the pack (its last tile almost all past the pack)."""
+    specs = [(1, 0, 0), (7, 8, 15), (0, 0, 0), (1, 8, 16), (15, 16, 15), (40, 24, 40), (3, 0, 0)]
+    T = int(oracle.pack(specs)[0][-1])
+    q, k, v, do = random_inputs(T, 2, 64, 65)
+    rec, sto = _bwd_both(cuda_lib, specs, q, k, v, do)
+    _oracle_check(specs, q, k, v, do, sto)
+    assert torch.equal(rec[1], sto[1]) and torch.equal(rec[2], sto[2])
+
+
+def test_empty_pack(cuda_lib):
+    mf = cuda_lib
+    cu = torch.zeros(2, dtype=torch.int32, device="cuda")
+    e = torch.empty((0, 2, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((2, 0), dtype=torch.float32, device="cuda")
+    ws = mf.workspace(0, 1, 2, 128, True, store_ds_max_len=0)
+    dq, dk, dv = mf.varlen_attn_bwd(e, e, e, e, lse, e, cu, None, 0, ws=ws)
+    mf.get_status(ws)
+    assert dq.shape == (0, 2, 128)
+
+
+def test_bad_seqlens_write_nothing(cuda_lib):
+    """A malformed cu_seqlens with the stored-dS workspace: MF_ERR_BAD_SEQLENS, and no
+    gradient row written."""
+    from test_gpu_guards import PAT16, _guarded
+    mf = cuda_lib
+    T, h, d = 64, 1, 64
+    q, k, v, do = (dev(x) for x in random_inputs(T, h, d, 66))
+    cu_ok = torch.tensor([0, 40, 64], dtype=torch.int32, device="cuda")
+    o, lse = mf.varlen_attn_fwd(q, k, v, cu_ok, None, 64)
+    ws = mf.workspace(T, 2, h, d, True, store_ds_max_len=64)
+    bufs = [_guarded((T, h, d), torch.bfloat16) for _ in range(3)]
+    for b, _ in bufs:
+        b.view(torch.int16).fill_(PAT16)
+    cu_bad = torch.tensor([0, 40, 30], dtype=torch.int32, device="cuda")
+    mf.varlen_attn_bwd(q, k, v, o, lse, do, cu_bad, None, 64, dq=bufs[0][1], dk=bufs[1][1],
+                       dv=bufs[2][1], ws=ws)
+    with pytest.raises(mf.MFError) as ei:
+        mf.get_status(ws)
+    assert ei.value.status == 6  # MF_ERR_BAD_SEQLENS
+    torch.cuda.synchronize()
+    for b, _ in bufs:
+        assert bool((b.view(torch.int16) == PAT16).all())
+
+
+def test_wait_that_runs_out_is_reported_and_the_next_call_is_right(cuda_lib):
+    """The time-out path through both kernels of the stored-dS form (the test hook
+    stalls every CTA's MMA thread): MF_ERR_TIMEOUT, no gradient written, then a normal
+    backward on the same workspace matches the oracle."""
+    import ctypes
+    from test_gpu_guards import PAT16, SPECS, _guarded
+    mf = cuda_lib
+    lib = mf.load()
+    h, d = 2, 128
+    cu, pos = mf.pack(SPECS)
+    T, max_len = mf.pack_size(SPECS)
+    n = len(SPECS)
+    qb, kb, vb, dob = random_inputs(T, h, d, 67)
+    q, k, v, do = dev(qb), dev(kb), dev(vb), dev(dob)
+    o, lse = mf.varlen_attn_fwd(q, k, v, cu, pos, max_len)
+    bufs = [_guarded((T, h, d), torch.bfloat16) for _ in range(3)]
+    ws = mf.workspace(T, n, h, d, True, store_ds_max_len=max_len)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = lib.mf_test_varlen_attn_bwd_stalled(p(q), p(k), p(v), p(o), p(lse), p(do), p(cu), p(pos),
+                                             n, T, max_len, h, d, 0.0, p(bufs[0][1]),
+                                             p(bufs[1][1]), p(bufs[2][1]), p(ws), ws.numel(),
+                                             20000, stream)
+    assert rc == 0, mf.STATUS_NAMES.get(rc, rc)
+    with pytest.raises(mf.MFError) as ei:
+        mf.get_status(ws)
+    assert ei.value.status == 5  # MF_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    for b, _ in bufs:
+        assert bool((b.view(torch.int16) == PAT16).all())
+    g = mf.varlen_attn_bwd(q, k, v, o, lse, do, cu, pos, max_len, ws=ws)
+    mf.get_status(ws)
+    _oracle_check(SPECS, qb, kb, vb, dob, g)
