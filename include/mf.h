@@ -128,16 +128,16 @@ size_t mf_attn_workspace_bytes(int32_t T, int32_t n, int32_t heads, int32_t head
 
 /*
  * Workspace bytes for the backward calls that selects their stored-dS form: the
- * dK / dV kernel also writes each (sample, head)'s scaled fp16 dS^T (its rows
- * padded to 128) into the workspace, and dQ = scale R(-theta) dS K' is then one
- * streaming GEMM over it instead of a kernel that recomputes S and dP.  Faster,
- * at the cost of memory: about 2 heads (T + 128 n) max_len bytes on top of
- * mf_attn_workspace_bytes(..., 1) (10.5 GB for 48k tokens, 24 heads, max_len
- * 4,291).  Any of the backward calls given a workspace of at least this size,
- * for the same T, n, heads and max_len, uses that form; results agree with the
- * other form within the backward's tolerance (not bit for bit: the two forms
- * round dS from differently ordered GEMMs).  Returns 0 on invalid sizes, or when
- * heads (T + 128 n) reaches 2^31 (the form is then unavailable).
+ * dK / dV kernel also writes each (sample, head)'s scaled fp16 dS^T (its keys and
+ * queries padded to multiples of 128) into the workspace, and dQ = scale R(-theta)
+ * dS K' is then one streaming GEMM over it instead of a kernel that recomputes S
+ * and dP.  Faster, at the cost of memory: 256 heads (ceil(T / 128) + n) max_len'
+ * bytes (max_len' = max_len rounded up to 128) on top of
+ * mf_attn_workspace_bytes(..., 1) (11.4 GB in all for 48k tokens, 24 heads,
+ * max_len 4,291).  Any of the backward calls given a workspace of at least this
+ * size, for the same T, n, heads and max_len, uses that form; its results equal
+ * the other form's (the same fp16 dS values summed in the same order).  Returns 0
+ * on invalid sizes.
  * No counterpart on the pages: a memory-for-time form of the backward.
  */
 size_t mf_attn_workspace_bytes_ds(int32_t T, int32_t n, int32_t heads, int32_t head_dim,

@@ -67,11 +67,10 @@ WsLayout ws_layout(int64_t T, int64_t n, int64_t heads, int64_t head_dim, bool b
 
 size_t ds_layout_bytes(int64_t T, int64_t n, int64_t heads, int64_t max_len, int64_t* cols) {
   const int64_t A = (max_len > 0 ? (max_len + 127) / 128 : 1) * 128;
-  const int64_t rows = heads * (T + 128 * n);
-  // TMA row coordinates are int32: the last tile's rows must stay below 2^31
-  if (T < 0 || n < 0 || heads < 1 || rows > INT32_MAX - 256 || A > INT32_MAX) return 0;
+  const int64_t tiles = heads * ((T + 127) / 128 + n);  // 128-key tiles, see ds_tile_base
+  if (T < 0 || n < 0 || heads < 1 || A > INT32_MAX || tiles > (INT64_MAX / 256) / A) return 0;
   if (cols) *cols = A;
-  return static_cast<size_t>(rows) * static_cast<size_t>(A) * 2;
+  return static_cast<size_t>(tiles) * 128 * static_cast<size_t>(A) * 2;
 }
 
 static bool aligned(const void* p, uintptr_t a) {

@@ -239,19 +239,22 @@ struct BwdParams {
   // test hook (0 = off): the MMA thread first waits, at most this many
   // microseconds, on a barrier that nothing arrives on (failure-detection tests)
   uint32_t stall_us;
-  // stored-dS form: scaled fp16 dS^T of ds_rows key rows and ds_cols queries in
-  // 8-query units, unit g of row r at (g ds_rows + r) (null: dQ recomputes)
+  // stored-dS form: scaled fp16 dS^T in 128-key tiles of ds_cols / 8 units of 8
+  // queries (null: dQ recomputes); see ds_tile_base
   uint16_t* ds;
-  int64_t ds_rows, ds_cols;
+  int64_t ds_cols;
 };
 
-// First row of (sample, head)'s dS^T block in the stored-dS array: samples at
-// heads (cu[i] + 128 i), heads a_i rows apart, a_i = L_i rounded up to 128.  The
-// blocks never overlap: heads a_i <= heads (L_i + 127) < the next sample's offset.
-__device__ __forceinline__ int64_t ds_block_row(int32_t heads, int32_t start, int32_t sample,
+// The stored-dS array holds 128-key tiles, each [ds_cols / 8 units][128 keys][8
+// queries] (2 KB a unit), so a tile's 16-unit query block is 32 contiguous KB and
+// 32 consecutive keys of one unit are 512 contiguous bytes.  First tile of (sample,
+// head)'s block: heads (ceil(cu[i] / 128) + i) + head a_i / 128, a_i = L_i rounded
+// up to 128.  The blocks never overlap: a sample's heads a_i / 128 tiles end at or
+// before heads (ceil(cu[i + 1] / 128) + i + 1), the next sample's first tile.
+__device__ __forceinline__ int64_t ds_tile_base(int32_t heads, int32_t start, int32_t sample,
                                                 int32_t head, int32_t padded_len) {
-  return static_cast<int64_t>(heads) * (static_cast<int64_t>(start) + 128LL * sample) +
-         static_cast<int64_t>(head) * padded_len;
+  return static_cast<int64_t>(heads) * ((static_cast<int64_t>(start) + 127) / 128 + sample) +
+         static_cast<int64_t>(head) * (padded_len / 128);
 }
 
 // 2^e with e = floor(log2(2^15 / bound)) clamped to [-64, 64]: scaled |dS| stays
@@ -563,11 +566,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // dS is staged in fp16 as ds_mul * dS (a power of two; see ds_scale_for)
       const float ds_mul = ds_scale_for(p.hmax[w.head], p.hmax[p.heads + w.head]);
       const uint64_t dsm2 = f32x2_pack(ds_mul, ds_mul);
-      // stored-dS form: this thread's key row; its 8-query unit g sits at
-      // ds_row + g ds_rows 8 (consecutive rows adjacent)
+      // stored-dS form: this thread's key row in its 128-key tile; its 8-query unit
+      // g sits at ds_row + g 1024 (consecutive rows adjacent)
       uint16_t* ds_row = nullptr;
       if (p.ds != nullptr)
-        ds_row = p.ds + (ds_block_row(p.heads, w.start, w.sample, w.head, nq * C::BQ) + k0 + row) * 8;
+        ds_row = p.ds + ((ds_tile_base(p.heads, w.start, w.sample, w.head, nq * C::BQ) + w.blk) *
+                             (p.ds_cols / 8) * 128 + row) * 8;
       for (int32_t i = 0; i < nq; ++i) {
         const int32_t g = gt + i, st = g % C::NST;
         ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_full + 8 * st, (g / C::NST) & 1, &s_abort) &&
@@ -663,7 +667,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-              *reinterpret_cast<uint4*>(ds_row + (i * 16 + 8 * h + 4 * c + u) * p.ds_rows * 8) =
+              *reinterpret_cast<uint4*>(ds_row + (i * 16 + 8 * h + 4 * c + u) * 1024) =
                   make_uint4(xs[c][4 * u], xs[c][4 * u + 1], xs[c][4 * u + 2], xs[c][4 * u + 3]);
         }
       }
@@ -1054,7 +1058,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // fp16 dS^T read back from memory instead of recomputing S and dP.  Persistent,
 // one item per (sample, head, 128-query tile) as in attn_bwd_q_kernel.  Per key
 // tile j the TMA warp copies the dS^T block [keys of j][queries of the item] --
-// 16 runs of 128 rows x 16 bytes, one per 8-query unit, which land as the
+// 32 contiguous KB, 16 units of 128 keys x 8 queries, which land as the
 // unswizzled MN-major core-matrix layout (8 keys x 8 queries per 128 bytes) --
 // and K'_j into one of DQ_NS stages; the MMA thread issues dQ += dS K'_j (both
 // operands MN-major: dS^T rows are keys, K' rows are keys) into one of two TMEM
@@ -1120,7 +1124,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       WorkItemB w;
       for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
         const int32_t q0 = w.blk * C::BQ, nk = (w.len + C::BK - 1) / C::BK;
-        const int64_t row0 = ds_block_row(p.heads, w.start, w.sample, w.head, nk * C::BK);
+        const int64_t tile0 = ds_tile_base(p.heads, w.start, w.sample, w.head, nk * C::BK);
         for (int32_t j = 0; j < nk; ++j) {
           const int32_t g = gs + j, st = g % C::DQ_NS, use = g / C::DQ_NS;
           if (use > 0 &&
@@ -1137,11 +1141,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           w.start + j * C::BK);
           }
           __syncwarp();  // the byte count is posted before any copy can complete
-          if (lane < 16) {  // unit q0 / 8 + lane: keys row0 + 128 j .. + 127, 2 KB
+          if (lane < 2) {  // units q0 / 8 + 8 lane .. + 7 of key tile j: 16 contiguous KB
             const uint16_t* src =
-                p.ds + ((static_cast<int64_t>(q0 / 8 + static_cast<int>(lane))) * p.ds_rows +
-                        row0 + static_cast<int64_t>(j) * C::BK) * 8;
-            bulk_load(sds + lane * 2048, src, 2048, bar_full + 8 * st);
+                p.ds + ((tile0 + j) * (p.ds_cols / 8) + q0 / 8 + 8 * static_cast<int>(lane)) * 1024;
+            bulk_load(sds + lane * 16384, src, 16384, bar_full + 8 * st);
           }
           issued = g + 1;
         }
@@ -1312,7 +1315,6 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
   p.stall_us = a.stall_us;
   p.ds = a.ds;
   p.ds_cols = a.ds_cols;
-  p.ds_rows = static_cast<int64_t>(a.heads) * (static_cast<int64_t>(a.T) + 128LL * a.n);
   // both kernels: one item per (sample, head, 128-row tile), longest samples
   // first; one persistent CTA per SM (at most one per item)
   const int64_t items = (static_cast<int64_t>(a.T + 127) / 128 + a.n) * a.heads;

@@ -205,12 +205,10 @@ struct AttnBwdArgs {
   uint16_t* ds = nullptr;
   int64_t ds_cols = 0;
 };
-// Bytes of the stored-dS region for these sizes.  Rows (keys): (sample i, head a)
-// owns rows [r, r + a_i) from r = heads (cu[i] + 128 i) + a a_i, a_i = L_i rounded
-// up to 128, of R = heads (T + 128 n) rows.  Columns (queries) in groups of 8:
-// element (row, q) at ((q / 8) R + row) 8 + q % 8, for q below cols = max_len
-// rounded up to 128 -- so the 8-query units of consecutive rows are adjacent.
-// 0 if R does not fit int32.
+// Bytes of the stored-dS region for these sizes: heads (ceil(T / 128) + n) tiles of
+// 128 keys x cols queries in fp16, cols = max_len rounded up to 128; each tile is
+// [cols / 8 units of 8 queries][128 keys][8].  (Sample i, head a) owns the tiles
+// from heads (ceil(cu[i] / 128) + i) + a a_i / 128, a_i = L_i rounded up to 128.
 size_t ds_layout_bytes(int64_t T, int64_t n, int64_t heads, int64_t max_len, int64_t* cols);
 cudaError_t launch_attn_bwd(const AttnBwdArgs& a, cudaStream_t s);
 

@@ -222,16 +222,16 @@ def test_fused_rope_forward_argument_errors_on_host():
 
 
 def test_stored_ds_workspace_size():
-    """mf_attn_workspace_bytes_ds: the backward workspace plus heads (T + 128 n)
-    rows of max_len rounded up to 128 fp16 columns; 0 for invalid sizes and when
-    the row count reaches 2^31 (the form is then unavailable)."""
+    """mf_attn_workspace_bytes_ds: the backward workspace (rounded up to 1 KB) plus
+    heads (ceil(T / 128) + n) tiles of 128 keys x (max_len rounded up to 128)
+    fp16 queries; 0 for invalid sizes."""
     lib = mf.load()
     T, n, h, d, L = 48019, 18, 24, 128, 4291
     base = lib.mf_attn_workspace_bytes(T, n, h, d, 1)
     got = lib.mf_attn_workspace_bytes_ds(T, n, h, d, L)
-    ds = h * (T + 128 * n) * (-(-L // 128) * 128) * 2
+    ds = h * (-(-T // 128) + n) * 128 * (-(-L // 128) * 128) * 2
     assert got == -(-base // 1024) * 1024 + ds
     assert mf.attn_workspace_bytes_ds(T, n, h, d, L) == got
     assert lib.mf_attn_workspace_bytes_ds(T, n, h, 96, L) == 0
     assert lib.mf_attn_workspace_bytes_ds(T, n, h, d, -1) == 0
-    assert lib.mf_attn_workspace_bytes_ds(2 ** 30, 1, 64, d, 16) == 0  # rows past 2^31
+    assert lib.mf_attn_workspace_bytes_ds(-1, n, h, d, L) == 0
