@@ -662,13 +662,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // After the release (the tensor core runs dK meanwhile): queries
           // [i BQ + 64h + 32c + 8u, +8) of the key row, as unit
           // g = 16 i + 8h + 4c + u.  The 32 lanes of a warp hold consecutive key
-          // rows, so each store writes 512 contiguous bytes.
+          // rows, so each store writes 512 contiguous bytes; streaming stores (read
+          // once, much later) leave L2 to the Q' / dO tiles the CTAs re-read.
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-              *reinterpret_cast<uint4*>(ds_row + (i * 16 + 8 * h + 4 * c + u) * 1024) =
-                  make_uint4(xs[c][4 * u], xs[c][4 * u + 1], xs[c][4 * u + 2], xs[c][4 * u + 3]);
+              __stcs(reinterpret_cast<uint4*>(ds_row + (i * 16 + 8 * h + 4 * c + u) * 1024),
+                     make_uint4(xs[c][4 * u], xs[c][4 * u + 1], xs[c][4 * u + 2], xs[c][4 * u + 3]));
         }
       }
       if (!ok) break;
