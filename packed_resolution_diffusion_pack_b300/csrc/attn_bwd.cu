@@ -1248,7 +1248,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // Multiprocessor count of the current device (cached per device).
-static int sm_count() {
+int device_sm_count() {
   static int cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
@@ -1320,7 +1320,7 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
   // first; one persistent CTA per SM (at most one per item)
   const int64_t items = (static_cast<int64_t>(a.T + 127) / 128 + a.n) * a.heads;
   if (items > 0) {
-    const unsigned grid = static_cast<unsigned>(items < sm_count() ? items : sm_count());
+    const unsigned grid = static_cast<unsigned>(items < device_sm_count() ? items : device_sm_count());
     {
       KernelTimer kt(MF_K_ATTN_BWD, s);
       attn_bwd_kv_kernel<D><<<grid, kBwdThreads, C::KV_SMEM, s>>>(tq, tk, tv, tdo, p);

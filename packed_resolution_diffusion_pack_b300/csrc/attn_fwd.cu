@@ -200,10 +200,13 @@ struct WorkItem {
 };
 // Per-CTA scalars kept in the dynamic shared-memory region.
 struct CtaMisc {
-  WorkItem w;
-  int valid;
   uint32_t tmem;
   uint32_t abort;
+  // each softmax warp's current item and counters (item index, S steps and
+  // items of its Q tile so far), read back from shared memory where used: kept
+  // out of the registers its score row needs
+  WorkItem sw[8];
+  int32_t cnt[8][4];
 };
 __device__ __forceinline__ bool find_item(const int32_t* __restrict__ cu,
                                           const int32_t* __restrict__ order,
@@ -249,15 +252,16 @@ struct FwdCfg {
   static constexpr int NSLOT = F8 ? 8 : (D == 128 ? 4 : 8);  // K/V ring slots
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = 2 * TILE;
-  // bf16 O staging of the epilogue: the tile's own Q buffer, except in the 8-bit
-  // variant whose Q tiles are half that size (a separate 2 x BM x D x 2 bytes)
+  // bf16 O staging of the epilogue: 32 rows x 64 bytes per softmax warp (one
+  // 32-column chunk of its rows at a time), apart from the Q buffers, which the
+  // next item's Q tiles take as soon as this item's last S GEMMs are done
   static constexpr int OFF_STG = OFF_KV + NSLOT * TILE;
-  static constexpr int STG = F8 ? 2 * BM * D * 2 : 0;
+  static constexpr int STG = 8 * 32 * 64;
   static constexpr int OFF_BAR = OFF_STG + STG;
   static constexpr int OFF_MISC = OFF_BAR + (ROT ? 512 : 256);
   // rotate-on-load form: token positions staged per transform warp, int2 [2][192]
   // (its rows of Q tile 0, Q tile 1 and the current K tile)
-  static constexpr int OFF_POS = OFF_MISC + 64;
+  static constexpr int OFF_POS = OFF_MISC + 320;
   static constexpr int SMEM = OFF_POS + (ROT ? 2 * 192 * 8 : 0);
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
   // S = Q'K'^T and O += P V' (V' MN-major); operand format code 0 is fp16 under
@@ -438,20 +442,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t sbase = smem_u32(smem_raw);
   CtaMisc& misc = *reinterpret_cast<CtaMisc*>(smem_raw + C::OFF_MISC);
-  WorkItem& s_w = misc.w;
-  int& s_valid = misc.valid;
+  static_assert(sizeof(CtaMisc) <= 320, "per-CTA scalars");
   uint32_t& s_tmem = misc.tmem;
   volatile uint32_t& s_abort = misc.abort;
   if (sbase & 1023u) {
     if (threadIdx.x == 0) atomicOr(p.status, kFlagSmemAlign);
     return;
   }
+  if ((*p.status & kFlagBadSeqlens) != 0) return;  // the schedule listed no work
   const uint32_t sQ = sbase + C::OFF_Q;
   const uint32_t sKV = sbase + C::OFF_KV;
   const uint32_t bars = sbase + C::OFF_BAR;
   // barrier addresses (8 bytes each)
-  const uint32_t bar_q = bars;
-  const uint32_t bar_full = bars + 8;                     // [NSLOT]
+  const uint32_t bar_q = bars;                            // an item's Q tiles loaded
+  const uint32_t bar_qfree = bars + 8;                    // ... and read by its last S GEMMs
+  const uint32_t bar_full = bars + 16;                    // [NSLOT]
   const uint32_t bar_empty = bar_full + 8 * C::NSLOT;     // [NSLOT]
   const uint32_t bar_s = bar_empty + 8 * C::NSLOT;        // [2]
   const uint32_t bar_p = bar_s + 16;                      // [2]
@@ -462,38 +467,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t bar_qr = bar_stall + 8;     // [2]
   const uint32_t bar_rdy = bar_qr + 16;      // [NSLOT]
   static_assert(!ROT || !F8, "the rotate-on-load form is a 16-bit forward");
-  static_assert(8 * (ROT ? 10 + 3 * C::NSLOT : 8 + 2 * C::NSLOT) <= C::OFF_MISC - C::OFF_BAR,
+  static_assert(8 * (ROT ? 11 + 3 * C::NSLOT : 9 + 2 * C::NSLOT) <= C::OFF_MISC - C::OFF_BAR,
                 "barrier region too small");
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     s_abort = 0;
-    s_valid = ((*p.status & kFlagBadSeqlens) == 0) &&
-              find_item(p.cu, p.order, p.prefix, p.n, 2 * C::BM, blockIdx.x, s_w);
-    if (s_valid) {
-      mbar_init(bar_q, 1);
-      for (int i = 0; i < C::NSLOT; ++i) {
-        mbar_init(bar_full + 8 * i, 1);
-        mbar_init(bar_empty + 8 * i, 1);
-      }
-      mbar_init(bar_s, 1);
-      mbar_init(bar_s + 8, 1);
-      mbar_init(bar_p, 128);
-      mbar_init(bar_p + 8, 128);
-      mbar_init(bar_o, 1);
-      mbar_init(bar_o + 8, 1);
-      mbar_init(bar_drain, 1);
-      mbar_init(bar_stall, 1);
-      if (ROT) {
-        mbar_init(bar_qr, 64);
-        mbar_init(bar_qr + 8, 64);
-        for (int i = 0; i < C::NSLOT; ++i) mbar_init(bar_rdy + 8 * i, 64);
-      }
-      fence_mbar_init();
+    mbar_init(bar_q, 1);
+    mbar_init(bar_qfree, 1);
+    for (int i = 0; i < C::NSLOT; ++i) {
+      mbar_init(bar_full + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, 1);
     }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_s + 8, 1);
+    mbar_init(bar_p, 128);
+    mbar_init(bar_p + 8, 128);
+    mbar_init(bar_o, 1);
+    mbar_init(bar_o + 8, 1);
+    mbar_init(bar_drain, 1);
+    mbar_init(bar_stall, 1);
+    if (ROT) {
+      mbar_init(bar_qr, 64);
+      mbar_init(bar_qr + 8, 64);
+      for (int i = 0; i < C::NSLOT; ++i) mbar_init(bar_rdy + 8 * i, 64);
+    }
+    fence_mbar_init();
   }
   __syncthreads();
-  if (!s_valid) return;
   if (warp == 9) {
     tmem_alloc(smem_u32(&s_tmem), 512);
     tmem_relinquish();
@@ -503,10 +504,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  const WorkItem w = s_w;
-  const int32_t q0 = w.blk * 2 * C::BM;            // first query row (in sample)
-  const bool has1 = q0 + C::BM < w.len;             // second Q tile holds rows
-  const int32_t nkv = (w.len + C::BN - 1) / C::BN;  // K/V tiles
+  // Persistent: in wave k the CTA takes item k gridDim.x + blockIdx.x of the ranked
+  // list (longest samples first), or k gridDim.x + gridDim.x - 1 - blockIdx.x in odd
+  // waves, so that each CTA's items sum to nearly the same work; every role walks
+  // the same sequence.  Ring position c counts the K and V tiles across items (K_j
+  // of an item whose first tile is c0 at c0 + 2j, V_j at c0 + 2j + 1).
+  auto cta_item = [&](int32_t k, WorkItem& w) -> bool {
+    const int64_t idx = static_cast<int64_t>(k) * gridDim.x +
+                        ((k & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
+    if (idx > INT32_MAX) return false;
+    return find_item(p.cu, p.order, p.prefix, p.n, 2 * C::BM, static_cast<int32_t>(idx), w);
+  };
 
   if (warp >= 8) {
     warpgroup_reg_dealloc<kFwdRegsLow>();
@@ -516,26 +524,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
-        mbar_arrive_expect_tx(bar_q, (has1 ? 2 : 1) * C::TILE);
-        for (int t = 0; t < (has1 ? 2 : 1); ++t)
-          for (int ch = 0; ch < C::NCH; ++ch)
-            tma_load_3d(sQ + t * C::TILE + ch * C::CHUNK, &tm_q, bar_q, ch * (128 / C::EB), w.head,
-                        w.start + q0 + t * C::BM);
-        int32_t issued = 0;
+        int32_t c = 0, items = 0;
         bool ok = true;
-        for (int32_t j = 0; j < nkv && ok; ++j) {
-          for (int kv = 0; kv < 2; ++kv) {
-            const int32_t c = 2 * j + kv;
-            const int32_t slot = c % C::NSLOT, use = c / C::NSLOT;
-            if (use > 0 && !mbar_wait_bk(bar_empty + 8 * slot, (use - 1) & 1, &s_abort)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(bar_full + 8 * slot, C::TILE);
+        WorkItem w;
+        for (int32_t k = 0; ok && cta_item(k, w); ++k) {
+          const int32_t q0 = w.blk * 2 * C::BM;
+          const bool has1 = q0 + C::BM < w.len;
+          const int32_t nkv = (w.len + C::BN - 1) / C::BN;
+          // the Q buffers are free once the previous item's last S GEMMs are done
+          if (k > 0 && !(ok = mbar_wait_bk(bar_qfree, (k - 1) & 1, &s_abort))) break;
+          mbar_arrive_expect_tx(bar_q, (has1 ? 2 : 1) * C::TILE);
+          for (int t = 0; t < (has1 ? 2 : 1); ++t)
             for (int ch = 0; ch < C::NCH; ++ch)
-              tma_load_3d(sKV + slot * C::TILE + ch * C::CHUNK, kv ? &tm_v : &tm_k,
-                          bar_full + 8 * slot, ch * (128 / C::EB), w.head, w.start + j * C::BN);
-            ++issued;
+              tma_load_3d(sQ + t * C::TILE + ch * C::CHUNK, &tm_q, bar_q, ch * (128 / C::EB),
+                          w.head, w.start + q0 + t * C::BM);
+          ++items;
+          for (int32_t j = 0; j < nkv && ok; ++j) {
+            for (int kv = 0; kv < 2; ++kv, ++c) {
+              const int32_t slot = c % C::NSLOT, use = c / C::NSLOT;
+              if (use > 0 && !mbar_wait_bk(bar_empty + 8 * slot, (use - 1) & 1, &s_abort)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(bar_full + 8 * slot, C::TILE);
+              for (int ch = 0; ch < C::NCH; ++ch)
+                tma_load_3d(sKV + slot * C::TILE + ch * C::CHUNK, kv ? &tm_v : &tm_k,
+                            bar_full + 8 * slot, ch * (128 / C::EB), w.head, w.start + j * C::BN);
+            }
           }
         }
         if (!ok) {
@@ -543,17 +558,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           atomicOr(p.status, kFlagTimeout);
         }
         // let every issued copy land before the CTA can exit
-        mbar_wait_drain(bar_q, 0);
-        for (int32_t c = (issued > C::NSLOT ? issued - C::NSLOT : 0); c < issued; ++c)
-          mbar_wait_drain(bar_full + 8 * (c % C::NSLOT), (c / C::NSLOT) & 1);
+        if (items > 0) mbar_wait_drain(bar_q, (items - 1) & 1);
+        for (int32_t i = (c > C::NSLOT ? c - C::NSLOT : 0); i < c; ++i)
+          mbar_wait_drain(bar_full + 8 * (i % C::NSLOT), (i / C::NSLOT) & 1);
       }
     } else if (warp == 9) {
       // -------------------------------------------------------------- MMA issuer
       if (lane == 0) {
         bool ok = p.stall_us == 0 ||
                   mbar_wait_for(bar_stall, 0, &s_abort, static_cast<uint64_t>(p.stall_us) * 1000u);
-        ok = ok && mbar_wait(ROT ? bar_qr : bar_q, 0, &s_abort);
-        tc_fence_after();
         auto kv_wait = [&](int32_t c) -> bool {
           const bool r = mbar_wait((ROT ? bar_rdy : bar_full) + 8 * (c % C::NSLOT),
                                    (c / C::NSLOT) & 1, &s_abort);
@@ -561,77 +574,98 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           return r;
         };
         // Shared-memory descriptors: one base per buffer, then the start-address
-        // field (16-byte units) advanced by constant offsets.
+        // field (16-byte units, low word) advanced by constant offsets.  The high
+        // word (stride 1024 bytes, version, 128B swizzle) is the same for all three.
         const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
         const uint64_t dkv_k = sdesc_sw128(sKV, 16, 1024);          // K-major (K tiles)
         const uint64_t dkv_m = sdesc_sw128(sKV, C::CHUNK, 1024);    // MN-major (V tiles)
-        constexpr uint64_t kTile = C::TILE >> 4;
-        // K step kk starts kk * 32 bytes into the 128-byte rows (next chunk every 4)
-        auto kofs = [](int kk) -> uint64_t { return ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4; };
-        auto issue_s = [&](int t, int32_t j) {
-          const uint64_t a0 = dq0 + t * kTile;
-          const uint64_t b0 = dkv_k + ((2 * j) % C::NSLOT) * kTile;
+        const uint32_t hi = static_cast<uint32_t>(dq0 >> 32);
+        const uint32_t q_lo = static_cast<uint32_t>(dq0), k_lo = static_cast<uint32_t>(dkv_k),
+                       v_lo = static_cast<uint32_t>(dkv_m);
+        constexpr uint32_t kTile = C::TILE >> 4;
+        auto issue_s = [&](int t, int32_t c) {  // S_t = Q_t K^T, K at ring position c
+          const uint32_t a0 = q_lo + t * kTile;
+          const uint32_t b0 = k_lo + (c % C::NSLOT) * kTile;
           const uint32_t d = tmem + (t ? C::S_COL1 : C::S_COL0);
-  #pragma unroll
+          // K step kk starts kk * 32 bytes into the 128-byte rows (next chunk every 4)
+#pragma unroll
           for (int kk = 0; kk < D / C::KSTEP; ++kk) {
-            if constexpr (F8)
-              mma_ss_f8(d, a0 + kofs(kk), b0 + kofs(kk), C::IDESC_S, kk > 0);
-            else
-              mma_ss(d, a0 + kofs(kk), b0 + kofs(kk), C::IDESC_S, kk > 0);
+            const uint32_t o = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+            mma_ss_w<F8>(d, a0 + o, hi, b0 + o, hi, C::IDESC_S, kk > 0);
           }
           mma_commit(bar_s + 8 * t);
         };
-        auto issue_pv = [&](int t, int32_t j) {
-          const uint64_t b0 = dkv_m + ((2 * j + 1) % C::NSLOT) * kTile;
+        auto issue_pv = [&](int t, int32_t c, bool first) {  // O_t += P_t V, V at c
+          const uint32_t b0 = v_lo + (c % C::NSLOT) * kTile;
           const uint32_t d = tmem + (t ? C::O_COL1 : C::O_COL0);
           const uint32_t a = tmem + (t ? C::S_COL1 : C::S_COL0);
           // P step kk: 32 bytes of each TMEM lane (8 columns); V rows kk * KSTEP on
-  #pragma unroll
-          for (int kk = 0; kk < C::BN / C::KSTEP; ++kk) {
-            const uint64_t b = b0 + ((kk * C::KSTEP * 128) >> 4);
-            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-            if constexpr (F8)
-              mma_ts_f8(d, a + kk * 8, b, C::IDESC_PV, acc);
-            else
-              mma_ts(d, a + kk * 8, b, C::IDESC_PV, acc);
-          }
+#pragma unroll
+          for (int kk = 0; kk < C::BN / C::KSTEP; ++kk)
+            mma_ts_w<F8>(d, a + kk * 8, b0 + ((kk * C::KSTEP * 128) >> 4), hi, C::IDESC_PV,
+                         (!first || kk > 0) ? 1u : 0u);
         };
-        if (ok) ok = kv_wait(0);
-        if (ok) {
-          issue_s(0, 0);
-          if (ROT && has1) {
-            ok = mbar_wait(bar_qr + 8, 0, &s_abort);
-            tc_fence_after();
+        // parities: n0 / n1 S steps of Q tile 0 / 1 so far, i1 items with a tile 1
+        int32_t c0 = 0, n0 = 0, n1 = 0, i1 = 0;
+        WorkItem w;
+        for (int32_t k = 0; ok && cta_item(k, w); ++k) {
+          const int32_t q0 = w.blk * 2 * C::BM;
+          const bool has1 = q0 + C::BM < w.len;
+          const int32_t nkv = (w.len + C::BN - 1) / C::BN;
+          ok = mbar_wait(ROT ? bar_qr : bar_q, k & 1, &s_abort);
+          tc_fence_after();
+          // The first S GEMM of this item overwrites S_0, and its first P V (no
+          // accumulate) O_0, while the previous item may still be in its epilogue:
+          // S_0 held that item's last P, already read by its last P V (issued
+          // earlier, and MMAs run in order); O_0 is overwritten only after the
+          // softmax warpgroup has arrived on bar_p for this item, which it does
+          // after loading the previous item's O.
+          if (ok) ok = kv_wait(c0);
+          if (ok) {
+            issue_s(0, c0);
+            if (ROT && has1) {
+              ok = mbar_wait(bar_qr + 8, i1 & 1, &s_abort);
+              tc_fence_after();
+            }
           }
-        }
-        if (ok) {
-          if (has1) issue_s(1, 0);
-          mma_commit(bar_empty + 8 * (0 % C::NSLOT));
-        }
-        for (int32_t j = 0; j < nkv && ok; ++j) {
-          ok = mbar_wait(bar_p, j & 1, &s_abort) && kv_wait(2 * j + 1);
+          if (ok) {
+            if (has1) issue_s(1, c0);
+            if (nkv == 1) mma_commit(bar_qfree);
+            mma_commit(bar_empty + 8 * (c0 % C::NSLOT));
+          }
+          for (int32_t j = 0; j < nkv && ok; ++j) {
+            const int32_t ck = c0 + 2 * j;  // K_j; V_j at ck + 1
+            ok = mbar_wait(bar_p, (n0 + j) & 1, &s_abort) && kv_wait(ck + 1);
+            if (!ok) break;
+            issue_pv(0, ck + 1, j == 0);
+            const bool more = j + 1 < nkv;
+            if (more) {
+              if (!(ok = kv_wait(ck + 2))) break;
+              issue_s(0, ck + 2);
+            }
+            if (has1) {
+              if (!(ok = mbar_wait(bar_p + 8, (n1 + j) & 1, &s_abort))) break;
+              tc_fence_after();
+              issue_pv(1, ck + 1, j == 0);
+            }
+            mma_commit(bar_empty + 8 * ((ck + 1) % C::NSLOT));
+            if (more) {
+              if (has1) issue_s(1, ck + 2);
+              if (j + 2 == nkv) mma_commit(bar_qfree);  // the item's last S GEMMs
+              mma_commit(bar_empty + 8 * ((ck + 2) % C::NSLOT));
+            }
+          }
           if (!ok) break;
-          issue_pv(0, j);
-          const bool more = j + 1 < nkv;
-          if (more) {
-            if (!(ok = kv_wait(2 * j + 2))) break;
-            issue_s(0, j + 1);
-          }
-          if (has1) {
-            if (!(ok = mbar_wait(bar_p + 8, j & 1, &s_abort))) break;
-            tc_fence_after();
-            issue_pv(1, j);
-          }
-          mma_commit(bar_empty + 8 * ((2 * j + 1) % C::NSLOT));
-          if (more) {
-            if (has1) issue_s(1, j + 1);
-            mma_commit(bar_empty + 8 * ((2 * j + 2) % C::NSLOT));
-          }
-        }
-        if (ok) {
           mma_commit(bar_o);
           if (has1) mma_commit(bar_o + 8);
-        } else {
+          c0 += 2 * nkv;
+          n0 += nkv;
+          if (has1) {
+            n1 += nkv;
+            ++i1;
+          }
+        }
+        if (!ok) {
           s_abort = 1;
           atomicOr(p.status, kFlagTimeout);
         }
@@ -647,7 +681,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint32_t tid = threadIdx.x - 320;
       float vmax = 0.f;
       uint32_t bad = 0;
-      const int64_t qrow0 = static_cast<int64_t>(w.start) + q0;
       const int2* pos2 = reinterpret_cast<const int2*>(p.pos);
       const bool has_pos = pos2 != nullptr;
       const int wi = static_cast<int>(warp) - 10;
@@ -661,46 +694,57 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(bar);
       };
-      sp[lane] = pos_ld(qrow0, lane);
-      sp[lane + 32] = pos_ld(qrow0, lane + 32);
-      sp[64 + lane] = pos_ld(qrow0 + C::BM, lane);
-      sp[96 + lane] = pos_ld(qrow0 + C::BM, lane + 32);
-      int2 ka = pos_ld(w.start, lane), kb = pos_ld(w.start, lane + 32);  // next K tile's
-      __syncwarp();
-      bool ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_q, 0, &s_abort));
-      if (ok) {
+      bool ok = true;
+      int32_t c0 = 0;
+      WorkItem w;
+      for (int32_t k = 0; ok && cta_item(k, w); ++k) {
+        const int32_t q0 = w.blk * 2 * C::BM;
+        const bool has1 = q0 + C::BM < w.len;
+        const int32_t nkv = (w.len + C::BN - 1) / C::BN;
+        const int64_t qrow0 = static_cast<int64_t>(w.start) + q0;
+        // (the previous item's positions are no longer read: its tiles are done)
+        __syncwarp();
+        sp[lane] = pos_ld(qrow0, lane);
+        sp[lane + 32] = pos_ld(qrow0, lane + 32);
+        sp[64 + lane] = pos_ld(qrow0 + C::BM, lane);
+        sp[96 + lane] = pos_ld(qrow0 + C::BM, lane + 32);
+        int2 ka = pos_ld(w.start, lane), kb = pos_ld(w.start, lane + 32);  // next K tile's
+        __syncwarp();
+        ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_q, k & 1, &s_abort));
+        if (!ok) break;
         rot_tile_qk<D>(smem_raw + C::OFF_Q, qrow0, p.T, has_pos, sp, p.rtab, p.rtab_rows, tid,
                        vmax, bad);
         release(bar_qr);
-      }
-      for (int32_t c = 0; ok && c < 2 * nkv; ++c) {
-        const int32_t slot = c % C::NSLOT;
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait_bk(bar_full + 8 * slot, (c / C::NSLOT) & 1, &s_abort));
-        if (!ok) break;
-        uint8_t* tile = smem_raw + C::OFF_KV + slot * C::TILE;
-        const int64_t krow0 = static_cast<int64_t>(w.start) + (c >> 1) * C::BN;
-        if (c & 1) {
-          cvt_tile_v<D>(tile, tid, vmax);
-        } else {
-          // stage this K tile's positions, then prefetch the next tile's
-          __syncwarp();
-          sp[128 + lane] = ka;
-          sp[160 + lane] = kb;
-          __syncwarp();
-          if ((c >> 1) + 1 < nkv) {
-            ka = pos_ld(krow0 + C::BN, lane);
-            kb = pos_ld(krow0 + C::BN, lane + 32);
+        for (int32_t cc = 0; ok && cc < 2 * nkv; ++cc) {
+          const int32_t c = c0 + cc, slot = c % C::NSLOT;
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait_bk(bar_full + 8 * slot, (c / C::NSLOT) & 1, &s_abort));
+          if (!ok) break;
+          uint8_t* tile = smem_raw + C::OFF_KV + slot * C::TILE;
+          const int64_t krow0 = static_cast<int64_t>(w.start) + (cc >> 1) * C::BN;
+          if (cc & 1) {
+            cvt_tile_v<D>(tile, tid, vmax);
+          } else {
+            // stage this K tile's positions, then prefetch the next tile's
+            __syncwarp();
+            sp[128 + lane] = ka;
+            sp[160 + lane] = kb;
+            __syncwarp();
+            if ((cc >> 1) + 1 < nkv) {
+              ka = pos_ld(krow0 + C::BN, lane);
+              kb = pos_ld(krow0 + C::BN, lane + 32);
+            }
+            rot_tile_qk<D>(tile, krow0, p.T, has_pos, sp + 128, p.rtab, p.rtab_rows, tid, vmax,
+                           bad);
           }
-          rot_tile_qk<D>(tile, krow0, p.T, has_pos, sp + 128, p.rtab, p.rtab_rows, tid, vmax,
-                         bad);
+          release(bar_rdy + 8 * slot);
+          if (cc == 0 && has1) {
+            rot_tile_qk<D>(smem_raw + C::OFF_Q + C::TILE, qrow0 + C::BM, p.T, has_pos, sp + 64,
+                           p.rtab, p.rtab_rows, tid, vmax, bad);
+            release(bar_qr + 8);
+          }
         }
-        release(bar_rdy + 8 * slot);
-        if (c == 0 && has1) {
-          rot_tile_qk<D>(smem_raw + C::OFF_Q + C::TILE, qrow0 + C::BM, p.T, has_pos, sp + 64,
-                         p.rtab, p.rtab_rows, tid, vmax, bad);
-          release(bar_qr + 8);
-        }
+        c0 += 2 * nkv;
       }
       if (!ok) {
         s_abort = 1;
@@ -713,25 +757,53 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     warpgroup_reg_alloc<kFwdRegsHigh>();
     // ---------------------------------------------------- softmax warpgroups
     const int t = warp >> 2;  // Q tile of this warpgroup
-    if (t == 0 || has1) {
-      const uint32_t row = threadIdx.x & 127;
-      const uint32_t lane_off = ((warp & 3) * 32) << 16;
-      const uint32_t tS = tmem + lane_off + (t ? C::S_COL1 : C::S_COL0);
-      const uint32_t tO = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
-      const int32_t qrow = q0 + t * C::BM + static_cast<int32_t>(row);
+    const uint32_t row = threadIdx.x & 127;
+    const uint32_t lane_off = ((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (t ? C::S_COL1 : C::S_COL0);
+    // this warp's O staging: 32 rows x 64 bytes (one 32-column chunk at a time)
+    uint8_t* so = smem_raw + C::OFF_STG + warp * (32 * 64);
+    bool ok = true;
+    volatile WorkItem& w = misc.sw[warp];
+    volatile int32_t* cnt = misc.cnt[warp];  // k; S steps, items of this Q tile (parities)
+    cnt[0] = 0;
+    cnt[1] = 0;
+    cnt[2] = 0;
+    __syncwarp();
+    while (ok) {
+      {
+        __syncwarp();  // every lane done with the previous item's fields
+        const int32_t k = cnt[0];
+        WorkItem wk;
+        const bool more = cta_item(k, wk);
+        __syncwarp();  // ... and has read k
+        if (!more) break;
+        if (lane == 0) cnt[0] = k + 1;
+        w.sample = wk.sample;  // (the same values from every lane)
+        w.head = wk.head;
+        w.blk = wk.blk;
+        w.start = wk.start;
+        w.len = wk.len;
+        __syncwarp();
+      }
+      const int32_t q0 = w.blk * 2 * C::BM;
+      const bool has1 = q0 + C::BM < w.len;
+      if (t == 1 && !has1) continue;
+      const int32_t nkv = (w.len + C::BN - 1) / C::BN;
       // logit scale in base 2; the 8-bit variant folds in the row's Q scale and the
       // head's K scale (kept positive, so that masked -inf columns stay -inf)
       float sl2 = p.scale_log2;
       if constexpr (F8) {
         const float sk = e4m3_scale(sqrtf(__uint_as_float(p.amax2[w.head]))).s;
         const float sq =
-            qrow < w.len ? p.qscale[(static_cast<int64_t>(w.start) + qrow) * p.heads + w.head] : 0.f;
+            q0 + t * C::BM + static_cast<int32_t>(row) < w.len
+                ? p.qscale[(static_cast<int64_t>(w.start) + q0 + t * C::BM + row) * p.heads + w.head]
+                : 0.f;
         sl2 = fmaxf(sl2 * sq * sk, 1e-30f);
       }
       float m = -INFINITY, l = 0.f;
-      bool ok = true;
+      const int32_t par0 = cnt[1], len = w.len;
       for (int32_t j = 0; j < nkv; ++j) {
-        ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_s + 8 * t, j & 1, &s_abort));
+        ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_s + 8 * t, (par0 + j) & 1, &s_abort));
         if (!ok) break;
         tc_fence_after();
         uint32_t s[128];
@@ -743,7 +815,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int u = 0; u < 32; ++u) s[c * 32 + u] = r[u];
         }
         tmem_wait_ld();
-        const int32_t nvalid = w.len - j * C::BN;
+        const int32_t nvalid = len - j * C::BN;
         if (nvalid < C::BN) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
@@ -775,14 +847,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               l *= f;
               m = m_new;
             }
+            // (16 columns at a time: the score row is live here)
+            const uint32_t tO = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-              uint32_t r[32];
-              tmem_ld32(tO + cc * 32, r);
+            for (int cc = 0; cc < D / 16; ++cc) {
+              uint32_t r[16];
+              tmem_ld16(tO + cc * 16, r);
               tmem_wait_ld();
 #pragma unroll
-              for (int u = 0; u < 32; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * f);
-              tmem_st32(tO + cc * 32, r);
+              for (int u = 0; u < 16; ++u) r[u] = __float_as_uint(__uint_as_float(r[u]) * f);
+              tmem_st16(tO + cc * 16, r);
             }
             tmem_wait_st();
           }
@@ -840,20 +914,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_before();
         mbar_arrive(bar_p + 8 * t);
       }
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_o + 8 * t, 0, &s_abort));
-      // the warpgroup's four warps agree before the epilogue's barrier
-      const bool all_ok = !(t ? named_bar_or(2, 128, !ok) : named_bar_or(1, 128, !ok));
-      if (all_ok) {
-        tc_fence_after();
-        // O rows (bf16) staged in this tile's Q buffer (idle once every MMA is
-        // done) as [128 rows][D], 16-byte units XOR-swizzled by row, then written
-        // out with coalesced row stores by the warpgroup
-        constexpr int UNITS = D / 8;
-        uint8_t* so = smem_raw + (F8 ? C::OFF_STG + t * C::BM * D * 2 : C::OFF_Q + t * C::TILE);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_o + 8 * t, cnt[2] & 1, &s_abort));
+      // the warpgroup's four warps agree before they leave the item
+      if (t ? named_bar_or(2, 128, !ok) : named_bar_or(1, 128, !ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // Epilogue: O / l in bf16, one 32-column chunk at a time through the warp's
+      // staging (16-byte units of row r XOR-swizzled by (r / 2) % 4: conflict-free
+      // both ways), then out as 64-byte row pieces, 8 rows a store.  O is loaded
+      // from TMEM before this warpgroup's next arrival on bar_p, which is what
+      // lets the next item's first P V overwrite it.
+      {
         // the 8-bit variant's head V scale
         const float sv = F8 ? e4m3_scale(sqrtf(__uint_as_float(p.amax2[p.heads + w.head]))).s : 1.f;
         const float inv = sv / l;
-#pragma unroll
+        const int32_t tile0 = w.blk * 2 * C::BM + t * C::BM;  // first row of the Q tile (in sample)
+        const int32_t wrow0 = tile0 + static_cast<int32_t>(warp & 3) * 32;
+        const uint32_t tO = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
+        const int rr0 = static_cast<int>(lane >> 2), un = static_cast<int>(lane & 3);
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t r[32];
           tmem_ld32(tO + cc * 32, r);
@@ -865,26 +945,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 pack_bf16x2(__uint_as_float(r[8 * u + 2]) * inv, __uint_as_float(r[8 * u + 3]) * inv),
                 pack_bf16x2(__uint_as_float(r[8 * u + 4]) * inv, __uint_as_float(r[8 * u + 5]) * inv),
                 pack_bf16x2(__uint_as_float(r[8 * u + 6]) * inv, __uint_as_float(r[8 * u + 7]) * inv));
-            const int unit = cc * 4 + u;
-            *reinterpret_cast<uint4*>(so + row * (D * 2) + ((unit ^ (row % UNITS)) << 4)) = val;
+            *reinterpret_cast<uint4*>(so + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) = val;
           }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rr = rr0 + 8 * i;
+            const uint4 val =
+                *reinterpret_cast<const uint4*>(so + rr * 64 + ((un ^ ((rr >> 1) & 3)) << 4));
+            if (wrow0 + rr < w.len) {
+              const int64_t g =
+                  ((static_cast<int64_t>(w.start) + wrow0 + rr) * p.heads + w.head) * D + cc * 32 +
+                  un * 8;
+              *reinterpret_cast<uint4*>(p.o + g) = val;
+            }
+          }
+          __syncwarp();
         }
-        if (qrow < w.len)
-          p.lse[static_cast<int64_t>(w.head) * p.T + w.start + qrow] =
+        if (tile0 + static_cast<int32_t>(row) < w.len)
+          p.lse[static_cast<int64_t>(w.head) * p.T + w.start + tile0 + row] =
               (m + log2f(l)) * 0.69314718055994530942f;
-        if (t) named_bar_sync(2, 128); else named_bar_sync(1, 128);
-        const int32_t r0 = q0 + t * C::BM;  // first query row of the tile (in sample)
-        const int32_t nrows = min(C::BM, w.len - r0);
-        const int u = static_cast<int>(row) % UNITS;
-        for (int r = static_cast<int>(row) / UNITS; r < nrows; r += 128 / UNITS) {
-          const int64_t g = ((static_cast<int64_t>(w.start) + r0 + r) * p.heads + w.head) * D + u * 8;
-          *reinterpret_cast<uint4*>(p.o + g) =
-              *reinterpret_cast<const uint4*>(so + r * (D * 2) + ((u ^ (r % UNITS)) << 4));
-        }
-      } else {
-        s_abort = 1;
-        atomicOr(p.status, kFlagTimeout);
       }
+      __syncwarp();
+      if (lane == 0) {
+        cnt[1] = cnt[1] + nkv;
+        cnt[2] = cnt[2] + 1;
+      }
+      __syncwarp();
+    }
+    if (!ok) {
+      s_abort = 1;
+      atomicOr(p.status, kFlagTimeout);
     }
   }
   tc_fence_before();
@@ -933,8 +1024,11 @@ static cudaError_t launch_fwd_d(const AttnFwdArgs& a, cudaStream_t s) {
   p.pos = a.pos;
   p.rtab = reinterpret_cast<const float4*>(a.rtab);
   p.rtab_rows = a.rtab_rows;
-  const int64_t blocks = (static_cast<int64_t>(a.T + 2 * C::BM - 1) / (2 * C::BM) + a.n) * a.heads;
-  if (blocks <= 0) return cudaSuccess;
+  // an upper bound on the items (256-row query blocks of every (sample, head));
+  // persistent grid: one CTA per SM at most
+  const int64_t items = (static_cast<int64_t>(a.T + 2 * C::BM - 1) / (2 * C::BM) + a.n) * a.heads;
+  if (items <= 0) return cudaSuccess;
+  const int64_t blocks = items < device_sm_count() ? items : device_sm_count();
   {
     KernelTimer kt(F8 ? MF_K_ATTN_FWD_F8 : ROT ? MF_K_ATTN_FWD_ROT : MF_K_ATTN_FWD, s);
     attn_fwd_kernel<D, F8, ROT>

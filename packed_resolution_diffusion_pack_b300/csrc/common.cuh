@@ -172,6 +172,8 @@ struct AttnFwdArgs {
   int32_t rtab_rows = 0;
 };
 cudaError_t launch_attn_fwd(const AttnFwdArgs& a, cudaStream_t s);
+// Multiprocessor count of the current device (the persistent kernels' grid).
+int device_sm_count();
 // The rotate-on-load forward's table: (cos, sin) of v * omega_P (2D frequencies)
 // for v in [0, rows), as [rows][head_dim / 2] float pairs.
 cudaError_t launch_rope_table(int32_t head_dim, int32_t rows, float* tab, cudaStream_t s);

@@ -278,6 +278,48 @@ __device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The SS and TS forms with each shared-memory descriptor passed as its two 32-bit
+// words: the low word (start address, leading byte offset) changes from tile to
+// tile, the high word (stride byte offset, version, swizzle) is often one value
+// for every tile of a kernel.  A chain of MMAs then keeps 32-bit start words in
+// registers instead of 64-bit descriptors.
+template <bool F8 = false>
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                         uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                         uint32_t accumulate) {
+  if constexpr (F8)
+    asm volatile(
+        "{\n.reg .pred P;\n.reg .b64 A, B;\nsetp.ne.b32 P, %6, 0;\n"
+        "mov.b64 A, {%1, %2};\nmov.b64 B, {%3, %4};\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], A, B, %5, P;\n}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n.reg .pred P;\n.reg .b64 A, B;\nsetp.ne.b32 P, %6, 0;\n"
+        "mov.b64 A, {%1, %2};\nmov.b64 B, {%3, %4};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], A, B, %5, P;\n}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+template <bool F8 = false>
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                         uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  if constexpr (F8)
+    asm volatile(
+        "{\n.reg .pred P;\n.reg .b64 B;\nsetp.ne.b32 P, %5, 0;\n"
+        "mov.b64 B, {%2, %3};\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], B, %4, P;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n.reg .pred P;\n.reg .b64 B;\nsetp.ne.b32 P, %5, 0;\n"
+        "mov.b64 B, {%2, %3};\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], B, %4, P;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
