@@ -777,12 +777,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const bool more = cta_item(k, wk);
         __syncwarp();  // ... and has read k
         if (!more) break;
-        if (lane == 0) cnt[0] = k + 1;
-        w.sample = wk.sample;  // (the same values from every lane)
-        w.head = wk.head;
-        w.blk = wk.blk;
-        w.start = wk.start;
-        w.len = wk.len;
+        if (lane == 0) {
+          cnt[0] = k + 1;
+          w.sample = wk.sample;
+          w.head = wk.head;
+          w.blk = wk.blk;
+          w.start = wk.start;
+          w.len = wk.len;
+        }
         __syncwarp();
       }
       const int32_t q0 = w.blk * 2 * C::BM;
