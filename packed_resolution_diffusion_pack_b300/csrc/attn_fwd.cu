@@ -526,8 +526,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tma_prefetch_desc(&tm_v);
         int32_t c = 0, items = 0;
         bool ok = true;
-        WorkItem w;
-        for (int32_t k = 0; ok && cta_item(k, w); ++k) {
+        WorkItem wn;
+        bool more = cta_item(0, wn);
+        for (int32_t k = 0; ok && more; ++k) {
+          const WorkItem w = wn;
           const int32_t q0 = w.blk * 2 * C::BM;
           const bool has1 = q0 + C::BM < w.len;
           const int32_t nkv = (w.len + C::BN - 1) / C::BN;
@@ -539,6 +541,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               tma_load_3d(sQ + t * C::TILE + ch * C::CHUNK, &tm_q, bar_q, ch * (128 / C::EB),
                           w.head, w.start + q0 + t * C::BM);
           ++items;
+          more = cta_item(k + 1, wn);  // looked up while this item's tiles stream
           for (int32_t j = 0; j < nkv && ok; ++j) {
             for (int kv = 0; kv < 2; ++kv, ++c) {
               const int32_t slot = c % C::NSLOT, use = c / C::NSLOT;
@@ -607,11 +610,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         };
         // parities: n0 / n1 S steps of Q tile 0 / 1 so far, i1 items with a tile 1
         int32_t c0 = 0, n0 = 0, n1 = 0, i1 = 0;
-        WorkItem w;
-        for (int32_t k = 0; ok && cta_item(k, w); ++k) {
-          const int32_t q0 = w.blk * 2 * C::BM;
-          const bool has1 = q0 + C::BM < w.len;
-          const int32_t nkv = (w.len + C::BN - 1) / C::BN;
+        WorkItem wn;
+        bool more = cta_item(0, wn);
+        for (int32_t k = 0; ok && more; ++k) {
+          const int32_t q0 = wn.blk * 2 * C::BM;
+          const bool has1 = q0 + C::BM < wn.len;
+          const int32_t nkv = (wn.len + C::BN - 1) / C::BN;
           ok = mbar_wait(ROT ? bar_qr : bar_q, k & 1, &s_abort);
           tc_fence_after();
           // The first S GEMM of this item overwrites S_0, and its first P V (no
@@ -633,6 +637,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (nkv == 1) mma_commit(bar_qfree);
             mma_commit(bar_empty + 8 * (c0 % C::NSLOT));
           }
+          more = cta_item(k + 1, wn);  // the next item, looked up while the softmax runs
           for (int32_t j = 0; j < nkv && ok; ++j) {
             const int32_t ck = c0 + 2 * j;  // K_j; V_j at ck + 1
             ok = mbar_wait(bar_p, (n0 + j) & 1, &s_abort) && kv_wait(ck + 1);
@@ -764,32 +769,39 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     uint8_t* so = smem_raw + C::OFF_STG + warp * (32 * 64);
     bool ok = true;
     volatile WorkItem& w = misc.sw[warp];
-    volatile int32_t* cnt = misc.cnt[warp];  // k; S steps, items of this Q tile (parities)
-    cnt[0] = 0;
-    cnt[1] = 0;
-    cnt[2] = 0;
+    // the next item to look up; S steps, items of this Q tile so far (parities)
+    volatile int32_t* cnt = misc.cnt[warp];
+    WorkItem wn;  // the next item, looked up while the current one finishes
+    bool more = cta_item(0, wn);
+    if (lane == 0) {
+      cnt[0] = 1;
+      cnt[1] = 0;
+      cnt[2] = 0;
+    }
     __syncwarp();
-    while (ok) {
-      {
-        __syncwarp();  // every lane done with the previous item's fields
-        const int32_t k = cnt[0];
-        WorkItem wk;
-        const bool more = cta_item(k, wk);
-        __syncwarp();  // ... and has read k
-        if (!more) break;
-        if (lane == 0) {
-          cnt[0] = k + 1;
-          w.sample = wk.sample;
-          w.head = wk.head;
-          w.blk = wk.blk;
-          w.start = wk.start;
-          w.len = wk.len;
-        }
-        __syncwarp();
+    auto fetch_next = [&]() {
+      const int32_t kn = cnt[0];
+      more = cta_item(kn, wn);
+      __syncwarp();  // every lane has read kn
+      if (lane == 0) cnt[0] = kn + 1;
+      __syncwarp();
+    };
+    while (ok && more) {
+      __syncwarp();  // every lane done with the previous item's fields
+      if (lane == 0) {
+        w.sample = wn.sample;
+        w.head = wn.head;
+        w.blk = wn.blk;
+        w.start = wn.start;
+        w.len = wn.len;
       }
+      __syncwarp();
       const int32_t q0 = w.blk * 2 * C::BM;
       const bool has1 = q0 + C::BM < w.len;
-      if (t == 1 && !has1) continue;
+      if (t == 1 && !has1) {
+        fetch_next();
+        continue;
+      }
       const int32_t nkv = (w.len + C::BN - 1) / C::BN;
       // logit scale in base 2; the 8-bit variant folds in the row's Q scale and the
       // head's K scale (kept positive, so that masked -inf columns stay -inf)
@@ -916,6 +928,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_before();
         mbar_arrive(bar_p + 8 * t);
       }
+      fetch_next();  // its loads overlap the wait for the item's last P V
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_o + 8 * t, cnt[2] & 1, &s_abort));
       // the warpgroup's four warps agree before they leave the item
       if (t ? named_bar_or(2, 128, !ok) : named_bar_or(1, 128, !ok)) {
@@ -936,17 +949,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int32_t wrow0 = tile0 + static_cast<int32_t>(warp & 3) * 32;
         const uint32_t tO = tmem + lane_off + (t ? C::O_COL1 : C::O_COL0);
         const int rr0 = static_cast<int>(lane >> 2), un = static_cast<int>(lane & 3);
+        // the row's whole O in one round of TMEM loads (the score row is dead here)
+        uint32_t r[D];
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc)
+          tmem_ld32(tO + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(r + cc * 32));
+        tmem_wait_ld();
+#pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(tO + cc * 32, r);
-          tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
+            const uint32_t* v = r + cc * 32 + 8 * u;
             const uint4 val = make_uint4(
-                pack_bf16x2(__uint_as_float(r[8 * u]) * inv, __uint_as_float(r[8 * u + 1]) * inv),
-                pack_bf16x2(__uint_as_float(r[8 * u + 2]) * inv, __uint_as_float(r[8 * u + 3]) * inv),
-                pack_bf16x2(__uint_as_float(r[8 * u + 4]) * inv, __uint_as_float(r[8 * u + 5]) * inv),
-                pack_bf16x2(__uint_as_float(r[8 * u + 6]) * inv, __uint_as_float(r[8 * u + 7]) * inv));
+                pack_bf16x2(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv),
+                pack_bf16x2(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv),
+                pack_bf16x2(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv),
+                pack_bf16x2(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv));
             *reinterpret_cast<uint4*>(so + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) = val;
           }
           __syncwarp();
