@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t* __restric
   __shared__ int64_t s_part[1024];
   const int tid = threadIdx.x, nt = blockDim.x;
   for (int i = tid; i < nzero; i += nt) zero[i] = 0.f;
+  // words 1-7 of the status block: the attention kernels' work-item counters
+  if (tid >= 1 && tid < 8) status[tid] = 0u;
   if (tid == 0) s_bad = (cu[0] != 0 || cu[n] != T) ? 1 : 0;
   __syncthreads();
   for (int i = tid; i < n; i += nt) {
@@ -202,11 +204,13 @@ struct WorkItem {
 struct CtaMisc {
   uint32_t tmem;
   uint32_t abort;
-  // each softmax warp's current item and counters (item index, S steps and
-  // items of its Q tile so far), read back from shared memory where used: kept
-  // out of the registers its score row needs
-  WorkItem sw[8];
+  // each softmax warp's counters (item index, S steps and items of its Q tile so
+  // far), read back from shared memory where used: kept out of the registers its
+  // score row needs
   int32_t cnt[8][4];
+  // forward: the work items the producer has claimed, ring slot k % 4 for the
+  // CTA's k-th item (sample < 0: no more items)
+  WorkItem ring[4];
 };
 __device__ __forceinline__ bool find_item(const int32_t* __restrict__ cu,
                                           const int32_t* __restrict__ order,
@@ -258,10 +262,10 @@ struct FwdCfg {
   static constexpr int OFF_STG = OFF_KV + NSLOT * TILE;
   static constexpr int STG = 8 * 32 * 64;
   static constexpr int OFF_BAR = OFF_STG + STG;
-  static constexpr int OFF_MISC = OFF_BAR + (ROT ? 512 : 256);
+  static constexpr int OFF_MISC = OFF_BAR + 512;
   // rotate-on-load form: token positions staged per transform warp, int2 [2][192]
   // (its rows of Q tile 0, Q tile 1 and the current K tile)
-  static constexpr int OFF_POS = OFF_MISC + 320;
+  static constexpr int OFF_POS = OFF_MISC + 384;
   static constexpr int SMEM = OFF_POS + (ROT ? 2 * 192 * 8 : 0);
   static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
   // S = Q'K'^T and O += P V' (V' MN-major); operand format code 0 is fp16 under
@@ -296,6 +300,9 @@ struct FwdParams {
   const int32_t* pos;
   const float4* rtab;
   int32_t rtab_rows;
+  // work-item counter, zeroed by the schedule kernel: each CTA claims its next
+  // item (an index into the ranked list) with an atomic add
+  uint32_t* next_item;
 };
 
 // ------------------------------------------------------ rotation on load
@@ -442,7 +449,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t sbase = smem_u32(smem_raw);
   CtaMisc& misc = *reinterpret_cast<CtaMisc*>(smem_raw + C::OFF_MISC);
-  static_assert(sizeof(CtaMisc) <= 320, "per-CTA scalars");
+  static_assert(sizeof(CtaMisc) <= 384, "per-CTA scalars");
   uint32_t& s_tmem = misc.tmem;
   volatile uint32_t& s_abort = misc.abort;
   if (sbase & 1023u) {
@@ -463,12 +470,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t bar_o = bar_p + 16;                      // [2]
   const uint32_t bar_drain = bar_o + 16;
   const uint32_t bar_stall = bar_drain + 8;  // test hook: never arrived on
+  // work-item ring: slot published by the producer / read by every role
+  const uint32_t bar_ifull = bar_stall + 8;  // [4]
+  const uint32_t bar_iempty = bar_ifull + 32;  // [4]
   // rotate-on-load form: Q tile t / ring slot rewritten in place and fenced
-  const uint32_t bar_qr = bar_stall + 8;     // [2]
+  const uint32_t bar_qr = bar_iempty + 32;   // [2]
   const uint32_t bar_rdy = bar_qr + 16;      // [NSLOT]
   static_assert(!ROT || !F8, "the rotate-on-load form is a 16-bit forward");
-  static_assert(8 * (ROT ? 11 + 3 * C::NSLOT : 9 + 2 * C::NSLOT) <= C::OFF_MISC - C::OFF_BAR,
+  static_assert(8 * (ROT ? 19 + 3 * C::NSLOT : 17 + 2 * C::NSLOT) <= C::OFF_MISC - C::OFF_BAR,
                 "barrier region too small");
+  // readers of each work item: the MMA thread, the 8 softmax warps, the 2 rotation warps
+  constexpr uint32_t kTakers = ROT ? 11 : 9;
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -487,6 +499,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(bar_o + 8, 1);
     mbar_init(bar_drain, 1);
     mbar_init(bar_stall, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar_ifull + 8 * i, 1);
+      mbar_init(bar_iempty + 8 * i, kTakers);
+    }
     if (ROT) {
       mbar_init(bar_qr, 64);
       mbar_init(bar_qr + 8, 64);
@@ -504,17 +520,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  // Persistent: in wave k the CTA takes item k gridDim.x + blockIdx.x of the ranked
-  // list (longest samples first), or k gridDim.x + gridDim.x - 1 - blockIdx.x in odd
-  // waves, so that each CTA's items sum to nearly the same work; every role walks
-  // the same sequence.  Ring position c counts the K and V tiles across items (K_j
-  // of an item whose first tile is c0 at c0 + 2j, V_j at c0 + 2j + 1).
-  auto cta_item = [&](int32_t k, WorkItem& w) -> bool {
-    const int64_t idx = static_cast<int64_t>(k) * gridDim.x +
-                        ((k & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
-    if (idx > INT32_MAX) return false;
-    return find_item(p.cu, p.order, p.prefix, p.n, 2 * C::BM, static_cast<int32_t>(idx), w);
-  };
+  // Persistent: each CTA claims work items from the ranked list (longest samples
+  // first) with an atomic counter, so that a CTA that finishes early takes more.
+  // The producer claims item k + 1 while item k's tiles stream and publishes it in
+  // ring slot (k + 1) % 4; every other role reads its items from the ring.  Ring
+  // position c counts the K and V tiles across items (K_j of an item whose first
+  // tile is c0 at c0 + 2j, V_j at c0 + 2j + 1).
+  volatile WorkItem* ring = misc.ring;
 
   if (warp >= 8) {
     warpgroup_reg_dealloc<kFwdRegsLow>();
@@ -524,10 +536,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        // claims the CTA's k-th item into ring slot k % 4 (once its last reader is done
+        // with the item four before); false on a time-out
+        auto claim = [&](int32_t k, WorkItem& w, bool& valid) -> bool {
+          const int32_t slot = k & 3;
+          if (k >= 4 && !mbar_wait_bk(bar_iempty + 8 * slot, ((k >> 2) - 1) & 1, &s_abort))
+            return false;
+          const uint32_t idx = atomicAdd(p.next_item, 1u);
+          w = WorkItem{-1, 0, 0, 0, 0};
+          valid = idx <= static_cast<uint32_t>(INT32_MAX) &&
+                  find_item(p.cu, p.order, p.prefix, p.n, 2 * C::BM, static_cast<int32_t>(idx), w);
+          ring[slot].sample = valid ? w.sample : -1;
+          ring[slot].head = w.head;
+          ring[slot].blk = w.blk;
+          ring[slot].start = w.start;
+          ring[slot].len = w.len;
+          mbar_arrive(bar_ifull + 8 * slot);  // (release: the record is visible to its waiters)
+          return true;
+        };
         int32_t c = 0, items = 0;
-        bool ok = true;
         WorkItem wn;
-        bool more = cta_item(0, wn);
+        bool more = false;
+        bool ok = claim(0, wn, more);
         for (int32_t k = 0; ok && more; ++k) {
           const WorkItem w = wn;
           const int32_t q0 = w.blk * 2 * C::BM;
@@ -541,7 +571,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               tma_load_3d(sQ + t * C::TILE + ch * C::CHUNK, &tm_q, bar_q, ch * (128 / C::EB),
                           w.head, w.start + q0 + t * C::BM);
           ++items;
-          more = cta_item(k + 1, wn);  // looked up while this item's tiles stream
+          if (!(ok = claim(k + 1, wn, more))) break;  // while this item's tiles stream
           for (int32_t j = 0; j < nkv && ok; ++j) {
             for (int kv = 0; kv < 2; ++kv, ++c) {
               const int32_t slot = c % C::NSLOT, use = c / C::NSLOT;
@@ -610,12 +640,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         };
         // parities: n0 / n1 S steps of Q tile 0 / 1 so far, i1 items with a tile 1
         int32_t c0 = 0, n0 = 0, n1 = 0, i1 = 0;
-        WorkItem wn;
-        bool more = cta_item(0, wn);
-        for (int32_t k = 0; ok && more; ++k) {
-          const int32_t q0 = wn.blk * 2 * C::BM;
-          const bool has1 = q0 + C::BM < wn.len;
-          const int32_t nkv = (wn.len + C::BN - 1) / C::BN;
+        for (int32_t k = 0; ok; ++k) {
+          if (!(ok = mbar_wait(bar_ifull + 8 * (k & 3), (k >> 2) & 1, &s_abort))) break;
+          const int32_t sample = ring[k & 3].sample, blk = ring[k & 3].blk, len = ring[k & 3].len;
+          mbar_arrive(bar_iempty + 8 * (k & 3));
+          if (sample < 0) break;  // no more items
+          const int32_t q0 = blk * 2 * C::BM;
+          const bool has1 = q0 + C::BM < len;
+          const int32_t nkv = (len + C::BN - 1) / C::BN;
           ok = mbar_wait(ROT ? bar_qr : bar_q, k & 1, &s_abort);
           tc_fence_after();
           // The first S GEMM of this item overwrites S_0, and its first P V (no
@@ -637,7 +669,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (nkv == 1) mma_commit(bar_qfree);
             mma_commit(bar_empty + 8 * (c0 % C::NSLOT));
           }
-          more = cta_item(k + 1, wn);  // the next item, looked up while the softmax runs
           for (int32_t j = 0; j < nkv && ok; ++j) {
             const int32_t ck = c0 + 2 * j;  // K_j; V_j at ck + 1
             ok = mbar_wait(bar_p, (n0 + j) & 1, &s_abort) && kv_wait(ck + 1);
@@ -701,8 +732,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       };
       bool ok = true;
       int32_t c0 = 0;
-      WorkItem w;
-      for (int32_t k = 0; ok && cta_item(k, w); ++k) {
+      for (int32_t k = 0; ok; ++k) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_ifull + 8 * (k & 3), (k >> 2) & 1,
+                                                        &s_abort))))
+          break;
+        const WorkItem w{ring[k & 3].sample, ring[k & 3].head, ring[k & 3].blk, ring[k & 3].start,
+                         ring[k & 3].len};
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_iempty + 8 * (k & 3));
+        if (w.sample < 0) break;  // no more items
         const int32_t q0 = w.blk * 2 * C::BM;
         const bool has1 = q0 + C::BM < w.len;
         const int32_t nkv = (w.len + C::BN - 1) / C::BN;
@@ -768,38 +806,35 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // this warp's O staging: 32 rows x 64 bytes (one 32-column chunk at a time)
     uint8_t* so = smem_raw + C::OFF_STG + warp * (32 * 64);
     bool ok = true;
-    volatile WorkItem& w = misc.sw[warp];
-    // the next item to look up; S steps, items of this Q tile so far (parities)
+    // the CTA's item index k; S steps, items of this Q tile so far (parities)
     volatile int32_t* cnt = misc.cnt[warp];
-    WorkItem wn;  // the next item, looked up while the current one finishes
-    bool more = cta_item(0, wn);
     if (lane == 0) {
-      cnt[0] = 1;
+      cnt[0] = 0;
       cnt[1] = 0;
       cnt[2] = 0;
     }
     __syncwarp();
-    auto fetch_next = [&]() {
-      const int32_t kn = cnt[0];
-      more = cta_item(kn, wn);
-      __syncwarp();  // every lane has read kn
-      if (lane == 0) cnt[0] = kn + 1;
-      __syncwarp();
-    };
-    while (ok && more) {
-      __syncwarp();  // every lane done with the previous item's fields
+    // the current item is read from its ring slot, released once the epilogue is done
+    auto release_item = [&]() {
+      __syncwarp();  // every lane done with the item's fields
       if (lane == 0) {
-        w.sample = wn.sample;
-        w.head = wn.head;
-        w.blk = wn.blk;
-        w.start = wn.start;
-        w.len = wn.len;
+        const int32_t k = cnt[0];
+        mbar_arrive(bar_iempty + 8 * (k & 3));
+        cnt[0] = k + 1;
       }
       __syncwarp();
+    };
+    while (ok) {
+      const int32_t k = cnt[0];
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_ifull + 8 * (k & 3), (k >> 2) & 1,
+                                                      &s_abort))))
+        break;
+      volatile WorkItem& w = ring[k & 3];
+      if (w.sample < 0) break;  // no more items
       const int32_t q0 = w.blk * 2 * C::BM;
       const bool has1 = q0 + C::BM < w.len;
       if (t == 1 && !has1) {
-        fetch_next();
+        release_item();
         continue;
       }
       const int32_t nkv = (w.len + C::BN - 1) / C::BN;
@@ -928,7 +963,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_before();
         mbar_arrive(bar_p + 8 * t);
       }
-      fetch_next();  // its loads overlap the wait for the item's last P V
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_o + 8 * t, cnt[2] & 1, &s_abort));
       // the warpgroup's four warps agree before they leave the item
       if (t ? named_bar_or(2, 128, !ok) : named_bar_or(1, 128, !ok)) {
@@ -991,7 +1025,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         cnt[1] = cnt[1] + nkv;
         cnt[2] = cnt[2] + 1;
       }
-      __syncwarp();
+      release_item();
     }
     if (!ok) {
       s_abort = 1;
@@ -1044,6 +1078,7 @@ static cudaError_t launch_fwd_d(const AttnFwdArgs& a, cudaStream_t s) {
   p.pos = a.pos;
   p.rtab = reinterpret_cast<const float4*>(a.rtab);
   p.rtab_rows = a.rtab_rows;
+  p.next_item = a.status + 1;  // (the status block's second word; see launch_schedule)
   // an upper bound on the items (256-row query blocks of every (sample, head));
   // persistent grid: one CTA per SM at most
   const int64_t items = (static_cast<int64_t>(a.T + 2 * C::BM - 1) / (2 * C::BM) + a.n) * a.heads;
