@@ -30,7 +30,11 @@ struct CtaMiscB {
   int valid;
   uint32_t tmem;
   uint32_t abort;
+  // dK / dV kernel: the work items its producer has claimed, ring slot k % 4 for
+  // the CTA's k-th item (sample < 0: no more items)
+  WorkItemB ring[4];
 };
+static_assert(sizeof(CtaMiscB) <= 128, "per-CTA scalars: 128 bytes in each kernel's layout");
 __device__ __forceinline__ bool find_item_b(const int32_t* __restrict__ cu,
                                             const int32_t* __restrict__ order,
                                             const int32_t* __restrict__ prefix, int32_t n,
@@ -179,21 +183,21 @@ struct BwdCfg {
   static constexpr int KV_OFF_VEC = KV_OFF_DO + NST * TILE;
   static constexpr int KV_OFF_BAR = KV_OFF_VEC + NST * VEC;
   static constexpr int KV_OFF_MISC = KV_OFF_BAR + 256;
-  static constexpr int KV_SMEM = KV_OFF_MISC + 64;
+  static constexpr int KV_SMEM = KV_OFF_MISC + 128;
   // q kernel: Q', dO resident; K'_j through a ring of KSLOT tiles, V_j of VSLOT
   static constexpr int KSLOT = 3, VSLOT = 2;
   static constexpr int Q_OFF_Q = 0, Q_OFF_DO = TILE, Q_OFF_K = 2 * TILE;
   static constexpr int Q_OFF_V = Q_OFF_K + KSLOT * TILE;
   static constexpr int Q_OFF_BAR = Q_OFF_V + VSLOT * TILE;
   static constexpr int Q_OFF_MISC = Q_OFF_BAR + 256;
-  static constexpr int Q_SMEM = Q_OFF_MISC + 64;
+  static constexpr int Q_SMEM = Q_OFF_MISC + 128;
   // dQ-from-stored-dS kernel: (dS^T tile, K' tile) per stage, DQ_NS stages
   static constexpr int DS_TILE = 128 * 128 * 2;
   static constexpr int DQ_STAGE = DS_TILE + TILE;
   static constexpr int DQ_NS = D == 128 ? 3 : 4;
   static constexpr int DQ_OFF_BAR = DQ_NS * DQ_STAGE;
   static constexpr int DQ_OFF_MISC = DQ_OFF_BAR + 256;
-  static constexpr int DQ_SMEM = DQ_OFF_MISC + 64;
+  static constexpr int DQ_SMEM = DQ_OFF_MISC + 128;
   // TMEM columns
   static constexpr uint32_t KV_ST = 0, KV_DPT = 128, KV_DV = 256, KV_DK = 256 + D;
   static constexpr uint32_t Q_S = 0, Q_DP = 128, Q_DQ = 384;  // DP: two buffers
@@ -210,7 +214,7 @@ struct BwdCfg {
   static_assert(KV_SMEM <= 232448 && Q_SMEM <= 232448 && DQ_SMEM <= 232448,
                 "shared memory over the per-CTA limit");
   static_assert(DQ_STAGE % 1024 == 0 && DS_TILE % 1024 == 0, "dS / K' tiles on 1024-byte boundaries");
-  static_assert(8 * (2 + 2 * NST + 9) <= 256 && 8 * (2 + 2 * (KSLOT + VSLOT) + 12) <= 256,
+  static_assert(8 * (2 + 2 * NST + 17) <= 256 && 8 * (2 + 2 * (KSLOT + VSLOT) + 12) <= 256,
                 "barrier areas");
 };
 
@@ -243,6 +247,9 @@ struct BwdParams {
   // queries (null: dQ recomputes); see ds_tile_base
   uint16_t* ds;
   int64_t ds_cols;
+  // dK / dV kernel: work-item counter, zeroed by the schedule kernel; each CTA
+  // claims its next item (an index into the ranked list) with an atomic add
+  uint32_t* next_item;
 };
 
 // The stored-dS array holds 128-key tiles, each [ds_cols / 8 units][128 keys][8
@@ -376,10 +383,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t bar_acc_free = bar_done + 8;        // ... and loaded (256 arrivals)
   const uint32_t bar_drain = bar_acc_free + 8;
   const uint32_t bar_stall = bar_drain + 8;          // test hook: never arrived on
+  // work-item ring: slot published by the producer / read by the MMA thread and the
+  // 8 elementwise warps
+  const uint32_t bar_ifull = bar_stall + 8;          // [4]
+  const uint32_t bar_iempty = bar_ifull + 32;        // [4]
+  volatile WorkItemB* ring = misc.ring;
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     s_abort = 0;
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar_ifull + 8 * i, 1);
+      mbar_init(bar_iempty + 8 * i, 9);
+    }
     mbar_init(bar_kv, 1);
     mbar_init(bar_kv_free, 1);
     for (int i = 0; i < C::NST; ++i) {
@@ -415,11 +431,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
     }
-    __syncwarp();
+    // Lane 0 claims the CTA's items from the ranked list with an atomic counter (a
+    // CTA that finishes early takes more) and publishes each in ring slot k % 4 once
+    // its readers are done with the item four before; item k + 1 is claimed while
+    // item k's tiles stream.
+    auto publish = [&](int32_t k, uint32_t idx) -> bool {
+      const int32_t slot = k & 3;
+      if (k >= 4 && !mbar_wait_bk(bar_iempty + 8 * slot, ((k >> 2) - 1) & 1, &s_abort))
+        return false;
+      WorkItemB wi{-1, 0, 0, 0, 0};
+      const bool valid =
+          idx <= static_cast<uint32_t>(INT32_MAX) &&
+          find_item_b(p.cu, p.order, p.prefix, p.n, 128, static_cast<int32_t>(idx), wi);
+      ring[slot].sample = valid ? wi.sample : -1;
+      ring[slot].head = wi.head;
+      ring[slot].blk = wi.blk;
+      ring[slot].start = wi.start;
+      ring[slot].len = wi.len;
+      mbar_arrive(bar_ifull + 8 * slot);  // (release: the record is visible to its waiters)
+      return true;
+    };
     bool ok = true;
+    if (lane == 0) ok = publish(0, atomicAdd(p.next_item, 1u));
+    ok = __shfl_sync(0xffffffffu, ok, 0);
     int32_t gt = 0, items = 0;  // tiles issued (all items), items started
-    WorkItemB w;
-    for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
+    for (int32_t k = 0; ok; ++k) {
+      __syncwarp();  // lane 0's record for item k is in place
+      const WorkItemB w{ring[k & 3].sample, ring[k & 3].head, ring[k & 3].blk, ring[k & 3].start,
+                        ring[k & 3].len};
+      if (w.sample < 0) break;  // no more items
       const int32_t k0 = w.blk * C::BK, nq = (w.len + C::BQ - 1) / C::BQ;
       if (k > 0 &&
           !__all_sync(0xffffffffu, mbar_wait_bk(bar_kv_free, (k - 1) & 1, &s_abort))) {
@@ -434,6 +474,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       ++items;
+      const uint32_t idx_next = lane == 0 ? atomicAdd(p.next_item, 1u) : 0u;  // the next item
       const int64_t gbase_row = static_cast<int64_t>(w.head) * p.T + w.start;
       for (int32_t i = 0; i < nq; ++i, ++gt) {
         const int32_t st = gt % C::NST, use = gt / C::NST;
@@ -462,6 +503,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      q_ok ? p.delta + gbase_row + qi : p.pad + C::BQ + q);
         }
         cp_async_arrive_noinc(bar_full + 8 * st);
+      }
+      if (ok) {  // the next item, once this one's tiles are issued
+        if (lane == 0) ok = publish(k + 1, idx_next);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
     }
     if (!ok) {
@@ -507,9 +552,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = p.stall_us == 0 ||
                 mbar_wait_for(bar_stall, 0, &s_abort, static_cast<uint64_t>(p.stall_us) * 1000u);
       int32_t gt = 0;  // tiles of earlier items
-      WorkItemB w;
-      for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
-        const int32_t nq = (w.len + C::BQ - 1) / C::BQ;
+      for (int32_t k = 0; ok; ++k) {
+        if (!(ok = mbar_wait(bar_ifull + 8 * (k & 3), (k >> 2) & 1, &s_abort))) break;
+        const int32_t sample = ring[k & 3].sample, len = ring[k & 3].len;
+        mbar_arrive(bar_iempty + 8 * (k & 3));
+        if (sample < 0) break;  // no more items
+        const int32_t nq = (len + C::BQ - 1) / C::BQ;
         if (!(ok = wait(bar_kv, k & 1) && full(gt))) break;
         issue_st(gt);
         issue_dp(gt);
@@ -559,8 +607,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     float dsmax = 0.f;  // scaled |dS|: flag values outside the fp16 range
     bool ok = true;
     int32_t gt = 0;
-    WorkItemB w;
-    for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
+    for (int32_t k = 0; ok; ++k) {
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_ifull + 8 * (k & 3), (k >> 2) & 1,
+                                                      &s_abort))))
+        break;
+      const WorkItemB w{ring[k & 3].sample, ring[k & 3].head, ring[k & 3].blk, ring[k & 3].start,
+                        ring[k & 3].len};
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_iempty + 8 * (k & 3));
+      if (w.sample < 0) break;  // no more items
       const int32_t k0 = w.blk * C::BK, nq = (w.len + C::BQ - 1) / C::BQ;
       const bool key_ok = k0 + static_cast<int32_t>(row) < w.len;
       // dS is staged in fp16 as ds_mul * dS (a power of two; see ds_scale_for)
@@ -1316,6 +1371,7 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
   p.stall_us = a.stall_us;
   p.ds = a.ds;
   p.ds_cols = a.ds_cols;
+  p.next_item = a.status + 2;  // (the status block's third word; see launch_schedule)
   // both kernels: one item per (sample, head, 128-row tile), longest samples
   // first; one persistent CTA per SM (at most one per item)
   const int64_t items = (static_cast<int64_t>(a.T + 127) / 128 + a.n) * a.heads;
