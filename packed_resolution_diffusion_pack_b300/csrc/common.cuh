@@ -91,7 +91,8 @@ __device__ __forceinline__ E4m3Scale e4m3_scale(float A) {
 }
 
 // --------------------------------------------------------- workspace layout
-// [0, 256)            device status word (uint32, flags kFlag*)
+// [0, 256)            device status word (uint32, flags kFlag*); words 1-2 the forward's
+//                      and the dK / dV kernel's work-item counters
 // [256, +sched)       schedule: int32 order[n], int32 prefix[n+1]
 // then 1024-aligned:  q16, k16  fp16 [T][h][d]  (rotated Q', K')
 // fwd only:           v16 fp16 [T][h][d]
@@ -141,7 +142,8 @@ cudaError_t launch_prep_e4m3(const uint16_t* q, const uint16_t* k, const uint16_
                              uint32_t* amax2, const int32_t* d_pos, int32_t naxes, int32_t T,
                              int32_t heads, int32_t head_dim, cudaStream_t s);
 // Builds the longest-first work list (items of `blk` rows per sample and head)
-// and validates cu_seqlens; zeroes the status word first, and `nzero` floats at
+// and validates cu_seqlens; zeroes the status word and the work-item counters
+// after it (words 1-7) first, and `nzero` floats at
 // `zero` (may be null).
 cudaError_t launch_schedule(const int32_t* d_cu, int32_t n, int32_t T, int32_t max_len,
                             int32_t heads, int32_t blk, uint32_t* status, int32_t* order,
