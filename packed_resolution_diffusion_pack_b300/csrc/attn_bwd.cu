@@ -214,7 +214,7 @@ struct BwdCfg {
   static_assert(KV_SMEM <= 232448 && Q_SMEM <= 232448 && DQ_SMEM <= 232448,
                 "shared memory over the per-CTA limit");
   static_assert(DQ_STAGE % 1024 == 0 && DS_TILE % 1024 == 0, "dS / K' tiles on 1024-byte boundaries");
-  static_assert(8 * (2 + 2 * NST + 17) <= 256 && 8 * (2 + 2 * (KSLOT + VSLOT) + 12) <= 256,
+  static_assert(8 * (2 + 2 * NST + 17) <= 256 && 8 * (2 + 2 * (KSLOT + VSLOT) + 20) <= 256,
                 "barrier areas");
 };
 
@@ -247,7 +247,8 @@ struct BwdParams {
   // queries (null: dQ recomputes); see ds_tile_base
   uint16_t* ds;
   int64_t ds_cols;
-  // dK / dV kernel: work-item counter, zeroed by the schedule kernel; each CTA
+  // work-item counters, zeroed by the schedule kernel: the dK / dV kernel's at
+  // next_item[0], the recompute form's dQ kernel's at next_item[1]; each CTA
   // claims its next item (an index into the ranked list) with an atomic add
   uint32_t* next_item;
 };
@@ -818,10 +819,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t bar_acc_free = bar_o + 8;               // ... and loaded (256 arrivals)
   const uint32_t bar_drain = bar_acc_free + 8;
   const uint32_t bar_stall = bar_drain + 8;              // test hook: never arrived on
+  // work-item ring: slot published by the producer / read by the MMA thread and the
+  // 8 elementwise warps
+  const uint32_t bar_ifull = bar_stall + 8;              // [4]
+  const uint32_t bar_iempty = bar_ifull + 32;            // [4]
+  volatile WorkItemB* ring = misc.ring;
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     s_abort = 0;
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar_ifull + 8 * i, 1);
+      mbar_init(bar_iempty + 8 * i, 9);
+    }
     mbar_init(bar_q, 1);
     mbar_init(bar_q_free, 1);
     for (int i = 0; i < C::KSLOT; ++i) {
@@ -861,10 +871,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      bool ok = true;
+      // The CTA's items are claimed from the ranked list with an atomic counter (a
+      // CTA that finishes early takes more) and published in ring slot k % 4 once
+      // their readers are done with the item four before; item k + 1 is claimed
+      // while item k's tiles stream.
+      uint32_t* const counter = p.next_item + 1;
+      auto publish = [&](int32_t k, uint32_t idx, WorkItemB& wi, bool& valid) -> bool {
+        const int32_t slot = k & 3;
+        if (k >= 4 && !mbar_wait_bk(bar_iempty + 8 * slot, ((k >> 2) - 1) & 1, &s_abort))
+          return false;
+        wi = WorkItemB{-1, 0, 0, 0, 0};
+        valid = idx <= static_cast<uint32_t>(INT32_MAX) &&
+                find_item_b(p.cu, p.order, p.prefix, p.n, 128, static_cast<int32_t>(idx), wi);
+        ring[slot].sample = valid ? wi.sample : -1;
+        ring[slot].head = wi.head;
+        ring[slot].blk = wi.blk;
+        ring[slot].start = wi.start;
+        ring[slot].len = wi.len;
+        mbar_arrive(bar_ifull + 8 * slot);  // (release: the record is visible to its waiters)
+        return true;
+      };
       int32_t gs = 0, items = 0;  // steps (K', V copies) of earlier items, items started
-      WorkItemB w;
-      for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
+      WorkItemB wn;
+      bool more = false;
+      bool ok = publish(0, atomicAdd(counter, 1u), wn, more);
+      for (int32_t k = 0; ok && more; ++k) {
+        const WorkItemB w = wn;
         const int32_t q0 = w.blk * C::BQ, nk = (w.len + C::BK - 1) / C::BK;
         if (k > 0 && !mbar_wait_bk(bar_q_free, (k - 1) & 1, &s_abort)) {
           ok = false;
@@ -876,6 +908,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(sDO + ch * C::CHUNK, &tm_do, bar_q, ch * 64, w.head, w.start + q0);
         }
         ++items;
+        const uint32_t idx_next = atomicAdd(counter, 1u);  // read once the K', V loads are issued
         for (int32_t j = 0; j < nk; ++j) {
           const int32_t g = gs + j;
           const int32_t ks = g % C::KSLOT, ku = g / C::KSLOT;
@@ -898,6 +931,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         w.head, w.start + j * C::BK);
         }
         gs += nk;
+        if (ok) ok = publish(k + 1, idx_next, wn, more);
       }
       if (!ok) {
         s_abort = 1;
@@ -947,9 +981,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = p.stall_us == 0 ||
                 mbar_wait_for(bar_stall, 0, &s_abort, static_cast<uint64_t>(p.stall_us) * 1000u);
       int32_t gs = 0;  // steps of earlier items
-      WorkItemB w;
-      for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
-        const int32_t nk = (w.len + C::BK - 1) / C::BK;
+      for (int32_t k = 0; ok; ++k) {
+        if (!(ok = mbar_wait(bar_ifull + 8 * (k & 3), (k >> 2) & 1, &s_abort))) break;
+        const int32_t sample = ring[k & 3].sample, len = ring[k & 3].len;
+        mbar_arrive(bar_iempty + 8 * (k & 3));
+        if (sample < 0) break;  // no more items
+        const int32_t nk = (len + C::BK - 1) / C::BK;
         if (!(ok = wait(bar_q, k & 1))) break;
         // S is free once the elementwise warps have copied out the previous step's
         if (gs > 0 && !(ok = wait(bar_s_free, (gs - 1) & 1))) break;
@@ -996,8 +1033,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     float dsmax = 0.f;
     bool ok = true;
     int32_t gs = 0;
-    WorkItemB w;
-    for (int32_t k = 0; ok && cta_item(p, k, w); ++k) {
+    for (int32_t k = 0; ok; ++k) {
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bk(bar_ifull + 8 * (k & 3), (k >> 2) & 1,
+                                                      &s_abort))))
+        break;
+      const WorkItemB w{ring[k & 3].sample, ring[k & 3].head, ring[k & 3].blk, ring[k & 3].start,
+                        ring[k & 3].len};
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_iempty + 8 * (k & 3));
+      if (w.sample < 0) break;  // no more items
       const int32_t q0 = w.blk * C::BQ, nk = (w.len + C::BK - 1) / C::BK;
       const int32_t qrow = q0 + static_cast<int32_t>(row);
       const bool row_ok = qrow < w.len;
@@ -1371,7 +1415,7 @@ static cudaError_t launch_bwd_d(const AttnBwdArgs& a, cudaStream_t s) {
   p.stall_us = a.stall_us;
   p.ds = a.ds;
   p.ds_cols = a.ds_cols;
-  p.next_item = a.status + 2;  // (the status block's third word; see launch_schedule)
+  p.next_item = a.status + 2;  // (the status block's words 2-3; see launch_schedule)
   // both kernels: one item per (sample, head, 128-row tile), longest samples
   // first; one persistent CTA per SM (at most one per item)
   const int64_t items = (static_cast<int64_t>(a.T + 127) / 128 + a.n) * a.heads;

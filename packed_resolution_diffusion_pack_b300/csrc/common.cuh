@@ -91,8 +91,9 @@ __device__ __forceinline__ E4m3Scale e4m3_scale(float A) {
 }
 
 // --------------------------------------------------------- workspace layout
-// [0, 256)            device status word (uint32, flags kFlag*); words 1-2 the forward's
-//                      and the dK / dV kernel's work-item counters
+// [0, 256)            device status word (uint32, flags kFlag*); words 1-3 the work-item
+//                      counters of the forward, the dK / dV kernel and the recompute
+//                      form's dQ kernel
 // [256, +sched)       schedule: int32 order[n], int32 prefix[n+1]
 // then 1024-aligned:  q16, k16  fp16 [T][h][d]  (rotated Q', K')
 // fwd only:           v16 fp16 [T][h][d]
