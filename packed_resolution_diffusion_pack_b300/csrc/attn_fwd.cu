@@ -6,15 +6,21 @@
 //   O_j = sum_k softmax_k(scale <q'_j, k'_k>) v_k over the keys of sample i only,
 //   LSE_j = ln sum_k exp(scale <q'_j, k'_k>).
 //
-// Design (one CTA = one sample, one head, 256 query rows = two 128-row Q tiles;
-// three warpgroups, registers moved from the third to the first two):
-//   warp 8      TMA producer: Q tiles once, then K_j, V_j tiles through a ring
-//               of shared-memory slots (128B-swizzled, 64-column chunks).
+// Design: a work item is one sample, one head and 256 query rows (two 128-row Q
+// tiles).  Persistent CTAs, one per SM, claim items from the longest-first list
+// through an atomic counter and keep TMEM and their barriers across items.  Three
+// warpgroups, registers moved from the third to the first two:
+//   warp 8      TMA producer: claims the items and publishes them to the other
+//               roles in a four-slot ring; per item the Q tiles, then K_j, V_j
+//               tiles through a ring of shared-memory slots (128B-swizzled,
+//               64-column chunks) that runs on across items.  The next item's Q
+//               tiles load once the current item's last S GEMMs are done.
 //   warp 9      MMA issuer (one thread): S_t = Q'_t K'_j^T (SS, into TMEM), then
 //               O_t += P_t V'_j with P_t read from TMEM (TS).  Q', K', V', P are
 //               fp16 (11 significant bits), accumulation fp32.  The two Q tiles
 //               ping-pong so the tensor core works on one while the other's
-//               softmax runs.
+//               softmax runs; an item's first S GEMMs run during the previous
+//               item's epilogue.
 //   warps 10-11 idle (they complete the third warpgroup), except in the
 //               rotate-on-load form (ROT): there they apply the 2D rotation to
 //               the bf16 Q and K tiles in shared memory as soon as TMA has
@@ -26,8 +32,8 @@
 //               exponentials, a lazy rescale
 //               of O (only when the running max grows by more than 2^8), P
 //               written back to TMEM as fp16 over the S columns.  Epilogue: O / l
-//               staged in the tile's Q buffer, written out with coalesced row
-//               stores; LSE.
+//               in bf16 through a per-warp staging chunk, written out as 64-byte
+//               row pieces; LSE.
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D).
 // Tiles never cross a sample: K/V tiles start at the sample's first token, key
 // columns past the sample end are masked to -inf, query rows past it not stored.
