@@ -7,11 +7,16 @@
 //   dS = P o (dP - D),  dQ' = scale dS K',  dK' = scale dS^T Q',
 //   dQ = R(-theta) dQ',  dK = R(-theta) dK'   (R orthogonal, R^T = R(-theta)).
 //
-// Kernels:
+// Kernels (the attention ones persistent, one CTA per SM, over work items of one
+// sample, head and 128-row tile, longest samples first):
 //   bwd_pre_kernel      D = rowsum(dO o O) and -LSE log2 e in fp32 ([h][T]);
 //                       per-head maxima of ||dO|| and ||v||.
-//   attn_bwd_kv_kernel  dK, dV: one CTA per sample, head and 128-key tile.
-//   attn_bwd_q_kernel   dQ: one CTA per sample, head and 128-query tile.
+//   attn_bwd_kv_kernel  dK, dV per 128-key tile (CTAs claim items through an
+//                       atomic counter); in the stored-dS form also writes dS^T.
+//   attn_bwd_dq_kernel  dQ per 128-query tile as one streaming GEMM over the
+//                       stored dS^T (CTAs stride over the list).
+//   attn_bwd_q_kernel   dQ per 128-query tile recomputing S and dP (the recompute
+//                       form; CTAs claim items through an atomic counter).
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -340,12 +345,12 @@ __device__ __forceinline__ bool cta_item(const BwdParams& p, int32_t k, WorkItem
 }
 
 // ------------------------------------------------------------- dK, dV kernel
-// Persistent: one CTA per SM walks its share of the (sample, head, key tile)
-// items.  Per item: K', V loaded once (as soon as the previous item's last S^T
-// and dP^T have read theirs), (Q'_i, dO_i) through the stage ring that runs on
-// across items, the dV / dK accumulators freed for the next item as soon as the
-// elementwise warps have loaded them; the epilogue's conversion and stores then
-// overlap the next item's first GEMMs.
+// Persistent: one CTA per SM claims (sample, head, key tile) items from the
+// longest-first list through an atomic counter.  Per item: K', V loaded once (as
+// soon as the previous item's last S^T and dP^T have read theirs), (Q'_i, dO_i)
+// through the stage ring that runs on across items, the dV / dK accumulators
+// freed for the next item as soon as the elementwise warps have loaded them; the
+// epilogue's conversion and stores then overlap the next item's first GEMMs.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q,
