@@ -692,6 +692,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (more) {
               if (!(ok = kv_wait(ck + 2))) break;
               issue_s(0, ck + 2);
+            } else {
+              // O_0 is final once this P V is done: tile 0's epilogue need not wait
+              // for tile 1's last softmax and P V
+              mma_commit(bar_o);
             }
             if (has1) {
               if (!(ok = mbar_wait(bar_p + 8, (n1 + j) & 1, &s_abort))) break;
@@ -706,7 +710,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
           }
           if (!ok) break;
-          mma_commit(bar_o);
           if (has1) mma_commit(bar_o + 8);
           c0 += 2 * nkv;
           n0 += nkv;
