@@ -146,9 +146,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
 }
 
 // ------------------------------------------------------------ main kernels
-// The backward runs as two kernels that need no atomics: each output row is
-// written by exactly one CTA.
-//  attn_bwd_kv_kernel  one CTA = one sample, one head, one 128-key tile (K', V
+// The backward runs as two kernels that need no atomics on the data: each output
+// row is written by exactly one work item.
+//  attn_bwd_kv_kernel  one item = one sample, one head, one 128-key tile (K', V
 //    resident): over the sample's 128-row query tiles i it accumulates
 //      S^T_i  = K' Q'_i^T      M=128 keys, N=128, K=d    SS fp16  -> TMEM ST
 //      P^T_i  = exp2(S^T scale log2e - LSE log2e)  (bf16, back into ST)
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
 //      dV    += P^T_i dO_i     M=128 keys, N=d,   K=128  TS bf16 (P^T from TMEM)
 //      dK    += dS^T_i Q'_i    M=128 keys, N=d,   K=128  TS fp16 (dS^T from TMEM)
 //    and writes dV and R(-theta) scale dK / ds_mul.
-//  attn_bwd_q_kernel   one CTA = one sample, one head, one 128-query tile (Q',
+//  attn_bwd_q_kernel   one item = one sample, one head, one 128-query tile (Q',
 //    dO resident): over the sample's 128-key tiles j it recomputes
 //      S_j  = Q' K'_j^T        M=128 queries, N=128, K=d  SS fp16  -> TMEM S
 //      dP_j = dO V_j^T         M=128 queries, N=128, K=d  SS bf16  -> TMEM DP[j % 2]
