@@ -68,7 +68,7 @@ __device__ __forceinline__ bool find_item_b(const int32_t* __restrict__ cu,
 // floats order like their bit patterns).  Block 0 also writes the pad rows
 // (128 x -inf as -LSE log2 e, 128 x 0 as D) that stand in for query rows past a
 // sample (they make P = 0 there).
-constexpr int kPreRowsPerBlock = 512;
+constexpr int kPreRowsPerBlock = 128;
 constexpr int kPreMaxHeads = 256;
 
 __device__ __forceinline__ void bf16x8_dot(const uint4& a, const uint4& b, float& acc) {
