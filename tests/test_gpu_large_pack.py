@@ -5,7 +5,8 @@ stored-dS array holds 35 GB).  The forward and the stored-dS backward run on the
 whole pack; the first sample and the last one (whose rows all lie past 2^31
 elements) are compared with the FP64 oracle run on that sample alone
 (paperlayer.ai summary 3.2.1: attention stays within each packed sample, so a
-sample's outputs depend on its own tokens only)."""
+sample's outputs depend on its own tokens only).  The rotate-on-load forward must
+equal the two-pass one bit for bit; the 8-bit forward gets a coarse check."""
 import numpy as np
 import pytest
 import torch
@@ -48,3 +49,15 @@ def test_pack_beyond_2_31_elements(cuda_lib):
         g_ref = oracle.attn_bwd(qs, ks, vs, dos, cu_1, pos_1)
         for name, gg, r in zip(("dq", "dk", "dv"), (dq, dk, dv), g_ref):
             check_grad(f64(gg[rows].contiguous()), r, f"{name} of sample {s}")
+    # the rotate-on-load forward: bit for bit the two-pass one, over the whole pack
+    o_r, lse_r = mf.varlen_attn_fwd_fused_rope(q, k, v, cu, pos, max_len, ws=ws)
+    mf.get_status(ws)
+    assert torch.equal(o_r, o) and torch.equal(lse_r, lse)
+    # the 8-bit forward: a coarse check of its offsets past 2^31 elements (its error
+    # bounds are checked on smaller packs): within 0.05 of the 16-bit O, whose
+    # entries here are of order 0.1
+    o8, lse8 = mf.varlen_attn_fwd_fp8(q, k, v, cu, pos, max_len, ws=ws)
+    mf.get_status(ws)
+    rows = slice((N_IMG - 1) * L, N_IMG * L)
+    assert (o8[rows].float() - o[rows].float()).abs().max().item() <= 0.05
+    assert (lse8[:, rows] - lse[:, rows]).abs().max().item() <= 0.05
